@@ -1,0 +1,269 @@
+"""CPU oracle for the unified-precision FP8 linear layer -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / reference leg of
+``bench.py`` may import this package.  The product path (``block_scaled_fp8_x1_gb300``) never
+imports, links or calls it, and it never calls the product path: the two share no code.
+
+The arithmetic lives in plain C (``fp8rl_oracle.c``, compiled here with gcc,
+``-ffp-contract=off``); this module only marshals numpy arrays.  What each routine computes,
+and which passage of "Technical summary: Jet-RL" (section "Quantization Scheme") it
+follows, is written beside the C code.
+
+Array conventions (all numpy, C-contiguous):
+  * BF16 tensors travel as ``uint16`` bit patterns.
+  * E4M3 codes are ``uint8``; scales are ``float32``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fp8rl_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``fp8rl_oracle.c`` into ``liboracle.so`` (gcc, OpenMP, no FMA contraction)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+           "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        sig = {
+            "orc_set_threads": (None, [ctypes.c_int]),
+            "orc_get_threads": (ctypes.c_int, []),
+            "orc_have_openmp": (ctypes.c_int, []),
+            "orc_bf16_to_f32": (ctypes.c_float, [ctypes.c_uint16]),
+            "orc_f64_to_bf16": (ctypes.c_uint16, [ctypes.c_double]),
+            "orc_f32_to_bf16": (ctypes.c_uint16, [ctypes.c_float]),
+            "orc_e4m3_decode": (ctypes.c_double, [ctypes.c_uint8]),
+            "orc_e4m3_encode": (ctypes.c_uint8, [ctypes.c_float]),
+            "orc_e4m3_encode_array": (None, [P, P, I64]),
+            "orc_e4m3_encode_bits_range": (None, [ctypes.c_uint32, I64, P]),
+            "orc_quant_group_f32": (None, [P, I64, P, P]),
+            "orc_quantize_1x128": (None, [P, I64, I64, I64, P, I64, P]),
+            "orc_quantize_128x1": (None, [P, I64, I64, I64, P, I64, P]),
+            "orc_quantize_128x128": (None, [P, I64, I64, I64, P, I64, P, P]),
+            "orc_rmsnorm": (None, [P, P, ctypes.c_float, I64, I64, P, P, P]),
+            "orc_silu_mul": (I64, [P, I64, I64, P, P]),
+            "orc_gemm": (None, [P, I64, P, I64, P, I64, P, I64, I64, I64, I64, I64, I64, P]),
+            "orc_gemm_sampled": (None, [P, I64, P, I64, P, I64, P, I64, I64, I64, I64, P, P,
+                                        I64, P]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        lib.orc_set_threads(os.cpu_count() or 1)
+        _lib = lib
+        return lib
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def set_threads(n: int) -> None:
+    _load().orc_set_threads(int(n))
+
+
+def threads() -> int:
+    lib = _load()
+    return lib.orc_get_threads() if lib.orc_have_openmp() else 1
+
+
+# ------------------------------------------------------------------ scalar formats
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """BF16 bit patterns -> float32 (exact: the bits are the top half)."""
+    b = _c(bits, np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def f64_to_bf16(v: np.ndarray) -> np.ndarray:
+    """Round binary64 values to BF16 (nearest, ties to even); returns uint16 bits."""
+    lib = _load()
+    flat = np.asarray(v, dtype=np.float64).ravel()
+    out = np.fromiter((lib.orc_f64_to_bf16(float(x)) for x in flat), dtype=np.uint16,
+                      count=flat.size)
+    return out.reshape(np.shape(v))
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    """E4M3 codes -> binary64 values (NaN for 0x7F/0xFF)."""
+    lib = _load()
+    table = np.array([lib.orc_e4m3_decode(b) for b in range(256)], dtype=np.float64)
+    return table[_c(codes, np.uint8)]
+
+
+def e4m3_encode(v: np.ndarray) -> np.ndarray:
+    """Finite binary32 values -> E4M3 codes (RNE, saturating at +-448)."""
+    x = _c(v, np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().orc_e4m3_encode_array(_p(x), _p(out), x.size)
+    return out
+
+
+def e4m3_encode_bits_range(first: int, count: int) -> np.ndarray:
+    """Codes for every binary32 bit pattern first, first+1, ..., first+count-1."""
+    out = np.empty(count, dtype=np.uint8)
+    _load().orc_e4m3_encode_bits_range(first, count, _p(out))
+    return out
+
+
+# ------------------------------------------------------------------ quantizers
+
+def quant_group(x: np.ndarray):
+    """One group of binary32 values -> (codes, scale)."""
+    v = _c(x, np.float32).ravel()
+    q = np.empty(v.size, dtype=np.uint8)
+    s = np.empty(1, dtype=np.float32)
+    _load().orc_quant_group_f32(_p(v), v.size, _p(q), _p(s))
+    return q, s[0]
+
+
+def quantize_1x128(a_bf16: np.ndarray):
+    """A[R,C] (uint16 BF16 bits) -> q[R,C] uint8, s[C/128, R] float32."""
+    a = _c(a_bf16, np.uint16)
+    R, C = a.shape
+    assert C % 128 == 0
+    q = np.empty((R, C), dtype=np.uint8)
+    s = np.empty((C // 128, R), dtype=np.float32)
+    _load().orc_quantize_1x128(_p(a), R, C, C, _p(q), C, _p(s))
+    return q, s
+
+
+def quantize_128x1(x_bf16: np.ndarray):
+    """X[M,K] -> transposed codes qT[K,M] uint8, sT[M/128, K] float32."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    assert M % 128 == 0
+    qT = np.empty((K, M), dtype=np.uint8)
+    sT = np.empty((M // 128, K), dtype=np.float32)
+    _load().orc_quantize_128x1(_p(x), M, K, K, _p(qT), M, _p(sT))
+    return qT, sT
+
+
+def quantize_128x128(w_bf16: np.ndarray, with_transpose: bool = True):
+    """W[N,K] -> q[N,K], s[N/128, K/128], and qT[K,N] (or None)."""
+    w = _c(w_bf16, np.uint16)
+    N, K = w.shape
+    assert N % 128 == 0 and K % 128 == 0
+    q = np.empty((N, K), dtype=np.uint8)
+    s = np.empty((N // 128, K // 128), dtype=np.float32)
+    qT = np.empty((K, N), dtype=np.uint8) if with_transpose else None
+    _load().orc_quantize_128x128(_p(w), N, K, K, _p(q), K, _p(s),
+                                 _p(qT) if qT is not None else None)
+    return q, s, qT
+
+
+def rmsnorm(x_bf16: np.ndarray, gamma_bf16: np.ndarray, eps: float, rstd_in=None):
+    """y = bf16((x*rstd)*gamma); returns (y uint16 [M,K], rstd float32 [M])."""
+    x = _c(x_bf16, np.uint16)
+    g = _c(gamma_bf16, np.uint16)
+    M, K = x.shape
+    y = np.empty((M, K), dtype=np.uint16)
+    r = np.empty(M, dtype=np.float32)
+    rin = _c(rstd_in, np.float32) if rstd_in is not None else None
+    _load().orc_rmsnorm(_p(x), _p(g), ctypes.c_float(eps), M, K, _p(y), _p(r),
+                        _p(rin) if rin is not None else None)
+    return y, r
+
+
+def silu_mul(gu_bf16: np.ndarray):
+    """GU[M, 2I] -> (h uint16 [M,I], alt uint16 [M,I], n_flagged).
+
+    ``alt`` differs from ``h`` only where the binary64 value lies within 2^-16 relative of a
+    BF16 rounding midpoint; there it holds the other BF16 neighbour."""
+    gu = _c(gu_bf16, np.uint16)
+    M, I2 = gu.shape
+    assert I2 % 2 == 0
+    I = I2 // 2
+    h = np.empty((M, I), dtype=np.uint16)
+    alt = np.empty((M, I), dtype=np.uint16)
+    n = _load().orc_silu_mul(_p(gu), M, I, _p(h), _p(alt))
+    return h, alt, int(n)
+
+
+def rmsnorm_quant(x_bf16, gamma_bf16, eps, rstd_in=None):
+    """RMSNorm then the two quantizations of y: (q, s, qT, sT, rstd, y)."""
+    y, r = rmsnorm(x_bf16, gamma_bf16, eps, rstd_in)
+    q, s = quantize_1x128(y)
+    qT, sT = quantize_128x1(y) if y.shape[0] % 128 == 0 else (None, None)
+    return q, s, qT, sT, r, y
+
+
+# ------------------------------------------------------------------ block-scaled GEMM
+
+_MODES = ("fwd", "dgrad", "wgrad")
+
+
+def _scale_strides(mode: str, R2: int, Kr: int):
+    if mode == "fwd":       # B = W[N,K], scales [N/128, K/128]
+        return 1, Kr // 128, 128
+    if mode == "dgrad":     # B = W^T[K,N], scales of W: [N/128 (=kb), K/128 (=r2/128)]
+        return R2 // 128, 1, 128
+    if mode == "wgrad":     # B = X^T[K,M], scales [M/128 (=kb), K (=r2)]
+        return R2, 1, 1
+    raise ValueError(mode)
+
+
+def gemm(A, sa, B, sb, mode: str):
+    """Block-scaled C[R1,R2] = sum_kb sa(kb,r1) sb(kb,r2) (A_kb . B_kb) in binary64.
+
+    A[R1,Kr], B[R2,Kr] uint8 codes (reduction contiguous); sa[Kr/128, R1];
+    sb laid out as for ``mode`` (see ``_scale_strides``)."""
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    sa = _c(sa, np.float32)
+    sb = _c(sb, np.float32)
+    R1, Kr = A.shape
+    R2, Kr2 = B.shape
+    assert Kr == Kr2 and Kr % 128 == 0
+    sb_kb, sb_r, sb_rdiv = _scale_strides(mode, R2, Kr)
+    y = np.empty((R1, R2), dtype=np.float64)
+    _load().orc_gemm(_p(A), Kr, _p(sa), R1, _p(B), Kr, _p(sb), sb_kb, sb_r, sb_rdiv, R1, R2,
+                     Kr, _p(y))
+    return y
+
+
+def gemm_sampled(A, sa, B, sb, mode: str, r1, r2):
+    """The same as ``gemm`` but only at output positions (r1[i], r2[i])."""
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    sa = _c(sa, np.float32)
+    sb = _c(sb, np.float32)
+    R1, Kr = A.shape
+    R2, _ = B.shape
+    sb_kb, sb_r, sb_rdiv = _scale_strides(mode, R2, Kr)
+    i1 = _c(r1, np.int64)
+    i2 = _c(r2, np.int64)
+    y = np.empty(i1.size, dtype=np.float64)
+    _load().orc_gemm_sampled(_p(A), Kr, _p(sa), R1, _p(B), Kr, _p(sb), sb_kb, sb_r, sb_rdiv,
+                             Kr, _p(i1), _p(i2), i1.size, _p(y))
+    return y

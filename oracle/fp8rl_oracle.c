@@ -1,0 +1,374 @@
+/*
+ * fp8rl_oracle.c -- plain, slow CPU oracle for the unified-precision FP8 linear layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library, its Python
+ * binding) may link, load or call this file.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg use it.  It shares no code, header, table or constant
+ * generator with the CUDA path.
+ *
+ * What it follows: "Technical summary: Jet-RL" (gist.science, paper 2601.14243):
+ *   - section "Quantization Scheme": activations are quantized per 1x128 group, weights per
+ *     128x128 block, DGrad and WGrad run in FP8 with 1x128 and 128x1 operand quantization;
+ *     saved activations are FP8 and produced by the preceding fused operator; gradients
+ *     between operators stay BF16.
+ *   - section "Core architecture": rollout and training forward share the same quantization
+ *     granularity and precision (one quantizer, one GEMM numerics).
+ *   - section "Implementation": fused activation (SiLU-mul) and RMSNorm kernels feed the
+ *     quantizer.
+ * The pages fix no formula.  Readings taken here (each is also listed in the design notes):
+ *   R1  FP8 format = OCP E4M3 "FN": bias 7, max 448, no infinities, 0x7F/0xFF = NaN.
+ *   R2  scale s = fl32(amax / 448) (IEEE single division); an all-zero group has s = 0 and
+ *       all codes 0x00.
+ *   R3  code = E4M3 round-to-nearest-even of fl32(x / s), saturating at +-448; the sign of a
+ *       value that rounds to zero is kept (0x80 for negative).
+ *   R4  block-scaled GEMM: per reduction block kb of 128, P_kb = sum of decoded products
+ *       (exact in binary64), y = sum_kb sa*sb*P_kb in binary64, unrounded.
+ *   R5  RMSNorm: sum of squares in binary64, ms = fl32(sum/K), rstd = 1/sqrt(ms+eps) in
+ *       IEEE single, y = bf16_rne((x*rstd)*gamma) in IEEE single; y is rounded to BF16
+ *       before it is quantized.
+ *   R6  SiLU-mul: h = bf16_rne(silu(g)*u) evaluated in binary64, g = first I columns.
+ *
+ * Every routine is written as the plain definition: scalar loops, no blocking or fusion.
+ * Independent groups are spread over OpenMP threads only to make big inputs finish.
+ * Compile with -ffp-contract=off so that no multiply-add is fused.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_API __attribute__((visibility("default")))
+
+static int g_threads = 1;
+
+ORC_API void orc_set_threads(int n) { g_threads = n > 0 ? n : 1; }
+ORC_API int orc_get_threads(void) { return g_threads; }
+ORC_API int orc_have_openmp(void) {
+#ifdef _OPENMP
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+/* ---------------------------------------------------------------- BF16 (R5, R6) */
+
+/* BF16 -> binary32 is exact: the BF16 bits are the top half of the binary32 bits. */
+ORC_API float orc_bf16_to_f32(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static uint16_t f32_bits_hi(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+/* Round a finite binary64 value to the nearest BF16, ties to the even significand.
+ * Definition: in v's binade the BF16 grid has spacing 2^(e-7); the two grid points that
+ * bracket |v| are compared by distance, and a tie goes to the even multiple of the spacing
+ * (the one whose last significand bit is 0). */
+ORC_API uint16_t orc_f64_to_bf16(double v) {
+    if (v == 0.0) return signbit(v) ? 0x8000 : 0x0000;
+    int neg = v < 0;
+    double a = fabs(v);
+    /* BF16 has 8 significant bits; spacing at a is 2^(e-7) for a in [2^e, 2^(e+1)),
+       and 2^-133 in the subnormal range (below 2^-126). */
+    int e;
+    frexp(a, &e);
+    e -= 1;
+    if (e < -126) e = -126;
+    double ulp = ldexp(1.0, e - 7);
+    double n = a / ulp; /* exact: scaling by a power of two */
+    double lo = floor(n), hi = lo + 1.0;
+    double r;
+    if (n - lo < hi - n) r = lo;
+    else if (n - lo > hi - n) r = hi;
+    else r = (fmod(lo, 2.0) == 0.0) ? lo : hi;
+    double mag = r * ulp;
+    /* mag is exactly a BF16 value (or 2^128 on overflow, which finite inputs here never
+       reach); read its bits through binary32, where it is exact. */
+    float f = (float)(neg ? -mag : mag);
+    return f32_bits_hi(f);
+}
+
+ORC_API uint16_t orc_f32_to_bf16(float v) { return orc_f64_to_bf16((double)v); }
+
+/* ---------------------------------------------------------------- E4M3 (R1, R3) */
+
+/* Decode an E4M3 code: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits.
+ * Exponent field 0 is subnormal (m * 2^-9); S.1111.111 is NaN; there is no infinity. */
+ORC_API double orc_e4m3_decode(uint8_t b) {
+    int sign = b >> 7;
+    int e = (b >> 3) & 0xF;
+    int m = b & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Encode a finite binary32 value as E4M3: round to nearest, ties to even, saturating at
+ * +-448.  Magnitudes below 2^-6 use the subnormal spacing 2^-9; a normal binade [2^e,2^(e+1))
+ * has spacing 2^(e-3).  The rounded integer count of spacings is even exactly when the
+ * mantissa field is even, so ties-to-even on the count is ties-to-even on the code. */
+ORC_API uint8_t orc_e4m3_encode(float v) {
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs((double)v);
+    if (a >= 448.0) return sign | 0x7E;
+    int e;
+    if (a < ldexp(1.0, -6)) {
+        e = -6;
+    } else {
+        frexp(a, &e);
+        e -= 1;
+    }
+    double ulp = ldexp(1.0, e - 3);
+    double n = a / ulp;
+    double lo = floor(n), hi = lo + 1.0;
+    double r;
+    if (n - lo < hi - n) r = lo;
+    else if (n - lo > hi - n) r = hi;
+    else r = (fmod(lo, 2.0) == 0.0) ? lo : hi;
+    double mag = r * ulp; /* <= 448 because a < 448 and 448 is a grid point */
+    if (mag == 0.0) return sign;
+    if (mag < ldexp(1.0, -6)) return sign | (uint8_t)(mag / ldexp(1.0, -9));
+    int e2;
+    frexp(mag, &e2);
+    e2 -= 1;
+    int m = (int)((mag / ldexp(1.0, e2) - 1.0) * 8.0);
+    return sign | (uint8_t)(((e2 + 7) << 3) | m);
+}
+
+ORC_API void orc_e4m3_encode_array(const float* v, uint8_t* out, int64_t n) {
+    #pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_encode(v[i]);
+}
+
+/* Encode every binary32 pattern in [first, first+count) (as raw bits). */
+ORC_API void orc_e4m3_encode_bits_range(uint32_t first, int64_t count, uint8_t* out) {
+    #pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t i = 0; i < count; ++i) {
+        uint32_t u = first + (uint32_t)i;
+        float f;
+        memcpy(&f, &u, sizeof f);
+        out[i] = orc_e4m3_encode(f);
+    }
+}
+
+/* ---------------------------------------------------------------- one quantization group */
+
+/* Quantize n values read from x[i*xs] (binary32, already exact copies of BF16 inputs):
+ * amax = max |x|, s = fl32(amax/448), code_i = E4M3(fl32(x_i/s)); s = 0 gives zero codes. */
+static void quant_group(const float* x, int64_t n, int64_t xs, uint8_t* q, int64_t qs,
+                        float* s_out) {
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf(x[i * xs]);
+        if (a > amax) amax = a;
+    }
+    float s = amax / 448.0f;
+    *s_out = s;
+    for (int64_t i = 0; i < n; ++i) {
+        if (s == 0.0f) q[i * qs] = 0x00;
+        else q[i * qs] = orc_e4m3_encode(x[i * xs] / s);
+    }
+}
+
+ORC_API void orc_quant_group_f32(const float* x, int64_t n, uint8_t* q, float* s) {
+    quant_group(x, n, 1, q, 1, s);
+}
+
+/* ---------------------------------------------------------------- quantizers */
+
+/* 1x128 groups along the columns of a BF16 matrix A[R,C] (row stride lda, C % 128 == 0).
+ * Codes q[r*ldq + c]; scales s[(c/128)*R + r]  (reduction-block-major). */
+ORC_API void orc_quantize_1x128(const uint16_t* a, int64_t R, int64_t C, int64_t lda,
+                                uint8_t* q, int64_t ldq, float* s) {
+    int64_t nb = C / 128;
+    #pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t r = 0; r < R; ++r) {
+        float buf[128];
+        for (int64_t b = 0; b < nb; ++b) {
+            for (int i = 0; i < 128; ++i) buf[i] = orc_bf16_to_f32(a[r * lda + b * 128 + i]);
+            quant_group(buf, 128, 1, q + r * ldq + b * 128, 1, &s[b * R + r]);
+        }
+    }
+}
+
+/* 128x1 groups: 128 consecutive rows of one column of X[M,K] (M % 128 == 0).  By definition
+ * this is the 1x128 quantization of the transpose: codes qT[k*ldqt + m], scales
+ * sT[(m/128)*K + k].  Written literally as transpose-then-quantize. */
+ORC_API void orc_quantize_128x1(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                                uint8_t* qT, int64_t ldqt, float* sT) {
+    int64_t nb = M / 128;
+    #pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t k = 0; k < K; ++k) {
+        float buf[128];
+        for (int64_t b = 0; b < nb; ++b) {
+            for (int i = 0; i < 128; ++i) buf[i] = orc_bf16_to_f32(x[(b * 128 + i) * ldx + k]);
+            quant_group(buf, 128, 1, qT + k * ldqt + b * 128, 1, &sT[b * K + k]);
+        }
+    }
+}
+
+/* 128x128 blocks of a BF16 weight W[N,K] (N, K multiples of 128).  Codes q[n*ldq + k],
+ * scales s[(n/128)*(K/128) + k/128].  The transposed copy qT[k*N + n] holds the same codes
+ * (a block is one group, so its transpose needs no new scale). */
+ORC_API void orc_quantize_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw,
+                                  uint8_t* q, int64_t ldq, float* s, uint8_t* qT) {
+    int64_t nbn = N / 128, nbk = K / 128;
+    #pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t bn = 0; bn < nbn; ++bn) {
+        static __thread float buf[128 * 128];
+        static __thread uint8_t qb[128 * 128];
+        for (int64_t bk = 0; bk < nbk; ++bk) {
+            for (int i = 0; i < 128; ++i)
+                for (int j = 0; j < 128; ++j)
+                    buf[i * 128 + j] = orc_bf16_to_f32(w[(bn * 128 + i) * ldw + bk * 128 + j]);
+            quant_group(buf, 128 * 128, 1, qb, 1, &s[bn * nbk + bk]);
+            for (int i = 0; i < 128; ++i)
+                for (int j = 0; j < 128; ++j) {
+                    q[(bn * 128 + i) * ldq + bk * 128 + j] = qb[i * 128 + j];
+                    if (qT) qT[(bk * 128 + j) * N + bn * 128 + i] = qb[i * 128 + j];
+                }
+        }
+    }
+}
+
+/* ---------------------------------------------------------------- RMSNorm (R5) */
+
+/* y[M,K] = bf16_rne((x*rstd)*gamma).  rstd_out (nullable) receives rstd.  If rstd_in is
+ * given, its values replace the computed rstd (used to re-check downstream bytes against a
+ * device rstd that differs in the last place). */
+ORC_API void orc_rmsnorm(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M,
+                         int64_t K, uint16_t* y, float* rstd_out, const float* rstd_in) {
+    #pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t m = 0; m < M; ++m) {
+        double sum = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double v = (double)orc_bf16_to_f32(x[m * K + k]);
+            sum += v * v;
+        }
+        float ms = (float)(sum / (double)K);
+        float rstd = 1.0f / sqrtf(ms + eps);
+        if (rstd_in) rstd = rstd_in[m];
+        if (rstd_out) rstd_out[m] = rstd;
+        for (int64_t k = 0; k < K; ++k) {
+            float xv = orc_bf16_to_f32(x[m * K + k]);
+            float g = orc_bf16_to_f32(gamma[k]);
+            float t = xv * rstd;
+            float yv = t * g;
+            y[m * K + k] = orc_f32_to_bf16(yv);
+        }
+    }
+}
+
+/* ---------------------------------------------------------------- SiLU-mul (R6) */
+
+/* Distance test: is the binary64 value v within rel*|v| of a BF16 rounding midpoint? */
+static int near_bf16_midpoint(double v, double rel) {
+    if (v == 0.0) return 0;
+    double a = fabs(v);
+    int e;
+    frexp(a, &e);
+    e -= 1;
+    if (e < -126) e = -126;
+    double ulp = ldexp(1.0, e - 7);
+    double mid = (floor(a / ulp) + 0.5) * ulp;
+    return fabs(a - mid) <= rel * a;
+}
+
+/* gu[M, 2I] holds g = gu[:, :I] and u = gu[:, I:].  h[M,I] = bf16_rne(silu(g)*u) from a
+ * binary64 evaluation, silu(g) = g / (1 + exp(-g)).  alt[M,I] (nullable) receives the other
+ * BF16 neighbour where the binary64 value lies within 2^-16 relative of a BF16 midpoint
+ * (there a binary32 evaluation may round either way), else a copy of h.  Returns the count
+ * of such near-midpoint elements. */
+ORC_API int64_t orc_silu_mul(const uint16_t* gu, int64_t M, int64_t I, uint16_t* h,
+                             uint16_t* alt) {
+    int64_t flagged = 0;
+    #pragma omp parallel for schedule(static) num_threads(g_threads) reduction(+ : flagged)
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t i = 0; i < I; ++i) {
+            double g = (double)orc_bf16_to_f32(gu[m * 2 * I + i]);
+            double u = (double)orc_bf16_to_f32(gu[m * 2 * I + I + i]);
+            double sg = g / (1.0 + exp(-g));
+            double v = sg * u;
+            uint16_t hb = orc_f64_to_bf16(v);
+            h[m * I + i] = hb;
+            if (alt) {
+                alt[m * I + i] = hb;
+                if (near_bf16_midpoint(v, ldexp(1.0, -16))) {
+                    /* the two BF16 neighbours of v, taken in v's binade */
+                    double a = fabs(v);
+                    int e;
+                    frexp(a, &e);
+                    e -= 1;
+                    if (e < -126) e = -126;
+                    double ulp = ldexp(1.0, e - 7);
+                    double lo = floor(a / ulp) * ulp, hi = lo + ulp;
+                    double hv = fabs((double)orc_bf16_to_f32(hb));
+                    double other = (hv == lo) ? hi : lo;
+                    alt[m * I + i] = orc_f64_to_bf16(v < 0 ? -other : other);
+                    flagged += 1;
+                }
+            }
+        }
+    }
+    return flagged;
+}
+
+/* ---------------------------------------------------------------- block-scaled GEMM (R4) */
+
+/* One output element of C[r1, r2] = sum over reduction blocks kb of
+ *     sa(kb, r1) * sb(kb, r2) * sum_{k in kb} dec(A[r1,k]) * dec(B[r2,k])
+ * A is [R1, Kr] codes (row stride lda), B is [R2, Kr] codes (row stride ldb); both hold the
+ * reduction dimension contiguously.  Scale indexing:
+ *     sa(kb, r1) = sa[kb*sa_kb + r1]
+ *     sb(kb, r2) = sb[kb*sb_kb + (r2/sb_rdiv)*sb_r]
+ * Forward (B = W, 128x128 blocks):  sb_rdiv = 128, sb_r = Kr/128, sb_kb = 1.
+ * DGrad   (B = W^T, same blocks):   sb_rdiv = 128, sb_r = 1,      sb_kb = R2/128.
+ * WGrad   (B = X^T, 128x1 groups):  sb_rdiv = 1,   sb_r = 1,      sb_kb = R2.
+ * Each block's partial sum is exact in binary64 (codes are multiples of 2^-9 below 448, so
+ * a 128-term sum spans fewer than 53 bits); the scale products are exact in binary64. */
+static double gemm_elem(const uint8_t* A, int64_t lda, const float* sa, int64_t sa_kb,
+                        const uint8_t* B, int64_t ldb, const float* sb, int64_t sb_kb,
+                        int64_t sb_r, int64_t sb_rdiv, int64_t Kr, int64_t r1, int64_t r2) {
+    double y = 0.0;
+    for (int64_t kb = 0; kb < Kr / 128; ++kb) {
+        double p = 0.0;
+        for (int64_t k = kb * 128; k < kb * 128 + 128; ++k)
+            p += orc_e4m3_decode(A[r1 * lda + k]) * orc_e4m3_decode(B[r2 * ldb + k]);
+        double scale = (double)sa[kb * sa_kb + r1] * (double)sb[kb * sb_kb + (r2 / sb_rdiv) * sb_r];
+        y += scale * p;
+    }
+    return y;
+}
+
+/* Full output y[R1, R2] (binary64, unrounded). */
+ORC_API void orc_gemm(const uint8_t* A, int64_t lda, const float* sa, int64_t sa_kb,
+                      const uint8_t* B, int64_t ldb, const float* sb, int64_t sb_kb,
+                      int64_t sb_r, int64_t sb_rdiv, int64_t R1, int64_t R2, int64_t Kr,
+                      double* y) {
+    #pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t r1 = 0; r1 < R1; ++r1)
+        for (int64_t r2 = 0; r2 < R2; ++r2)
+            y[r1 * R2 + r2] = gemm_elem(A, lda, sa, sa_kb, B, ldb, sb, sb_kb, sb_r, sb_rdiv, Kr,
+                                        r1, r2);
+}
+
+/* Sampled outputs: y[i] = C[r1[i], r2[i]]. */
+ORC_API void orc_gemm_sampled(const uint8_t* A, int64_t lda, const float* sa, int64_t sa_kb,
+                              const uint8_t* B, int64_t ldb, const float* sb, int64_t sb_kb,
+                              int64_t sb_r, int64_t sb_rdiv, int64_t Kr, const int64_t* r1,
+                              const int64_t* r2, int64_t n, double* y) {
+    #pragma omp parallel for schedule(dynamic, 16) num_threads(g_threads)
+    for (int64_t i = 0; i < n; ++i)
+        y[i] = gemm_elem(A, lda, sa, sa_kb, B, ldb, sb, sb_kb, sb_r, sb_rdiv, Kr, r1[i], r2[i]);
+}
