@@ -1,0 +1,421 @@
+// api.cu -- the extern "C" boundary of libfp8rl (declared in include/fp8rl.h).
+//
+// Validates arguments on the host (nothing is launched on an error), checks that the
+// current device is compute capability 10.3, builds the TMA descriptors of the GEMM
+// operands and picks the kernel form.  All compute happens in the CUDA kernels of
+// quantize.cu and gemm.cu.
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include "../../include/fp8rl.h"
+#include "gemm.h"
+
+namespace fp8rl {
+fp8rl_status read_and_clear_device_status(cudaStream_t st);  // gemm.cu
+}
+
+using namespace fp8rl;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    int state = 0;  // 0 unknown, 1 supported, -1 unsupported
+    int num_sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+fp8rl_status current_device(int* sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8RL_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FP8RL_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (d.state == 0) {
+        int major = 0, minor = 0, n = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FP8RL_ERR_CUDA;
+        d.state = (major == 10 && minor == 3) ? 1 : -1;
+        d.num_sms = n;
+    }
+    if (d.state < 0) return FP8RL_ERR_UNSUPPORTED_DEVICE;
+    if (sms) *sms = d.num_sms;
+    return FP8RL_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline fp8rl_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8RL_OK : FP8RL_ERR_CUDA; }
+
+// ---------------------------------------------------------------- TMA descriptors
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Row-major byte matrix [rows][cols] (row stride ld bytes), box of box_rows x 128 bytes,
+// 128-byte swizzle (the K-major layout the tcgen05 descriptors expect).
+fp8rl_status make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld,
+                       int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return FP8RL_ERR_CUDA;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld};
+    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                     es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8RL_OK : FP8RL_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- GEMM planning
+
+int decode_bn(int64_t M) { return M <= 64 ? 64 : (M <= 128 ? 128 : 256); }
+
+// Reduction slices for the decode form: minimise the longest chain of K-blocks any CTA
+// runs (waves x blocks per slice), preferring fewer slices on ties.
+int choose_splits(int64_t tiles, int64_t nkb, int num_sms) {
+    int best = 1;
+    int64_t best_cost = INT64_MAX;
+    for (int s = 1; s <= 16 && s <= nkb; ++s) {
+        const int64_t items = tiles * s;
+        const int64_t waves = (items + num_sms - 1) / num_sms;
+        const int64_t per = (nkb + s - 1) / s;
+        const int64_t cost = waves * per + (s > 1 ? 1 : 0);  // a slice pays one reduction
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+size_t counter_bytes(int64_t tiles) { return align_up((size_t)tiles * 4, 256); }
+
+size_t decode_ws_bytes(int64_t M, int64_t N, int64_t K, int splits) {
+    const int64_t tiles = (N + 127) / 128;
+    const int bn = decode_bn(M);
+    size_t b = counter_bytes(tiles);
+    if (splits > 1) b += (size_t)tiles * splits * bn * 128 * sizeof(float);
+    (void)K;
+    return b;
+}
+
+struct TiledArgs {
+    const uint8_t* A; const float* sa; int64_t sa_kb;
+    const uint8_t* B; const float* sb; int64_t sb_kb, sb_r; int b_mode;
+    uint16_t* c; int64_t ldc;
+    int64_t R1, R2, Kr;
+};
+
+fp8rl_status run_tiled(const TiledArgs& t, int grid_req, int num_sms, cudaStream_t st) {
+    CUtensorMap ta, tb;
+    fp8rl_status e = make_tmap(&ta, t.A, t.R1, t.Kr, t.Kr, 128);
+    if (e != FP8RL_OK) return e;
+    e = make_tmap(&tb, t.B, t.R2, t.Kr, t.Kr, 256);
+    if (e != FP8RL_OK) return e;
+    GemmParams p = {};
+    p.R1 = t.R1; p.R2 = t.R2; p.Kr = t.Kr;
+    p.sa = t.sa; p.sa_kb = t.sa_kb; p.sa_r = 0;
+    p.sb = t.sb; p.sb_kb = t.sb_kb; p.sb_r = t.sb_r;
+    p.c = t.c; p.ldc = t.ldc;
+    p.splits = 0;
+    p.m_tiles = (int)((t.R1 + 127) / 128);
+    p.n_tiles = (int)((t.R2 + 255) / 256);
+    p.nkb = (int)(t.Kr / 128);
+    p.num_items = p.m_tiles * p.n_tiles;
+    p.timeout_ns = g_timeout_ns.load();
+    int grid = grid_req > 0 ? grid_req : num_sms;
+    grid = std::max(1, std::min(grid, p.num_items));
+    return cuda_status(launch_gemm_tiled(ta, tb, p, t.b_mode, grid, st));
+}
+
+fp8rl_status run_decode(const uint8_t* qx, const float* sx, const uint8_t* qw, const float* sw,
+                        uint16_t* y, int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes,
+                        int splits_req, int num_sms, cudaStream_t st) {
+    const int bn = decode_bn(M);
+    const int64_t tiles = (N + 127) / 128;
+    const int64_t nkb = K / 128;
+    int splits = splits_req > 0 ? (int)std::min<int64_t>(splits_req, nkb)
+                                : choose_splits(tiles, nkb, num_sms);
+    const size_t need = decode_ws_bytes(M, N, K, splits);
+    if (ws == nullptr || ws_bytes < need) return FP8RL_ERR_WORKSPACE;
+    if (!aligned16(ws)) return FP8RL_ERR_ALIGN;
+    CUtensorMap ta, tb;
+    fp8rl_status e = make_tmap(&ta, qw, N, K, K, 128);
+    if (e != FP8RL_OK) return e;
+    e = make_tmap(&tb, qx, M, K, K, bn);
+    if (e != FP8RL_OK) return e;
+    GemmParams p = {};
+    p.R1 = N; p.R2 = M; p.Kr = K;
+    p.sa = sw; p.sa_kb = 1; p.sa_r = K / 128;
+    p.sb = sx; p.sb_kb = M; p.sb_r = 0;
+    p.c = y; p.ldc = N;
+    p.counters = reinterpret_cast<unsigned int*>(ws);
+    p.ws = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + counter_bytes(tiles));
+    p.splits = splits;
+    p.m_tiles = (int)tiles;
+    p.n_tiles = 1;
+    p.nkb = (int)nkb;
+    p.num_items = (int)(tiles * splits);
+    p.timeout_ns = g_timeout_ns.load();
+    const int grid = std::max(1, std::min(num_sms, p.num_items));
+    return cuda_status(launch_gemm_splitk(ta, tb, p, bn, grid, st));
+}
+
+}  // namespace
+
+// ====================================================================================
+extern "C" {
+
+int fp8rl_version(void) { return (0 << 16) | 1; }
+
+const char* fp8rl_status_string(fp8rl_status st) {
+    switch (st) {
+        case FP8RL_OK: return "FP8RL_OK";
+        case FP8RL_ERR_INVALID_ARG: return "FP8RL_ERR_INVALID_ARG";
+        case FP8RL_ERR_SHAPE: return "FP8RL_ERR_SHAPE";
+        case FP8RL_ERR_ALIGN: return "FP8RL_ERR_ALIGN";
+        case FP8RL_ERR_UNSUPPORTED_DEVICE: return "FP8RL_ERR_UNSUPPORTED_DEVICE";
+        case FP8RL_ERR_WORKSPACE: return "FP8RL_ERR_WORKSPACE";
+        case FP8RL_ERR_CUDA: return "FP8RL_ERR_CUDA";
+        case FP8RL_ERR_DEVICE_TIMEOUT: return "FP8RL_ERR_DEVICE_TIMEOUT";
+        case FP8RL_ERR_DEVICE_BOUNDS: return "FP8RL_ERR_DEVICE_BOUNDS";
+    }
+    return "FP8RL_ERR_UNKNOWN";
+}
+
+fp8rl_status fp8rl_init(int device) {
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess) return FP8RL_ERR_CUDA;
+    if (device < 0 || device >= n) return FP8RL_ERR_INVALID_ARG;
+    if (cudaSetDevice(device) != cudaSuccess) return FP8RL_ERR_CUDA;
+    return current_device(nullptr);
+}
+
+void fp8rl_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns > 0 ? ns : 1); }
+
+fp8rl_status fp8rl_check_status(fp8rl_stream_t stream) {
+    fp8rl_status e = current_device(nullptr);
+    if (e != FP8RL_OK) return e;
+    return read_and_clear_device_status(stream);
+}
+
+// ---------------------------------------------------------------- quantizers
+
+fp8rl_status fp8rl_quantize_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                                  float* s, uint8_t* qT, float* sT, fp8rl_stream_t stream) {
+    if (M < 0 || K <= 0 || ldx < K) return FP8RL_ERR_INVALID_ARG;
+    if ((qT == nullptr) != (sT == nullptr)) return FP8RL_ERR_INVALID_ARG;
+    if (K % 128 != 0) return FP8RL_ERR_SHAPE;
+    if (qT && M % 128 != 0) return FP8RL_ERR_SHAPE;
+    if (M == 0) return FP8RL_OK;
+    if (!x || !q || !s) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(s) || (ldx * 2) % 16 != 0) return FP8RL_ERR_ALIGN;
+    if (qT && (!aligned16(qT) || !aligned16(sT))) return FP8RL_ERR_ALIGN;
+    int sms = 0;
+    fp8rl_status e = current_device(&sms);
+    if (e != FP8RL_OK) return e;
+    if (qT) return cuda_status(launch_quant_dual(x, M, K, ldx, q, s, qT, sT, stream));
+    return cuda_status(launch_quant_1x128(x, M, K, ldx, q, s, sms, stream));
+}
+
+fp8rl_status fp8rl_quantize_128x1(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                                  uint8_t* qT, float* sT, fp8rl_stream_t stream) {
+    if (M < 0 || K <= 0 || ldx < K) return FP8RL_ERR_INVALID_ARG;
+    if (K % 128 != 0 || M % 128 != 0) return FP8RL_ERR_SHAPE;
+    if (M == 0) return FP8RL_OK;
+    if (!x || !qT || !sT) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(qT) || !aligned16(sT) || (ldx * 2) % 16 != 0) return FP8RL_ERR_ALIGN;
+    fp8rl_status e = current_device(nullptr);
+    if (e != FP8RL_OK) return e;
+    return cuda_status(launch_quant_dual(x, M, K, ldx, nullptr, nullptr, qT, sT, stream));
+}
+
+fp8rl_status fp8rl_quantize_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw,
+                                    uint8_t* q, float* s, uint8_t* qT, fp8rl_stream_t stream) {
+    if (N < 0 || K <= 0 || ldw < K) return FP8RL_ERR_INVALID_ARG;
+    if (K % 128 != 0 || N % 128 != 0) return FP8RL_ERR_SHAPE;
+    if (N == 0) return FP8RL_OK;
+    if (!w || !q || !s) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(q) || !aligned16(s) || (ldw * 2) % 16 != 0) return FP8RL_ERR_ALIGN;
+    if (qT && !aligned16(qT)) return FP8RL_ERR_ALIGN;
+    fp8rl_status e = current_device(nullptr);
+    if (e != FP8RL_OK) return e;
+    return cuda_status(launch_quant_128x128(w, N, K, ldw, q, s, qT, stream));
+}
+
+fp8rl_status fp8rl_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M,
+                                 int64_t K, uint8_t* q, float* s, uint8_t* qT, float* sT,
+                                 float* rstd, fp8rl_stream_t stream) {
+    if (M < 0 || K <= 0 || !(eps >= 0.0f) || eps > 3.0e38f) return FP8RL_ERR_INVALID_ARG;
+    if ((qT == nullptr) != (sT == nullptr)) return FP8RL_ERR_INVALID_ARG;
+    if (K % 128 != 0) return FP8RL_ERR_SHAPE;
+    if (qT && M % 128 != 0) return FP8RL_ERR_SHAPE;
+    if (M == 0) return FP8RL_OK;
+    if (!x || !gamma || !q || !s) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(q) || !aligned16(s)) return FP8RL_ERR_ALIGN;
+    if (qT && (!aligned16(qT) || !aligned16(sT))) return FP8RL_ERR_ALIGN;
+    if (rstd && !aligned16(rstd)) return FP8RL_ERR_ALIGN;
+    fp8rl_status e = current_device(nullptr);
+    if (e != FP8RL_OK) return e;
+    return cuda_status(launch_rmsnorm_quant(x, gamma, eps, M, K, q, s, qT, sT, rstd, stream));
+}
+
+fp8rl_status fp8rl_silu_mul_quant(const uint16_t* gu, int64_t M, int64_t I, uint8_t* q, float* s,
+                                  uint8_t* qT, float* sT, fp8rl_stream_t stream) {
+    if (M < 0 || I <= 0) return FP8RL_ERR_INVALID_ARG;
+    if ((qT == nullptr) != (sT == nullptr)) return FP8RL_ERR_INVALID_ARG;
+    if (I % 128 != 0) return FP8RL_ERR_SHAPE;
+    if (qT && M % 128 != 0) return FP8RL_ERR_SHAPE;
+    if (M == 0) return FP8RL_OK;
+    if (!gu || !q || !s) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(gu) || !aligned16(q) || !aligned16(s)) return FP8RL_ERR_ALIGN;
+    if (qT && (!aligned16(qT) || !aligned16(sT))) return FP8RL_ERR_ALIGN;
+    fp8rl_status e = current_device(nullptr);
+    if (e != FP8RL_OK) return e;
+    return cuda_status(launch_silu_mul_quant(gu, M, I, q, s, qT, sT, stream));
+}
+
+// ---------------------------------------------------------------- GEMMs
+
+size_t fp8rl_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {
+    return fp8rl_gemm_workspace_bytes_ex(op, M, N, K, nullptr);
+}
+
+size_t fp8rl_gemm_workspace_bytes_ex(int op, int64_t M, int64_t N, int64_t K,
+                                     const fp8rl_gemm_opts* opts) {
+    if (op != FP8RL_OP_FWD || M <= 0 || N <= 0 || K <= 0 || K % 128 != 0) return 0;
+    const int variant = opts ? opts->variant : FP8RL_VARIANT_AUTO;
+    const bool decode = variant == FP8RL_VARIANT_SPLITK || (variant == FP8RL_VARIANT_AUTO && M <= 256);
+    if (!decode || M > 256) return 0;
+    int sms = 0;
+    if (current_device(&sms) != FP8RL_OK) sms = 148;
+    const int64_t tiles = (N + 127) / 128, nkb = K / 128;
+    const int splits = (opts && opts->splits > 0) ? (int)std::min<int64_t>(opts->splits, nkb)
+                                                  : choose_splits(tiles, nkb, sms);
+    return decode_ws_bytes(M, N, K, splits);
+}
+
+fp8rl_status fp8rl_gemm_fwd_ex(const uint8_t* qx, const float* sx, const uint8_t* qw,
+                               const float* sw, uint16_t* y, int64_t M, int64_t N, int64_t K,
+                               void* ws, size_t ws_bytes, const fp8rl_gemm_opts* opts,
+                               fp8rl_stream_t stream) {
+    if (M < 0 || N < 0 || K <= 0) return FP8RL_ERR_INVALID_ARG;
+    const int variant = opts ? opts->variant : FP8RL_VARIANT_AUTO;
+    if (variant < FP8RL_VARIANT_AUTO || variant > FP8RL_VARIANT_SPLITK) return FP8RL_ERR_INVALID_ARG;
+    if (K % 128 != 0 || N % 128 != 0) return FP8RL_ERR_SHAPE;
+    if (M == 0 || N == 0) return FP8RL_OK;
+    if (!qx || !sx || !qw || !sw || !y) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(qx) || !aligned16(sx) || !aligned16(qw) || !aligned16(sw) || !aligned16(y))
+        return FP8RL_ERR_ALIGN;
+    const bool decode = variant == FP8RL_VARIANT_SPLITK || (variant == FP8RL_VARIANT_AUTO && M <= 256);
+    if (decode && M > 256) return FP8RL_ERR_SHAPE;
+    int sms = 0;
+    fp8rl_status e = current_device(&sms);
+    if (e != FP8RL_OK) return e;
+    if (decode)
+        return run_decode(qx, sx, qw, sw, y, M, N, K, ws, ws_bytes, opts ? opts->splits : 0, sms, stream);
+    TiledArgs t;
+    t.A = qx; t.sa = sx; t.sa_kb = M;
+    t.B = qw; t.sb = sw; t.sb_kb = 1; t.sb_r = K / 128; t.b_mode = SCALE_BLOCK;
+    t.c = y; t.ldc = N;
+    t.R1 = M; t.R2 = N; t.Kr = K;
+    return run_tiled(t, opts ? opts->grid : 0, sms, stream);
+}
+
+fp8rl_status fp8rl_gemm_fwd(const uint8_t* qx, const float* sx, const uint8_t* qw, const float* sw,
+                            uint16_t* y, int64_t M, int64_t N, int64_t K, void* ws,
+                            size_t ws_bytes, fp8rl_stream_t stream) {
+    return fp8rl_gemm_fwd_ex(qx, sx, qw, sw, y, M, N, K, ws, ws_bytes, nullptr, stream);
+}
+
+fp8rl_status fp8rl_gemm_dgrad(const uint8_t* qdy, const float* sdy, const uint8_t* qwT,
+                              const float* sw, uint16_t* dx, int64_t M, int64_t N, int64_t K,
+                              void* ws, size_t ws_bytes, fp8rl_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    if (M < 0 || N < 0 || K <= 0) return FP8RL_ERR_INVALID_ARG;
+    if (K % 128 != 0 || N % 128 != 0) return FP8RL_ERR_SHAPE;
+    if (M == 0) return FP8RL_OK;
+    if (N == 0) return FP8RL_ERR_SHAPE;
+    if (!qdy || !sdy || !qwT || !sw || !dx) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(qdy) || !aligned16(sdy) || !aligned16(qwT) || !aligned16(sw) || !aligned16(dx))
+        return FP8RL_ERR_ALIGN;
+    int sms = 0;
+    fp8rl_status e = current_device(&sms);
+    if (e != FP8RL_OK) return e;
+    TiledArgs t;
+    t.A = qdy; t.sa = sdy; t.sa_kb = M;
+    t.B = qwT; t.sb = sw; t.sb_kb = K / 128; t.sb_r = 1; t.b_mode = SCALE_BLOCK;
+    t.c = dx; t.ldc = K;
+    t.R1 = M; t.R2 = K; t.Kr = N;
+    return run_tiled(t, 0, sms, stream);
+}
+
+fp8rl_status fp8rl_gemm_wgrad(const uint8_t* qdyT, const float* sdyT, const uint8_t* qxT,
+                              const float* sxT, uint16_t* dw, int64_t M, int64_t N, int64_t K,
+                              void* ws, size_t ws_bytes, fp8rl_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    if (M < 0 || N < 0 || K <= 0) return FP8RL_ERR_INVALID_ARG;
+    if (K % 128 != 0 || N % 128 != 0 || M % 128 != 0) return FP8RL_ERR_SHAPE;
+    if (N == 0) return FP8RL_OK;
+    if (!qdyT || !sdyT || !qxT || !sxT || !dw) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(qdyT) || !aligned16(sdyT) || !aligned16(qxT) || !aligned16(sxT) || !aligned16(dw))
+        return FP8RL_ERR_ALIGN;
+    int sms = 0;
+    fp8rl_status e = current_device(&sms);
+    if (e != FP8RL_OK) return e;
+    if (M == 0) return cuda_status(cudaMemsetAsync(dw, 0, (size_t)N * K * 2, stream));
+    TiledArgs t;
+    t.A = qdyT; t.sa = sdyT; t.sa_kb = N;
+    t.B = qxT; t.sb = sxT; t.sb_kb = K; t.sb_r = 0; t.b_mode = SCALE_ROW;
+    t.c = dw; t.ldc = K;
+    t.R1 = N; t.R2 = K; t.Kr = M;
+    return run_tiled(t, 0, sms, stream);
+}
+
+// ---------------------------------------------------------------- diagnostics
+
+fp8rl_status fp8rl_debug_e4m3_encode(const float* in, uint8_t* out, int64_t n,
+                                     fp8rl_stream_t stream) {
+    if (n < 0) return FP8RL_ERR_INVALID_ARG;
+    if (n == 0) return FP8RL_OK;
+    if (!in || !out) return FP8RL_ERR_INVALID_ARG;
+    fp8rl_status e = current_device(nullptr);
+    if (e != FP8RL_OK) return e;
+    return cuda_status(launch_debug_e4m3(in, out, n, stream));
+}
+
+fp8rl_status fp8rl_debug_wait_timeout(uint64_t timeout_ns, fp8rl_stream_t stream) {
+    fp8rl_status e = current_device(nullptr);
+    if (e != FP8RL_OK) return e;
+    return cuda_status(launch_debug_wait_timeout(timeout_ns, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,52 @@
+// gemm.h -- parameters and launchers of the block-scaled GEMM kernels (internal).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp8rl {
+
+// How an operand's per-K-block scale is indexed.
+enum ScaleMode : int {
+    SCALE_ROW = 0,    // one scale per row of the operand: s[kb*s_kb + row]
+    SCALE_BLOCK = 1   // one scale per 128-row block:      s[(row/128)*s_r + kb*s_kb]
+};
+
+struct GemmParams {
+    int64_t R1, R2, Kr;      // C is R1 x R2; reduction length Kr (multiple of 128)
+    const float* sa;         // scales of A (rows r1)
+    int64_t sa_kb, sa_r;
+    const float* sb;         // scales of B (rows r2)
+    int64_t sb_kb, sb_r;
+    uint16_t* c;             // tiled: c[r1*ldc + r2];  split-K form: c[r2*ldc + r1]
+    int64_t ldc;
+    float* ws;               // split-K partials [tiles][splits][BN][128]
+    unsigned int* counters;  // split-K arrival counters [tiles], zero between calls
+    int splits;              // 0: tiled form; >= 1: decode (split-K) form
+    int m_tiles, n_tiles, nkb;
+    int num_items;
+    uint64_t timeout_ns;
+};
+
+cudaError_t launch_gemm_tiled(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                              int b_mode, int grid, cudaStream_t st);
+cudaError_t launch_gemm_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                               int bn, int grid, cudaStream_t st);
+cudaError_t launch_debug_wait_timeout(uint64_t timeout_ns, cudaStream_t st);
+
+// quantize.cu
+cudaError_t launch_quant_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                               float* s, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_dual(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                              float* s, uint8_t* qT, float* sT, cudaStream_t st);
+cudaError_t launch_silu_mul_quant(const uint16_t* gu, int64_t M, int64_t I, uint8_t* q, float* s,
+                                  uint8_t* qT, float* sT, cudaStream_t st);
+cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M,
+                                 int64_t K, uint8_t* q, float* s, uint8_t* qT, float* sT,
+                                 float* rstd, cudaStream_t st);
+cudaError_t launch_quant_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
+                                 float* s, uint8_t* qT, cudaStream_t st);
+cudaError_t launch_debug_e4m3(const float* in, uint8_t* out, int64_t n, cudaStream_t st);
+
+}  // namespace fp8rl

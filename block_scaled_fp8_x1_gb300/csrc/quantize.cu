@@ -1,0 +1,501 @@
+// quantize.cu -- BF16 -> E4M3 quantizers (1x128, 128x1 transposed, 128x128 blocks) and
+// the fused RMSNorm / SiLU-mul producers that feed them.
+//
+// "Technical summary: Jet-RL", section "Quantization Scheme": activations 1x128 per group,
+// weights 128x128 per block, WGrad operands additionally 128x1; activations saved for the
+// backward pass are FP8 and produced by the preceding fused operator.  Section
+// "Implementation": quantization, transposition and fused activation / RMSNorm kernels.
+//
+// All quantizers are HBM-bound.  The panel kernels read a 128-row x 128-column BF16
+// sub-tile once and emit both the 1x128 (row-group) codes and the transposed 128x1
+// (column-group) codes from registers.  Thread layout in a 256-thread CTA: warp w, lane l
+// owns rows 16w + 8*(l/16) + [0,8) and columns 8*(l%16) + [0,8) of the sub-tile, so each
+// warp-wide load reads two full 256-byte rows, a row group is reduced over 16 lanes and a
+// column group over the two half-warps and the 8 warps.
+#include <cooperative_groups.h>
+
+#include <algorithm>
+
+#include "gemm.h"
+#include "quant_common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace fp8rl {
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void stg_v2(void* p, uint32_t a, uint32_t b) {
+    asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
+// ------------------------------------------------------------------------------------
+// 1x128 quantization of rows, any M.  16 threads per group (8 BF16 each), groups ordered
+// block-major (g = kb*M + m) so that the scale stores of neighbouring groups coalesce.
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_quant_1x128(const uint16_t* __restrict__ x, int64_t M,
+                                                     int64_t K, int64_t ldx,
+                                                     uint8_t* __restrict__ q,
+                                                     float* __restrict__ s) {
+    const int sub = threadIdx.x & 15;
+    const int half = (threadIdx.x >> 4) & 1;
+    const int warp = threadIdx.x >> 5;
+    const int64_t ngroups = M * (K / 128);
+    const int64_t step = (int64_t)gridDim.x * 16;
+    // warp-uniform loop: both half-warps always execute the shuffles together
+    for (int64_t base = (int64_t)blockIdx.x * 16 + warp * 2; base < ngroups; base += step) {
+        const int64_t g = base + half;
+        const bool valid = g < ngroups;
+        const int64_t kb = valid ? g / M : 0;
+        const int64_t m = valid ? g - kb * M : 0;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (valid) v = ldg_nc_v4(x + m * ldx + kb * 128 + sub * 8);
+        uint32_t mx = absmax2(absmax2(absmax2(absmax2(0u, v.x), v.y), v.z), v.w);
+        mx = max(mx & 0xFFFFu, mx >> 16);
+        #pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const GroupScale gs = make_scale(bf16_bits_amax_to_f32(mx));
+        const uint32_t c0 = encode_pair(bf16_lo(v.x), bf16_hi(v.x), gs);
+        const uint32_t c1 = encode_pair(bf16_lo(v.y), bf16_hi(v.y), gs);
+        const uint32_t c2 = encode_pair(bf16_lo(v.z), bf16_hi(v.z), gs);
+        const uint32_t c3 = encode_pair(bf16_lo(v.w), bf16_hi(v.w), gs);
+        if (valid) {
+            stg_v2(q + m * K + kb * 128 + sub * 8, c0 | (c1 << 16), c2 | (c3 << 16));
+            if (sub == 0) s[kb * M + m] = gs.s;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// Panel kernel: 128-row panels, 128-column sub-tiles, optional fused producer.
+// ------------------------------------------------------------------------------------
+enum Prologue : int { PRO_COPY = 0, PRO_SILU = 1, PRO_RMSNORM = 2 };
+
+struct PanelArgs {
+    const uint16_t* x;      // COPY / RMSNORM: x[M][ldx];  SILU: gu[M][ldx], ldx = 2*K
+    int64_t ldx;
+    const uint16_t* gamma;  // RMSNORM: gamma[K]
+    float eps;
+    float* rstd_out;        // RMSNORM: rstd[M] (nullable)
+    int64_t M, K;           // K = number of quantized columns (I for SiLU-mul)
+    uint8_t* q;             // 1x128 codes q[M][K]
+    float* s;               // scales s[K/128][M]
+    uint8_t* qT;            // 128x1 codes, transposed: qT[K][M]
+    float* sT;              // scales sT[M/128][K]
+    int tiles_per_cta;      // 128-column sub-tiles handled by one CTA
+};
+
+// Accurate sum of squares: binary32 pairs (hi, lo) updated with the exact two-sum, so
+// that a row's total is known to about 2^-44 relative before it is rounded to binary32.
+struct F2 {
+    float hi, lo;
+};
+__device__ __forceinline__ F2 two_sum_acc(F2 a, float v) {
+    const float s = __fadd_rn(a.hi, v);
+    const float bp = __fsub_rn(s, a.hi);
+    const float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bp)), __fsub_rn(v, bp));
+    return F2{s, __fadd_rn(a.lo, e)};
+}
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+    F2 r = two_sum_acc(F2{a.hi, __fadd_rn(a.lo, b.lo)}, b.hi);
+    // renormalise so that |lo| stays below half an ulp of hi
+    const float s = __fadd_rn(r.hi, r.lo);
+    const float e = __fsub_rn(r.lo, __fsub_rn(s, r.hi));
+    return F2{s, e};
+}
+
+template <int PRO>
+__device__ __forceinline__ void load_rows(const PanelArgs& a, int64_t m0, int R0, int64_t k0,
+                                          int C0, const float* s_rstd, uint32_t (&w)[8][4]) {
+    float gam[8];
+    if (PRO == PRO_RMSNORM) {
+        const uint4 gv = ldg_nc_v4(a.gamma + k0 + C0);
+        gam[0] = bf16_lo(gv.x); gam[1] = bf16_hi(gv.x);
+        gam[2] = bf16_lo(gv.y); gam[3] = bf16_hi(gv.y);
+        gam[4] = bf16_lo(gv.z); gam[5] = bf16_hi(gv.z);
+        gam[6] = bf16_lo(gv.w); gam[7] = bf16_hi(gv.w);
+    }
+    uint4 v[8], u[8];
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t m = m0 + R0 + i;
+        v[i] = make_uint4(0, 0, 0, 0);
+        u[i] = make_uint4(0, 0, 0, 0);
+        if (m < a.M) {
+            v[i] = ldg_nc_v4(a.x + m * a.ldx + k0 + C0);
+            if (PRO == PRO_SILU) u[i] = ldg_nc_v4(a.x + m * a.ldx + a.K + k0 + C0);
+        }
+    }
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t xv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        const uint32_t uv[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+        if (PRO == PRO_COPY) {
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) w[i][j] = xv[j];
+        } else if (PRO == PRO_RMSNORM) {
+            const float r = s_rstd[R0 + i];
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float y0 = __fmul_rn(__fmul_rn(bf16_lo(xv[j]), r), gam[2 * j]);
+                const float y1 = __fmul_rn(__fmul_rn(bf16_hi(xv[j]), r), gam[2 * j + 1]);
+                w[i][j] = pack_bf16x2(y0, y1);
+            }
+        } else {  // SILU: h = bf16(silu(g) * u), silu(g) = g / (1 + exp(-g))
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float g0 = bf16_lo(xv[j]), g1 = bf16_hi(xv[j]);
+                const float u0 = bf16_lo(uv[j]), u1 = bf16_hi(uv[j]);
+                const float h0 = __fmul_rn(__fdividef(g0, 1.0f + __expf(-g0)), u0);
+                const float h1 = __fmul_rn(__fdividef(g1, 1.0f + __expf(-g1)), u1);
+                w[i][j] = pack_bf16x2(h0, h1);
+            }
+        }
+    }
+}
+
+template <int PRO, bool ROW_OUT, bool COL_OUT>
+__global__ void __launch_bounds__(256) k_quant_panel(const PanelArgs a) {
+    __shared__ __align__(16) uint32_t s_rowmax[64];     // 128 row maxima (BF16 bits)
+    __shared__ __align__(16) uint32_t s_colmax[8][64];  // per-warp column maxima
+    __shared__ __align__(16) float s_row_s[128], s_row_r[128];
+    __shared__ __align__(16) float s_col_s[128], s_col_r[128];
+    __shared__ __align__(16) float s_rstd[128];
+    __shared__ __align__(16) F2 s_part[128];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int half = lane >> 4, cl = lane & 15;
+    const int R0 = 16 * warp + 8 * half, C0 = 8 * cl;
+    const int64_t panel = blockIdx.y;
+    const int64_t m0 = panel * 128;
+    const int64_t ntiles = a.K / 128;
+    const int64_t t_begin = (int64_t)blockIdx.x * a.tiles_per_cta;
+    const int64_t t_end = (t_begin + a.tiles_per_cta < ntiles) ? t_begin + a.tiles_per_cta : ntiles;
+
+    if (PRO == PRO_RMSNORM) {
+        // Pass 1: this CTA's share of every row's sum of squares.
+        F2 acc[8];
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = F2{0.0f, 0.0f};
+        for (int64_t t = t_begin; t < t_end; ++t) {
+            uint4 v[8];
+            #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int64_t m = m0 + R0 + i;
+                v[i] = (m < a.M) ? ldg_nc_v4(a.x + m * a.ldx + t * 128 + C0) : make_uint4(0, 0, 0, 0);
+            }
+            #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t xv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float x0 = bf16_lo(xv[j]), x1 = bf16_hi(xv[j]);
+                    acc[i] = two_sum_acc(acc[i], __fmul_rn(x0, x0));
+                    acc[i] = two_sum_acc(acc[i], __fmul_rn(x1, x1));
+                }
+            }
+        }
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            #pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) {
+                F2 o;
+                o.hi = __shfl_xor_sync(0xffffffffu, acc[i].hi, off);
+                o.lo = __shfl_xor_sync(0xffffffffu, acc[i].lo, off);
+                acc[i] = f2_add(acc[i], o);
+            }
+        }
+        if (cl == 0) {
+            #pragma unroll
+            for (int i = 0; i < 8; ++i) s_part[R0 + i] = acc[i];
+        }
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        if (tid < 128) {
+            const unsigned nranks = cluster.num_blocks();
+            F2 tot = F2{0.0f, 0.0f};
+            for (unsigned rk = 0; rk < nranks; ++rk) {
+                const F2* peer = cluster.map_shared_rank(s_part, rk);
+                tot = f2_add(tot, peer[tid]);
+            }
+            const double sum = (double)tot.hi + (double)tot.lo;
+            const float ms = __double2float_rn(sum / (double)a.K);
+            const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
+            s_rstd[tid] = rstd;
+            const int64_t m = m0 + tid;
+            if (a.rstd_out && cluster.block_rank() == 0 && m < a.M) a.rstd_out[m] = rstd;
+        }
+        __syncthreads();
+    }
+
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        const int64_t k0 = t * 128;
+        uint32_t w[8][4];
+        load_rows<PRO>(a, m0, R0, k0, C0, s_rstd, w);
+
+        if (ROW_OUT) {
+            uint32_t pm[4];
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t e = 0, o = 0;
+                #pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    e = absmax2(e, w[2 * j][c]);
+                    o = absmax2(o, w[2 * j + 1][c]);
+                }
+                pm[j] = max(e & 0xFFFFu, e >> 16) | (max(o & 0xFFFFu, o >> 16) << 16);
+            }
+            #pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) {
+                #pragma unroll
+                for (int j = 0; j < 4; ++j) pm[j] = __vmaxu2(pm[j], __shfl_xor_sync(0xffffffffu, pm[j], off));
+            }
+            if (cl == 0) *reinterpret_cast<uint4*>(&s_rowmax[R0 / 2]) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
+        }
+        if (COL_OUT) {
+            uint32_t cm[4];
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t c = 0;
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) c = absmax2(c, w[i][j]);
+                cm[j] = __vmaxu2(c, __shfl_xor_sync(0xffffffffu, c, 16));
+            }
+            if (half == 0) *reinterpret_cast<uint4*>(&s_colmax[warp][cl * 4]) = make_uint4(cm[0], cm[1], cm[2], cm[3]);
+        }
+        __syncthreads();
+        if (ROW_OUT && tid < 128) {
+            const uint32_t mx = reinterpret_cast<const uint16_t*>(s_rowmax)[tid];
+            const GroupScale g = make_scale(bf16_bits_amax_to_f32(mx));
+            s_row_s[tid] = g.s;
+            s_row_r[tid] = g.r;
+            if (m0 + tid < a.M) a.s[t * a.M + m0 + tid] = g.s;
+        }
+        if (COL_OUT && tid >= 128) {
+            const int c = tid - 128;
+            uint32_t mx = 0;
+            #pragma unroll
+            for (int ww = 0; ww < 8; ++ww) mx = max(mx, (uint32_t)reinterpret_cast<const uint16_t*>(s_colmax[ww])[c]);
+            const GroupScale g = make_scale(bf16_bits_amax_to_f32(mx));
+            s_col_s[c] = g.s;
+            s_col_r[c] = g.r;
+            a.sT[panel * a.K + k0 + c] = g.s;
+        }
+        __syncthreads();
+        if (ROW_OUT) {
+            #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                GroupScale g;
+                g.s = s_row_s[R0 + i];
+                g.r = s_row_r[R0 + i];
+                g.zero = (g.s == 0.0f);
+                g.slow = (g.s < 1.17549435e-38f);
+                uint32_t c[4];
+                #pragma unroll
+                for (int j = 0; j < 4; ++j) c[j] = encode_pair(bf16_lo(w[i][j]), bf16_hi(w[i][j]), g);
+                const int64_t m = m0 + R0 + i;
+                if (m < a.M) stg_v2(a.q + m * a.K + k0 + C0, c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+            }
+        }
+        if (COL_OUT) {
+            #pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                GroupScale g;
+                g.s = s_col_s[C0 + j];
+                g.r = s_col_r[C0 + j];
+                g.zero = (g.s == 0.0f);
+                g.slow = (g.s < 1.17549435e-38f);
+                uint32_t c[4];
+                #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t wa = w[2 * i][j >> 1], wb = w[2 * i + 1][j >> 1];
+                    const float xa = (j & 1) ? bf16_hi(wa) : bf16_lo(wa);
+                    const float xb = (j & 1) ? bf16_hi(wb) : bf16_lo(wb);
+                    c[i] = encode_pair(xa, xb, g);
+                }
+                stg_v2(a.qT + (k0 + C0 + j) * a.M + m0 + R0, c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+            }
+        }
+    }
+    if (PRO == PRO_RMSNORM) {
+        // Keep this CTA's partial sums alive until every peer has read them.
+        cg::this_cluster().sync();
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// 128x128 weight blocks (+ optional transposed copy with the same scale).
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_quant_128x128(const uint16_t* __restrict__ w_in,
+                                                       int64_t N, int64_t K, int64_t ldw,
+                                                       uint8_t* __restrict__ q,
+                                                       float* __restrict__ s,
+                                                       uint8_t* __restrict__ qT) {
+    __shared__ uint32_t s_wmax[8];
+    __shared__ float s_scale[2];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int half = lane >> 4, cl = lane & 15;
+    const int R0 = 16 * warp + 8 * half, C0 = 8 * cl;
+    const int64_t bk = blockIdx.x, bn = blockIdx.y;
+    const int64_t n0 = bn * 128, k0 = bk * 128;
+
+    uint32_t w[8][4];
+    uint4 v[8];
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = ldg_nc_v4(w_in + (n0 + R0 + i) * ldw + k0 + C0);
+    uint32_t mx = 0;
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        w[i][0] = v[i].x; w[i][1] = v[i].y; w[i][2] = v[i].z; w[i][3] = v[i].w;
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) mx = absmax2(mx, w[i][j]);
+    }
+    mx = max(mx & 0xFFFFu, mx >> 16);
+    #pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) s_wmax[warp] = mx;
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t m = 0;
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) m = max(m, s_wmax[i]);
+        const GroupScale g = make_scale(bf16_bits_amax_to_f32(m));
+        s_scale[0] = g.s;
+        s_scale[1] = g.r;
+        s[bn * (K / 128) + bk] = g.s;
+    }
+    __syncthreads();
+    GroupScale g;
+    g.s = s_scale[0];
+    g.r = s_scale[1];
+    g.zero = (g.s == 0.0f);
+    g.slow = (g.s < 1.17549435e-38f);
+    // codes of the 8x8 block, row-major and (if wanted) transposed
+    uint32_t rc[8][2];
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t c[4];
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) c[j] = encode_pair(bf16_lo(w[i][j]), bf16_hi(w[i][j]), g);
+        rc[i][0] = c[0] | (c[1] << 16);
+        rc[i][1] = c[2] | (c[3] << 16);
+        stg_v2(q + (n0 + R0 + i) * K + k0 + C0, rc[i][0], rc[i][1]);
+    }
+    if (qT) {
+        // transpose the 8x8 byte block held in rc: byte (i, j) = row i, column j
+        #pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t lo = 0, hi = 0;
+            #pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                lo |= ((rc[i][j >> 2] >> (8 * (j & 3))) & 0xFFu) << (8 * i);
+                hi |= ((rc[i + 4][j >> 2] >> (8 * (j & 3))) & 0xFFu) << (8 * i);
+            }
+            stg_v2(qT + (k0 + C0 + j) * N + n0 + R0, lo, hi);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// Diagnostic: the raw device encoder over an array.
+// ------------------------------------------------------------------------------------
+__global__ void k_debug_e4m3(const float* __restrict__ in, uint8_t* __restrict__ out, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = (uint8_t)(e4m3x2(in[i], 0.0f) & 0xFFu);
+}
+
+// ------------------------------------------------------------------------------------
+// Host-side launchers (argument checks are done by the C ABI layer).
+// ------------------------------------------------------------------------------------
+cudaError_t launch_quant_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                               float* s, int num_sms, cudaStream_t st) {
+    const int64_t ngroups = M * (K / 128);
+    const int64_t blocks_needed = (ngroups + 15) / 16;
+    const int64_t blocks = std::min<int64_t>(blocks_needed, (int64_t)num_sms * 16);
+    k_quant_1x128<<<(unsigned)blocks, 256, 0, st>>>(x, M, K, ldx, q, s);
+    return cudaGetLastError();
+}
+
+template <int PRO, bool ROW_OUT, bool COL_OUT>
+static cudaError_t launch_panel_t(const PanelArgs& a, int cluster, cudaStream_t st) {
+    const int64_t ntiles = a.K / 128;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((ntiles + a.tiles_per_cta - 1) / a.tiles_per_cta),
+                       (unsigned)((a.M + 127) / 128), 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    cfg.numAttrs = 0;
+    if (cluster > 0) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, k_quant_panel<PRO, ROW_OUT, COL_OUT>, a);
+}
+
+// quantize 1x128 with the transposed 128x1 output (dual), or 128x1 alone
+cudaError_t launch_quant_dual(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                              float* s, uint8_t* qT, float* sT, cudaStream_t st) {
+    PanelArgs a = {};
+    a.x = x; a.ldx = ldx; a.M = M; a.K = K; a.q = q; a.s = s; a.qT = qT; a.sT = sT;
+    a.tiles_per_cta = 1;
+    if (q) return launch_panel_t<PRO_COPY, true, true>(a, 0, st);
+    return launch_panel_t<PRO_COPY, false, true>(a, 0, st);
+}
+
+cudaError_t launch_silu_mul_quant(const uint16_t* gu, int64_t M, int64_t I, uint8_t* q, float* s,
+                                  uint8_t* qT, float* sT, cudaStream_t st) {
+    PanelArgs a = {};
+    a.x = gu; a.ldx = 2 * I; a.M = M; a.K = I; a.q = q; a.s = s; a.qT = qT; a.sT = sT;
+    a.tiles_per_cta = 1;
+    if (qT) return launch_panel_t<PRO_SILU, true, true>(a, 0, st);
+    return launch_panel_t<PRO_SILU, true, false>(a, 0, st);
+}
+
+// Number of CTAs that split one 128-row panel of an RMSNorm along K: the largest divisor
+// of K/128 that is at most 8 (a portable cluster size).
+int rmsnorm_cluster_size(int64_t K) {
+    const int64_t nt = K / 128;
+    for (int c = 8; c >= 1; --c)
+        if (nt % c == 0) return c;
+    return 1;
+}
+
+cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M,
+                                 int64_t K, uint8_t* q, float* s, uint8_t* qT, float* sT,
+                                 float* rstd, cudaStream_t st) {
+    PanelArgs a = {};
+    a.x = x; a.ldx = K; a.gamma = gamma; a.eps = eps; a.rstd_out = rstd;
+    a.M = M; a.K = K; a.q = q; a.s = s; a.qT = qT; a.sT = sT;
+    const int c = rmsnorm_cluster_size(K);
+    a.tiles_per_cta = (int)((K / 128) / c);
+    if (qT) return launch_panel_t<PRO_RMSNORM, true, true>(a, c, st);
+    return launch_panel_t<PRO_RMSNORM, true, false>(a, c, st);
+}
+
+cudaError_t launch_quant_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
+                                 float* s, uint8_t* qT, cudaStream_t st) {
+    dim3 grid((unsigned)(K / 128), (unsigned)(N / 128), 1);
+    k_quant_128x128<<<grid, 256, 0, st>>>(w, N, K, ldw, q, s, qT);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_debug_e4m3(const float* in, uint8_t* out, int64_t n, cudaStream_t st) {
+    const int64_t blocks = std::max<int64_t>(std::min<int64_t>((n + 255) / 256, 4096), 1);
+    k_debug_e4m3<<<(unsigned)blocks, 256, 0, st>>>(in, out, n);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8rl

@@ -1,0 +1,247 @@
+"""Torch-facing binding of libfp8rl: argument marshalling only.
+
+Every function here hands raw device pointers, sizes and the current CUDA stream to the C
+ABI (same names without the ``fp8rl_`` prefix); all arithmetic runs in the CUDA kernels.
+PyTorch supplies the device memory (outputs are allocated with ``torch.empty``) and the
+stream.  BF16 tensors travel as their bit patterns, E4M3 codes as ``torch.uint8`` (a
+``torch.float8_e4m3fn`` view is available through ``as_e4m3``), scales as ``float32``.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from typing import Optional
+
+import torch
+
+from . import _abi
+from ._abi import GemmOpts, check, lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _require(t: torch.Tensor, dtype: torch.dtype, name: str, device=None) -> None:
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+
+
+def _contig(t: torch.Tensor, name: str) -> None:
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+
+
+def as_e4m3(q: torch.Tensor) -> torch.Tensor:
+    """View uint8 codes as torch.float8_e4m3fn (no copy)."""
+    return q.view(torch.float8_e4m3fn)
+
+
+# ------------------------------------------------------------------ status / diagnostics
+
+def version() -> int:
+    return lib().fp8rl_version()
+
+
+def init(device: int = 0) -> None:
+    check(lib().fp8rl_init(int(device)), "fp8rl_init")
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    lib().fp8rl_set_wait_timeout_ns(int(ns))
+
+
+def check_status(device: Optional[torch.device] = None) -> int:
+    """Wait for the current stream and return (and clear) the device status word."""
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    return int(lib().fp8rl_check_status(_stream(device)))
+
+
+def debug_e4m3_encode(v: torch.Tensor) -> torch.Tensor:
+    _require(v, torch.float32, "v")
+    _contig(v, "v")
+    out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+    check(lib().fp8rl_debug_e4m3_encode(_ptr(v), _ptr(out), v.numel(), _stream(v.device)),
+          "fp8rl_debug_e4m3_encode")
+    return out
+
+
+def debug_wait_timeout(timeout_ns: int, device: Optional[torch.device] = None) -> None:
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    check(lib().fp8rl_debug_wait_timeout(int(timeout_ns), _stream(device)),
+          "fp8rl_debug_wait_timeout")
+
+
+# ------------------------------------------------------------------ quantizers
+
+def quantize_1x128(x: torch.Tensor, dual: bool = False):
+    """x bf16 [M,K] -> (q u8 [M,K], s f32 [K/128,M]) and, if dual, (qT [K,M], sT [M/128,K])."""
+    _require(x, torch.bfloat16, "x")
+    M, K = x.shape
+    if x.stride(1) != 1:
+        raise ValueError("x: rows must be contiguous")
+    dev = x.device
+    q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    s = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+    qT = sT = None
+    if dual:
+        qT = torch.empty((K, M), dtype=torch.uint8, device=dev)
+        sT = torch.empty((M // 128, K), dtype=torch.float32, device=dev)
+    check(lib().fp8rl_quantize_1x128(_ptr(x), M, K, x.stride(0), _ptr(q), _ptr(s), _ptr(qT),
+                                     _ptr(sT), _stream(dev)), "fp8rl_quantize_1x128")
+    return (q, s, qT, sT) if dual else (q, s)
+
+
+def quantize_128x1(x: torch.Tensor):
+    """x bf16 [M,K] -> (qT u8 [K,M], sT f32 [M/128,K])."""
+    _require(x, torch.bfloat16, "x")
+    M, K = x.shape
+    if x.stride(1) != 1:
+        raise ValueError("x: rows must be contiguous")
+    dev = x.device
+    qT = torch.empty((K, M), dtype=torch.uint8, device=dev)
+    sT = torch.empty((M // 128, K), dtype=torch.float32, device=dev)
+    check(lib().fp8rl_quantize_128x1(_ptr(x), M, K, x.stride(0), _ptr(qT), _ptr(sT),
+                                     _stream(dev)), "fp8rl_quantize_128x1")
+    return qT, sT
+
+
+def quantize_128x128(w: torch.Tensor, transpose: bool = True):
+    """w bf16 [N,K] -> (q u8 [N,K], s f32 [N/128,K/128], qT u8 [K,N] or None)."""
+    _require(w, torch.bfloat16, "w")
+    N, K = w.shape
+    if w.stride(1) != 1:
+        raise ValueError("w: rows must be contiguous")
+    dev = w.device
+    q = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    s = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
+    qT = torch.empty((K, N), dtype=torch.uint8, device=dev) if transpose else None
+    check(lib().fp8rl_quantize_128x128(_ptr(w), N, K, w.stride(0), _ptr(q), _ptr(s), _ptr(qT),
+                                       _stream(dev)), "fp8rl_quantize_128x128")
+    return q, s, qT
+
+
+def rmsnorm_quant(x: torch.Tensor, gamma: torch.Tensor, eps: float, dual: bool = True):
+    """Fused RMSNorm -> quantize: (q, s, qT, sT, rstd); qT/sT are None unless dual."""
+    _require(x, torch.bfloat16, "x")
+    _require(gamma, torch.bfloat16, "gamma", x.device)
+    _contig(x, "x")
+    _contig(gamma, "gamma")
+    M, K = x.shape
+    dev = x.device
+    q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    s = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+    rstd = torch.empty((M,), dtype=torch.float32, device=dev)
+    qT = sT = None
+    if dual:
+        qT = torch.empty((K, M), dtype=torch.uint8, device=dev)
+        sT = torch.empty((M // 128, K), dtype=torch.float32, device=dev)
+    check(lib().fp8rl_rmsnorm_quant(_ptr(x), _ptr(gamma), ctypes.c_float(eps), M, K, _ptr(q),
+                                    _ptr(s), _ptr(qT), _ptr(sT), _ptr(rstd), _stream(dev)),
+          "fp8rl_rmsnorm_quant")
+    return q, s, qT, sT, rstd
+
+
+def silu_mul_quant(gu: torch.Tensor, dual: bool = True):
+    """gu bf16 [M, 2I] -> (q [M,I], s [I/128,M], qT [I,M] or None, sT [M/128,I] or None)."""
+    _require(gu, torch.bfloat16, "gu")
+    _contig(gu, "gu")
+    M, I2 = gu.shape
+    I = I2 // 2
+    dev = gu.device
+    q = torch.empty((M, I), dtype=torch.uint8, device=dev)
+    s = torch.empty((I // 128, M), dtype=torch.float32, device=dev)
+    qT = sT = None
+    if dual:
+        qT = torch.empty((I, M), dtype=torch.uint8, device=dev)
+        sT = torch.empty((M // 128, I), dtype=torch.float32, device=dev)
+    check(lib().fp8rl_silu_mul_quant(_ptr(gu), M, I, _ptr(q), _ptr(s), _ptr(qT), _ptr(sT),
+                                     _stream(dev)), "fp8rl_silu_mul_quant")
+    return q, s, qT, sT
+
+
+# ------------------------------------------------------------------ GEMMs
+
+_ws_lock = threading.Lock()
+_ws_cache: dict = {}
+
+
+def gemm_workspace_bytes(op: int, M: int, N: int, K: int) -> int:
+    return int(lib().fp8rl_gemm_workspace_bytes(int(op), M, N, K))
+
+
+def workspace(nbytes: int, device: torch.device) -> torch.Tensor:
+    """A zero-initialised byte buffer of at least nbytes, cached per device.
+
+    The split-K kernel leaves its arrival counters at zero after every call, so one
+    buffer serves every call issued in stream order on that device."""
+    key = (device.type, device.index)
+    with _ws_lock:
+        buf = _ws_cache.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+            _ws_cache[key] = buf
+        return buf
+
+
+def _check_gemm_inputs(qa, sa, qb, sb):
+    _require(qa, torch.uint8, "codes A")
+    _require(qb, torch.uint8, "codes B", qa.device)
+    _require(sa, torch.float32, "scales A", qa.device)
+    _require(sb, torch.float32, "scales B", qa.device)
+    for t, n in ((qa, "codes A"), (qb, "codes B"), (sa, "scales A"), (sb, "scales B")):
+        _contig(t, n)
+
+
+def gemm_fwd(qx, sx, qw, sw, out=None, variant: int = _abi.FP8RL_VARIANT_AUTO, splits: int = 0,
+             grid: int = 0, ws: Optional[torch.Tensor] = None):
+    """Y = X W^T: qx [M,K], sx [K/128,M], qw [N,K], sw [N/128,K/128] -> y bf16 [M,N]."""
+    _check_gemm_inputs(qx, sx, qw, sw)
+    M, K = qx.shape
+    N = qw.shape[0]
+    dev = qx.device
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    decode = variant == _abi.FP8RL_VARIANT_SPLITK or (
+        variant == _abi.FP8RL_VARIANT_AUTO and M <= 256)
+    opts = GemmOpts(int(variant), int(splits), int(grid))
+    wsb = None
+    if decode:
+        need = int(lib().fp8rl_gemm_workspace_bytes_ex(_abi.FP8RL_OP_FWD, M, N, K,
+                                                       ctypes.byref(opts)))
+        wsb = ws if ws is not None else workspace(need, dev)
+    check(lib().fp8rl_gemm_fwd_ex(_ptr(qx), _ptr(sx), _ptr(qw), _ptr(sw), _ptr(y), M, N, K,
+                                  _ptr(wsb), wsb.numel() if wsb is not None else 0,
+                                  ctypes.byref(opts), _stream(dev)), "fp8rl_gemm_fwd_ex")
+    return y
+
+
+def gemm_dgrad(qdy, sdy, qwT, sw, out=None):
+    """dX = dY W: qdy [M,N], sdy [N/128,M], qwT [K,N], sw [N/128,K/128] -> dx bf16 [M,K]."""
+    _check_gemm_inputs(qdy, sdy, qwT, sw)
+    M, N = qdy.shape
+    K = qwT.shape[0]
+    dev = qdy.device
+    dx = out if out is not None else torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    check(lib().fp8rl_gemm_dgrad(_ptr(qdy), _ptr(sdy), _ptr(qwT), _ptr(sw), _ptr(dx), M, N, K,
+                                 None, 0, _stream(dev)), "fp8rl_gemm_dgrad")
+    return dx
+
+
+def gemm_wgrad(qdyT, sdyT, qxT, sxT, out=None):
+    """dW = dY^T X: qdyT [N,M], sdyT [M/128,N], qxT [K,M], sxT [M/128,K] -> dw bf16 [N,K]."""
+    _check_gemm_inputs(qdyT, sdyT, qxT, sxT)
+    N, M = qdyT.shape
+    K = qxT.shape[0]
+    dev = qdyT.device
+    dw = out if out is not None else torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    check(lib().fp8rl_gemm_wgrad(_ptr(qdyT), _ptr(sdyT), _ptr(qxT), _ptr(sxT), _ptr(dw), M, N,
+                                 K, None, 0, _stream(dev)), "fp8rl_gemm_wgrad")
+    return dw

@@ -1,0 +1,239 @@
+/*
+ * fp8rl.h -- C ABI of libfp8rl, the GB300 (sm_103a) unified-precision FP8 linear layer.
+ *
+ * The scheme is the one stated in "Technical summary: Jet-RL" (gist.science, paper
+ * 2601.14243), section "Quantization Scheme":
+ *   - activations are quantized per 1x128 group,
+ *   - weights are quantized per 128x128 block,
+ *   - activations saved for the backward pass are stored in FP8 by the preceding (fused)
+ *     operator, gradients passed between operators stay BF16,
+ *   - DGrad and WGrad run in FP8, WGrad with 1x128 and 128x1 operand quantization.
+ * Section "Core architecture" requires the inference (rollout) graph to be a sub-graph of
+ * the training forward graph with the same quantization granularity and precision: the
+ * same quantizers and GEMM numerics below serve both, including the small-M decode path.
+ * Section "Implementation" names fused activation (SiLU-mul) and RMSNorm operators that
+ * feed the quantizer; fp8rl_rmsnorm_quant and fp8rl_silu_mul_quant are those operators.
+ *
+ * Number formats and readings the pages leave open:
+ *   - FP8 is OCP E4M3 ("FN": bias 7, max 448, no infinities).
+ *   - A group's scale is s = fl32(amax / 448) in IEEE single precision; a group whose amax
+ *     is 0 has s = 0 and all codes 0x00.
+ *   - code = E4M3 round-to-nearest-even of fl32(x / s) (IEEE single division), saturated
+ *     to +-448.  Dequantized value = decode(code) * s.
+ *   - GEMMs multiply E4M3 codes exactly, accumulate each 128-long reduction block in FP32
+ *     on the tensor cores, promote it into an FP32 accumulator with the product of the two
+ *     operands' scales for that block, and round the result to BF16 (nearest even).
+ *
+ * Layouts (all row-major, element = one byte for codes, 4 bytes for scales, 2 bytes for
+ * BF16 which travels as uint16_t bit patterns):
+ *   1x128 codes of A[R,C]   : q[R][C]                 scales s[C/128][R]
+ *   128x1 codes of X[M,K]   : emitted TRANSPOSED, qT[K][M]   scales sT[M/128][K]
+ *                             (this is the 1x128 quantization of X^T along M)
+ *   128x128 codes of W[N,K] : q[N][K]                 scales s[N/128][K/128]
+ *                             optional transposed copy qT[K][N] uses the same scales.
+ *
+ * Shape rules: K % 128 == 0 always; N % 128 == 0 for weights and GEMM outputs; M % 128 == 0
+ * wherever M is grouped 128x1 (the transposed outputs and WGrad).  M may be any value >= 0
+ * elsewhere; M == 0 is a no-op that returns FP8RL_OK.  Other shapes return FP8RL_ERR_SHAPE.
+ *
+ * Memory and execution: the caller owns every buffer (device memory unless stated).  All
+ * device pointers must be 16-byte aligned and every leading dimension a multiple of 16
+ * bytes, else FP8RL_ERR_ALIGN.  Every call is asynchronous on the given stream; argument
+ * errors are returned synchronously and launch nothing.  Device-side errors (a bounded
+ * wait that ran out) are recorded in a per-device status word and returned by
+ * fp8rl_check_status.  Inputs must be finite; NaN or Inf inputs give unspecified codes.
+ * The library allocates no device memory of its own: split-K partial sums live in the
+ * caller's workspace (fp8rl_gemm_workspace_bytes).
+ *
+ * Threading: the entry points are stateless apart from the status word and a per-device
+ * cache of kernel attributes; they may be called from several host threads.  Each call
+ * runs on the CUDA device that is current in the calling thread.
+ */
+#ifndef FP8RL_H
+#define FP8RL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported from libfp8rl.so (the library is built with hidden visibility otherwise). */
+#if defined(__GNUC__)
+#define FP8RL_API __attribute__((visibility("default")))
+#else
+#define FP8RL_API
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* fp8rl_stream_t;
+
+typedef enum {
+    FP8RL_OK = 0,
+    FP8RL_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad enum */
+    FP8RL_ERR_SHAPE = 2,              /* a shape rule above is broken */
+    FP8RL_ERR_ALIGN = 3,              /* pointer or leading dimension not 16-byte aligned */
+    FP8RL_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
+    FP8RL_ERR_WORKSPACE = 5,          /* workspace null or smaller than required */
+    FP8RL_ERR_CUDA = 6,               /* a CUDA runtime/driver call failed */
+    FP8RL_ERR_DEVICE_TIMEOUT = 7,     /* a kernel's bounded wait ran out (device status) */
+    FP8RL_ERR_DEVICE_BOUNDS = 8       /* a kernel's own bounds check fired (device status) */
+} fp8rl_status;
+
+/* Library version, (major << 16) | minor. */
+FP8RL_API int fp8rl_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+FP8RL_API const char* fp8rl_status_string(fp8rl_status st);
+
+/* Checks that `device` is a compute-capability 10.3 GPU, makes it current in the calling
+ * thread and prepares the kernels for it (function attributes).  Optional: every entry
+ * point performs the same check for the current device on first use.  Returns
+ * FP8RL_ERR_UNSUPPORTED_DEVICE on any other device, FP8RL_ERR_CUDA if CUDA fails. */
+FP8RL_API fp8rl_status fp8rl_init(int device);
+
+/* Upper bound, in nanoseconds, of every spin-wait inside the GEMM kernels (mbarrier waits
+ * between the copy, tensor-core and epilogue warps).  When a wait runs out the kernel
+ * records FP8RL_ERR_DEVICE_TIMEOUT, drains its own copies and returns.  Default 2e9 ns.
+ * Applies to launches made after the call, on every device. */
+FP8RL_API void fp8rl_set_wait_timeout_ns(uint64_t ns);
+
+/* Waits for `stream`, then reads and clears the current device's status word.
+ * Returns FP8RL_OK or the first device-side error recorded since the last check. */
+FP8RL_API fp8rl_status fp8rl_check_status(fp8rl_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * Quantizers ("Quantization Scheme": activations 1x128, weights 128x128, WGrad operands
+ * 128x1; the transposed 128x1 output is the layout WGrad consumes).
+ * -------------------------------------------------------------------------------------- */
+
+/* Activation quantization, 1x128 groups along K.
+ *   x  : BF16 [M][ldx] (first K columns used), ldx >= K
+ *   q  : E4M3 [M][K];  s : float [K/128][M]
+ *   qT, sT (both NULL or both set; then M % 128 == 0): the 128x1 quantization of the same
+ *        x, transposed: qT [K][M], sT [M/128][K].  One read of x feeds both outputs. */
+FP8RL_API fp8rl_status fp8rl_quantize_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                                  uint8_t* q, float* s, uint8_t* qT, float* sT,
+                                  fp8rl_stream_t stream);
+
+/* 128x1 quantization along M (WGrad operand), transposed output.
+ *   x : BF16 [M][ldx], M % 128 == 0;  qT : E4M3 [K][M];  sT : float [M/128][K] */
+FP8RL_API fp8rl_status fp8rl_quantize_128x1(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                                  uint8_t* qT, float* sT, fp8rl_stream_t stream);
+
+/* Weight quantization, 128x128 blocks (re-run from the BF16 master weights after each
+ * optimizer step: "Core architecture", master weights stay BF16).
+ *   w : BF16 [N][ldw];  q : E4M3 [N][K];  s : float [N/128][K/128]
+ *   qT (nullable): E4M3 [K][N], the transposed copy DGrad reads; same scales. */
+FP8RL_API fp8rl_status fp8rl_quantize_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw,
+                                    uint8_t* q, float* s, uint8_t* qT,
+                                    fp8rl_stream_t stream);
+
+/* Fused RMSNorm -> quantize ("Implementation": fused RMSNorm kernel; "Quantization
+ * Scheme": the saved activation is FP8, produced by the preceding operator).
+ *   y[m,k] = bf16_rne( (x[m,k] * rstd[m]) * gamma[k] ),
+ *   rstd[m] = 1 / sqrt( fl32(sum_k x[m,k]^2 / K) + eps )   (IEEE single sqrt and divide)
+ * then y is quantized 1x128 (q [M][K], s [K/128][M]) and, if qT/sT are set, 128x1
+ * transposed (qT [K][M], sT [M/128][K]; needs M % 128 == 0).  y itself is not stored.
+ *   x : BF16 [M][K] (contiguous);  gamma : BF16 [K];  rstd (nullable): float [M] */
+FP8RL_API fp8rl_status fp8rl_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float eps,
+                                 int64_t M, int64_t K, uint8_t* q, float* s, uint8_t* qT,
+                                 float* sT, float* rstd, fp8rl_stream_t stream);
+
+/* Fused SiLU-mul -> quantize ("Implementation": fused activation kernel).
+ *   gu : BF16 [M][2*I], gate = columns [0, I), up = columns [I, 2I)
+ *   h[m,i] = bf16_rne( silu(g) * u ), silu(g) = g / (1 + exp(-g)) evaluated in FP32
+ * then h is quantized 1x128 (q [M][I], s [I/128][M]) and, if qT/sT are set, 128x1
+ * transposed (qT [I][M], sT [M/128][I]).  I % 128 == 0. */
+FP8RL_API fp8rl_status fp8rl_silu_mul_quant(const uint16_t* gu, int64_t M, int64_t I, uint8_t* q,
+                                  float* s, uint8_t* qT, float* sT, fp8rl_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * Block-scaled FP8 GEMMs ("Quantization Scheme": forward, DGrad and WGrad in FP8).
+ * Output element = bf16_rne( sum_kb sA(kb,row) * sB(kb,col) * sum_{k in kb} a*b ), with
+ * the inner block sum in FP32 on the tensor cores and the outer sum in FP32 registers.
+ * -------------------------------------------------------------------------------------- */
+
+/* Operation selector for fp8rl_gemm_workspace_bytes and fp8rl_gemm_opts. */
+typedef enum { FP8RL_OP_FWD = 0, FP8RL_OP_DGRAD = 1, FP8RL_OP_WGRAD = 2 } fp8rl_gemm_op;
+
+/* Forward Y = X W^T.
+ *   qx : E4M3 [M][K] (1x128), sx : float [K/128][M]
+ *   qw : E4M3 [N][K] (128x128), sw : float [N/128][K/128]
+ *   y  : BF16 [M][N]
+ * Small M (<= 256) takes the decode-shaped kernel (weights stream once through the SMs,
+ * reduction split across CTAs, partial sums reduced in a fixed order by the last CTA of
+ * each output tile); it needs fp8rl_gemm_workspace_bytes(FP8RL_OP_FWD, M, N, K) bytes of
+ * workspace.  The workspace must be zero-filled before its first use; every call that
+ * completes leaves its arrival counters at zero again, so one workspace serves calls
+ * issued in order on one stream (calls that overlap in time need separate workspaces;
+ * after a device error, zero it again).  Larger M needs no workspace (ws may be NULL). */
+FP8RL_API fp8rl_status fp8rl_gemm_fwd(const uint8_t* qx, const float* sx, const uint8_t* qw,
+                            const float* sw, uint16_t* y, int64_t M, int64_t N, int64_t K,
+                            void* ws, size_t ws_bytes, fp8rl_stream_t stream);
+
+/* DGrad dX = dY W.
+ *   qdy : E4M3 [M][N] (1x128 along N), sdy : float [N/128][M]
+ *   qwT : E4M3 [K][N], the transposed weight copy from fp8rl_quantize_128x128
+ *   sw  : float [N/128][K/128] (the weight's block scales)
+ *   dx  : BF16 [M][K]
+ * ws may be NULL (no workspace is used at present). */
+FP8RL_API fp8rl_status fp8rl_gemm_dgrad(const uint8_t* qdy, const float* sdy, const uint8_t* qwT,
+                              const float* sw, uint16_t* dx, int64_t M, int64_t N,
+                              int64_t K, void* ws, size_t ws_bytes, fp8rl_stream_t stream);
+
+/* WGrad dW = dY^T X, both operands quantized 128x1 along the token dimension M.
+ *   qdyT : E4M3 [N][M], sdyT : float [M/128][N]   (fp8rl_quantize_128x1 of dY)
+ *   qxT  : E4M3 [K][M], sxT  : float [M/128][K]   (128x1 of the saved activation)
+ *   dw   : BF16 [N][K];  M % 128 == 0. */
+FP8RL_API fp8rl_status fp8rl_gemm_wgrad(const uint8_t* qdyT, const float* sdyT, const uint8_t* qxT,
+                              const float* sxT, uint16_t* dw, int64_t M, int64_t N,
+                              int64_t K, void* ws, size_t ws_bytes, fp8rl_stream_t stream);
+
+/* Workspace bytes the given GEMM needs with the automatic kernel choice (0 if none). */
+FP8RL_API size_t fp8rl_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K);
+
+/* Explicit kernel choice, for tests and benchmarks. */
+typedef enum {
+    FP8RL_VARIANT_AUTO = 0,   /* what fp8rl_gemm_fwd picks */
+    FP8RL_VARIANT_TILED = 1,  /* persistent 128 x BN tiles over (M, N) */
+    FP8RL_VARIANT_SPLITK = 2  /* decode-shaped: weight rows as MMA M, tokens as MMA N,
+                                 reduction split over `splits` CTAs */
+} fp8rl_variant;
+
+typedef struct {
+    int variant;  /* fp8rl_variant */
+    int splits;   /* SPLITK: number of reduction slices (0 = choose); ignored otherwise */
+    int grid;     /* TILED: persistent CTAs (0 = one per SM); ignored otherwise */
+} fp8rl_gemm_opts;
+
+/* Workspace bytes fp8rl_gemm_fwd_ex needs with these options (opts may be NULL = AUTO). */
+FP8RL_API size_t fp8rl_gemm_workspace_bytes_ex(int op, int64_t M, int64_t N, int64_t K,
+                                     const fp8rl_gemm_opts* opts);
+
+/* fp8rl_gemm_fwd with an explicit variant; opts may be NULL (= AUTO). */
+FP8RL_API fp8rl_status fp8rl_gemm_fwd_ex(const uint8_t* qx, const float* sx, const uint8_t* qw,
+                               const float* sw, uint16_t* y, int64_t M, int64_t N,
+                               int64_t K, void* ws, size_t ws_bytes,
+                               const fp8rl_gemm_opts* opts, fp8rl_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * Diagnostics (used by the tests).
+ * -------------------------------------------------------------------------------------- */
+
+/* The device's E4M3 encoder (the exact routine the quantizers use) applied to n binary32
+ * values: out[i] = E4M3_rne_satfinite(in[i]).  Device pointers. */
+FP8RL_API fp8rl_status fp8rl_debug_e4m3_encode(const float* in, uint8_t* out, int64_t n,
+                                     fp8rl_stream_t stream);
+
+/* Launches one CTA that waits, with the GEMM kernels' bounded wait, on an mbarrier that
+ * nothing completes; after `timeout_ns` it records FP8RL_ERR_DEVICE_TIMEOUT and returns.
+ * Exercises the failure path without faulting or hanging the GPU. */
+FP8RL_API fp8rl_status fp8rl_debug_wait_timeout(uint64_t timeout_ns, fp8rl_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8RL_H */

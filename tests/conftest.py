@@ -36,4 +36,6 @@ def fp8lib():
     from block_scaled_fp8_x1_gb300 import build_library, ops
     build_library()
     ops.init(0)
+    # a healthy kernel never waits this long on one barrier; fail fast instead of hanging
+    ops.set_wait_timeout_ns(int(float(os.environ.get("FP8RL_TEST_WAIT_NS", "1e9"))))
     return ops

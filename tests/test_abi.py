@@ -1,0 +1,85 @@
+"""The C ABI library builds, loads and exports every entry point include/fp8rl.h declares;
+host-side argument checks answer without a GPU (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8rl.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8rl_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def abi():
+    from block_scaled_fp8_x1_gb300 import build_library
+    from block_scaled_fp8_x1_gb300 import _abi
+    build_library()
+    return _abi
+
+
+def test_every_declared_symbol_is_exported(abi):
+    L = abi.lib()
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in abi.SIGNATURES, f"binding lacks {n}"
+
+
+def test_binding_names_are_declared(abi):
+    assert set(abi.SIGNATURES) == set(declared_functions())
+
+
+def test_status_strings(abi):
+    L = abi.lib()
+    for code, name in abi.STATUS_NAMES.items():
+        assert L.fp8rl_status_string(code).decode() == name
+
+
+def test_host_side_validation_without_gpu(abi):
+    L = abi.lib()
+    fake = ctypes.c_void_p(0x10000)      # never dereferenced: every call below fails first
+    odd = ctypes.c_void_p(0x10004)
+    null = None
+    # shape rules
+    assert L.fp8rl_quantize_1x128(fake, 4, 100, 100, fake, fake, null, null, null) == abi.FP8RL_ERR_SHAPE
+    assert L.fp8rl_quantize_1x128(fake, 100, 128, 128, fake, fake, fake, fake, null) == abi.FP8RL_ERR_SHAPE
+    assert L.fp8rl_quantize_128x1(fake, 100, 128, 128, fake, fake, null) == abi.FP8RL_ERR_SHAPE
+    assert L.fp8rl_quantize_128x128(fake, 100, 128, 128, fake, fake, null, null) == abi.FP8RL_ERR_SHAPE
+    assert L.fp8rl_silu_mul_quant(fake, 4, 100, fake, fake, null, null, null) == abi.FP8RL_ERR_SHAPE
+    assert L.fp8rl_gemm_fwd(fake, fake, fake, fake, fake, 4, 100, 128, null, 0, null) == abi.FP8RL_ERR_SHAPE
+    assert L.fp8rl_gemm_wgrad(fake, fake, fake, fake, fake, 100, 128, 128, null, 0, null) == abi.FP8RL_ERR_SHAPE
+    # bad arguments
+    assert L.fp8rl_quantize_1x128(fake, -1, 128, 128, fake, fake, null, null, null) == abi.FP8RL_ERR_INVALID_ARG
+    assert L.fp8rl_quantize_1x128(fake, 4, 128, 64, fake, fake, null, null, null) == abi.FP8RL_ERR_INVALID_ARG
+    assert L.fp8rl_quantize_1x128(fake, 128, 128, 128, fake, fake, fake, null, null) == abi.FP8RL_ERR_INVALID_ARG
+    assert L.fp8rl_quantize_1x128(null, 4, 128, 128, fake, fake, null, null, null) == abi.FP8RL_ERR_INVALID_ARG
+    assert L.fp8rl_rmsnorm_quant(fake, fake, ctypes.c_float(-1.0), 4, 128, fake, fake, null, null, null, null) == abi.FP8RL_ERR_INVALID_ARG
+    opts = abi.GemmOpts(7, 0, 0)
+    assert L.fp8rl_gemm_fwd_ex(fake, fake, fake, fake, fake, 4, 128, 128, null, 0, ctypes.byref(opts), null) == abi.FP8RL_ERR_INVALID_ARG
+    # alignment (16 bytes for every device pointer)
+    assert L.fp8rl_quantize_1x128(odd, 4, 128, 128, fake, fake, null, null, null) == abi.FP8RL_ERR_ALIGN
+    assert L.fp8rl_quantize_1x128(fake, 4, 128, 132, fake, fake, null, null, null) == abi.FP8RL_ERR_ALIGN
+    assert L.fp8rl_gemm_dgrad(fake, fake, odd, fake, fake, 4, 128, 128, null, 0, null) == abi.FP8RL_ERR_ALIGN
+    # empty problems are no-ops
+    assert L.fp8rl_quantize_1x128(null, 0, 128, 128, null, null, null, null, null) == abi.FP8RL_OK
+    assert L.fp8rl_gemm_fwd(null, null, null, null, null, 0, 128, 128, null, 0, null) == abi.FP8RL_OK
+    assert L.fp8rl_gemm_dgrad(null, null, null, null, null, 0, 128, 128, null, 0, null) == abi.FP8RL_OK
+
+
+def test_workspace_sizes(abi):
+    L = abi.lib()
+    # decode form (M <= 256) needs counters at least; tiled form needs none
+    assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 64, 3584, 3584) >= 256
+    assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 8192, 3584, 3584) == 0
+    assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_WGRAD, 8192, 3584, 3584) == 0
+    opts = abi.GemmOpts(abi.FP8RL_VARIANT_SPLITK, 4, 0)
+    need = L.fp8rl_gemm_workspace_bytes_ex(abi.FP8RL_OP_FWD, 256, 3584, 3584, ctypes.byref(opts))
+    assert need == 256 + 28 * 4 * 256 * 128 * 4

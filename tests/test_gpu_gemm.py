@@ -1,0 +1,131 @@
+"""Block-scaled FP8 GEMMs on the GPU vs the CPU oracle.
+
+"Technical summary: Jet-RL", section "Quantization Scheme": forward, DGrad and WGrad run
+in FP8 (1x128 activations/gradients, 128x128 weights, 128x1 WGrad operands); section "Core
+architecture": the rollout (decode-shaped, split-K) kernel shares the training forward
+pass's numerics.  Every output element must satisfy
+    |y - y_ref| <= 2^-7 |y_ref| + 1e-3 rms(y_ref)
+against the oracle's unrounded binary64 result on the same codes and scales.  The codes
+come from the oracle-checked GPU quantizers and are re-derived on the host by the oracle,
+so both sides see identical operands.
+"""
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_fp8_x1_gb300 import _abi, synth
+from parity import assert_same_bits_f32, assert_same_u8, bits16, f32, gemm_tolerance_check, u8
+
+pytestmark = pytest.mark.gpu
+
+
+def fwd_operands(fp8lib, oracle, M, N, K, seed):
+    x = synth.normal_bf16((M, K), 1.0, seed, "cuda", outlier_channels=max(1, K // 1000),
+                          outlier_scale=30.0)
+    w = synth.normal_bf16((N, K), 0.02, seed + 1, "cuda")
+    qx, sx = fp8lib.quantize_1x128(x)
+    qw, sw, qwT = fp8lib.quantize_128x128(w)
+    # the host sees the same operands: re-derive them with the oracle and compare
+    qxr, sxr = oracle.quantize_1x128(bits16(x))
+    assert_same_u8(u8(qx), qxr, "qx")
+    assert_same_bits_f32(f32(sx), sxr, "sx")
+    return qx, sx, qw, sw, qwT
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (256, 512, 512), (300, 384, 640),
+                                   (1000, 1280, 1024), (129, 128, 256)])
+def test_fwd_tiled(fp8lib, oracle, M, N, K):
+    qx, sx, qw, sw, _ = fwd_operands(fp8lib, oracle, M, N, K, M + N + K)
+    y = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_TILED)
+    y_ref = oracle.gemm(u8(qx), f32(sx), u8(qw), f32(sw), "fwd")
+    gemm_tolerance_check(bits16(y), y_ref, f"fwd {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M", [1, 5, 64, 100, 128, 200, 256])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_fwd_decode(fp8lib, oracle, M, splits):
+    N, K = 1280, 1024
+    qx, sx, qw, sw, _ = fwd_operands(fp8lib, oracle, M, N, K, 7 * M + splits)
+    y = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_SPLITK, splits=splits)
+    y_ref = oracle.gemm(u8(qx), f32(sx), u8(qw), f32(sw), "fwd")
+    gemm_tolerance_check(bits16(y), y_ref, f"decode M={M} splits={splits}")
+    # deterministic: the same call gives the same bytes
+    y2 = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_SPLITK, splits=splits)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+def test_fwd_auto_matches_forms(fp8lib, oracle):
+    """AUTO picks the decode form for M <= 256; both forms obey the same bound."""
+    M, N, K = 192, 768, 2048
+    qx, sx, qw, sw, _ = fwd_operands(fp8lib, oracle, M, N, K, 99)
+    y_ref = oracle.gemm(u8(qx), f32(sx), u8(qw), f32(sw), "fwd")
+    for v in (_abi.FP8RL_VARIANT_AUTO, _abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK):
+        gemm_tolerance_check(bits16(fp8lib.gemm_fwd(qx, sx, qw, sw, variant=v)), y_ref, f"variant {v}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (300, 384, 512), (512, 1024, 768)])
+def test_dgrad(fp8lib, oracle, M, N, K):
+    dy = synth.normal_bf16((M, N), 1e-3, M + 3, "cuda")
+    w = synth.normal_bf16((N, K), 0.02, K + 5, "cuda")
+    qdy, sdy = fp8lib.quantize_1x128(dy)
+    _, sw, qwT = fp8lib.quantize_128x128(w)
+    dx = fp8lib.gemm_dgrad(qdy, sdy, qwT, sw)
+    ref = oracle.gemm(u8(qdy), f32(sdy), u8(qwT), f32(sw), "dgrad")
+    gemm_tolerance_check(bits16(dx), ref, f"dgrad {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 512), (1024, 256, 768)])
+def test_wgrad(fp8lib, oracle, M, N, K):
+    dy = synth.normal_bf16((M, N), 1e-3, M + 11, "cuda")
+    x = synth.normal_bf16((M, K), 1.0, K + 13, "cuda", outlier_channels=2, outlier_scale=30.0)
+    qdyT, sdyT = fp8lib.quantize_128x1(dy)
+    qxT, sxT = fp8lib.quantize_128x1(x)
+    dw = fp8lib.gemm_wgrad(qdyT, sdyT, qxT, sxT)
+    ref = oracle.gemm(u8(qdyT), f32(sdyT), u8(qxT), f32(sxT), "wgrad")
+    gemm_tolerance_check(bits16(dw), ref, f"wgrad {M}x{N}x{K}")
+
+
+def test_exactly_representable_gemm(fp8lib, oracle):
+    """Operands on the E4M3 grid with power-of-two scales: quantization is the identity and
+    the exact product is numpy's float64 matmul; the GPU must be within BF16 rounding."""
+    rng = np.random.default_rng(5)
+    M, N, K = 256, 256, 512
+    codes_x = rng.integers(0x20, 0x48, size=(M, K)).astype(np.uint8) | (rng.integers(0, 2, (M, K)).astype(np.uint8) << 7)
+    codes_w = rng.integers(0x20, 0x48, size=(N, K)).astype(np.uint8) | (rng.integers(0, 2, (N, K)).astype(np.uint8) << 7)
+    x = oracle.e4m3_decode(codes_x)
+    w = oracle.e4m3_decode(codes_w)
+    x[:, ::128] = 448.0          # every 1x128 group has max 448 -> scale 1
+    w[::128, ::128] = 448.0      # every 128x128 block has max 448 -> scale 1
+    xt = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).cuda()
+    wt = torch.from_numpy(w.astype(np.float32)).to(torch.bfloat16).cuda()
+    qx, sx = fp8lib.quantize_1x128(xt)
+    qw, sw, _ = fp8lib.quantize_128x128(wt)
+    assert torch.all(sx == 1.0) and torch.all(sw == 1.0)
+    exact = x @ w.T
+    for v in (_abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK):
+        y = bits16(fp8lib.gemm_fwd(qx, sx, qw, sw, variant=v))
+        yf = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        assert np.all(np.abs(yf - exact) <= np.abs(exact) * 2.0 ** -8 + 1e-30)
+
+
+def test_scaling_law_on_device(fp8lib, oracle):
+    """Y(2^a X, 2^b W) = 2^(a+b) Y: the scales absorb powers of two exactly."""
+    M, N, K = 256, 512, 1024
+    x = synth.normal_bf16((M, K), 1.0, 21, "cuda")
+    w = synth.normal_bf16((N, K), 0.02, 22, "cuda")
+    qx, sx = fp8lib.quantize_1x128(x)
+    qw, sw, _ = fp8lib.quantize_128x128(w)
+    qx2, sx2 = fp8lib.quantize_1x128((x.float() * 8.0).to(torch.bfloat16))
+    qw2, sw2, _ = fp8lib.quantize_128x128((w.float() * 0.25).to(torch.bfloat16))
+    for v in (_abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK):
+        y = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=v).float()
+        y2 = fp8lib.gemm_fwd(qx2, sx2, qw2, sw2, variant=v).float()
+        assert torch.equal(y2, y * 2.0)
+
+
+def test_tiled_deterministic_and_grid_independent(fp8lib, oracle):
+    M, N, K = 640, 1536, 1024
+    qx, sx, qw, sw, _ = fwd_operands(fp8lib, oracle, M, N, K, 3)
+    y1 = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_TILED)
+    y2 = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_TILED, grid=7)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
