@@ -1,0 +1,563 @@
+"""Benchmark of the unified-precision FP8 linear layer on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over the Llama-3.1-8B MLP at training shape
+(8192 tokens, hidden 4096, intermediate 14336) plus a 256-token rollout decode through the
+same FP8 weights ("Technical summary: Jet-RL": rollout and training forward share one
+quantization flow; master weights stay BF16 and are re-quantized each step):
+
+  weight refresh   quantize_128x128(W_gate_up), quantize_128x128(W_down)  (+ W^T copies)
+  forward          rmsnorm_quant(X) -> gemm_fwd(gate_up) -> silu_mul_quant -> gemm_fwd(down)
+  backward down    quantize_1x128 dual(dY_down) -> gemm_dgrad -> gemm_wgrad
+  backward gate_up quantize_1x128 dual(dY_gate_up) -> gemm_dgrad -> gemm_wgrad
+  rollout decode   quantize_1x128(X_dec) -> gemm_fwd(gate_up, M=256) -> silu_mul_quant
+                   -> gemm_fwd(down, M=256)
+
+value = GEMM FLOPs of the step / device time of the step (TFLOP/s), inputs resident in HBM
+and larger than L2.  e2e = the same with the step's inputs copied from pinned host memory
+and its results copied back inside the timed region.  Per-kernel CUDA-event times give the
+quantizers' GB/s and the roofline of the dominant kernel.
+
+`--impl reference` times the CPU oracle (test infrastructure, unchanged) on the host cores
+on a bounded sample of the same step and reports the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 block-scaled GEMM TFLOP/s & % FP8 peak; quantize GB/s vs HBM peak"
+M_TOK, HID, INTER, M_DEC = 8192, 4096, 14336, 256
+WORKLOAD = ("Llama-3.1-8B MLP layer: training step at 8192 tokens (fwd + DGrad + WGrad, "
+            "weight refresh) + 256-token rollout decode")
+FP8_PER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor throughput ratio on GB300
+
+
+def gemm_flops():
+    f = {}
+    f["fwd_gate_up"] = 2.0 * M_TOK * 2 * INTER * HID
+    f["fwd_down"] = 2.0 * M_TOK * HID * INTER
+    f["dgrad_down"] = f["fwd_down"]
+    f["wgrad_down"] = f["fwd_down"]
+    f["dgrad_gate_up"] = f["fwd_gate_up"]
+    f["wgrad_gate_up"] = f["fwd_gate_up"]
+    f["decode_gate_up"] = 2.0 * M_DEC * 2 * INTER * HID
+    f["decode_down"] = 2.0 * M_DEC * HID * INTER
+    return f
+
+
+def quant_bytes():
+    """Algorithmic HBM bytes per launch of each quantizer: BF16 in, codes and FP32 scales out
+    (two code sets for the dual outputs), SiLU-mul reads gate and up."""
+    E_x, E_h, E_gu = M_TOK * HID, M_TOK * INTER, M_TOK * 2 * INTER
+    dual = lambda E: 2 * E + 2 * E + 2 * 4 * E / 128
+    b = {}
+    b["wq_gate_up"] = 2 * E_gu + E_gu + E_gu + 4 * E_gu / 16384   # codes + W^T copy + scales
+    E_w = HID * INTER
+    b["wq_down"] = 2 * E_w + E_w + E_w + 4 * E_w / 16384
+    b["rmsnorm_quant"] = dual(E_x) + 2 * HID + 4 * M_TOK
+    b["silu_mul_quant"] = 2 * 2 * E_h + E_h + E_h + 2 * 4 * E_h / 128
+    b["dq_dy_down"] = dual(E_x)
+    b["dq_dy_gate_up"] = dual(E_gu)
+    b["decode_quant"] = 2 * M_DEC * HID + M_DEC * HID + 4 * M_DEC * HID / 128
+    b["decode_silu"] = 2 * 2 * M_DEC * INTER + M_DEC * INTER + 4 * M_DEC * INTER / 128
+    return b
+
+
+def decode_bytes():
+    """HBM bytes of a decode-shaped GEMM: the FP8 weight stream, its scales, the BF16
+    activations and the BF16 output (the activations are quantized by the kernel before)."""
+    d = {}
+    for name, N, K in (("decode_gate_up", 2 * INTER, HID), ("decode_down", HID, INTER)):
+        d[name] = N * K + 4 * (N // 128) * (K // 128) + M_DEC * K + 4 * M_DEC * K / 128 + 2 * M_DEC * N
+    return d
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                rows.append((float(p[1]), float(p[2]), p[5], p[6], p[7], p[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                "sw_power_cap"), r[2:]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- peaks
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+class Step:
+    """All buffers of one step, resident on the device, and the launches in order."""
+
+    def __init__(self, dev):
+        import torch
+        from block_scaled_fp8_x1_gb300 import _abi, ops, synth
+        self.torch, self.ops, self._abi = torch, ops, _abi
+        w = synth.LLAMA8B_MLP_M8192
+        wb = synth.LLAMA8B_MLP_BWD_M8192
+        gate_up, down = w.linears
+        self.x = synth.activation(w, M_TOK, HID, 0, dev)
+        self.gamma = torch.ones(HID, dtype=torch.bfloat16, device=dev)
+        self.w_gu = synth.weight(w, gate_up, 1, dev)
+        self.w_d = synth.weight(w, down, 2, dev)
+        self.dy_d = synth.gradient(wb, M_TOK, HID, 3, dev)
+        self.dy_gu = synth.gradient(wb, M_TOK, 2 * INTER, 4, dev)
+        self.x_dec = synth.activation(synth.QWEN7B_DECODE, M_DEC, HID, 5, dev)
+        self.eps = w.extra["eps"]
+        self.dev = dev
+        self.inputs = ["x", "gamma", "w_gu", "w_d", "dy_d", "dy_gu", "x_dec"]
+        self.outputs = {}
+
+    def run(self, marks=None):
+        """Launch the step; if `marks` is a list, append (name, event) after each launch."""
+        ops, V = self.ops, self._abi
+        torch = self.torch
+
+        def mark(name):
+            if marks is not None:
+                e = torch.cuda.Event(enable_timing=True)
+                e.record()
+                marks.append((name, e))
+
+        mark("start")
+        q_gu, s_gu, qT_gu = ops.quantize_128x128(self.w_gu); mark("wq_gate_up")
+        q_d, s_d, qT_d = ops.quantize_128x128(self.w_d); mark("wq_down")
+        qx, sx, qxT, sxT, rstd = ops.rmsnorm_quant(self.x, self.gamma, self.eps); mark("rmsnorm_quant")
+        gu = ops.gemm_fwd(qx, sx, q_gu, s_gu, variant=V.FP8RL_VARIANT_TILED); mark("fwd_gate_up")
+        qh, sh, qhT, shT = ops.silu_mul_quant(gu); mark("silu_mul_quant")
+        y = ops.gemm_fwd(qh, sh, q_d, s_d, variant=V.FP8RL_VARIANT_TILED); mark("fwd_down")
+        qdy, sdy, qdyT, sdyT = ops.quantize_1x128(self.dy_d, dual=True); mark("dq_dy_down")
+        dh = ops.gemm_dgrad(qdy, sdy, qT_d, s_d); mark("dgrad_down")
+        dw_d = ops.gemm_wgrad(qdyT, sdyT, qhT, shT); mark("wgrad_down")
+        qg, sg, qgT, sgT = ops.quantize_1x128(self.dy_gu, dual=True); mark("dq_dy_gate_up")
+        dx = ops.gemm_dgrad(qg, sg, qT_gu, s_gu); mark("dgrad_gate_up")
+        dw_gu = ops.gemm_wgrad(qgT, sgT, qxT, sxT); mark("wgrad_gate_up")
+        qxd, sxd = ops.quantize_1x128(self.x_dec); mark("decode_quant")
+        gud = ops.gemm_fwd(qxd, sxd, q_gu, s_gu); mark("decode_gate_up")
+        qhd, shd, _, _ = ops.silu_mul_quant(gud, dual=False); mark("decode_silu")
+        yd = ops.gemm_fwd(qhd, shd, q_d, s_d); mark("decode_down")
+        # results read back by the end-to-end leg; dH stays on the device (it feeds the
+        # SiLU-mul backward, which lies outside this path)
+        self.keep = dh
+        self.outputs = {"y": y, "dx": dx, "dw_gu": dw_gu, "dw_d": dw_d, "y_dec": yd}
+        return self.outputs
+
+    LAUNCHES_PER_STEP = 16
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from block_scaled_fp8_x1_gb300 import build_library, ops
+    build_library()
+    ops.init(local)
+
+    step = Step(dev)
+    flops = gemm_flops()
+    step_flops = sum(flops.values())
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step.run()
+    barrier()
+
+    # ---- device-resident timed region: whole steps, then per-kernel split
+    clocks = ClockSampler(local)
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    t0.record()
+    for _ in range(args.steps):
+        step.run()
+    t1.record()
+    barrier()
+    ms_total = t0.elapsed_time(t1)
+    # per-kernel durations from events between launches (separate pass, same work)
+    per = {}
+    for _ in range(args.steps):
+        marks = []
+        step.run(marks)
+        torch.cuda.synchronize()
+        for (_, a), (name, b) in zip(marks[:-1], marks[1:]):
+            per.setdefault(name, []).append(a.elapsed_time(b))
+    clk = clocks.stop()
+    st = ops.check_status()
+
+    ms_step = ms_total / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    # ---- end to end: host buffers, copies inside the timed region
+    host_in = {n: torch.empty_like(getattr(step, n), device="cpu").pin_memory() for n in step.inputs}
+    for n in step.inputs:
+        host_in[n].copy_(getattr(step, n))
+    outs = step.run()
+    host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in outs.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for n in step.inputs:
+            getattr(step, n).copy_(host_in[n], non_blocking=True)
+        o = step.run()
+        for k, v in o.items():
+            host_out[k].copy_(v, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    barrier()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks = measured_peaks()
+    fp8_peak_sustained = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
+    kern = {}
+    qb = quant_bytes()
+    db = decode_bytes()
+    for name, v in per.items():
+        ms = statistics.mean(v)
+        e = {"ms": round(ms, 4)}
+        if name in db:
+            gbs = db[name] / (ms * 1e-3) / 1e9
+            e.update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3),
+                      "TFLOP/s": round(flops[name] / (ms * 1e-3) / 1e12, 1)})
+        elif name in flops:
+            tf = flops[name] / (ms * 1e-3) / 1e12
+            e.update({"TFLOP/s": round(tf, 1), "frac_fp8_peak": round(tf / fp8_peak_sustained, 3)})
+        elif name in qb:
+            gbs = qb[name] / (ms * 1e-3) / 1e9
+            e.update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3)})
+        kern[name] = e
+    dominant = max(kern, key=lambda n: kern[n]["ms"])
+    dom_ms = kern[dominant]["ms"]
+    if dominant in flops and dominant not in db:
+        achieved = flops[dominant] / (dom_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak_sustained, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / fp8_peak_sustained, 3),
+                "traffic": load_traffic(dominant), "kernel": dominant,
+                "peak_note": f"{peaks['source']} sustained bf16 x {FP8_PER_BF16} (nominal FP8/BF16 ratio)"}
+    else:
+        nbytes = qb.get(dominant, db.get(dominant, 0.0))
+        achieved = nbytes / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 3), "traffic": load_traffic(dominant),
+                "kernel": dominant, "peak_note": f"{peaks['source']} copy bandwidth"}
+    value = step_flops * world / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": M_TOK, "hidden": HID, "intermediate": INTER,
+                   "decode_tokens": M_DEC, "gemm_flops_per_step": step_flops,
+                   "l2": "inputs larger than L2 (X 64 MB, W_gate_up 224 MB, dY_gate_up 448 MB per step)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "e2e": {"value": round(step_flops * world / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)},
+        "gpu_launches": Step.LAUNCHES_PER_STEP * args.steps,
+        "clocks": clk,
+        "kernels": kern,
+        "device_status": st,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on
+    the current kernel source (profiles/traffic.json)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        e = d.get(kernel)
+        return e["bytes_per_launch"] if e else None
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def oracle_step_estimate(rows: int, n_samp: int):
+    """Time the CPU oracle on a bounded sample of every kernel of the step (quantizers on
+    `rows` token rows, GEMMs on `n_samp` output elements) and extrapolate each to its full
+    size.  Returns (estimated seconds for one full step, threads, sample description)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from block_scaled_fp8_x1_gb300 import synth
+
+    threads = oracle.threads()
+    w = synth.LLAMA8B_MLP_M8192
+    rng = np.random.default_rng(0)
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    x = bits(synth.activation(w, rows, HID, 0))
+    gu = bits(synth.normal_bf16((rows, 2 * INTER), 2.0, 9))
+    wq_rows = 128
+    wgu = bits(synth.weight(w, w.linears[0], 1)[:wq_rows])
+    est = 0.0
+    parts = []
+
+    def timed(fn):
+        t = time.perf_counter()
+        out = fn()
+        return time.perf_counter() - t, out
+
+    # quantizers (sampled rows, scaled by full rows / sampled rows)
+    t, _ = timed(lambda: oracle.quantize_128x128(wgu))
+    est += t * (2 * INTER + HID) / wq_rows
+    t, r = timed(lambda: oracle.rmsnorm_quant(x, np.full(HID, 0x3F80, np.uint16), 1e-5))
+    est += t * M_TOK / rows
+    t, h = timed(lambda: oracle.silu_mul(gu))
+    t2, _ = timed(lambda: (oracle.quantize_1x128(h[0]), oracle.quantize_128x1(h[0])))
+    est += (t + t2) * M_TOK / rows
+    t, _ = timed(lambda: (oracle.quantize_1x128(x), oracle.quantize_128x1(x)))
+    est += t * M_TOK / rows * (1 + 2 * INTER / HID)        # dY_down and dY_gate_up
+    parts.append(f"quantizers on {rows} rows")
+    # GEMMs: sampled output elements, scaled by outputs / samples
+    qx, sx = r[0], r[1]
+    qw, sw, _ = oracle.quantize_128x128(bits(synth.weight(w, w.linears[0], 1)[:256]))
+    i1 = rng.integers(0, rows, n_samp)
+    i2 = rng.integers(0, 256, n_samp)
+    t, _ = timed(lambda: oracle.gemm_sampled(qx, sx, qw, sw, "fwd", i1, i2))
+    per_flop = t / (2.0 * HID * n_samp)
+    est += per_flop * sum(gemm_flops().values())
+    parts.append(f"{n_samp} GEMM outputs (K={HID}) extrapolated per FLOP")
+    return est, threads, "; ".join(parts)
+
+
+def cpu_baseline():
+    est, threads, sample = oracle_step_estimate(rows=1024, n_samp=4096)
+    flops = sum(gemm_flops().values())
+    return {"value": round(flops / est / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "sample": sample + f"; full step extrapolated to {est:.1f} s",
+            "ms_per_step_extrapolated": round(est * 1e3, 1)}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    for _ in range(args.warmup):
+        oracle_step_estimate(rows=256, n_samp=1024)
+    ests = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e, threads, sample = oracle_step_estimate(rows=256, n_samp=1024)
+        ests.append(e)
+    wall = time.perf_counter() - t0
+    est = statistics.median(ests)
+    flops = sum(gemm_flops().values())
+    value = flops / est / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(est * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (oracle: binary64 block sums, binary32 quantizers)",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": M_TOK, "hidden": HID, "intermediate": INTER,
+                   "decode_tokens": M_DEC},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle", "sample": sample + f"; {args.steps} samples in {wall:.1f} s"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_kernel(args):
+    """One kernel form on one shape, `reps` launches after one warm-up, with CUDA-event
+    timing (used for ncu captures on small cases and for kernel sweeps)."""
+    import torch
+    from block_scaled_fp8_x1_gb300 import _abi, build_library, ops, synth
+    build_library()
+    ops.init(0)
+    dev = torch.device("cuda", 0)
+    dims = [int(v) for v in args.shape.split(",")]
+    k = args.kernel
+    if k.startswith("gemm"):
+        M, N, K = dims
+        if k == "gemm_wgrad":
+            a = ops.quantize_128x1(synth.normal_bf16((M, N), 1e-3, 1, dev))
+            b = ops.quantize_128x1(synth.normal_bf16((M, K), 1.0, 2, dev))
+            fn = lambda: ops.gemm_wgrad(a[0], a[1], b[0], b[1])
+        else:
+            lhs_cols = N if k == "gemm_dgrad" else K
+            qa, sa = ops.quantize_1x128(synth.normal_bf16((M, lhs_cols), 1.0, 1, dev))
+            if k == "gemm_dgrad":
+                _, sw, qwT = ops.quantize_128x128(synth.normal_bf16((N, K), 0.02, 2, dev))
+                fn = lambda: ops.gemm_dgrad(qa, sa, qwT, sw)
+            else:
+                qw, sw, _ = ops.quantize_128x128(synth.normal_bf16((N, K), 0.02, 2, dev), transpose=False)
+                var = _abi.FP8RL_VARIANT_SPLITK if k == "gemm_decode" else _abi.FP8RL_VARIANT_TILED
+                fn = lambda: ops.gemm_fwd(qa, sa, qw, sw, variant=var)
+        work, unit = 2.0 * M * N * K, "TFLOP/s"
+    else:
+        M, K = dims
+        if k == "rmsnorm_quant":
+            x = synth.normal_bf16((M, K), 1.0, 1, dev)
+            g = torch.ones(K, dtype=torch.bfloat16, device=dev)
+            fn = lambda: ops.rmsnorm_quant(x, g, 1e-5)
+            work = M * K * (2 + 2) + 8 * M * K / 128
+        elif k == "silu_mul_quant":
+            x = synth.normal_bf16((M, 2 * K), 1.0, 1, dev)
+            fn = lambda: ops.silu_mul_quant(x)
+            work = M * K * (4 + 2) + 8 * M * K / 128
+        elif k == "quant_dual":
+            x = synth.normal_bf16((M, K), 1.0, 1, dev)
+            fn = lambda: ops.quantize_1x128(x, dual=True)
+            work = M * K * (2 + 2) + 8 * M * K / 128
+        elif k == "quant_128x128":
+            x = synth.normal_bf16((M, K), 0.02, 1, dev)
+            fn = lambda: ops.quantize_128x128(x)
+            work = M * K * (2 + 2) + 4 * M * K / 16384
+        else:
+            raise SystemExit(f"unknown kernel {k}")
+        unit = "GB/s"
+    fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.reps):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record()
+        fn()
+        ev1.record()
+        torch.cuda.synchronize()
+        times.append(ev0.elapsed_time(ev1))
+    ms = statistics.median(times)
+    rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    print(json.dumps({"kernel": k, "shape": dims, "ms": round(ms, 4), unit: round(rate, 1),
+                      "status": ops.check_status()}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", default=None,
+                    help="run one kernel form alone (for profiling): gemm_fwd, gemm_dgrad, "
+                         "gemm_wgrad, gemm_decode, rmsnorm_quant, silu_mul_quant, quant_dual, "
+                         "quant_128x128")
+    ap.add_argument("--shape", default=None, help="M,N,K (GEMMs) or M,K (quantizers)")
+    ap.add_argument("--reps", type=int, default=3)
+    args = ap.parse_args()
+    if args.kernel:
+        run_kernel(args)
+        return
+    if args.warmup < 3 and args.impl == "native":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
