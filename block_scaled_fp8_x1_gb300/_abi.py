@@ -73,6 +73,8 @@ SIGNATURES = {
                                                         ctypes.POINTER(GemmOpts)]),
     "fp8rl_gemm_fwd_ex": (ST, [P, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t,
                                ctypes.POINTER(GemmOpts), STREAM]),
+    "fp8rl_gemm_fwd_decode_noalloc": (ST, [P, P, P, P, P, I64, I64, I64, STREAM]),
+    "fp8rl_gemm_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "fp8rl_debug_e4m3_encode": (ST, [P, P, I64, STREAM]),
     "fp8rl_debug_wait_timeout": (ST, [ctypes.c_uint64, STREAM]),
 }

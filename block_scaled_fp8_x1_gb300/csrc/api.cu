@@ -13,6 +13,8 @@
 
 namespace fp8rl {
 fp8rl_status read_and_clear_device_status(cudaStream_t st);  // gemm.cu
+size_t noalloc_scratch_bytes();                              // gemm_noalloc.cu
+cudaError_t noalloc_scratch(void** out);                     // gemm_noalloc.cu
 }
 
 using namespace fp8rl;
@@ -399,6 +401,37 @@ fp8rl_status fp8rl_gemm_wgrad(const uint8_t* qdyT, const float* sdyT, const uint
     t.R1 = N; t.R2 = K; t.Kr = M;
     return run_tiled(t, 0, sms, stream);
 }
+
+// ---------------------------------------------------------------- no-allocation decode
+
+// Decode-shaped forward GEMM on the library's own fixed scratch array (see
+// gemm_noalloc.cu): the same kernel, split and reduction order as fp8rl_gemm_fwd_ex with
+// FP8RL_VARIANT_SPLITK and automatic splits, but no workspace argument and no allocation.
+fp8rl_status fp8rl_gemm_fwd_decode_noalloc(const uint8_t* qx, const float* sx, const uint8_t* qw,
+                                           const float* sw, uint16_t* y, int64_t M, int64_t N,
+                                           int64_t K, fp8rl_stream_t stream) {
+    if (M < 0 || N < 0 || K <= 0) return FP8RL_ERR_INVALID_ARG;
+    if (K % 128 != 0 || N % 128 != 0 || M > 256) return FP8RL_ERR_SHAPE;
+    if (M == 0 || N == 0) return FP8RL_OK;
+    if (!qx || !sx || !qw || !sw || !y) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(qx) || !aligned16(sx) || !aligned16(qw) || !aligned16(sw) || !aligned16(y))
+        return FP8RL_ERR_ALIGN;
+    int sms = 0;
+    fp8rl_status e = current_device(&sms);
+    if (e != FP8RL_OK) return e;
+    const int64_t tiles = (N + 127) / 128;
+    const int splits = choose_splits(tiles, K / 128, sms);
+    const size_t need = decode_ws_bytes(M, N, K, splits);
+    const size_t have = noalloc_scratch_bytes();
+    if (need > have) return FP8RL_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    if (noalloc_scratch(&scratch) != cudaSuccess) return FP8RL_ERR_CUDA;
+    // the array keeps the previous call's contents: the arrival counters must start at zero
+    if (cudaMemsetAsync(scratch, 0, counter_bytes(tiles), stream) != cudaSuccess) return FP8RL_ERR_CUDA;
+    return run_decode(qx, sx, qw, sw, y, M, N, K, scratch, have, splits, sms, stream);
+}
+
+size_t fp8rl_gemm_noalloc_scratch_bytes(void) { return noalloc_scratch_bytes(); }
 
 // ---------------------------------------------------------------- diagnostics
 

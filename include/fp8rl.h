@@ -218,6 +218,31 @@ FP8RL_API fp8rl_status fp8rl_gemm_fwd_ex(const uint8_t* qx, const float* sx, con
                                int64_t K, void* ws, size_t ws_bytes,
                                const fp8rl_gemm_opts* opts, fp8rl_stream_t stream);
 
+/* Decode-shaped forward GEMM that allocates nothing and takes no workspace.  It has no
+ * counterpart in the scheme's pages; it exists for callers that cannot provide device
+ * memory: a C/C++ decode loop that links only this library and owns no allocator, or a
+ * serving loop that must not allocate between decode steps (allocating and freeing
+ * device memory can synchronize the device and stall the loop).
+ * Same operands, layouts, result and numerics as fp8rl_gemm_fwd_ex with
+ * FP8RL_VARIANT_SPLITK and automatic splits (M <= 256).  Its split-K partial sums and
+ * arrival counters live in a fixed scratch array inside the library,
+ * fp8rl_gemm_noalloc_scratch_bytes() bytes (32 MiB) per device, reserved on every GPU
+ * that loads the library and held until the process exits.
+ *   - A problem whose split needs more scratch than that returns FP8RL_ERR_WORKSPACE and
+ *     launches nothing; M > 256 returns FP8RL_ERR_SHAPE.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current) and caches it; make that first call before any stream capture.
+ *   - Every call on a device shares the array and clears its counters on entry (an
+ *     asynchronous memset on `stream`); calls whose kernels overlap on the GPU race on the
+ *     array and give wrong results, so order them on one stream. */
+FP8RL_API fp8rl_status fp8rl_gemm_fwd_decode_noalloc(const uint8_t* qx, const float* sx,
+                                                     const uint8_t* qw, const float* sw,
+                                                     uint16_t* y, int64_t M, int64_t N,
+                                                     int64_t K, fp8rl_stream_t stream);
+
+/* Size in bytes of the scratch array fp8rl_gemm_fwd_decode_noalloc uses on each device. */
+FP8RL_API size_t fp8rl_gemm_noalloc_scratch_bytes(void);
+
 /* ----------------------------------------------------------------------------------------
  * Diagnostics (used by the tests).
  * -------------------------------------------------------------------------------------- */
