@@ -494,7 +494,7 @@ def run_kernel(args):
             else:
                 qw, sw, _ = ops.quantize_128x128(synth.normal_bf16((N, K), 0.02, 2, dev), transpose=False)
                 var = _abi.FP8RL_VARIANT_SPLITK if k == "gemm_decode" else _abi.FP8RL_VARIANT_TILED
-                fn = lambda: ops.gemm_fwd(qa, sa, qw, sw, variant=var)
+                fn = lambda: ops.gemm_fwd(qa, sa, qw, sw, variant=var, tile_n=args.tile_n)
         work, unit = 2.0 * M * N * K, "TFLOP/s"
     else:
         M, K = dims
@@ -547,6 +547,7 @@ def main():
                          "quant_128x128")
     ap.add_argument("--shape", default=None, help="M,N,K (GEMMs) or M,K (quantizers)")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--tile-n", type=int, default=0, help="tiled forward GEMM tile width (128/256)")
     args = ap.parse_args()
     if args.kernel:
         run_kernel(args)

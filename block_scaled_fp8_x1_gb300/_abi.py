@@ -45,7 +45,8 @@ class Fp8rlError(RuntimeError):
 
 
 class GemmOpts(ctypes.Structure):
-    _fields_ = [("variant", ctypes.c_int), ("splits", ctypes.c_int), ("grid", ctypes.c_int)]
+    _fields_ = [("variant", ctypes.c_int), ("splits", ctypes.c_int), ("grid", ctypes.c_int),
+                ("tile_n", ctypes.c_int)]
 
 
 P = ctypes.c_void_p

@@ -57,12 +57,9 @@ inline fp8rl_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8RL
 
 // ---------------------------------------------------------------- TMA descriptors
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+}  // namespace
 
-EncodeTiledFn encode_fn() {
+EncodeTiledFn fp8rl::encode_tiled_fn() {
     static EncodeTiledFn fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -76,11 +73,13 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+namespace {
+
 // Row-major byte matrix [rows][cols] (row stride ld bytes), box of box_rows x 128 bytes,
 // 128-byte swizzle (the K-major layout the tcgen05 descriptors expect).
 fp8rl_status make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld,
                        int box_rows) {
-    EncodeTiledFn enc = encode_fn();
+    EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) return FP8RL_ERR_CUDA;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)ld};
@@ -94,24 +93,20 @@ fp8rl_status make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t c
 
 // ---------------------------------------------------------------- GEMM planning
 
-int decode_bn(int64_t M) { return M <= 64 ? 64 : (M <= 128 ? 128 : 256); }
+// The decode form is the tiled kernel (tokens as rows, weights as 256-wide columns) with
+// the reduction split into slices so that a handful of output tiles still occupy every SM.
+constexpr int kDecodeBN = 256;
 
-// Reduction slices for the decode form: minimise the longest chain of K-blocks any CTA
-// runs (waves x blocks per slice), preferring fewer slices on ties.
+int64_t decode_tiles(int64_t M, int64_t N) { return ((M + 127) / 128) * ((N + kDecodeBN - 1) / kDecodeBN); }
+
+// Slices per tile: as many as keep all (tile, slice) items within one wave of CTAs, at
+// most 16, and at least two K-blocks per slice.
 int choose_splits(int64_t tiles, int64_t nkb, int num_sms) {
-    int best = 1;
-    int64_t best_cost = INT64_MAX;
-    for (int s = 1; s <= 16 && s <= nkb; ++s) {
-        const int64_t items = tiles * s;
-        const int64_t waves = (items + num_sms - 1) / num_sms;
-        const int64_t per = (nkb + s - 1) / s;
-        const int64_t cost = waves * per + (s > 1 ? 1 : 0);  // a slice pays one reduction
-        if (cost < best_cost) {
-            best_cost = cost;
-            best = s;
-        }
-    }
-    return best;
+    if (tiles >= num_sms) return 1;
+    int64_t s = num_sms / tiles;
+    s = std::min<int64_t>(s, 16);
+    s = std::min<int64_t>(s, std::max<int64_t>(nkb / 2, 1));
+    return (int)std::max<int64_t>(s, 1);
 }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -119,10 +114,9 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 size_t counter_bytes(int64_t tiles) { return align_up((size_t)tiles * 4, 256); }
 
 size_t decode_ws_bytes(int64_t M, int64_t N, int64_t K, int splits) {
-    const int64_t tiles = (N + 127) / 128;
-    const int bn = decode_bn(M);
+    const int64_t tiles = decode_tiles(M, N);
     size_t b = counter_bytes(tiles);
-    if (splits > 1) b += (size_t)tiles * splits * bn * 128 * sizeof(float);
+    if (splits > 1) b += (size_t)tiles * splits * kDecodeBN * 128 * sizeof(float);
     (void)K;
     return b;
 }
@@ -134,11 +128,16 @@ struct TiledArgs {
     int64_t R1, R2, Kr;
 };
 
-fp8rl_status run_tiled(const TiledArgs& t, int grid_req, int num_sms, cudaStream_t st) {
+// Column-tile width of the tiled form: 256 halves the re-reads of A, 128 gives the tensor
+// pipe four TMEM buffers of lead over the promotion epilogue.
+int tiled_bn(int req) { return req == 128 ? 128 : 256; }
+
+fp8rl_status run_tiled(const TiledArgs& t, int grid_req, int bn_req, int num_sms, cudaStream_t st) {
+    const int bn = tiled_bn(bn_req);
     CUtensorMap ta, tb;
     fp8rl_status e = make_tmap(&ta, t.A, t.R1, t.Kr, t.Kr, 128);
     if (e != FP8RL_OK) return e;
-    e = make_tmap(&tb, t.B, t.R2, t.Kr, t.Kr, 256);
+    e = make_tmap(&tb, t.B, t.R2, t.Kr, t.Kr, bn);
     if (e != FP8RL_OK) return e;
     GemmParams p = {};
     p.R1 = t.R1; p.R2 = t.R2; p.Kr = t.Kr;
@@ -147,46 +146,45 @@ fp8rl_status run_tiled(const TiledArgs& t, int grid_req, int num_sms, cudaStream
     p.c = t.c; p.ldc = t.ldc;
     p.splits = 0;
     p.m_tiles = (int)((t.R1 + 127) / 128);
-    p.n_tiles = (int)((t.R2 + 255) / 256);
+    p.n_tiles = (int)((t.R2 + bn - 1) / bn);
     p.nkb = (int)(t.Kr / 128);
     p.num_items = p.m_tiles * p.n_tiles;
     p.timeout_ns = g_timeout_ns.load();
     int grid = grid_req > 0 ? grid_req : num_sms;
     grid = std::max(1, std::min(grid, p.num_items));
-    return cuda_status(launch_gemm_tiled(ta, tb, p, t.b_mode, grid, st));
+    return cuda_status(launch_gemm_tiled(ta, tb, p, t.b_mode, bn, grid, st));
 }
 
 fp8rl_status run_decode(const uint8_t* qx, const float* sx, const uint8_t* qw, const float* sw,
                         uint16_t* y, int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes,
                         int splits_req, int num_sms, cudaStream_t st) {
-    const int bn = decode_bn(M);
-    const int64_t tiles = (N + 127) / 128;
+    const int64_t tiles = decode_tiles(M, N);
     const int64_t nkb = K / 128;
-    int splits = splits_req > 0 ? (int)std::min<int64_t>(splits_req, nkb)
-                                : choose_splits(tiles, nkb, num_sms);
+    const int splits = splits_req > 0 ? (int)std::min<int64_t>(splits_req, nkb)
+                                      : choose_splits(tiles, nkb, num_sms);
     const size_t need = decode_ws_bytes(M, N, K, splits);
     if (ws == nullptr || ws_bytes < need) return FP8RL_ERR_WORKSPACE;
     if (!aligned16(ws)) return FP8RL_ERR_ALIGN;
     CUtensorMap ta, tb;
-    fp8rl_status e = make_tmap(&ta, qw, N, K, K, 128);
+    fp8rl_status e = make_tmap(&ta, qx, M, K, K, 128);
     if (e != FP8RL_OK) return e;
-    e = make_tmap(&tb, qx, M, K, K, bn);
+    e = make_tmap(&tb, qw, N, K, K, kDecodeBN);
     if (e != FP8RL_OK) return e;
     GemmParams p = {};
-    p.R1 = N; p.R2 = M; p.Kr = K;
-    p.sa = sw; p.sa_kb = 1; p.sa_r = K / 128;
-    p.sb = sx; p.sb_kb = M; p.sb_r = 0;
+    p.R1 = M; p.R2 = N; p.Kr = K;
+    p.sa = sx; p.sa_kb = M; p.sa_r = 0;
+    p.sb = sw; p.sb_kb = 1; p.sb_r = K / 128;
     p.c = y; p.ldc = N;
     p.counters = reinterpret_cast<unsigned int*>(ws);
     p.ws = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + counter_bytes(tiles));
     p.splits = splits;
-    p.m_tiles = (int)tiles;
-    p.n_tiles = 1;
+    p.m_tiles = (int)((M + 127) / 128);
+    p.n_tiles = (int)((N + kDecodeBN - 1) / kDecodeBN);
     p.nkb = (int)nkb;
     p.num_items = (int)(tiles * splits);
     p.timeout_ns = g_timeout_ns.load();
     const int grid = std::max(1, std::min(num_sms, p.num_items));
-    return cuda_status(launch_gemm_splitk(ta, tb, p, bn, grid, st));
+    return cuda_status(launch_gemm_splitk(ta, tb, p, grid, st));
 }
 
 }  // namespace
@@ -224,7 +222,9 @@ void fp8rl_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns > 0 ? ns : 1
 fp8rl_status fp8rl_check_status(fp8rl_stream_t stream) {
     fp8rl_status e = current_device(nullptr);
     if (e != FP8RL_OK) return e;
-    return read_and_clear_device_status(stream);
+    const fp8rl_status g = read_and_clear_device_status(stream);  // synchronizes the stream
+    const fp8rl_status q = read_and_clear_quant_status();
+    return g != FP8RL_OK ? g : q;
 }
 
 // ---------------------------------------------------------------- quantizers
@@ -242,7 +242,7 @@ fp8rl_status fp8rl_quantize_1x128(const uint16_t* x, int64_t M, int64_t K, int64
     int sms = 0;
     fp8rl_status e = current_device(&sms);
     if (e != FP8RL_OK) return e;
-    if (qT) return cuda_status(launch_quant_dual(x, M, K, ldx, q, s, qT, sT, stream));
+    if (qT) return cuda_status(launch_quant_dual(x, M, K, ldx, q, s, qT, sT, g_timeout_ns.load(), stream));
     return cuda_status(launch_quant_1x128(x, M, K, ldx, q, s, sms, stream));
 }
 
@@ -255,7 +255,7 @@ fp8rl_status fp8rl_quantize_128x1(const uint16_t* x, int64_t M, int64_t K, int64
     if (!aligned16(x) || !aligned16(qT) || !aligned16(sT) || (ldx * 2) % 16 != 0) return FP8RL_ERR_ALIGN;
     fp8rl_status e = current_device(nullptr);
     if (e != FP8RL_OK) return e;
-    return cuda_status(launch_quant_dual(x, M, K, ldx, nullptr, nullptr, qT, sT, stream));
+    return cuda_status(launch_quant_dual(x, M, K, ldx, nullptr, nullptr, qT, sT, g_timeout_ns.load(), stream));
 }
 
 fp8rl_status fp8rl_quantize_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw,
@@ -285,7 +285,7 @@ fp8rl_status fp8rl_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float
     if (rstd && !aligned16(rstd)) return FP8RL_ERR_ALIGN;
     fp8rl_status e = current_device(nullptr);
     if (e != FP8RL_OK) return e;
-    return cuda_status(launch_rmsnorm_quant(x, gamma, eps, M, K, q, s, qT, sT, rstd, stream));
+    return cuda_status(launch_rmsnorm_quant(x, gamma, eps, M, K, q, s, qT, sT, rstd, g_timeout_ns.load(), stream));
 }
 
 fp8rl_status fp8rl_silu_mul_quant(const uint16_t* gu, int64_t M, int64_t I, uint8_t* q, float* s,
@@ -300,7 +300,7 @@ fp8rl_status fp8rl_silu_mul_quant(const uint16_t* gu, int64_t M, int64_t I, uint
     if (qT && (!aligned16(qT) || !aligned16(sT))) return FP8RL_ERR_ALIGN;
     fp8rl_status e = current_device(nullptr);
     if (e != FP8RL_OK) return e;
-    return cuda_status(launch_silu_mul_quant(gu, M, I, q, s, qT, sT, stream));
+    return cuda_status(launch_silu_mul_quant(gu, M, I, q, s, qT, sT, g_timeout_ns.load(), stream));
 }
 
 // ---------------------------------------------------------------- GEMMs
@@ -317,7 +317,7 @@ size_t fp8rl_gemm_workspace_bytes_ex(int op, int64_t M, int64_t N, int64_t K,
     if (!decode || M > 256) return 0;
     int sms = 0;
     if (current_device(&sms) != FP8RL_OK) sms = 148;
-    const int64_t tiles = (N + 127) / 128, nkb = K / 128;
+    const int64_t tiles = decode_tiles(M, N), nkb = K / 128;
     const int splits = (opts && opts->splits > 0) ? (int)std::min<int64_t>(opts->splits, nkb)
                                                   : choose_splits(tiles, nkb, sms);
     return decode_ws_bytes(M, N, K, splits);
@@ -347,7 +347,7 @@ fp8rl_status fp8rl_gemm_fwd_ex(const uint8_t* qx, const float* sx, const uint8_t
     t.B = qw; t.sb = sw; t.sb_kb = 1; t.sb_r = K / 128; t.b_mode = SCALE_BLOCK;
     t.c = y; t.ldc = N;
     t.R1 = M; t.R2 = N; t.Kr = K;
-    return run_tiled(t, opts ? opts->grid : 0, sms, stream);
+    return run_tiled(t, opts ? opts->grid : 0, opts ? opts->tile_n : 0, sms, stream);
 }
 
 fp8rl_status fp8rl_gemm_fwd(const uint8_t* qx, const float* sx, const uint8_t* qw, const float* sw,
@@ -376,7 +376,7 @@ fp8rl_status fp8rl_gemm_dgrad(const uint8_t* qdy, const float* sdy, const uint8_
     t.B = qwT; t.sb = sw; t.sb_kb = K / 128; t.sb_r = 1; t.b_mode = SCALE_BLOCK;
     t.c = dx; t.ldc = K;
     t.R1 = M; t.R2 = K; t.Kr = N;
-    return run_tiled(t, 0, sms, stream);
+    return run_tiled(t, 0, 0, sms, stream);
 }
 
 fp8rl_status fp8rl_gemm_wgrad(const uint8_t* qdyT, const float* sdyT, const uint8_t* qxT,
@@ -399,7 +399,7 @@ fp8rl_status fp8rl_gemm_wgrad(const uint8_t* qdyT, const float* sdyT, const uint
     t.B = qxT; t.sb = sxT; t.sb_kb = K; t.sb_r = 0; t.b_mode = SCALE_ROW;
     t.c = dw; t.ldc = K;
     t.R1 = N; t.R2 = K; t.Kr = M;
-    return run_tiled(t, 0, sms, stream);
+    return run_tiled(t, 0, 0, sms, stream);
 }
 
 // ---------------------------------------------------------------- no-allocation decode
@@ -419,7 +419,7 @@ fp8rl_status fp8rl_gemm_fwd_decode_noalloc(const uint8_t* qx, const float* sx, c
     int sms = 0;
     fp8rl_status e = current_device(&sms);
     if (e != FP8RL_OK) return e;
-    const int64_t tiles = (N + 127) / 128;
+    const int64_t tiles = decode_tiles(M, N);
     const int splits = choose_splits(tiles, K / 128, sms);
     const size_t need = decode_ws_bytes(M, N, K, splits);
     const size_t have = noalloc_scratch_bytes();

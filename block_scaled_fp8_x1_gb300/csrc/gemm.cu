@@ -10,12 +10,18 @@
 //           P_kb = sum_{k in block kb} A[r1, k] * B[r2, k]      (E4M3 x E4M3, FP32)
 // with A [R1, Kr] and B [R2, Kr] stored K-major (reduction dimension contiguous).
 //
-// Structure (one CTA of 320 threads per SM, persistent over work items):
-//   warp 0      TMA producer: 128x128 A tile and BNx128 B tile per K-block into a
-//               STAGES-deep shared-memory ring (128-byte swizzle).
-//   warp 1      allocates TMEM and issues, per K-block, four tcgen05.mma (K = 32 each)
-//               into one of two TMEM partial-sum buffers (fresh accumulate per block).
-//   warps 2-9   epilogue: per K-block, load the 128 x BN FP32 partial from TMEM, release
+// Structure (one CTA of 384 threads per SM, persistent over work items):
+//   warp 0      copies: lane 0 issues the TMA loads of the 128x128 A tile and the BNx128
+//               B tile of each K-block into a STAGES-deep shared-memory ring (128-byte
+//               swizzle); all 32 lanes copy the K-block's scales (cp.async) into an
+//               8-slot scale ring that the epilogue releases, so no scale load sits on the
+//               epilogue's critical path.
+//   warp 1      allocates all 512 TMEM columns and issues, per K-block, four tcgen05.mma
+//               (K = 32 each) into one of 512/BN partial-sum buffers (fresh accumulate per
+//               block), so the tensor pipe runs up to 512/BN - 1 blocks ahead of the
+//               epilogue.
+//   warps 2-3   idle (they complete warpgroup 0, whose registers go to the epilogue).
+//   warps 4-11  epilogue: per K-block, load the 128 x BN FP32 partial from TMEM, release
 //               the buffer, and promote it into FP32 registers with the block's scales
 //               ("per-block scale promotion"); finally round to BF16 and store, or, in
 //               the split-K form, store FP32 partials and let the last CTA of a tile sum
@@ -39,30 +45,24 @@ struct WorkItem {
     int split;     // split-K: slice index
 };
 
+// Items are (output tile, reduction slice) pairs; slices of one tile are adjacent items.
+// Tiles follow a grouped order: GROUP m-tiles share each sweep over the n-tiles, so the
+// CTAs running at the same time reuse the same A rows and B columns through L2.
 __device__ __forceinline__ WorkItem work_item(const GemmParams& p, int item) {
     WorkItem w;
-    if (p.splits <= 0) {
-        // tiled: grouped order, GROUP m-tiles share each sweep over the n-tiles
-        constexpr int GROUP = 16;
-        const int per_group = GROUP * p.n_tiles;
-        const int g = item / per_group;
-        const int first_m = g * GROUP;
-        const int gm = min(GROUP, p.m_tiles - first_m);
-        const int r = item - g * per_group;
-        w.mt = first_m + r % gm;
-        w.nt = r / gm;
-        w.kb_begin = 0;
-        w.kb_end = p.nkb;
-        w.tile = 0;
-        w.split = 0;
-    } else {
-        w.tile = item / p.splits;
-        w.split = item - w.tile * p.splits;
-        w.mt = w.tile;
-        w.nt = 0;
-        w.kb_begin = (int)(((int64_t)w.split * p.nkb) / p.splits);
-        w.kb_end = (int)(((int64_t)(w.split + 1) * p.nkb) / p.splits);
-    }
+    const int splits = p.splits > 1 ? p.splits : 1;
+    w.tile = item / splits;
+    w.split = item - w.tile * splits;
+    constexpr int GROUP = 16;
+    const int per_group = GROUP * p.n_tiles;
+    const int g = w.tile / per_group;
+    const int first_m = g * GROUP;
+    const int gm = min(GROUP, p.m_tiles - first_m);
+    const int r = w.tile - g * per_group;
+    w.mt = first_m + r % gm;
+    w.nt = r / gm;
+    w.kb_begin = (int)(((int64_t)w.split * p.nkb) / splits);
+    w.kb_end = (int)(((int64_t)(w.split + 1) * p.nkb) / splits);
     return w;
 }
 
@@ -70,42 +70,53 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-template <int BN>
+// Shared-memory plan of one CTA.
+template <int BN, int STAGES>
 struct GemmSmem {
-    static constexpr int A_BYTES = 128 * 128;
-    static constexpr int B_BYTES = BN * 128;
+    static constexpr int A_BYTES = 128 * 128;                 // one 128x128 E4M3 tile of A
+    static constexpr int B_BYTES = BN * 128;                  // one BNx128 E4M3 tile of B
+    static constexpr int NS = 8;                              // scale-ring slots
+    static constexpr int SLOT = 128 + BN;                     // floats: A scales, B scales
+    static constexpr int RING_BYTES = NS * SLOT * 4;
+    static constexpr int NTB = 512 / BN;                      // TMEM partial-sum buffers
+    static constexpr int NBARS = 2 * STAGES + 2 * NTB + 2 * NS + 1;
+    static constexpr size_t BYTES = 1024 /* alignment slack */ + (size_t)STAGES * (A_BYTES + B_BYTES) +
+                                    RING_BYTES + NBARS * 8 + 16;
 };
 
-constexpr int kGemmThreads = 320;
+constexpr int kGemmThreads = 384;
 
-template <int BN, int A_MODE, int B_MODE, int STAGES, bool DECODE>
+template <int BN, int A_MODE, int B_MODE, int STAGES, bool SPLITK>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_bs(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const GemmParams p) {
-    constexpr int A_BYTES = GemmSmem<BN>::A_BYTES;
-    constexpr int B_BYTES = GemmSmem<BN>::B_BYTES;
+    using S = GemmSmem<BN, STAGES>;
     constexpr int HALF = BN / 2;      // columns per epilogue thread
-    constexpr int NCH = HALF / 16;    // 16-column TMEM loads per K-block
-    constexpr uint32_t TMEM_COLS = 2 * BN;
+    constexpr int GRP = HALF >= 64 ? 64 : 32;   // TMEM columns loaded per wait
+    constexpr int NG = HALF / GRP;                // waits per K-block
+    constexpr int NS = S::NS;
+    constexpr int NTB = S::NTB;
+    constexpr uint32_t TMEM_COLS = 512;
     constexpr uint32_t IDESC = idesc_e4m3_f32(128, BN);
-    static_assert(HALF % 32 == 0, "BN must be a multiple of 64");
-    static_assert(kGemmThreads == 320, "2 role warps + 8 epilogue warps");
+    static_assert(HALF % GRP == 0 && HALF >= 32, "BN must be 64, 128 or 256");
+    static_assert(B_MODE == SCALE_ROW || BN >= 128, "block scales of B need whole 128-column blocks");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
-    uint8_t* sB = smem + STAGES * A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+    uint8_t* sB = smem + STAGES * S::A_BYTES;
+    float* ring = reinterpret_cast<float*>(sB + STAGES * S::B_BYTES);   // [NS][SLOT]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ring) + S::RING_BYTES);
     uint64_t* full_bar = bars;                 // [STAGES] TMA -> MMA
     uint64_t* empty_bar = bars + STAGES;       // [STAGES] MMA -> TMA
-    uint64_t* tfull_bar = bars + 2 * STAGES;   // [2] MMA -> epilogue
-    uint64_t* tempty_bar = tfull_bar + 2;      // [2] epilogue -> MMA
-    uint64_t* drain_bar = tempty_bar + 2;      // [1] MMA completion at exit
+    uint64_t* tfull_bar = bars + 2 * STAGES;   // [NTB] MMA -> epilogue
+    uint64_t* tempty_bar = tfull_bar + NTB;    // [NTB] epilogue -> MMA
+    uint64_t* sfull_bar = tempty_bar + NTB;    // [NS] scale copies -> epilogue
+    uint64_t* sempty_bar = sfull_bar + NS;     // [NS] epilogue -> scale copies
+    uint64_t* drain_bar = sempty_bar + NS;     // [1] MMA completion at exit
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* last_flag = reinterpret_cast<int*>(tmem_slot + 2);
-    // [8 warps][HALF] column scales, 16-byte aligned for vector reads
-    float* bvec = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~uintptr_t(15));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -115,9 +126,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
         }
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < NTB; ++t) {
             mbar_init(smem_u32(&tfull_bar[t]), 1);
             mbar_init(smem_u32(&tempty_bar[t]), 8);
+        }
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(smem_u32(&sfull_bar[s]), 32);
+            mbar_init(smem_u32(&sempty_bar[s]), 8);
         }
         mbar_init(smem_u32(drain_bar), 1);
         *abort_flag = 0;
@@ -135,47 +150,87 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            const uint64_t pol_a = (p.splits > 0) ? l2_policy_evict_first() : l2_policy_evict_last();
-            const uint64_t pol_b = l2_policy_evict_last();
-            uint32_t it = 0;
-            bool ok = true;
-            for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
-                const WorkItem w = work_item(p, item);
-                for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
-                    const uint32_t s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1;
-                    if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, p.timeout_ns, abort_flag)) {
-                        ok = false;
-                        break;
+    // Registers: launched at 168 per thread (384 x 168 = 64512); warpgroup 0 (copy, MMA and
+    // two idle warps) drops to REG_LO, the two epilogue warpgroups rise to REG_HI.
+    constexpr uint32_t REG_LO = 40, REG_HI = 232;
+    static_assert(128 * REG_LO + 256 * REG_HI <= 384 * 168, "register split");
+    if (warp < 4) {
+      warpgroup_reg_dealloc<REG_LO>();
+      if (warp == 0) {
+        // ------------------------------------------------------------ copies (whole warp)
+        // lane 0: TMA tiles of A and B; all lanes: this K-block's scales into the ring.
+        // split-K (decode) streams the weights (B) once: let them leave L2 first
+        const uint64_t pol_a = l2_policy_evict_last();
+        const uint64_t pol_b = SPLITK ? l2_policy_evict_first() : l2_policy_evict_last();
+        uint32_t it = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
+            const WorkItem w = work_item(p, item);
+            const int64_t m0 = (int64_t)w.mt * 128;
+            const int64_t n0 = (int64_t)w.nt * BN;
+            for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
+                const uint32_t s = it % STAGES;
+                bool good = true;
+                if (lane == 0) {
+                    good = mbar_wait(smem_u32(&empty_bar[s]), ((it / STAGES) & 1) ^ 1, p.timeout_ns, abort_flag);
+                    if (good) {
+                        const uint32_t fb = smem_u32(&full_bar[s]);
+                        mbar_arrive_expect_tx(fb, S::A_BYTES + S::B_BYTES);
+                        tma_load_2d(smem_u32(sA + s * S::A_BYTES), &tmA, fb, kb * 128, (int)m0, pol_a);
+                        tma_load_2d(smem_u32(sB + s * S::B_BYTES), &tmB, fb, kb * 128, (int)n0, pol_b);
                     }
-                    const uint32_t fb = smem_u32(&full_bar[s]);
-                    mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
-                    tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, fb, kb * 128, w.mt * 128, pol_a);
-                    tma_load_2d(smem_u32(sB + s * B_BYTES), &tmB, fb, kb * 128, w.nt * BN, pol_b);
                 }
+                if (!__shfl_sync(0xffffffffu, good ? 1 : 0, 0)) { ok = false; break; }
+                const uint32_t ss = it % NS;
+                good = mbar_wait(smem_u32(&sempty_bar[ss]), ((it / NS) & 1) ^ 1, p.timeout_ns, abort_flag);
+                if (!__all_sync(0xffffffffu, good)) { ok = false; break; }
+                const uint32_t slot = smem_u32(ring + ss * S::SLOT);
+                if (A_MODE == SCALE_ROW) {
+                    const float* src = p.sa + (int64_t)kb * p.sa_kb;
+                    #pragma unroll 1
+                    for (int i = lane; i < 128; i += 32) {
+                        const bool v = m0 + i < p.R1;
+                        cp_async_4(slot + 4 * i, src + (v ? m0 + i : 0), v ? 4u : 0u);
+                    }
+                } else if (lane == 0) {
+                    cp_async_4(slot, p.sa + (int64_t)w.mt * p.sa_r + (int64_t)kb * p.sa_kb, 4u);
+                }
+                if (B_MODE == SCALE_ROW) {
+                    const float* src = p.sb + (int64_t)kb * p.sb_kb;
+                    #pragma unroll 1
+                    for (int j = lane; j < BN; j += 32) {
+                        const bool v = n0 + j < p.R2;
+                        cp_async_4(slot + 4 * (128 + j), src + (v ? n0 + j : 0), v ? 4u : 0u);
+                    }
+                } else if (lane < BN / 128) {
+                    const int64_t c = n0 + lane * 128;
+                    const bool v = c < p.R2;
+                    cp_async_4(slot + 4 * (128 + lane), p.sb + (v ? (c / 128) * p.sb_r : 0) + (int64_t)kb * p.sb_kb,
+                               v ? 4u : 0u);
+                }
+                cp_async_arrive(smem_u32(&sfull_bar[ss]));
             }
-            // Drain: every issued copy must land before the CTA can exit.
+        }
+        // Drain: every issued copy lands before the CTA can exit.
+        cp_async_wait_all();
+        if (lane == 0) {
             const uint32_t n_out = it < STAGES ? it : STAGES;
             for (uint32_t j = it - n_out; j < it; ++j) {
                 volatile int no_abort = 0;
                 mbar_wait(smem_u32(&full_bar[j % STAGES]), (j / STAGES) & 1, p.timeout_ns, &no_abort);
             }
         }
-    } else if (warp == 1) {
+      } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t it = 0, acc_it = 0;
+            uint32_t it = 0;
             bool ok = true;
             const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
             for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
                 const WorkItem w = work_item(p, item);
-                for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it, ++acc_it) {
-                    const uint32_t ts = acc_it & 1;
-                    const uint32_t tph = (acc_it >> 1) & 1;
-                    if (!mbar_wait(smem_u32(&tempty_bar[ts]), tph ^ 1, p.timeout_ns, abort_flag)) {
+                for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
+                    const uint32_t ts = it % NTB;
+                    if (!mbar_wait(smem_u32(&tempty_bar[ts]), ((it / NTB) & 1) ^ 1, p.timeout_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -187,8 +242,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t d = tmem_base + ts * BN;
-                    const uint64_t da = sdesc_kmajor_sw128(a_base + s * A_BYTES);
-                    const uint64_t db = sdesc_kmajor_sw128(b_base + s * B_BYTES);
+                    const uint64_t da = sdesc_kmajor_sw128(a_base + s * S::A_BYTES);
+                    const uint64_t db = sdesc_kmajor_sw128(b_base + s * S::B_BYTES);
                     #pragma unroll
                     for (int k = 0; k < 4; ++k)  // 32-byte steps inside the 128-byte row
                         mma_f8(d, da + 2 * k, db + 2 * k, IDESC, k > 0 ? 1u : 0u);
@@ -201,106 +256,108 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             volatile int no_abort = 0;
             mbar_wait(smem_u32(drain_bar), 0, p.timeout_ns, &no_abort);
         }
+      }
     } else {
+        warpgroup_reg_alloc<REG_HI>();
         // ------------------------------------------------------------ epilogue warps
         // After an abort every warp keeps walking the same items and blocks (no waits, no
         // TMEM loads) so that all of them reach the same named barriers.
-        const int ew = warp - 2;            // 0..7
+        const int ew = warp - 4;            // 0..7
         const int quad = warp & 3;          // TMEM lane quadrant this warp may access
         const int col_base = (ew >> 2) * HALF;
         const int row_local = quad * 32 + lane;
         const uint32_t t_lane = (uint32_t)(quad * 32) << 16;
-        float* my_bvec = bvec + ew * HALF;
         uint32_t acc_it = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
             const WorkItem w = work_item(p, item);
             const int64_t r1 = (int64_t)w.mt * 128 + row_local;
-            const int64_t r1c = r1 < p.R1 ? r1 : p.R1 - 1;
             const int64_t n0 = (int64_t)w.nt * BN + col_base;  // first column of this thread
-            float acc[HALF];
+            float2 acc[HALF / 2];
             #pragma unroll
-            for (int c = 0; c < HALF; ++c) acc[c] = 0.0f;
+            for (int c = 0; c < HALF / 2; ++c) acc[c] = make_float2(0.0f, 0.0f);
 
             for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++acc_it) {
                 if (!ok) continue;
-                // scales of this K-block
-                float fa;
-                if (A_MODE == SCALE_ROW) fa = __ldg(p.sa + (int64_t)kb * p.sa_kb + r1c);
-                else fa = __ldg(p.sa + (int64_t)w.mt * p.sa_r + (int64_t)kb * p.sa_kb);
-                float fb_uniform = 1.0f;
-                if (B_MODE == SCALE_BLOCK) {
-                    const int64_t nb = n0 < p.R2 ? n0 / 128 : 0;
-                    fb_uniform = __ldg(p.sb + nb * p.sb_r + (int64_t)kb * p.sb_kb);
-                } else {
-                    // this warp's HALF column scales -> its own shared slice
-                    __syncwarp();
-                    #pragma unroll
-                    for (int c = lane; c < HALF; c += 32)
-                        my_bvec[c] = (n0 + c < p.R2) ? __ldg(p.sb + (int64_t)kb * p.sb_kb + n0 + c) : 0.0f;
-                    __syncwarp();
-                }
-                const uint32_t ts = acc_it & 1;
-                const uint32_t tph = (acc_it >> 1) & 1;
-                const bool got = mbar_wait(smem_u32(&tfull_bar[ts]), tph, p.timeout_ns, abort_flag);
+                const uint32_t ss = acc_it % NS;
+                const uint32_t ts = acc_it % NTB;
+                bool got = mbar_wait(smem_u32(&sfull_bar[ss]), (acc_it / NS) & 1, p.timeout_ns, abort_flag);
+                got = got && mbar_wait(smem_u32(&tfull_bar[ts]), (acc_it / NTB) & 1, p.timeout_ns, abort_flag);
                 ok = __all_sync(0xffffffffu, got);
                 if (!ok) continue;
                 tc_fence_after();
-                const float f = fa * fb_uniform;
+                const float* sl = ring + ss * S::SLOT;
+                const float fa = (A_MODE == SCALE_ROW) ? sl[row_local] : sl[0];
+                const float f = (B_MODE == SCALE_BLOCK) ? fa * sl[128 + (col_base >> 7)] : fa;
+                const float2 f2 = make_float2(f, f);
+                const float* sbv = sl + 128 + col_base;
+                const uint32_t tbase = tmem_base + t_lane + ts * BN + col_base;
+                // 64 columns (two 32-column loads) per wait: two round trips per K-block
                 #pragma unroll
-                for (int ch = 0; ch < NCH; ++ch) {
-                    uint32_t r[16];
-                    tmem_ld_32x32b_x16(tmem_base + t_lane + ts * BN + col_base + ch * 16, r);
-                    tmem_ld_wait();
-                    if (ch == NCH - 1) {
-                        // partial fully in registers: hand the TMEM buffer back
+                for (int g = 0; g < NG; ++g) {
+                    uint32_t ra[32], rb[32];
+                    tmem_ld_32x32b_x32(tbase + g * GRP, ra);
+                    if (GRP == 64) tmem_ld_32x32b_x32(tbase + g * GRP + 32, rb);
+                    tmem_ld_wait(ra);
+                    if (GRP == 64) tmem_ld_tie(rb);
+                    if (g == NG - 1) {
+                        // the whole partial is in registers: hand the TMEM buffer back
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[ts]));
                     }
-                    if (B_MODE == SCALE_BLOCK) {
-                        #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            acc[ch * 16 + j] = fmaf(__uint_as_float(r[j]), f, acc[ch * 16 + j]);
-                    } else {
-                        #pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
-                            const float4 sbv = *reinterpret_cast<const float4*>(my_bvec + ch * 16 + j);
-                            acc[ch * 16 + j + 0] = fmaf(__uint_as_float(r[j + 0]), fa * sbv.x, acc[ch * 16 + j + 0]);
-                            acc[ch * 16 + j + 1] = fmaf(__uint_as_float(r[j + 1]), fa * sbv.y, acc[ch * 16 + j + 1]);
-                            acc[ch * 16 + j + 2] = fmaf(__uint_as_float(r[j + 2]), fa * sbv.z, acc[ch * 16 + j + 2]);
-                            acc[ch * 16 + j + 3] = fmaf(__uint_as_float(r[j + 3]), fa * sbv.w, acc[ch * 16 + j + 3]);
+                    #pragma unroll
+                    for (int h = 0; h < GRP / 32; ++h) {
+                        uint32_t(&r)[32] = h ? rb : ra;
+                        const int c0 = g * GRP + h * 32;   // first column of these 32
+                        if (B_MODE == SCALE_BLOCK) {
+                            #pragma unroll
+                            for (int j = 0; j < 32; j += 2)
+                                acc[(c0 + j) / 2] = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                                                               f2, acc[(c0 + j) / 2]);
+                        } else {
+                            #pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                const float4 b4 = *reinterpret_cast<const float4*>(sbv + c0 + j);
+                                const float2 s01 = __fmul2_rn(f2, make_float2(b4.x, b4.y));
+                                const float2 s23 = __fmul2_rn(f2, make_float2(b4.z, b4.w));
+                                acc[(c0 + j) / 2] = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                                                               s01, acc[(c0 + j) / 2]);
+                                acc[(c0 + j) / 2 + 1] = __ffma2_rn(make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                                                                   s23, acc[(c0 + j) / 2 + 1]);
+                            }
                         }
                     }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sempty_bar[ss]));
             }
 
-            if (!DECODE) {
-                // ---- tiled: BF16 row segment of this thread
+            if (!SPLITK || p.splits <= 1) {
+                // ---- whole reduction in this CTA: BF16 row segment of this thread
                 if (ok && r1 < p.R1 && n0 < p.R2) {
                     uint16_t* dst = p.c + r1 * p.ldc + n0;
                     #pragma unroll
                     for (int c = 0; c < HALF; c += 8) {
                         uint4 v;
-                        v.x = pack_bf16x2(acc[c + 0], acc[c + 1]);
-                        v.y = pack_bf16x2(acc[c + 2], acc[c + 3]);
-                        v.z = pack_bf16x2(acc[c + 4], acc[c + 5]);
-                        v.w = pack_bf16x2(acc[c + 6], acc[c + 7]);
+                        v.x = pack_bf16x2(acc[c / 2 + 0].x, acc[c / 2 + 0].y);
+                        v.y = pack_bf16x2(acc[c / 2 + 1].x, acc[c / 2 + 1].y);
+                        v.z = pack_bf16x2(acc[c / 2 + 2].x, acc[c / 2 + 2].y);
+                        v.w = pack_bf16x2(acc[c / 2 + 3].x, acc[c / 2 + 3].y);
                         *reinterpret_cast<uint4*>(dst + c) = v;
                     }
                 }
-            } else if (p.splits == 1) {
-                // ---- decode, no split: transposed BF16 store C[r2][r1]
-                if (ok && r1 < p.R1) {
-                    #pragma unroll
-                    for (int c = 0; c < HALF; ++c)
-                        if (n0 + c < p.R2) p.c[(n0 + c) * p.ldc + r1] = (uint16_t)(pack_bf16x2(acc[c], 0.0f) & 0xFFFFu);
-                }
             } else {
-                // ---- decode, split-K: FP32 partial, then the last CTA of the tile reduces
-                float* part = p.ws + ((int64_t)w.tile * p.splits + w.split) * (int64_t)(BN * 128);
+                // ---- split-K: FP32 partial of this slice, then the last CTA of the tile sums
+                // the slices in slice order (deterministic) and stores BF16.  Partials are laid
+                // out [tile][slice][BN/4][128 rows][4] so that a warp's float4 accesses cover
+                // 32 consecutive rows: fully coalesced 512-byte transactions.
+                float4* part = reinterpret_cast<float4*>(p.ws) +
+                               ((int64_t)w.tile * p.splits + w.split) * (int64_t)(BN * 32) +
+                               (int64_t)(col_base / 4) * 128 + row_local;
                 #pragma unroll
-                for (int c = 0; c < HALF; ++c) __stcg(part + (int64_t)(col_base + c) * 128 + row_local, acc[c]);
+                for (int c = 0; c < HALF; c += 4)
+                    __stcg(part + (c / 4) * 128, make_float4(acc[c / 2].x, acc[c / 2].y, acc[c / 2 + 1].x, acc[c / 2 + 1].y));
                 __threadfence();
                 named_bar_sync(1, 256);
                 if (ew == 0 && lane == 0) {
@@ -310,14 +367,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 named_bar_sync(1, 256);
                 if (*last_flag) {
                     __threadfence();
-                    const float* tile_ws = p.ws + (int64_t)w.tile * p.splits * (int64_t)(BN * 128);
-                    for (int c = 0; c < HALF; ++c) {
-                        const int64_t col = col_base + c;
-                        float sum = 0.0f;
-                        for (int sp = 0; sp < p.splits; ++sp)
-                            sum += __ldcg(tile_ws + (int64_t)sp * (BN * 128) + col * 128 + row_local);
-                        if (r1 < p.R1 && col < p.R2)
-                            p.c[col * p.ldc + r1] = (uint16_t)(pack_bf16x2(sum, 0.0f) & 0xFFFFu);
+                    const float4* tile_ws = reinterpret_cast<const float4*>(p.ws) +
+                                            (int64_t)w.tile * p.splits * (int64_t)(BN * 32) +
+                                            (int64_t)(col_base / 4) * 128 + row_local;
+                    #pragma unroll 1
+                    for (int c0 = 0; c0 < HALF; c0 += 32) {
+                        float4 sum[8];
+                        #pragma unroll
+                        for (int j = 0; j < 8; ++j) sum[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        // the slices in slice order, two slices' loads in flight
+                        int sp = 0;
+                        #pragma unroll 1
+                        for (; sp + 2 <= p.splits; sp += 2) {
+                            float4 v[2][8];
+                            #pragma unroll
+                            for (int q = 0; q < 2; ++q)
+                                #pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    v[q][j] = __ldcg(tile_ws + (int64_t)(sp + q) * (BN * 32) + (c0 / 4 + j) * 128);
+                            #pragma unroll
+                            for (int q = 0; q < 2; ++q)
+                                #pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    sum[j].x += v[q][j].x; sum[j].y += v[q][j].y;
+                                    sum[j].z += v[q][j].z; sum[j].w += v[q][j].w;
+                                }
+                        }
+                        #pragma unroll 1
+                        for (; sp < p.splits; ++sp) {
+                            float4 v[8];
+                            #pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                v[j] = __ldcg(tile_ws + (int64_t)sp * (BN * 32) + (c0 / 4 + j) * 128);
+                            #pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                sum[j].x += v[j].x; sum[j].y += v[j].y;
+                                sum[j].z += v[j].z; sum[j].w += v[j].w;
+                            }
+                        }
+                        if (r1 < p.R1 && n0 + c0 < p.R2) {
+                            uint16_t* dst = p.c + r1 * p.ldc + n0 + c0;
+                            #pragma unroll
+                            for (int j = 0; j < 8; j += 2) {
+                                uint4 v;
+                                v.x = pack_bf16x2(sum[j].x, sum[j].y);
+                                v.y = pack_bf16x2(sum[j].z, sum[j].w);
+                                v.z = pack_bf16x2(sum[j + 1].x, sum[j + 1].y);
+                                v.w = pack_bf16x2(sum[j + 1].z, sum[j + 1].w);
+                                *reinterpret_cast<uint4*>(dst + 4 * j) = v;
+                            }
+                        }
                     }
                     named_bar_sync(1, 256);
                     if (ew == 0 && lane == 0) {
@@ -342,17 +441,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // ------------------------------------------------------------------------------------
 // Host side
 // ------------------------------------------------------------------------------------
-template <int BN, int STAGES>
-constexpr size_t gemm_smem_bytes() {
-    return 1024 + (size_t)STAGES * (GemmSmem<BN>::A_BYTES + GemmSmem<BN>::B_BYTES) +
-           (2 * STAGES + 5) * 8 + 16 + 16 + 8 * (BN / 2) * 4 + 64;
-}
 
-template <int BN, int A_MODE, int B_MODE, int STAGES, bool DECODE>
+template <int BN, int A_MODE, int B_MODE, int STAGES, bool SPLITK>
 static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
                             int grid, cudaStream_t st) {
-    auto kern = k_gemm_bs<BN, A_MODE, B_MODE, STAGES, DECODE>;
-    constexpr size_t smem = gemm_smem_bytes<BN, STAGES>();
+    auto kern = k_gemm_bs<BN, A_MODE, B_MODE, STAGES, SPLITK>;
+    constexpr size_t smem = GemmSmem<BN, STAGES>::BYTES;
     static_assert(smem <= 227 * 1024, "shared memory budget");
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -361,16 +455,18 @@ static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const 
 }
 
 cudaError_t launch_gemm_tiled(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                              int b_mode, int grid, cudaStream_t st) {
+                              int b_mode, int bn, int grid, cudaStream_t st) {
+    if (bn == 128) {
+        if (b_mode == SCALE_BLOCK) return launch_t<128, SCALE_ROW, SCALE_BLOCK, 6, false>(ta, tb, p, grid, st);
+        return launch_t<128, SCALE_ROW, SCALE_ROW, 6, false>(ta, tb, p, grid, st);
+    }
     if (b_mode == SCALE_BLOCK) return launch_t<256, SCALE_ROW, SCALE_BLOCK, 4, false>(ta, tb, p, grid, st);
     return launch_t<256, SCALE_ROW, SCALE_ROW, 4, false>(ta, tb, p, grid, st);
 }
 
 cudaError_t launch_gemm_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                               int bn, int grid, cudaStream_t st) {
-    if (bn == 64) return launch_t<64, SCALE_BLOCK, SCALE_ROW, 8, true>(ta, tb, p, grid, st);
-    if (bn == 128) return launch_t<128, SCALE_BLOCK, SCALE_ROW, 6, true>(ta, tb, p, grid, st);
-    return launch_t<256, SCALE_BLOCK, SCALE_ROW, 4, true>(ta, tb, p, grid, st);
+                               int grid, cudaStream_t st) {
+    return launch_t<256, SCALE_ROW, SCALE_BLOCK, 4, true>(ta, tb, p, grid, st);
 }
 
 // ------------------------------------------------------------------------------------

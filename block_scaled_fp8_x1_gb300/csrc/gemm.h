@@ -5,7 +5,16 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/fp8rl.h"
+
 namespace fp8rl {
+
+// cuTensorMapEncodeTiled, looked up once through the runtime's driver entry point.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
 
 // How an operand's per-K-block scale is indexed.
 enum ScaleMode : int {
@@ -19,32 +28,33 @@ struct GemmParams {
     int64_t sa_kb, sa_r;
     const float* sb;         // scales of B (rows r2)
     int64_t sb_kb, sb_r;
-    uint16_t* c;             // tiled: c[r1*ldc + r2];  split-K form: c[r2*ldc + r1]
+    uint16_t* c;             // c[r1*ldc + r2]
     int64_t ldc;
-    float* ws;               // split-K partials [tiles][splits][BN][128]
+    float* ws;               // split-K partials [tiles][splits][BN/4][128 rows][4]
     unsigned int* counters;  // split-K arrival counters [tiles], zero between calls
-    int splits;              // 0: tiled form; >= 1: decode (split-K) form
+    int splits;              // reduction slices per output tile (<= 1: none)
     int m_tiles, n_tiles, nkb;
     int num_items;
     uint64_t timeout_ns;
 };
 
 cudaError_t launch_gemm_tiled(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                              int b_mode, int grid, cudaStream_t st);
+                              int b_mode, int bn, int grid, cudaStream_t st);
 cudaError_t launch_gemm_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                               int bn, int grid, cudaStream_t st);
+                               int grid, cudaStream_t st);
 cudaError_t launch_debug_wait_timeout(uint64_t timeout_ns, cudaStream_t st);
 
 // quantize.cu
 cudaError_t launch_quant_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
                                float* s, int num_sms, cudaStream_t st);
 cudaError_t launch_quant_dual(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
-                              float* s, uint8_t* qT, float* sT, cudaStream_t st);
+                              float* s, uint8_t* qT, float* sT, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_silu_mul_quant(const uint16_t* gu, int64_t M, int64_t I, uint8_t* q, float* s,
-                                  uint8_t* qT, float* sT, cudaStream_t st);
+                                  uint8_t* qT, float* sT, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M,
                                  int64_t K, uint8_t* q, float* s, uint8_t* qT, float* sT,
-                                 float* rstd, cudaStream_t st);
+                                 float* rstd, uint64_t timeout_ns, cudaStream_t st);
+fp8rl_status read_and_clear_quant_status();
 cudaError_t launch_quant_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
                                  float* s, uint8_t* qT, cudaStream_t st);
 cudaError_t launch_debug_e4m3(const float* in, uint8_t* out, int64_t n, cudaStream_t st);

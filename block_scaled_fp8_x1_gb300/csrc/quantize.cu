@@ -89,6 +89,7 @@ struct PanelArgs {
     uint8_t* qT;            // 128x1 codes, transposed: qT[K][M]
     float* sT;              // scales sT[M/128][K]
     int tiles_per_cta;      // 128-column sub-tiles handled by one CTA
+    uint64_t timeout_ns;    // bound of every wait on a TMA copy
 };
 
 // Accurate sum of squares: binary32 pairs (hi, lo) updated with the exact two-sum, so
@@ -110,9 +111,13 @@ __device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
     return F2{s, e};
 }
 
+// One thread's 8 rows x 8 columns of the staged tile -> BF16 words of y (the value that is
+// quantized): x itself, bf16((x*rstd)*gamma), or bf16(silu(g)*u).  The stage holds the
+// 128x128 BF16 tile row-major (256 bytes per row); SiLU-mul stages the up tile after it.
 template <int PRO>
-__device__ __forceinline__ void load_rows(const PanelArgs& a, int64_t m0, int R0, int64_t k0,
-                                          int C0, const float* s_rstd, uint32_t (&w)[8][4]) {
+__device__ __forceinline__ void rows_from_smem(const uint8_t* stage, const PanelArgs& a, int64_t k0,
+                                               int R0, int C0, const float* s_rstd,
+                                               uint32_t (&w)[8][4]) {
     float gam[8];
     if (PRO == PRO_RMSNORM) {
         const uint4 gv = ldg_nc_v4(a.gamma + k0 + C0);
@@ -121,21 +126,10 @@ __device__ __forceinline__ void load_rows(const PanelArgs& a, int64_t m0, int R0
         gam[4] = bf16_lo(gv.z); gam[5] = bf16_hi(gv.z);
         gam[6] = bf16_lo(gv.w); gam[7] = bf16_hi(gv.w);
     }
-    uint4 v[8], u[8];
     #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int64_t m = m0 + R0 + i;
-        v[i] = make_uint4(0, 0, 0, 0);
-        u[i] = make_uint4(0, 0, 0, 0);
-        if (m < a.M) {
-            v[i] = ldg_nc_v4(a.x + m * a.ldx + k0 + C0);
-            if (PRO == PRO_SILU) u[i] = ldg_nc_v4(a.x + m * a.ldx + a.K + k0 + C0);
-        }
-    }
-    #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t xv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-        const uint32_t uv[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + (R0 + i) * 256 + C0 * 2);
+        const uint32_t xv[4] = {v.x, v.y, v.z, v.w};
         if (PRO == PRO_COPY) {
             #pragma unroll
             for (int j = 0; j < 4; ++j) w[i][j] = xv[j];
@@ -148,6 +142,8 @@ __device__ __forceinline__ void load_rows(const PanelArgs& a, int64_t m0, int R0
                 w[i][j] = pack_bf16x2(y0, y1);
             }
         } else {  // SILU: h = bf16(silu(g) * u), silu(g) = g / (1 + exp(-g))
+            const uint4 u = *reinterpret_cast<const uint4*>(stage + 128 * 256 + (R0 + i) * 256 + C0 * 2);
+            const uint32_t uv[4] = {u.x, u.y, u.z, u.w};
             #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float g0 = bf16_lo(xv[j]), g1 = bf16_hi(xv[j]);
@@ -160,8 +156,29 @@ __device__ __forceinline__ void load_rows(const PanelArgs& a, int64_t m0, int R0
     }
 }
 
+// Input stages of the TMA ring (each a 128x128 BF16 tile; SiLU-mul stages gate and up).
+template <int PRO>
+struct PanelStages {
+    static constexpr int NIN = (PRO == PRO_SILU) ? 2 : 1;
+    static constexpr int STAGE_BYTES = NIN * 128 * 128 * 2;
+    static constexpr int STAGES = (PRO == PRO_SILU) ? 3 : 3;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 128;  // + alignment slack
+};
+
+// Each CTA owns one 128-row panel and `tiles_per_cta` consecutive 128-column tiles of it.
+// Thread 0 streams the tiles through a ring of TMA stages in shared memory; all threads
+// pull a tile into registers, and once everyone has it (the first barrier of the tile)
+// thread 0 refills that stage, so copies of the next tiles overlap the current one's math.
+// RMSNorm streams the CTA's tiles twice: pass 1 sums squares, pass 2 quantizes.
 template <int PRO, bool ROW_OUT, bool COL_OUT>
-__global__ void __launch_bounds__(256) k_quant_panel(const PanelArgs a) {
+__global__ void __launch_bounds__(256) k_quant_panel(const __grid_constant__ CUtensorMap tmx,
+                                                     const PanelArgs a) {
+    using PS = PanelStages<PRO>;
+    constexpr int STAGES = PS::STAGES;
+    extern __shared__ uint8_t q_smem_raw[];
+    uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_smem_raw) + 127) & ~uintptr_t(127));
+    __shared__ __align__(8) uint64_t full_bar[STAGES];
+    __shared__ int abort_flag;
     __shared__ __align__(16) uint32_t s_rowmax[64];     // 128 row maxima (BF16 bits)
     __shared__ __align__(16) uint32_t s_colmax[8][64];  // per-warp column maxima
     __shared__ __align__(16) float s_row_s[128], s_row_r[128];
@@ -177,19 +194,50 @@ __global__ void __launch_bounds__(256) k_quant_panel(const PanelArgs a) {
     const int64_t ntiles = a.K / 128;
     const int64_t t_begin = (int64_t)blockIdx.x * a.tiles_per_cta;
     const int64_t t_end = (t_begin + a.tiles_per_cta < ntiles) ? t_begin + a.tiles_per_cta : ntiles;
+    const int n = (int)(t_end - t_begin);
+    const int total = (PRO == PRO_RMSNORM) ? 2 * n : n;   // items streamed through the ring
+
+    if (tid == 0) {
+        for (int st = 0; st < STAGES; ++st) mbar_init(smem_u32(&full_bar[st]), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmx);
+    }
+    __syncthreads();
+    auto issue = [&](int item) {
+        const int st = item % STAGES;
+        const int64_t k0 = (t_begin + item % n) * 128;
+        const uint32_t bar = smem_u32(&full_bar[st]);
+        uint8_t* dst = stages + st * PS::STAGE_BYTES;
+        mbar_arrive_expect_tx(bar, PS::STAGE_BYTES);
+        tma_load_2d(smem_u32(dst), &tmx, bar, (int)k0, (int)m0, 0);
+        if (PRO == PRO_SILU) tma_load_2d(smem_u32(dst + 128 * 128 * 2), &tmx, bar, (int)(a.K + k0), (int)m0, 0);
+    };
+    int issued = 0;
+    if (tid == 0)
+        for (; issued < STAGES && issued < total; ++issued) issue(issued);
+    // every thread waits for item `it`; the decision to stop is made block-wide
+    auto wait_item = [&](int it) -> bool {
+        const bool got = mbar_wait(smem_u32(&full_bar[it % STAGES]), (it / STAGES) & 1, a.timeout_ns, &abort_flag);
+        return !__syncthreads_or(got ? 0 : 1);
+    };
+    bool ok = true;
+    int item = 0;
 
     if (PRO == PRO_RMSNORM) {
         // Pass 1: this CTA's share of every row's sum of squares.
         F2 acc[8];
         #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = F2{0.0f, 0.0f};
-        for (int64_t t = t_begin; t < t_end; ++t) {
+        for (; ok && item < n; ++item) {
+            ok = wait_item(item);
+            if (!ok) break;
+            const uint8_t* stage = stages + (item % STAGES) * PS::STAGE_BYTES;
             uint4 v[8];
             #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int64_t m = m0 + R0 + i;
-                v[i] = (m < a.M) ? ldg_nc_v4(a.x + m * a.ldx + t * 128 + C0) : make_uint4(0, 0, 0, 0);
-            }
+            for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint4*>(stage + (R0 + i) * 256 + C0 * 2);
+            __syncthreads();                              // stage consumed: refill it
+            if (tid == 0 && issued < total) issue(issued++);
             #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const uint32_t xv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
@@ -215,6 +263,7 @@ __global__ void __launch_bounds__(256) k_quant_panel(const PanelArgs a) {
             #pragma unroll
             for (int i = 0; i < 8; ++i) s_part[R0 + i] = acc[i];
         }
+        // Every CTA of the cluster reaches both cluster barriers, also after an abort.
         cg::cluster_group cluster = cg::this_cluster();
         cluster.sync();
         if (tid < 128) {
@@ -229,15 +278,18 @@ __global__ void __launch_bounds__(256) k_quant_panel(const PanelArgs a) {
             const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
             s_rstd[tid] = rstd;
             const int64_t m = m0 + tid;
-            if (a.rstd_out && cluster.block_rank() == 0 && m < a.M) a.rstd_out[m] = rstd;
+            if (ok && a.rstd_out && cluster.block_rank() == 0 && m < a.M) a.rstd_out[m] = rstd;
         }
         __syncthreads();
     }
 
-    for (int64_t t = t_begin; t < t_end; ++t) {
-        const int64_t k0 = t * 128;
+    for (; ok && item < total; ++item) {
+        ok = wait_item(item);
+        if (!ok) break;
+        const int64_t k0 = (t_begin + item % n) * 128;
+        const int64_t t = t_begin + item % n;
         uint32_t w[8][4];
-        load_rows<PRO>(a, m0, R0, k0, C0, s_rstd, w);
+        rows_from_smem<PRO>(stages + (item % STAGES) * PS::STAGE_BYTES, a, k0, R0, C0, s_rstd, w);
 
         if (ROW_OUT) {
             uint32_t pm[4];
@@ -269,7 +321,8 @@ __global__ void __launch_bounds__(256) k_quant_panel(const PanelArgs a) {
             }
             if (half == 0) *reinterpret_cast<uint4*>(&s_colmax[warp][cl * 4]) = make_uint4(cm[0], cm[1], cm[2], cm[3]);
         }
-        __syncthreads();
+        __syncthreads();                                  // stage consumed: refill it
+        if (tid == 0 && issued < total) issue(issued++);
         if (ROW_OUT && tid < 128) {
             const uint32_t mx = reinterpret_cast<const uint16_t*>(s_rowmax)[tid];
             const GroupScale g = make_scale(bf16_bits_amax_to_f32(mx));
@@ -321,6 +374,13 @@ __global__ void __launch_bounds__(256) k_quant_panel(const PanelArgs a) {
                 }
                 stg_v2(a.qT + (k0 + C0 + j) * a.M + m0 + R0, c[0] | (c[1] << 16), c[2] | (c[3] << 16));
             }
+        }
+    }
+    if (tid == 0) {
+        // after an abort: let every issued copy land before the CTA exits
+        for (int j = item; j < issued; ++j) {
+            volatile int no_abort = 0;
+            mbar_wait(smem_u32(&full_bar[j % STAGES]), (j / STAGES) & 1, a.timeout_ns, &no_abort);
         }
     }
     if (PRO == PRO_RMSNORM) {
@@ -423,14 +483,35 @@ cudaError_t launch_quant_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t 
     return cudaGetLastError();
 }
 
+// 2-D tensor map of a BF16 matrix [rows][cols] (row stride ld elements), 128x128 boxes.
+static cudaError_t tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {128u, 128u};
+    cuuint32_t es[2] = {1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int PRO, bool ROW_OUT, bool COL_OUT>
-static cudaError_t launch_panel_t(const PanelArgs& a, int cluster, cudaStream_t st) {
+static cudaError_t launch_panel_t(const PanelArgs& a, int64_t in_cols, int cluster, cudaStream_t st) {
+    CUtensorMap tm;
+    cudaError_t e = tmap_bf16(&tm, a.x, a.M, in_cols, a.ldx);
+    if (e != cudaSuccess) return e;
+    auto kern = k_quant_panel<PRO, ROW_OUT, COL_OUT>;
+    constexpr size_t smem = PanelStages<PRO>::SMEM;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     const int64_t ntiles = a.K / 128;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((ntiles + a.tiles_per_cta - 1) / a.tiles_per_cta),
                        (unsigned)((a.M + 127) / 128), 1);
     cfg.blockDim = dim3(256, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     cfg.numAttrs = 0;
@@ -442,26 +523,31 @@ static cudaError_t launch_panel_t(const PanelArgs& a, int cluster, cudaStream_t 
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, k_quant_panel<PRO, ROW_OUT, COL_OUT>, a);
+    return cudaLaunchKernelEx(&cfg, kern, tm, a);
 }
+
+// Column tiles per CTA for the streaming kernels: enough to keep the TMA ring busy.
+static int stream_tiles_per_cta(int64_t ntiles) { return (int)std::min<int64_t>(ntiles, 4); }
 
 // quantize 1x128 with the transposed 128x1 output (dual), or 128x1 alone
 cudaError_t launch_quant_dual(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
-                              float* s, uint8_t* qT, float* sT, cudaStream_t st) {
+                              float* s, uint8_t* qT, float* sT, uint64_t timeout_ns, cudaStream_t st) {
     PanelArgs a = {};
     a.x = x; a.ldx = ldx; a.M = M; a.K = K; a.q = q; a.s = s; a.qT = qT; a.sT = sT;
-    a.tiles_per_cta = 1;
-    if (q) return launch_panel_t<PRO_COPY, true, true>(a, 0, st);
-    return launch_panel_t<PRO_COPY, false, true>(a, 0, st);
+    a.tiles_per_cta = stream_tiles_per_cta(K / 128);
+    a.timeout_ns = timeout_ns;
+    if (q) return launch_panel_t<PRO_COPY, true, true>(a, K, 0, st);
+    return launch_panel_t<PRO_COPY, false, true>(a, K, 0, st);
 }
 
 cudaError_t launch_silu_mul_quant(const uint16_t* gu, int64_t M, int64_t I, uint8_t* q, float* s,
-                                  uint8_t* qT, float* sT, cudaStream_t st) {
+                                  uint8_t* qT, float* sT, uint64_t timeout_ns, cudaStream_t st) {
     PanelArgs a = {};
     a.x = gu; a.ldx = 2 * I; a.M = M; a.K = I; a.q = q; a.s = s; a.qT = qT; a.sT = sT;
-    a.tiles_per_cta = 1;
-    if (qT) return launch_panel_t<PRO_SILU, true, true>(a, 0, st);
-    return launch_panel_t<PRO_SILU, true, false>(a, 0, st);
+    a.tiles_per_cta = stream_tiles_per_cta(I / 128);
+    a.timeout_ns = timeout_ns;
+    if (qT) return launch_panel_t<PRO_SILU, true, true>(a, 2 * I, 0, st);
+    return launch_panel_t<PRO_SILU, true, false>(a, 2 * I, 0, st);
 }
 
 // Number of CTAs that split one 128-row panel of an RMSNorm along K: the largest divisor
@@ -475,14 +561,15 @@ int rmsnorm_cluster_size(int64_t K) {
 
 cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M,
                                  int64_t K, uint8_t* q, float* s, uint8_t* qT, float* sT,
-                                 float* rstd, cudaStream_t st) {
+                                 float* rstd, uint64_t timeout_ns, cudaStream_t st) {
     PanelArgs a = {};
     a.x = x; a.ldx = K; a.gamma = gamma; a.eps = eps; a.rstd_out = rstd;
     a.M = M; a.K = K; a.q = q; a.s = s; a.qT = qT; a.sT = sT;
     const int c = rmsnorm_cluster_size(K);
     a.tiles_per_cta = (int)((K / 128) / c);
-    if (qT) return launch_panel_t<PRO_RMSNORM, true, true>(a, c, st);
-    return launch_panel_t<PRO_RMSNORM, true, false>(a, c, st);
+    a.timeout_ns = timeout_ns;
+    if (qT) return launch_panel_t<PRO_RMSNORM, true, true>(a, K, c, st);
+    return launch_panel_t<PRO_RMSNORM, true, false>(a, K, c, st);
 }
 
 cudaError_t launch_quant_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
@@ -490,6 +577,16 @@ cudaError_t launch_quant_128x128(const uint16_t* w, int64_t N, int64_t K, int64_
     dim3 grid((unsigned)(K / 128), (unsigned)(N / 128), 1);
     k_quant_128x128<<<grid, 256, 0, st>>>(w, N, K, ldw, q, s, qT);
     return cudaGetLastError();
+}
+
+// This translation unit's copy of the device status word (its TMA waits write it).
+fp8rl_status read_and_clear_quant_status() {
+    unsigned int v = 0;
+    const unsigned int zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof v) != cudaSuccess) return FP8RL_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero) != cudaSuccess)
+        return FP8RL_ERR_CUDA;
+    return static_cast<fp8rl_status>(v);
 }
 
 cudaError_t launch_debug_e4m3(const float* in, uint8_t* out, int64_t n, cudaStream_t st) {

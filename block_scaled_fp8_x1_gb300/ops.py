@@ -202,7 +202,7 @@ def _check_gemm_inputs(qa, sa, qb, sb):
 
 
 def gemm_fwd(qx, sx, qw, sw, out=None, variant: int = _abi.FP8RL_VARIANT_AUTO, splits: int = 0,
-             grid: int = 0, ws: Optional[torch.Tensor] = None):
+             grid: int = 0, ws: Optional[torch.Tensor] = None, tile_n: int = 0):
     """Y = X W^T: qx [M,K], sx [K/128,M], qw [N,K], sw [N/128,K/128] -> y bf16 [M,N]."""
     _check_gemm_inputs(qx, sx, qw, sw)
     M, K = qx.shape
@@ -211,7 +211,7 @@ def gemm_fwd(qx, sx, qw, sw, out=None, variant: int = _abi.FP8RL_VARIANT_AUTO, s
     y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     decode = variant == _abi.FP8RL_VARIANT_SPLITK or (
         variant == _abi.FP8RL_VARIANT_AUTO and M <= 256)
-    opts = GemmOpts(int(variant), int(splits), int(grid))
+    opts = GemmOpts(int(variant), int(splits), int(grid), int(tile_n))
     wsb = None
     if decode:
         need = int(lib().fp8rl_gemm_workspace_bytes_ex(_abi.FP8RL_OP_FWD, M, N, K,

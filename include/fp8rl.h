@@ -162,9 +162,9 @@ typedef enum { FP8RL_OP_FWD = 0, FP8RL_OP_DGRAD = 1, FP8RL_OP_WGRAD = 2 } fp8rl_
  *   qx : E4M3 [M][K] (1x128), sx : float [K/128][M]
  *   qw : E4M3 [N][K] (128x128), sw : float [N/128][K/128]
  *   y  : BF16 [M][N]
- * Small M (<= 256) takes the decode-shaped kernel (weights stream once through the SMs,
- * reduction split across CTAs, partial sums reduced in a fixed order by the last CTA of
- * each output tile); it needs fp8rl_gemm_workspace_bytes(FP8RL_OP_FWD, M, N, K) bytes of
+ * Small M (<= 256) takes the decode-shaped form (the same kernel with the reduction split
+ * into slices over more CTAs, so that the weights stream through every SM; the slices'
+ * FP32 partial sums are added in slice order by the last CTA of each output tile); it needs fp8rl_gemm_workspace_bytes(FP8RL_OP_FWD, M, N, K) bytes of
  * workspace.  The workspace must be zero-filled before its first use; every call that
  * completes leaves its arrival counters at zero again, so one workspace serves calls
  * issued in order on one stream (calls that overlap in time need separate workspaces;
@@ -198,14 +198,15 @@ FP8RL_API size_t fp8rl_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_
 typedef enum {
     FP8RL_VARIANT_AUTO = 0,   /* what fp8rl_gemm_fwd picks */
     FP8RL_VARIANT_TILED = 1,  /* persistent 128 x BN tiles over (M, N) */
-    FP8RL_VARIANT_SPLITK = 2  /* decode-shaped: weight rows as MMA M, tokens as MMA N,
-                                 reduction split over `splits` CTAs */
+    FP8RL_VARIANT_SPLITK = 2  /* decode-shaped: the reduction of each 128x256 output tile
+                                 is split over `splits` CTAs (M <= 256) */
 } fp8rl_variant;
 
 typedef struct {
     int variant;  /* fp8rl_variant */
     int splits;   /* SPLITK: number of reduction slices (0 = choose); ignored otherwise */
     int grid;     /* TILED: persistent CTAs (0 = one per SM); ignored otherwise */
+    int tile_n;   /* TILED: output tile width, 128 or 256 (0 = choose); ignored otherwise */
 } fp8rl_gemm_opts;
 
 /* Workspace bytes fp8rl_gemm_fwd_ex needs with these options (opts may be NULL = AUTO). */
@@ -229,7 +230,8 @@ FP8RL_API fp8rl_status fp8rl_gemm_fwd_ex(const uint8_t* qx, const float* sx, con
  * fp8rl_gemm_noalloc_scratch_bytes() bytes (32 MiB) per device, reserved on every GPU
  * that loads the library and held until the process exits.
  *   - A problem whose split needs more scratch than that returns FP8RL_ERR_WORKSPACE and
- *     launches nothing; M > 256 returns FP8RL_ERR_SHAPE.
+ *     launches nothing (the automatic split keeps at most one CTA wave of 128x256 FP32
+ *     partial tiles, under 20 MiB on a 152-SM GPU); M > 256 returns FP8RL_ERR_SHAPE.
  *   - The first call on a device looks up the array's device address (with that device
  *     current) and caches it; make that first call before any stream capture.
  *   - Every call on a device shares the array and clears its counters on entry (an
