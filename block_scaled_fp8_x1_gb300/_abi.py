@@ -77,6 +77,7 @@ SIGNATURES = {
     "fp8rl_gemm_fwd_decode_noalloc": (ST, [P, P, P, P, P, I64, I64, I64, STREAM]),
     "fp8rl_gemm_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "fp8rl_debug_e4m3_encode": (ST, [P, P, I64, STREAM]),
+    "fp8rl_debug_encode_check": (ST, [ctypes.c_uint32, ctypes.c_uint32, P, P, STREAM]),
     "fp8rl_debug_wait_timeout": (ST, [ctypes.c_uint64, STREAM]),
 }
 

@@ -445,6 +445,15 @@ fp8rl_status fp8rl_debug_e4m3_encode(const float* in, uint8_t* out, int64_t n,
     return cuda_status(launch_debug_e4m3(in, out, n, stream));
 }
 
+fp8rl_status fp8rl_debug_encode_check(uint32_t amax_lo, uint32_t amax_hi,
+                                      unsigned long long* mismatches, uint32_t* first_bad,
+                                      fp8rl_stream_t stream) {
+    if (!mismatches || !first_bad || amax_hi > 0x7F80u || amax_lo > amax_hi) return FP8RL_ERR_INVALID_ARG;
+    fp8rl_status e = current_device(nullptr);
+    if (e != FP8RL_OK) return e;
+    return cuda_status(launch_debug_encode_check(amax_lo, amax_hi, mismatches, first_bad, stream));
+}
+
 fp8rl_status fp8rl_debug_wait_timeout(uint64_t timeout_ns, fp8rl_stream_t stream) {
     fp8rl_status e = current_device(nullptr);
     if (e != FP8RL_OK) return e;

@@ -5,14 +5,8 @@
 //     s = fl32(amax / 448),   code(x) = E4M3_rne_satfinite( fl32(x / s) ),
 // and an all-zero group has s = 0 and codes 0x00.
 //
-// The division is the expensive part at HBM speed.  Each element is first encoded from
-// q0 = RN(x * RN(1/s)).  q0 and fl32(x/s) each lie within 2^-23 relative of x/s (two
-// roundings of relative size 2^-24 for q0, one for the quotient), so they are at most 3
-// consecutive binary32 values apart, also across a binade boundary.  E4M3 rounding is
-// monotone, so if the codes of |q0| moved 4 values down and 4 values up agree, that code
-// is the code of fl32(x/s).  Otherwise (q0 close to an E4M3 rounding midpoint,
-// or x = 0) the element is re-encoded from the IEEE quotient __fdiv_rn(x, s).  Groups
-// whose scale is subnormal (RN(1/s) could overflow) always take the IEEE path.
+// The division is the expensive part at HBM speed: see encode_pair for how the quotient is
+// formed from a reciprocal without a divide, exactly.
 #pragma once
 
 #include "common.cuh"
@@ -23,14 +17,20 @@ struct GroupScale {
     float s;    // the group's scale
     float r;    // RN(1/s); unused when slow
     bool zero;  // s == 0: every code is 0x00
-    bool slow;  // subnormal s: always divide
+    bool slow;  // tiny s: always divide
 };
+
+// Below this scale the division-free encode's residual could underflow for the elements
+// whose code is not a signed zero (|x| >= s * 2^-11), so such groups divide instead.
+constexpr float kMinFastScale = 3.3881317890172014e-21f;  // 2^-68
+
+__device__ __forceinline__ bool scale_is_slow(float s) { return s < kMinFastScale; }
 
 __device__ __forceinline__ GroupScale make_scale(float amax) {
     GroupScale g;
     g.s = __fdiv_rn(amax, 448.0f);
     g.zero = (g.s == 0.0f);
-    g.slow = (g.s < 1.17549435e-38f);  // below FLT_MIN (includes zero, handled first)
+    g.slow = scale_is_slow(g.s);  // includes zero, which is handled first
     g.r = g.slow ? 0.0f : __frcp_rn(g.s);
     return g;
 }
@@ -46,20 +46,35 @@ __device__ __forceinline__ uint32_t absmax2(uint32_t acc, uint32_t w) {
     return __vmaxu2(acc, w & 0x7FFF7FFFu);
 }
 
-// Encode two binary32 values (exact BF16 values or any finite floats) with one group
-// scale; returns the two codes packed (x0 in bits 0-7, x1 in bits 8-15).
+// Encode two BF16 values (given as binary32) with one group scale; returns the two codes
+// packed (x0 in bits 0-7, x1 in bits 8-15).
+//
+// fl32(x/s) is formed without a divide by Markstein's correction step (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): with r = RN(1/s) and q = RN(x*r), the residual e = x - s*q is exact in
+// one fused multiply-add and RN(q + e*r) is the correctly rounded quotient.  Both steps run
+// on packed FP32x2 pairs.  The sign is copied from x so that -0 keeps its code 0x80.
+// Groups with s < 2^-68 take IEEE division: there the residual of an element whose code
+// is not a signed zero could fall below the normal range, and the step needs it exact
+// (for s >= 2^-68 such elements have |x| >= s * 2^-11, so the residual stays far above
+// it; smaller elements encode to a signed zero whatever the last bits).  Every BF16 x
+// against every BF16 group maximum is checked against IEEE division by the exhaustive
+// device test (fp8rl_debug_encode_check).
 __device__ __forceinline__ uint32_t encode_pair(float x0, float x1, const GroupScale& g) {
     if (g.zero) return 0u;
-    const float q0 = x0 * g.r;
-    const float q1 = x1 * g.r;
-    const uint32_t a0 = __float_as_uint(q0) & 0x7FFFFFFFu;
-    const uint32_t a1 = __float_as_uint(q1) & 0x7FFFFFFFu;
-    const uint32_t lo = e4m3x2(__uint_as_float(a0 - 4u), __uint_as_float(a1 - 4u));
-    const uint32_t hi = e4m3x2(__uint_as_float(a0 + 4u), __uint_as_float(a1 + 4u));
-    if (!g.slow && lo == hi) {
-        const uint32_t b0 = __float_as_uint(x0), b1 = __float_as_uint(x1);
-        return lo | ((b0 >> 24) & 0x80u) | ((b1 >> 16) & 0x8000u);
-    }
+    if (g.slow) return e4m3x2(__fdiv_rn(x0, g.s), __fdiv_rn(x1, g.s));
+    const float2 x = make_float2(x0, x1);
+    const float2 q = __fmul2_rn(x, make_float2(g.r, g.r));
+    const float2 e = __ffma2_rn(q, make_float2(-g.s, -g.s), x);
+    const float2 c = __ffma2_rn(e, make_float2(g.r, g.r), q);
+    const float c0 = __uint_as_float((__float_as_uint(c.x) & 0x7FFFFFFFu) | (__float_as_uint(x0) & 0x80000000u));
+    const float c1 = __uint_as_float((__float_as_uint(c.y) & 0x7FFFFFFFu) | (__float_as_uint(x1) & 0x80000000u));
+    return e4m3x2(c0, c1);
+}
+
+// Reference: the same codes from the IEEE quotient (used by the exhaustive check only).
+__device__ __forceinline__ uint32_t encode_pair_ieee(float x0, float x1, const GroupScale& g) {
+    if (g.zero) return 0u;
     return e4m3x2(__fdiv_rn(x0, g.s), __fdiv_rn(x1, g.s));
 }
 

@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(256) k_quant_panel(const __grid_constant__ CUt
                 g.s = s_row_s[R0 + i];
                 g.r = s_row_r[R0 + i];
                 g.zero = (g.s == 0.0f);
-                g.slow = (g.s < 1.17549435e-38f);
+                g.slow = scale_is_slow(g.s);
                 uint32_t c[4];
                 #pragma unroll
                 for (int j = 0; j < 4; ++j) c[j] = encode_pair(bf16_lo(w[i][j]), bf16_hi(w[i][j]), g);
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(256) k_quant_panel(const __grid_constant__ CUt
                 g.s = s_col_s[C0 + j];
                 g.r = s_col_r[C0 + j];
                 g.zero = (g.s == 0.0f);
-                g.slow = (g.s < 1.17549435e-38f);
+                g.slow = scale_is_slow(g.s);
                 uint32_t c[4];
                 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(256) k_quant_128x128(const uint16_t* __restric
     g.s = s_scale[0];
     g.r = s_scale[1];
     g.zero = (g.s == 0.0f);
-    g.slow = (g.s < 1.17549435e-38f);
+    g.slow = scale_is_slow(g.s);
     // codes of the 8x8 block, row-major and (if wanted) transposed
     uint32_t rc[8][2];
     #pragma unroll
@@ -460,6 +460,38 @@ __global__ void __launch_bounds__(256) k_quant_128x128(const uint16_t* __restric
             stg_v2(qT + (k0 + C0 + j) * N + n0 + R0, lo, hi);
         }
     }
+}
+
+// ------------------------------------------------------------------------------------
+// Diagnostic: the production encode (reciprocal + correction) against IEEE division for
+// every BF16 group maximum in [amax_lo, amax_hi) and every BF16 x with |x| <= amax (both
+// signs, and both zeros).  Counts mismatching codes; records the first one found.
+// ------------------------------------------------------------------------------------
+__global__ void k_debug_encode_check(uint32_t amax_lo, uint32_t amax_hi,
+                                     unsigned long long* mismatches, uint32_t* first_bad) {
+    unsigned long long bad = 0;
+    for (uint32_t ab = amax_lo + blockIdx.x; ab < amax_hi; ab += gridDim.x) {
+        const GroupScale g = make_scale(bf16_bits_amax_to_f32(ab));
+        // x magnitudes 0 .. ab, both signs: 2*(ab+1) values, two per encode
+        for (uint32_t i = threadIdx.x; i <= ab; i += blockDim.x) {
+            const float xp = __uint_as_float(i << 16);
+            const float xn = __uint_as_float((i | 0x8000u) << 16);
+            const uint32_t a = encode_pair(xp, xn, g);
+            const uint32_t b = encode_pair_ieee(xp, xn, g);
+            if (a != b) {
+                ++bad;
+                atomicCAS(first_bad, 0xFFFFFFFFu, (ab << 16) | i);
+            }
+        }
+    }
+    if (bad) atomicAdd(mismatches, bad);
+}
+
+cudaError_t launch_debug_encode_check(uint32_t amax_lo, uint32_t amax_hi,
+                                      unsigned long long* mismatches, uint32_t* first_bad,
+                                      cudaStream_t st) {
+    k_debug_encode_check<<<2048, 256, 0, st>>>(amax_lo, amax_hi, mismatches, first_bad);
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------------------------

@@ -74,6 +74,18 @@ def debug_e4m3_encode(v: torch.Tensor) -> torch.Tensor:
     return out
 
 
+def debug_encode_check(amax_lo: int = 1, amax_hi: int = 0x7F80):
+    """(mismatches, first_bad) of the division-free encode vs IEEE division over every BF16
+    group maximum in [amax_lo, amax_hi) and every BF16 x with |x| <= amax."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+    first = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    check(lib().fp8rl_debug_encode_check(int(amax_lo), int(amax_hi), _ptr(cnt), _ptr(first),
+                                         _stream(dev)), "fp8rl_debug_encode_check")
+    torch.cuda.synchronize(dev)
+    return int(cnt.item()), int(first.item()) & 0xFFFFFFFF
+
+
 def debug_wait_timeout(timeout_ns: int, device: Optional[torch.device] = None) -> None:
     device = device or torch.device("cuda", torch.cuda.current_device())
     check(lib().fp8rl_debug_wait_timeout(int(timeout_ns), _stream(device)),

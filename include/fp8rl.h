@@ -254,6 +254,16 @@ FP8RL_API size_t fp8rl_gemm_noalloc_scratch_bytes(void);
 FP8RL_API fp8rl_status fp8rl_debug_e4m3_encode(const float* in, uint8_t* out, int64_t n,
                                      fp8rl_stream_t stream);
 
+/* Checks the quantizers' division-free encode against IEEE division on the device: for
+ * every BF16 group maximum with bits in [amax_lo, amax_hi) (positive finite: below 0x7F80)
+ * and every BF16 x with |x| <= amax, both signs, the code of E4M3(fl32(x / s)) with
+ * s = fl32(amax / 448) must equal the production encode.  Adds the number of mismatching
+ * pairs to *mismatches and stores the first one as (amax_bits << 16) | |x|_bits into
+ * *first_bad if that still holds 0xFFFFFFFF.  Device pointers. */
+FP8RL_API fp8rl_status fp8rl_debug_encode_check(uint32_t amax_lo, uint32_t amax_hi,
+                                                unsigned long long* mismatches,
+                                                uint32_t* first_bad, fp8rl_stream_t stream);
+
 /* Launches one CTA that waits, with the GEMM kernels' bounded wait, on an mbarrier that
  * nothing completes; after `timeout_ns` it records FP8RL_ERR_DEVICE_TIMEOUT and returns.
  * Exercises the failure path without faulting or hanging the GPU. */

@@ -122,3 +122,12 @@ def test_device_encoder_exhaustive(fp8lib, oracle):
         bad = (got != ref) & fin
         assert not bad.any(), f"chunk {c}: {int(bad.sum())} differ, e.g. bits {np.nonzero(bad)[0][0] + start:#x}"
         del idx, v
+
+
+def test_division_free_encode_is_exact_for_every_bf16_pair(fp8lib):
+    """The quantizers form x/s from RN(1/s) with one correction step instead of dividing.
+    Their inputs are BF16 values, so the whole domain is finite: every positive finite BF16
+    group maximum against every BF16 x with |x| <= amax (both signs and zeros) must give the
+    same E4M3 code as IEEE division."""
+    mismatches, first = fp8lib.debug_encode_check(1, 0x7F80)
+    assert mismatches == 0, f"{mismatches} mismatches, first amax/x bits {first:#010x}"
