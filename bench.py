@@ -23,6 +23,8 @@ on a bounded sample of the same step and reports the same metric.
 from __future__ import annotations
 
 import argparse
+import datetime
+import hashlib
 import json
 import os
 import statistics
@@ -83,7 +85,9 @@ def decode_bytes():
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock/throttle samples every 20 ms, kept only when their timestamp falls
+    inside the window passed to stop()."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -93,19 +97,27 @@ class ClockSampler:
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
 
     def start(self):
+        """Start sampling and return once the first sample is written (at most 5 s)."""
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        t_end = time.time() + 5.0
+        while time.time() < t_end and os.path.getsize(self.path) == 0:
+            time.sleep(0.02)
 
-    def stop(self):
+    def stop(self, window):
+        """Stop sampling; summarise the samples taken between window[0] and window[1]
+        (time.time() values)."""
         if self.proc is None:
             return None
+        time.sleep(0.05)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -115,22 +127,26 @@ class ClockSampler:
         rows = []
         for line in open(self.path):
             p = [x.strip() for x in line.split(",")]
-            if len(p) < 9:
+            if len(p) < 10:
                 continue
             try:
-                rows.append((float(p[1]), float(p[2]), p[5], p[6], p[7], p[8]))
+                ts = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(p[2]), float(p[3]), float(p[4]), p[6], p[7], p[8], p[9]))
             except ValueError:
                 continue
-        if not rows:
+        inside = [r for r in rows if window[0] <= r[0] <= window[1]]
+        if not inside:
             return None
         reasons = set()
-        for r in rows:
+        for r in inside:
             for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
-                                "sw_power_cap"), r[2:]):
+                                "sw_power_cap"), r[4:]):
                 if v.lower() == "active":
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": sorted(reasons), "samples": len(rows)}
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": sorted(reasons),
+                "power_w_median": statistics.median(r[3] for r in inside),
+                "samples": len(inside), "window_ms": round(1e3 * (window[1] - window[0]), 1)}
 
 
 # ----------------------------------------------------------------------------- peaks
@@ -243,11 +259,13 @@ def run_gpu(args):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     barrier()
+    w0 = time.time()
     t0.record()
     for _ in range(args.steps):
         step.run()
     t1.record()
     barrier()
+    w1 = time.time()
     ms_total = t0.elapsed_time(t1)
     # per-kernel durations from events between launches (separate pass, same work)
     per = {}
@@ -257,7 +275,7 @@ def run_gpu(args):
         torch.cuda.synchronize()
         for (_, a), (name, b) in zip(marks[:-1], marks[1:]):
             per.setdefault(name, []).append(a.elapsed_time(b))
-    clk = clocks.stop()
+    clk = clocks.stop((w0, w1))
     st = ops.check_status()
 
     ms_step = ms_total / args.steps
@@ -361,12 +379,26 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+GEMM_SOURCES = ("block_scaled_fp8_x1_gb300/csrc/gemm.cu", "block_scaled_fp8_x1_gb300/csrc/common.cuh",
+                "block_scaled_fp8_x1_gb300/csrc/gemm.h")
+
+
+def gemm_sources_hash() -> str:
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on
-    the current kernel source (profiles/traffic.json)."""
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/traffic.json), or None when that capture was taken on other GEMM sources."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)
+        if d.get("gemm_sources_sha256_16") != gemm_sources_hash():
+            return None
         e = d.get(kernel)
         return e["bytes_per_launch"] if e else None
     except Exception:
@@ -537,7 +569,7 @@ def run_kernel(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
