@@ -91,6 +91,22 @@ fp8rl_status make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t c
     return r == CUDA_SUCCESS ? FP8RL_OK : FP8RL_ERR_CUDA;
 }
 
+// 2-D tensor map of an FP32 scale array [outer][inner] (inner a multiple of 4, so that the
+// row stride is a multiple of 16 bytes), boxes of box_outer x box_inner scales.
+fp8rl_status make_tmap_scales(CUtensorMap* m, const float* base, int64_t outer, int64_t inner,
+                              int box_inner, int box_outer) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return FP8RL_ERR_CUDA;
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    cuuint64_t strides[1] = {(cuuint64_t)inner * 4};
+    cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+    cuuint32_t es[2] = {1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
+                     es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8RL_OK : FP8RL_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------- GEMM planning
 
 // The decode form is the tiled kernel (tokens as rows, weights as 256-wide columns) with
@@ -121,6 +137,34 @@ size_t decode_ws_bytes(int64_t M, int64_t N, int64_t K, int splits) {
     return b;
 }
 
+// Tensor maps that let the GEMM's copy warp move the scales by TMA (see launch_gemm_tiled):
+// A's row scales [K-block][R1] need R1 % 4 == 0; B's block scales need 4 | K-blocks
+// ([column block][K-block] storage) or 4 | column blocks ([K-block][column block]); B's
+// row scales [K-block][R2] always qualify (R2 % 128 == 0).  Returns false when they do not
+// all qualify, in which case the kernel takes the per-thread scale path.
+bool scale_maps(const GemmParams& p, int b_mode, int bn, CUtensorMap* tsa, CUtensorMap* tsb,
+                fp8rl_status* err) {
+    *err = FP8RL_OK;
+    const int64_t nkb = p.Kr / 128;
+    if (p.R1 % 4 != 0 || p.sa_kb != p.R1) return false;
+    if (b_mode == SCALE_ROW) {
+        if (p.sb_kb != p.R2 || p.R2 % 4 != 0) return false;
+    } else if (p.sb_kb == 1) {
+        if (nkb % 4 != 0 || p.sb_r != nkb) return false;
+    } else {
+        if (p.sb_r != 1 || p.sb_kb % 4 != 0) return false;
+    }
+    *err = make_tmap_scales(tsa, p.sa, nkb, p.R1, 128, 1);
+    if (*err != FP8RL_OK) return false;
+    if (b_mode == SCALE_ROW)
+        *err = make_tmap_scales(tsb, p.sb, nkb, p.R2, bn, 1);
+    else if (p.sb_kb == 1)
+        *err = make_tmap_scales(tsb, p.sb, (p.R2 + 127) / 128, nkb, 4, bn / 128);
+    else
+        *err = make_tmap_scales(tsb, p.sb, nkb, p.sb_kb, 4, 1);
+    return *err == FP8RL_OK;
+}
+
 struct TiledArgs {
     const uint8_t* A; const float* sa; int64_t sa_kb;
     const uint8_t* B; const float* sb; int64_t sb_kb, sb_r; int b_mode;
@@ -133,18 +177,24 @@ struct TiledArgs {
 int tiled_bn(int req) { return req == 128 ? 128 : 256; }
 
 fp8rl_status run_tiled(const TiledArgs& t, int grid_req, int bn_req, int num_sms, cudaStream_t st) {
-    const int bn = tiled_bn(bn_req);
-    CUtensorMap ta, tb;
-    fp8rl_status e = make_tmap(&ta, t.A, t.R1, t.Kr, t.Kr, 128);
-    if (e != FP8RL_OK) return e;
-    e = make_tmap(&tb, t.B, t.R2, t.Kr, t.Kr, bn);
-    if (e != FP8RL_OK) return e;
+    int bn = tiled_bn(bn_req);
     GemmParams p = {};
     p.R1 = t.R1; p.R2 = t.R2; p.Kr = t.Kr;
-    p.sa = t.sa; p.sa_kb = t.sa_kb; p.sa_r = 0;
+    p.sa = t.sa; p.sa_kb = t.sa_kb;
     p.sb = t.sb; p.sb_kb = t.sb_kb; p.sb_r = t.sb_r;
     p.c = t.c; p.ldc = t.ldc;
     p.splits = 0;
+    CUtensorMap tsa, tsb;
+    fp8rl_status e = FP8RL_OK;
+    bool tma_scales = scale_maps(p, t.b_mode, bn, &tsa, &tsb, &e);
+    if (e != FP8RL_OK) return e;
+    if (t.b_mode == SCALE_ROW && !tma_scales) return FP8RL_ERR_INVALID_ARG;
+    if (!tma_scales) bn = 256;   // the per-thread scale path is built for 256-wide tiles only
+    CUtensorMap ta, tb;
+    e = make_tmap(&ta, t.A, t.R1, t.Kr, t.Kr, 128);
+    if (e != FP8RL_OK) return e;
+    e = make_tmap(&tb, t.B, t.R2, t.Kr, t.Kr, bn);
+    if (e != FP8RL_OK) return e;
     p.m_tiles = (int)((t.R1 + 127) / 128);
     p.n_tiles = (int)((t.R2 + bn - 1) / bn);
     p.nkb = (int)(t.Kr / 128);
@@ -152,7 +202,8 @@ fp8rl_status run_tiled(const TiledArgs& t, int grid_req, int bn_req, int num_sms
     p.timeout_ns = g_timeout_ns.load();
     int grid = grid_req > 0 ? grid_req : num_sms;
     grid = std::max(1, std::min(grid, p.num_items));
-    return cuda_status(launch_gemm_tiled(ta, tb, p, t.b_mode, bn, grid, st));
+    return cuda_status(launch_gemm_tiled(ta, tb, tma_scales ? &tsa : nullptr, tma_scales ? &tsb : nullptr, p,
+                                         t.b_mode, bn, grid, st));
 }
 
 fp8rl_status run_decode(const uint8_t* qx, const float* sx, const uint8_t* qw, const float* sw,
@@ -172,7 +223,7 @@ fp8rl_status run_decode(const uint8_t* qx, const float* sx, const uint8_t* qw, c
     if (e != FP8RL_OK) return e;
     GemmParams p = {};
     p.R1 = M; p.R2 = N; p.Kr = K;
-    p.sa = sx; p.sa_kb = M; p.sa_r = 0;
+    p.sa = sx; p.sa_kb = M;
     p.sb = sw; p.sb_kb = 1; p.sb_r = K / 128;
     p.c = y; p.ldc = N;
     p.counters = reinterpret_cast<unsigned int*>(ws);
@@ -184,7 +235,11 @@ fp8rl_status run_decode(const uint8_t* qx, const float* sx, const uint8_t* qw, c
     p.num_items = (int)(tiles * splits);
     p.timeout_ns = g_timeout_ns.load();
     const int grid = std::max(1, std::min(num_sms, p.num_items));
-    return cuda_status(launch_gemm_splitk(ta, tb, p, grid, st));
+    CUtensorMap tsa, tsb;
+    const bool tma_scales = scale_maps(p, SCALE_BLOCK, kDecodeBN, &tsa, &tsb, &e);
+    if (e != FP8RL_OK) return e;
+    return cuda_status(launch_gemm_splitk(ta, tb, tma_scales ? &tsa : nullptr, tma_scales ? &tsb : nullptr, p,
+                                          grid, st));
 }
 
 }  // namespace

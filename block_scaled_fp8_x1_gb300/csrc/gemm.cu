@@ -10,22 +10,23 @@
 //           P_kb = sum_{k in block kb} A[r1, k] * B[r2, k]      (E4M3 x E4M3, FP32)
 // with A [R1, Kr] and B [R2, Kr] stored K-major (reduction dimension contiguous).
 //
-// Structure (one CTA of 384 threads per SM, persistent over work items):
-//   warp 0      copies: lane 0 issues the TMA loads of the 128x128 A tile and the BNx128
-//               B tile of each K-block into a STAGES-deep shared-memory ring (128-byte
-//               swizzle); all 32 lanes copy the K-block's scales (cp.async) into an
-//               8-slot scale ring that the epilogue releases, so no scale load sits on the
-//               epilogue's critical path.
+// Structure (one CTA of 640 threads per SM, persistent over work items):
+//   warp 0      copies (lane 0): TMA loads of the 128x128 A tile and the BNx128 B tile of
+//               each K-block into a STAGES-deep shared-memory ring (128-byte swizzle); when
+//               B has one scale per row (WGrad), also that K-block's BN scales of B into an
+//               8-slot scale ring that the epilogue releases.
 //   warp 1      allocates all 512 TMEM columns and issues, per K-block, four tcgen05.mma
 //               (K = 32 each) into one of 512/BN partial-sum buffers (fresh accumulate per
 //               block), so the tensor pipe runs up to 512/BN - 1 blocks ahead of the
 //               epilogue.
 //   warps 2-3   idle (they complete warpgroup 0, whose registers go to the epilogue).
-//   warps 4-11  epilogue: per K-block, load the 128 x BN FP32 partial from TMEM, release
-//               the buffer, and promote it into FP32 registers with the block's scales
-//               ("per-block scale promotion"); finally round to BF16 and store, or, in
-//               the split-K form, store FP32 partials and let the last CTA of a tile sum
-//               them in split order (deterministic, no spin-wait).
+//   warps 4-19  epilogue, four warps per TMEM lane quadrant, each owning 32 rows x BN/4
+//               columns: per K-block, load the FP32 partial from TMEM, release the buffer,
+//               and promote it into FP32 registers with the block's scales ("per-block
+//               scale promotion"); the row scales of A (and the block scales of B) are read
+//               from global memory a few K-blocks ahead.  Finally round to BF16 and store,
+//               or, in the split-K form, store FP32 partials and let the last CTA of a tile
+//               sum them in split order (deterministic, no spin-wait).
 // Every mbarrier wait is bounded; on timeout the CTA records FP8RL_ERR_DEVICE_TIMEOUT,
 // drains its own copies and MMAs, frees TMEM and returns.
 #include "common.cuh"
@@ -70,35 +71,104 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// Shared-memory plan of one CTA.
-template <int BN, int STAGES>
+// 4 warps (copies, MMA, two idle) + kEpiWarps epilogue warps, kEpiWarps / 4 per SM
+// sub-partition (one warp's TMEM loads do not overlap each other, so the read rate grows
+// with the warps).  Register split: warpgroup 0 drops to kRegLo, the epilogue rises to
+// kRegHi, within the kLaunchRegs per thread the CTA is launched with.
+constexpr int kEpiWarps = 8;
+constexpr int kGemmThreads = 128 + 32 * kEpiWarps;
+constexpr int kLaunchRegs = kEpiWarps == 16 ? 96 : 168;
+constexpr uint32_t kRegLo = kEpiWarps == 16 ? 32 : 40;
+constexpr uint32_t kRegHi = kEpiWarps == 16 ? 112 : 232;
+static_assert(128 * kRegLo + 32 * kEpiWarps * kRegHi <= kGemmThreads * kLaunchRegs, "register split");
+constexpr int kScalePD = 4;   // K-blocks of scale prefetch per epilogue thread
+
+// How the epilogue gets the per-K-block scales of A's rows and of B's column blocks.
+enum ScaleDelivery {
+    SD_TMA = 0,     // the copy warp's TMA puts each K-block's scales in the scale ring
+    SD_THREAD = 1   // each epilogue thread copies its own (any M; B rows still by TMA)
+};
+
+// Shared-memory plan of one CTA.  Scale-ring slot: 128 scales of A (SD_TMA), then the
+// scales of B (BN for SCALE_ROW, a box of at most 8 block scales for SCALE_BLOCK).
+template <int BN, int STAGES, int B_MODE, int SD>
 struct GemmSmem {
     static constexpr int A_BYTES = 128 * 128;                 // one 128x128 E4M3 tile of A
     static constexpr int B_BYTES = BN * 128;                  // one BNx128 E4M3 tile of B
     static constexpr int NS = 8;                              // scale-ring slots
-    static constexpr int SLOT = 128 + BN;                     // floats: A scales, B scales
+    static constexpr int SLOT_A = (SD == SD_TMA) ? 128 : 0;   // floats
+    // (a box of block scales takes at most 8 floats; padded so that every TMA destination
+    // in the ring starts on a 128-byte boundary, as tensor copies require)
+    static constexpr int SLOT_B = (B_MODE == SCALE_ROW) ? BN : ((SD == SD_TMA) ? 32 : 0);
+    static constexpr int SLOT = SLOT_A + SLOT_B;
+    static_assert((SLOT_A * 4) % 128 == 0 && (SLOT * 4) % 128 == 0, "TMA destinations 128-byte aligned");
+    static constexpr bool RING = SLOT > 0;
     static constexpr int RING_BYTES = NS * SLOT * 4;
     static constexpr int NTB = 512 / BN;                      // TMEM partial-sum buffers
+    // SD_THREAD: per epilogue thread, kScalePD slots of its scale words: A row (+ B block)
+    static constexpr int SC_WORDS = (B_MODE == SCALE_BLOCK) ? 2 : 1;
+    static constexpr int SC_BYTES = (SD == SD_THREAD) ? kScalePD * SC_WORDS * 32 * kEpiWarps * 4 : 0;
     static constexpr int NBARS = 2 * STAGES + 2 * NTB + 2 * NS + 1;
     static constexpr size_t BYTES = 1024 /* alignment slack */ + (size_t)STAGES * (A_BYTES + B_BYTES) +
-                                    RING_BYTES + NBARS * 8 + 16;
+                                    RING_BYTES + SC_BYTES + NBARS * 8 + 16;
 };
 
-constexpr int kGemmThreads = 384;
+// The scales one epilogue thread applies per K-block: the scale of its row of A and, when
+// B has one scale per 128-row block, the scale of the block its columns fall in.  The
+// cursor walks the (work item, K-block) sequence of the CTA in processing order; each
+// thread copies its own scale words (cp.async, one commit group per K-block) kScalePD
+// K-blocks ahead into private shared-memory slots, so no register ever waits on a load.
+template <int BN, int B_MODE>
+struct ScaleCursor {
+    int item, kb, kb_end;
+    int r1;      // row of A this thread scales
+    int col;     // first column of C this thread owns
 
-template <int BN, int A_MODE, int B_MODE, int STAGES, bool SPLITK>
+    __device__ __forceinline__ void enter(const GemmParams& p, int row_local, int col_base) {
+        if (item < p.num_items) {
+            const WorkItem w = work_item(p, item);
+            kb = w.kb_begin;
+            kb_end = w.kb_end;
+            r1 = w.mt * 128 + row_local;
+            col = w.nt * BN + col_base;
+        }
+    }
+    // Copy the scales of the current position into slot words `dst_a` (and `dst_b`); zero
+    // past the end of the sequence or outside A/C.  Then advance and close the group.
+    __device__ __forceinline__ void issue(const GemmParams& p, uint32_t dst_a, uint32_t dst_b,
+                                          int row_local, int col_base) {
+        const bool live = item < p.num_items;
+        const bool va = live && r1 < p.R1;
+        cp_async_4(dst_a, p.sa + (va ? (int64_t)kb * p.sa_kb + r1 : 0), va ? 4u : 0u);
+        if (B_MODE == SCALE_BLOCK) {
+            const bool vb = live && col < p.R2;
+            cp_async_4(dst_b, p.sb + (vb ? (int64_t)(col >> 7) * p.sb_r + (int64_t)kb * p.sb_kb : 0),
+                       vb ? 4u : 0u);
+        }
+        cp_async_commit();
+        if (live && ++kb >= kb_end) {
+            item += gridDim.x;
+            enter(p, row_local, col_base);
+        }
+    }
+};
+
+template <int BN, int SD, int B_MODE, int STAGES, bool SPLITK>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_bs(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
               const GemmParams p) {
-    using S = GemmSmem<BN, STAGES>;
-    constexpr int HALF = BN / 2;      // columns per epilogue thread
-    constexpr int GRP = HALF >= 64 ? 64 : 32;   // TMEM columns loaded per wait
-    constexpr int NG = HALF / GRP;                // waits per K-block
+    using S = GemmSmem<BN, STAGES, B_MODE, SD>;
+    constexpr int COLS = BN / (kEpiWarps / 4);   // columns per epilogue thread
+    constexpr int LW = kEpiWarps == 16 ? 16 : 32; // columns per TMEM load
+    constexpr int LPW = kEpiWarps == 16 ? 1 : 2;  // loads per wait
+    constexpr int NG = COLS / (LW * LPW);         // waits per K-block
     constexpr int NS = S::NS;
     constexpr int NTB = S::NTB;
+    constexpr int PD = kScalePD;
     constexpr uint32_t TMEM_COLS = 512;
     constexpr uint32_t IDESC = idesc_e4m3_f32(128, BN);
-    static_assert(HALF % GRP == 0 && HALF >= 32, "BN must be 64, 128 or 256");
+    static_assert(COLS % (LW * LPW) == 0, "BN must be 128 or 256");
     static_assert(B_MODE == SCALE_ROW || BN >= 128, "block scales of B need whole 128-column blocks");
 
     extern __shared__ uint8_t smem_raw[];
@@ -106,7 +176,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * S::A_BYTES;
     float* ring = reinterpret_cast<float*>(sB + STAGES * S::B_BYTES);   // [NS][SLOT]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ring) + S::RING_BYTES);
+    float* sc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ring) + S::RING_BYTES);  // [PD][W][thr]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sc) + S::SC_BYTES);
     uint64_t* full_bar = bars;                 // [STAGES] TMA -> MMA
     uint64_t* empty_bar = bars + STAGES;       // [STAGES] MMA -> TMA
     uint64_t* tfull_bar = bars + 2 * STAGES;   // [NTB] MMA -> epilogue
@@ -128,11 +199,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int t = 0; t < NTB; ++t) {
             mbar_init(smem_u32(&tfull_bar[t]), 1);
-            mbar_init(smem_u32(&tempty_bar[t]), 8);
+            mbar_init(smem_u32(&tempty_bar[t]), kEpiWarps);
         }
         for (int s = 0; s < NS; ++s) {
-            mbar_init(smem_u32(&sfull_bar[s]), 32);
-            mbar_init(smem_u32(&sempty_bar[s]), 8);
+            mbar_init(smem_u32(&sfull_bar[s]), 1);
+            mbar_init(smem_u32(&sempty_bar[s]), kEpiWarps);
         }
         mbar_init(smem_u32(drain_bar), 1);
         *abort_flag = 0;
@@ -140,6 +211,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (SD == SD_TMA) tma_prefetch_desc(&tmSA);
+        if (S::SLOT_B > 0) tma_prefetch_desc(&tmSB);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -150,74 +223,71 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    // Registers: launched at 168 per thread (384 x 168 = 64512); warpgroup 0 (copy, MMA and
-    // two idle warps) drops to REG_LO, the two epilogue warpgroups rise to REG_HI.
-    constexpr uint32_t REG_LO = 40, REG_HI = 232;
-    static_assert(128 * REG_LO + 256 * REG_HI <= 384 * 168, "register split");
+    constexpr uint32_t REG_LO = kRegLo, REG_HI = kRegHi;
     if (warp < 4) {
       warpgroup_reg_dealloc<REG_LO>();
       if (warp == 0) {
-        // ------------------------------------------------------------ copies (whole warp)
-        // lane 0: TMA tiles of A and B; all lanes: this K-block's scales into the ring.
-        // split-K (decode) streams the weights (B) once: let them leave L2 first
-        const uint64_t pol_a = l2_policy_evict_last();
-        const uint64_t pol_b = SPLITK ? l2_policy_evict_first() : l2_policy_evict_last();
-        uint32_t it = 0;
-        bool ok = true;
-        for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
-            const WorkItem w = work_item(p, item);
-            const int64_t m0 = (int64_t)w.mt * 128;
-            const int64_t n0 = (int64_t)w.nt * BN;
-            for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
-                const uint32_t s = it % STAGES;
-                bool good = true;
-                if (lane == 0) {
-                    good = mbar_wait(smem_u32(&empty_bar[s]), ((it / STAGES) & 1) ^ 1, p.timeout_ns, abort_flag);
-                    if (good) {
-                        const uint32_t fb = smem_u32(&full_bar[s]);
-                        mbar_arrive_expect_tx(fb, S::A_BYTES + S::B_BYTES);
-                        tma_load_2d(smem_u32(sA + s * S::A_BYTES), &tmA, fb, kb * 128, (int)m0, pol_a);
-                        tma_load_2d(smem_u32(sB + s * S::B_BYTES), &tmB, fb, kb * 128, (int)n0, pol_b);
-                    }
-                }
-                if (!__shfl_sync(0xffffffffu, good ? 1 : 0, 0)) { ok = false; break; }
-                const uint32_t ss = it % NS;
-                good = mbar_wait(smem_u32(&sempty_bar[ss]), ((it / NS) & 1) ^ 1, p.timeout_ns, abort_flag);
-                if (!__all_sync(0xffffffffu, good)) { ok = false; break; }
-                const uint32_t slot = smem_u32(ring + ss * S::SLOT);
-                if (A_MODE == SCALE_ROW) {
-                    const float* src = p.sa + (int64_t)kb * p.sa_kb;
-                    #pragma unroll 1
-                    for (int i = lane; i < 128; i += 32) {
-                        const bool v = m0 + i < p.R1;
-                        cp_async_4(slot + 4 * i, src + (v ? m0 + i : 0), v ? 4u : 0u);
-                    }
-                } else if (lane == 0) {
-                    cp_async_4(slot, p.sa + (int64_t)w.mt * p.sa_r + (int64_t)kb * p.sa_kb, 4u);
-                }
-                if (B_MODE == SCALE_ROW) {
-                    const float* src = p.sb + (int64_t)kb * p.sb_kb;
-                    #pragma unroll 1
-                    for (int j = lane; j < BN; j += 32) {
-                        const bool v = n0 + j < p.R2;
-                        cp_async_4(slot + 4 * (128 + j), src + (v ? n0 + j : 0), v ? 4u : 0u);
-                    }
-                } else if (lane < BN / 128) {
-                    const int64_t c = n0 + lane * 128;
-                    const bool v = c < p.R2;
-                    cp_async_4(slot + 4 * (128 + lane), p.sb + (v ? (c / 128) * p.sb_r : 0) + (int64_t)kb * p.sb_kb,
-                               v ? 4u : 0u);
-                }
-                cp_async_arrive(smem_u32(&sfull_bar[ss]));
-            }
-        }
-        // Drain: every issued copy lands before the CTA can exit.
-        cp_async_wait_all();
+        // ------------------------------------------------------------ copies (lane 0)
+        // TMA tiles of A and B per K-block, and that K-block's scales into the scale ring:
+        // the 128 row scales of A (SD_TMA) and B's scales (its BN row scales, or a box of
+        // block scales that holds the tile's column blocks).
         if (lane == 0) {
+            // split-K (decode) streams the weights (B) once: let them leave L2 first
+            const uint64_t pol_a = l2_policy_evict_last();
+            const uint64_t pol_b = SPLITK ? l2_policy_evict_first() : l2_policy_evict_last();
+            uint32_t it = 0, s_issued = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
+                const WorkItem w = work_item(p, item);
+                const int m0 = w.mt * 128;
+                const int n0 = w.nt * BN;
+                for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++it) {
+                    const uint32_t s = it % STAGES;
+                    if (!mbar_wait(smem_u32(&empty_bar[s]), ((it / STAGES) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full_bar[s]);
+                    mbar_arrive_expect_tx(fb, S::A_BYTES + S::B_BYTES);
+                    tma_load_2d(smem_u32(sA + s * S::A_BYTES), &tmA, fb, kb * 128, m0, pol_a);
+                    tma_load_2d(smem_u32(sB + s * S::B_BYTES), &tmB, fb, kb * 128, n0, pol_b);
+                    if (S::RING) {
+                        const uint32_t ss = it % NS;
+                        if (!mbar_wait(smem_u32(&sempty_bar[ss]), ((it / NS) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+                            ok = false;
+                            ++it;   // this K-block's tiles are in flight: drain them below
+                            break;
+                        }
+                        const uint32_t sb = smem_u32(&sfull_bar[ss]);
+                        float* slot = ring + ss * S::SLOT;
+                        if (B_MODE == SCALE_ROW) {
+                            mbar_arrive_expect_tx(sb, (S::SLOT_A + BN) * 4);
+                            tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, n0, kb, pol_a);
+                        } else if (p.sb_kb == 1) {
+                            // block scales stored [column block][K-block]: 4 K-blocks x the
+                            // tile's BN/128 column blocks, from a 4-aligned K-block
+                            mbar_arrive_expect_tx(sb, S::SLOT_A * 4 + 16 * (BN / 128));
+                            tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, kb & ~3, n0 >> 7, pol_a);
+                        } else {
+                            // block scales stored [K-block][column block]: 4 column blocks
+                            // from a 4-aligned one
+                            mbar_arrive_expect_tx(sb, S::SLOT_A * 4 + 16);
+                            tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, (n0 >> 7) & ~3, kb, pol_a);
+                        }
+                        if (SD == SD_TMA) tma_load_2d(smem_u32(slot), &tmSA, sb, m0, kb, pol_a);
+                        ++s_issued;
+                    }
+                }
+            }
+            // Drain: every issued copy lands before the CTA can exit.
+            volatile int no_abort = 0;
             const uint32_t n_out = it < STAGES ? it : STAGES;
-            for (uint32_t j = it - n_out; j < it; ++j) {
-                volatile int no_abort = 0;
+            for (uint32_t j = it - n_out; j < it; ++j)
                 mbar_wait(smem_u32(&full_bar[j % STAGES]), (j / STAGES) & 1, p.timeout_ns, &no_abort);
+            if (S::RING) {
+                const uint32_t s_out = s_issued < NS ? s_issued : NS;
+                for (uint32_t j = s_issued - s_out; j < s_issued; ++j)
+                    mbar_wait(smem_u32(&sfull_bar[j % NS]), (j / NS) & 1, p.timeout_ns, &no_abort);
             }
         }
       } else if (warp == 1) {
@@ -262,44 +332,74 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ------------------------------------------------------------ epilogue warps
         // After an abort every warp keeps walking the same items and blocks (no waits, no
         // TMEM loads) so that all of them reach the same named barriers.
-        const int ew = warp - 4;            // 0..7
+        const int ew = warp - 4;            // 0 .. kEpiWarps-1
         const int quad = warp & 3;          // TMEM lane quadrant this warp may access
-        const int col_base = (ew >> 2) * HALF;
+        const int col_base = (ew >> 2) * COLS;
         const int row_local = quad * 32 + lane;
         const uint32_t t_lane = (uint32_t)(quad * 32) << 16;
+        // SD_THREAD: scale slots of this thread, word (slot, w) at sc[(slot * SC_WORDS + w) * ET + et]
+        const int et = threadIdx.x - 128;
+        constexpr int ET = 32 * kEpiWarps;
+        const uint32_t sc_base = smem_u32(sc) + 4u * (uint32_t)et;
+        ScaleCursor<BN, B_MODE> cur;
+        if (SD == SD_THREAD) {
+            cur.item = blockIdx.x;
+            cur.enter(p, row_local, col_base);
+            #pragma unroll
+            for (int i = 0; i < PD; ++i)
+                cur.issue(p, sc_base + 4u * ET * (i * S::SC_WORDS), sc_base + 4u * ET * (i * S::SC_WORDS + 1),
+                          row_local, col_base);
+        }
         uint32_t acc_it = 0;
         bool ok = true;
         for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
             const WorkItem w = work_item(p, item);
             const int64_t r1 = (int64_t)w.mt * 128 + row_local;
             const int64_t n0 = (int64_t)w.nt * BN + col_base;  // first column of this thread
-            float2 acc[HALF / 2];
+            float2 acc[COLS / 2];
             #pragma unroll
-            for (int c = 0; c < HALF / 2; ++c) acc[c] = make_float2(0.0f, 0.0f);
+            for (int c = 0; c < COLS / 2; ++c) acc[c] = make_float2(0.0f, 0.0f);
 
             for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++acc_it) {
+                float f = 0.0f;
+                if (SD == SD_THREAD) {
+                    // this K-block's scales: its copy group is the oldest of the PD in flight
+                    const uint32_t slot = acc_it % PD;
+                    cp_async_wait_group<PD - 1>();
+                    const float* scw = sc + slot * S::SC_WORDS * ET + et;
+                    f = (B_MODE == SCALE_BLOCK) ? scw[0] * scw[ET] : scw[0];
+                    cur.issue(p, sc_base + 4u * ET * (slot * S::SC_WORDS), sc_base + 4u * ET * (slot * S::SC_WORDS + 1),
+                              row_local, col_base);
+                }
                 if (!ok) continue;
                 const uint32_t ss = acc_it % NS;
                 const uint32_t ts = acc_it % NTB;
-                bool got = mbar_wait(smem_u32(&sfull_bar[ss]), (acc_it / NS) & 1, p.timeout_ns, abort_flag);
+                bool got = true;
+                if (S::RING)
+                    got = mbar_wait(smem_u32(&sfull_bar[ss]), (acc_it / NS) & 1, p.timeout_ns, abort_flag);
                 got = got && mbar_wait(smem_u32(&tfull_bar[ts]), (acc_it / NTB) & 1, p.timeout_ns, abort_flag);
                 ok = __all_sync(0xffffffffu, got);
                 if (!ok) continue;
                 tc_fence_after();
-                const float* sl = ring + ss * S::SLOT;
-                const float fa = (A_MODE == SCALE_ROW) ? sl[row_local] : sl[0];
-                const float f = (B_MODE == SCALE_BLOCK) ? fa * sl[128 + (col_base >> 7)] : fa;
+                const float* slot = ring + ss * S::SLOT;
+                if (SD == SD_TMA) {
+                    f = slot[row_local];
+                    if (B_MODE == SCALE_BLOCK) {
+                        const int cb = (int)(n0 >> 7);   // column block of this thread
+                        f *= slot[128 + (p.sb_kb == 1 ? ((cb - ((w.nt * BN) >> 7)) * 4 + (kb & 3)) : (cb & 3))];
+                    }
+                }
                 const float2 f2 = make_float2(f, f);
-                const float* sbv = sl + 128 + col_base;
+                const float* sbv = slot + S::SLOT_A + col_base;
                 const uint32_t tbase = tmem_base + t_lane + ts * BN + col_base;
-                // 64 columns (two 32-column loads) per wait: two round trips per K-block
+                // LPW loads of LW columns per wait
                 #pragma unroll
                 for (int g = 0; g < NG; ++g) {
-                    uint32_t ra[32], rb[32];
-                    tmem_ld_32x32b_x32(tbase + g * GRP, ra);
-                    if (GRP == 64) tmem_ld_32x32b_x32(tbase + g * GRP + 32, rb);
-                    tmem_ld_wait(ra);
-                    if (GRP == 64) tmem_ld_tie(rb);
+                    uint32_t r[LPW][LW];
+                    #pragma unroll
+                    for (int h = 0; h < LPW; ++h) tmem_ld_cols(tbase + (g * LPW + h) * LW, r[h]);
+                    #pragma unroll
+                    for (int h = 0; h < LPW; ++h) tmem_ld_wait(r[h]);
                     if (g == NG - 1) {
                         // the whole partial is in registers: hand the TMEM buffer back
                         tc_fence_before();
@@ -307,30 +407,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[ts]));
                     }
                     #pragma unroll
-                    for (int h = 0; h < GRP / 32; ++h) {
-                        uint32_t(&r)[32] = h ? rb : ra;
-                        const int c0 = g * GRP + h * 32;   // first column of these 32
+                    for (int h = 0; h < LPW; ++h) {
+                        const int c0 = (g * LPW + h) * LW;   // first column of these LW
                         if (B_MODE == SCALE_BLOCK) {
                             #pragma unroll
-                            for (int j = 0; j < 32; j += 2)
-                                acc[(c0 + j) / 2] = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                            for (int j = 0; j < LW; j += 2)
+                                acc[(c0 + j) / 2] = __ffma2_rn(make_float2(__uint_as_float(r[h][j]), __uint_as_float(r[h][j + 1])),
                                                                f2, acc[(c0 + j) / 2]);
                         } else {
                             #pragma unroll
-                            for (int j = 0; j < 32; j += 4) {
+                            for (int j = 0; j < LW; j += 4) {
                                 const float4 b4 = *reinterpret_cast<const float4*>(sbv + c0 + j);
                                 const float2 s01 = __fmul2_rn(f2, make_float2(b4.x, b4.y));
                                 const float2 s23 = __fmul2_rn(f2, make_float2(b4.z, b4.w));
-                                acc[(c0 + j) / 2] = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                                acc[(c0 + j) / 2] = __ffma2_rn(make_float2(__uint_as_float(r[h][j]), __uint_as_float(r[h][j + 1])),
                                                                s01, acc[(c0 + j) / 2]);
-                                acc[(c0 + j) / 2 + 1] = __ffma2_rn(make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                                acc[(c0 + j) / 2 + 1] = __ffma2_rn(make_float2(__uint_as_float(r[h][j + 2]), __uint_as_float(r[h][j + 3])),
                                                                    s23, acc[(c0 + j) / 2 + 1]);
                             }
                         }
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sempty_bar[ss]));
+                if (S::RING) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sempty_bar[ss]));
+                }
             }
 
             if (!SPLITK || p.splits <= 1) {
@@ -338,7 +439,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (ok && r1 < p.R1 && n0 < p.R2) {
                     uint16_t* dst = p.c + r1 * p.ldc + n0;
                     #pragma unroll
-                    for (int c = 0; c < HALF; c += 8) {
+                    for (int c = 0; c < COLS; c += 8) {
                         uint4 v;
                         v.x = pack_bf16x2(acc[c / 2 + 0].x, acc[c / 2 + 0].y);
                         v.y = pack_bf16x2(acc[c / 2 + 1].x, acc[c / 2 + 1].y);
@@ -356,22 +457,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                ((int64_t)w.tile * p.splits + w.split) * (int64_t)(BN * 32) +
                                (int64_t)(col_base / 4) * 128 + row_local;
                 #pragma unroll
-                for (int c = 0; c < HALF; c += 4)
+                for (int c = 0; c < COLS; c += 4)
                     __stcg(part + (c / 4) * 128, make_float4(acc[c / 2].x, acc[c / 2].y, acc[c / 2 + 1].x, acc[c / 2 + 1].y));
                 __threadfence();
-                named_bar_sync(1, 256);
+                named_bar_sync(1, 32 * kEpiWarps);
                 if (ew == 0 && lane == 0) {
                     const unsigned prev = atomicAdd(p.counters + w.tile, 1u);
                     *last_flag = (prev == (unsigned)p.splits - 1) ? 1 : 0;
                 }
-                named_bar_sync(1, 256);
+                named_bar_sync(1, 32 * kEpiWarps);
                 if (*last_flag) {
                     __threadfence();
                     const float4* tile_ws = reinterpret_cast<const float4*>(p.ws) +
                                             (int64_t)w.tile * p.splits * (int64_t)(BN * 32) +
                                             (int64_t)(col_base / 4) * 128 + row_local;
                     #pragma unroll 1
-                    for (int c0 = 0; c0 < HALF; c0 += 32) {
+                    for (int c0 = 0; c0 < COLS; c0 += 32) {
                         float4 sum[8];
                         #pragma unroll
                         for (int j = 0; j < 8; ++j) sum[j] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -418,15 +519,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             }
                         }
                     }
-                    named_bar_sync(1, 256);
+                    named_bar_sync(1, 32 * kEpiWarps);
                     if (ew == 0 && lane == 0) {
                         p.counters[w.tile] = 0u;  // leave the counter ready for the next call
                         *last_flag = 0;
                     }
                 }
-                named_bar_sync(1, 256);
+                named_bar_sync(1, 32 * kEpiWarps);
             }
         }
+        if (SD == SD_THREAD) cp_async_wait_all();   // own scale copies land before exit
     }
 
     tc_fence_before();
@@ -442,31 +544,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // Host side
 // ------------------------------------------------------------------------------------
 
-template <int BN, int A_MODE, int B_MODE, int STAGES, bool SPLITK>
-static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                            int grid, cudaStream_t st) {
-    auto kern = k_gemm_bs<BN, A_MODE, B_MODE, STAGES, SPLITK>;
-    constexpr size_t smem = GemmSmem<BN, STAGES>::BYTES;
+template <int BN, int SD, int B_MODE, int STAGES, bool SPLITK>
+static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                            const CUtensorMap& tsb, const GemmParams& p, int grid, cudaStream_t st) {
+    auto kern = k_gemm_bs<BN, SD, B_MODE, STAGES, SPLITK>;
+    constexpr size_t smem = GemmSmem<BN, STAGES, B_MODE, SD>::BYTES;
     static_assert(smem <= 227 * 1024, "shared memory budget");
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kGemmThreads, smem, st>>>(ta, tb, p);
+    kern<<<grid, kGemmThreads, smem, st>>>(ta, tb, tsa, tsb, p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_tiled(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                              int b_mode, int bn, int grid, cudaStream_t st) {
-    if (bn == 128) {
-        if (b_mode == SCALE_BLOCK) return launch_t<128, SCALE_ROW, SCALE_BLOCK, 6, false>(ta, tb, p, grid, st);
-        return launch_t<128, SCALE_ROW, SCALE_ROW, 6, false>(ta, tb, p, grid, st);
+cudaError_t launch_gemm_tiled(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap* tsa,
+                              const CUtensorMap* tsb, const GemmParams& p, int b_mode, int bn, int grid,
+                              cudaStream_t st) {
+    if (b_mode == SCALE_ROW) {
+        // WGrad: both operands come from 128x1 quantization, every scale array is TMA-able
+        if (!tsa || !tsb) return cudaErrorInvalidValue;
+        if (bn == 128) return launch_t<128, SD_TMA, SCALE_ROW, 6, false>(ta, tb, *tsa, *tsb, p, grid, st);
+        return launch_t<256, SD_TMA, SCALE_ROW, 4, false>(ta, tb, *tsa, *tsb, p, grid, st);
     }
-    if (b_mode == SCALE_BLOCK) return launch_t<256, SCALE_ROW, SCALE_BLOCK, 4, false>(ta, tb, p, grid, st);
-    return launch_t<256, SCALE_ROW, SCALE_ROW, 4, false>(ta, tb, p, grid, st);
+    if (tsa && tsb) {
+        if (bn == 128) return launch_t<128, SD_TMA, SCALE_BLOCK, 6, false>(ta, tb, *tsa, *tsb, p, grid, st);
+        return launch_t<256, SD_TMA, SCALE_BLOCK, 4, false>(ta, tb, *tsa, *tsb, p, grid, st);
+    }
+    if (bn != 256) return cudaErrorInvalidValue;
+    return launch_t<256, SD_THREAD, SCALE_BLOCK, 4, false>(ta, tb, tb, tb, p, grid, st);
 }
 
-cudaError_t launch_gemm_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                               int grid, cudaStream_t st) {
-    return launch_t<256, SCALE_ROW, SCALE_BLOCK, 4, true>(ta, tb, p, grid, st);
+cudaError_t launch_gemm_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap* tsa,
+                               const CUtensorMap* tsb, const GemmParams& p, int grid, cudaStream_t st) {
+    if (tsa && tsb) return launch_t<256, SD_TMA, SCALE_BLOCK, 4, true>(ta, tb, *tsa, *tsb, p, grid, st);
+    return launch_t<256, SD_THREAD, SCALE_BLOCK, 4, true>(ta, tb, tb, tb, p, grid, st);
 }
 
 // ------------------------------------------------------------------------------------

@@ -24,8 +24,8 @@ enum ScaleMode : int {
 
 struct GemmParams {
     int64_t R1, R2, Kr;      // C is R1 x R2; reduction length Kr (multiple of 128)
-    const float* sa;         // scales of A (rows r1)
-    int64_t sa_kb, sa_r;
+    const float* sa;         // scales of A, one per row: sa[kb*sa_kb + r1]
+    int64_t sa_kb;
     const float* sb;         // scales of B (rows r2)
     int64_t sb_kb, sb_r;
     uint16_t* c;             // c[r1*ldc + r2]
@@ -38,10 +38,17 @@ struct GemmParams {
     uint64_t timeout_ns;
 };
 
-cudaError_t launch_gemm_tiled(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                              int b_mode, int bn, int grid, cudaStream_t st);
-cudaError_t launch_gemm_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                               int grid, cudaStream_t st);
+// Scale tensor maps (FP32, one K-block per box row): tsa over A's row scales
+// [K-block][R1], box 128 x 1; tsb over B's scales, box BN x 1 for row scales [K-block][R2],
+// 4 x BN/128 for block scales stored [column block][K-block] (sb_kb == 1), 4 x 1 for block
+// scales stored [K-block][column block].  With both maps the scales travel by TMA; when
+// either is null (strides that are not multiples of 16 bytes) each epilogue thread copies
+// its own.  B row scales (WGrad) always need both maps.
+cudaError_t launch_gemm_tiled(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap* tsa,
+                              const CUtensorMap* tsb, const GemmParams& p, int b_mode, int bn, int grid,
+                              cudaStream_t st);
+cudaError_t launch_gemm_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap* tsa,
+                               const CUtensorMap* tsb, const GemmParams& p, int grid, cudaStream_t st);
 cudaError_t launch_debug_wait_timeout(uint64_t timeout_ns, cudaStream_t st);
 
 // quantize.cu
