@@ -137,6 +137,21 @@ size_t decode_ws_bytes(int64_t M, int64_t N, int64_t K, int splits) {
     return b;
 }
 
+// 2-D tensor map of the BF16 output C [rows][ld] (ld a multiple of 8) for the GEMM's tile
+// stores: 32 x 32 boxes, 64-byte swizzle.
+fp8rl_status make_tmap_out(CUtensorMap* m, uint16_t* base, int64_t rows, int64_t cols, int64_t ld) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return FP8RL_ERR_CUDA;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t es[2] = {1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8RL_OK : FP8RL_ERR_CUDA;
+}
+
 // Tensor maps that let the GEMM's copy warp move the scales by TMA (see launch_gemm_tiled):
 // A's row scales [K-block][R1] need R1 % 4 == 0; B's block scales need 4 | K-blocks
 // ([column block][K-block] storage) or 4 | column blocks ([K-block][column block]); B's
@@ -202,8 +217,12 @@ fp8rl_status run_tiled(const TiledArgs& t, int grid_req, int bn_req, int num_sms
     p.timeout_ns = g_timeout_ns.load();
     int grid = grid_req > 0 ? grid_req : num_sms;
     grid = std::max(1, std::min(grid, p.num_items));
-    return cuda_status(launch_gemm_tiled(ta, tb, tma_scales ? &tsa : nullptr, tma_scales ? &tsb : nullptr, p,
-                                         t.b_mode, bn, grid, st));
+    if (t.ldc % 8 != 0) return FP8RL_ERR_ALIGN;
+    CUtensorMap tc;
+    e = make_tmap_out(&tc, t.c, t.R1, t.R2, t.ldc);
+    if (e != FP8RL_OK) return e;
+    return cuda_status(launch_gemm_tiled(ta, tb, tma_scales ? &tsa : nullptr, tma_scales ? &tsb : nullptr, tc,
+                                         p, t.b_mode, bn, grid, st));
 }
 
 fp8rl_status run_decode(const uint8_t* qx, const float* sx, const uint8_t* qw, const float* sw,

@@ -91,7 +91,7 @@ enum ScaleDelivery {
 
 // Shared-memory plan of one CTA.  Scale-ring slot: 128 scales of A (SD_TMA), then the
 // scales of B (BN for SCALE_ROW, a box of at most 8 block scales for SCALE_BLOCK).
-template <int BN, int STAGES, int B_MODE, int SD>
+template <int BN, int STAGES, int B_MODE, int SD, bool SPLITK>
 struct GemmSmem {
     static constexpr int A_BYTES = 128 * 128;                 // one 128x128 E4M3 tile of A
     static constexpr int B_BYTES = BN * 128;                  // one BNx128 E4M3 tile of B
@@ -109,8 +109,11 @@ struct GemmSmem {
     static constexpr int SC_WORDS = (B_MODE == SCALE_BLOCK) ? 2 : 1;
     static constexpr int SC_BYTES = (SD == SD_THREAD) ? kScalePD * SC_WORDS * 32 * kEpiWarps * 4 : 0;
     static constexpr int NBARS = 2 * STAGES + 2 * NTB + 2 * NS + 1;
+    // BF16 output staging for the TMA store: one 32 x 32 box per epilogue warp (the split-K
+    // form writes FP32 partials straight to global memory instead)
+    static constexpr int STAGE_C_BYTES = SPLITK ? 0 : kEpiWarps * 2048;
     static constexpr size_t BYTES = 1024 /* alignment slack */ + (size_t)STAGES * (A_BYTES + B_BYTES) +
-                                    RING_BYTES + SC_BYTES + NBARS * 8 + 16;
+                                    STAGE_C_BYTES + RING_BYTES + SC_BYTES + NBARS * 8 + 16;
 };
 
 // The scales one epilogue thread applies per K-block: the scale of its row of A and, when
@@ -157,8 +160,8 @@ template <int BN, int SD, int B_MODE, int STAGES, bool SPLITK>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_bs(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-              const GemmParams p) {
-    using S = GemmSmem<BN, STAGES, B_MODE, SD>;
+              const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+    using S = GemmSmem<BN, STAGES, B_MODE, SD, SPLITK>;
     constexpr int COLS = BN / (kEpiWarps / 4);   // columns per epilogue thread
     constexpr int LW = kEpiWarps == 16 ? 16 : 32; // columns per TMEM load
     constexpr int LPW = kEpiWarps == 16 ? 1 : 2;  // loads per wait
@@ -175,7 +178,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * S::A_BYTES;
-    float* ring = reinterpret_cast<float*>(sB + STAGES * S::B_BYTES);   // [NS][SLOT]
+    uint8_t* stage_c = sB + STAGES * S::B_BYTES;                     // [epilogue warp][2048]
+    float* ring = reinterpret_cast<float*>(stage_c + S::STAGE_C_BYTES);   // [NS][SLOT]
     float* sc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ring) + S::RING_BYTES);  // [PD][W][thr]
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sc) + S::SC_BYTES);
     uint64_t* full_bar = bars;                 // [STAGES] TMA -> MMA
@@ -213,6 +217,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tma_prefetch_desc(&tmB);
         if (SD == SD_TMA) tma_prefetch_desc(&tmSA);
         if (S::SLOT_B > 0) tma_prefetch_desc(&tmSB);
+        if (!SPLITK) tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -434,8 +439,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
             }
 
-            if (!SPLITK || p.splits <= 1) {
-                // ---- whole reduction in this CTA: BF16 row segment of this thread
+            if (!SPLITK) {
+                // ---- whole reduction in this CTA: the warp's 32 rows x COLS columns go out
+                // as 32 x 32 BF16 boxes staged in its own 2 KB buffer (64-byte swizzle: the
+                // 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3)) and written by
+                // TMA, which clips rows and columns outside C.
+                const uint32_t buf = smem_u32(stage_c + ew * 2048);
+                const int y0 = w.mt * 128 + quad * 32;
+                #pragma unroll
+                for (int q = 0; q < COLS / 32; ++q) {
+                    if (lane == 0) bulk_wait_read<0>();   // the previous box has left the buffer
+                    __syncwarp();
+                    #pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int cc = q * 32 + c * 8;    // first of these 8 columns
+                        uint4 v;
+                        v.x = pack_bf16x2(acc[cc / 2 + 0].x, acc[cc / 2 + 0].y);
+                        v.y = pack_bf16x2(acc[cc / 2 + 1].x, acc[cc / 2 + 1].y);
+                        v.z = pack_bf16x2(acc[cc / 2 + 2].x, acc[cc / 2 + 2].y);
+                        v.w = pack_bf16x2(acc[cc / 2 + 3].x, acc[cc / 2 + 3].y);
+                        st_shared_v4(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), v);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    const int x = w.nt * BN + col_base + q * 32;
+                    if (ok && lane == 0 && x < p.R2 && y0 < p.R1) {
+                        tma_store_2d(&tmC, buf, x, y0);
+                        bulk_commit();
+                    }
+                }
+            } else if (p.splits <= 1) {
+                // ---- split-K form run unsplit: BF16 row segment of this thread
                 if (ok && r1 < p.R1 && n0 < p.R2) {
                     uint16_t* dst = p.c + r1 * p.ldc + n0;
                     #pragma unroll
@@ -529,6 +563,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
         }
         if (SD == SD_THREAD) cp_async_wait_all();   // own scale copies land before exit
+        if (!SPLITK && lane == 0) bulk_wait_all();   // tile stores complete before exit
     }
 
     tc_fence_before();
@@ -546,37 +581,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 template <int BN, int SD, int B_MODE, int STAGES, bool SPLITK>
 static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                            const CUtensorMap& tsb, const GemmParams& p, int grid, cudaStream_t st) {
+                            const CUtensorMap& tsb, const CUtensorMap& tc, const GemmParams& p, int grid,
+                            cudaStream_t st) {
     auto kern = k_gemm_bs<BN, SD, B_MODE, STAGES, SPLITK>;
-    constexpr size_t smem = GemmSmem<BN, STAGES, B_MODE, SD>::BYTES;
+    constexpr size_t smem = GemmSmem<BN, STAGES, B_MODE, SD, SPLITK>::BYTES;
     static_assert(smem <= 227 * 1024, "shared memory budget");
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kGemmThreads, smem, st>>>(ta, tb, tsa, tsb, p);
+    kern<<<grid, kGemmThreads, smem, st>>>(ta, tb, tsa, tsb, tc, p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_tiled(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap* tsa,
-                              const CUtensorMap* tsb, const GemmParams& p, int b_mode, int bn, int grid,
-                              cudaStream_t st) {
+                              const CUtensorMap* tsb, const CUtensorMap& tc, const GemmParams& p, int b_mode,
+                              int bn, int grid, cudaStream_t st) {
     if (b_mode == SCALE_ROW) {
         // WGrad: both operands come from 128x1 quantization, every scale array is TMA-able
         if (!tsa || !tsb) return cudaErrorInvalidValue;
-        if (bn == 128) return launch_t<128, SD_TMA, SCALE_ROW, 6, false>(ta, tb, *tsa, *tsb, p, grid, st);
-        return launch_t<256, SD_TMA, SCALE_ROW, 4, false>(ta, tb, *tsa, *tsb, p, grid, st);
+        if (bn == 128) return launch_t<128, SD_TMA, SCALE_ROW, 6, false>(ta, tb, *tsa, *tsb, tc, p, grid, st);
+        return launch_t<256, SD_TMA, SCALE_ROW, 4, false>(ta, tb, *tsa, *tsb, tc, p, grid, st);
     }
     if (tsa && tsb) {
-        if (bn == 128) return launch_t<128, SD_TMA, SCALE_BLOCK, 6, false>(ta, tb, *tsa, *tsb, p, grid, st);
-        return launch_t<256, SD_TMA, SCALE_BLOCK, 4, false>(ta, tb, *tsa, *tsb, p, grid, st);
+        if (bn == 128) return launch_t<128, SD_TMA, SCALE_BLOCK, 6, false>(ta, tb, *tsa, *tsb, tc, p, grid, st);
+        return launch_t<256, SD_TMA, SCALE_BLOCK, 4, false>(ta, tb, *tsa, *tsb, tc, p, grid, st);
     }
     if (bn != 256) return cudaErrorInvalidValue;
-    return launch_t<256, SD_THREAD, SCALE_BLOCK, 4, false>(ta, tb, tb, tb, p, grid, st);
+    return launch_t<256, SD_THREAD, SCALE_BLOCK, 4, false>(ta, tb, tb, tb, tc, p, grid, st);
 }
 
 cudaError_t launch_gemm_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap* tsa,
                                const CUtensorMap* tsb, const GemmParams& p, int grid, cudaStream_t st) {
-    if (tsa && tsb) return launch_t<256, SD_TMA, SCALE_BLOCK, 4, true>(ta, tb, *tsa, *tsb, p, grid, st);
-    return launch_t<256, SD_THREAD, SCALE_BLOCK, 4, true>(ta, tb, tb, tb, p, grid, st);
+    // (the split-K form stores no BF16 boxes: tb stands in for the output map)
+    if (tsa && tsb) return launch_t<256, SD_TMA, SCALE_BLOCK, 4, true>(ta, tb, *tsa, *tsb, tb, p, grid, st);
+    return launch_t<256, SD_THREAD, SCALE_BLOCK, 4, true>(ta, tb, tb, tb, tb, p, grid, st);
 }
 
 // ------------------------------------------------------------------------------------

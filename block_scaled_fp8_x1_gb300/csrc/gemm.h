@@ -44,9 +44,10 @@ struct GemmParams {
 // scales stored [K-block][column block].  With both maps the scales travel by TMA; when
 // either is null (strides that are not multiples of 16 bytes) each epilogue thread copies
 // its own.  B row scales (WGrad) always need both maps.
+// tc: tensor map of C (BF16 [R1][ldc], box 32 x 32, 64-byte swizzle) for the tile stores.
 cudaError_t launch_gemm_tiled(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap* tsa,
-                              const CUtensorMap* tsb, const GemmParams& p, int b_mode, int bn, int grid,
-                              cudaStream_t st);
+                              const CUtensorMap* tsb, const CUtensorMap& tc, const GemmParams& p, int b_mode,
+                              int bn, int grid, cudaStream_t st);
 cudaError_t launch_gemm_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap* tsa,
                                const CUtensorMap* tsb, const GemmParams& p, int grid, cudaStream_t st);
 cudaError_t launch_debug_wait_timeout(uint64_t timeout_ns, cudaStream_t st);
