@@ -78,8 +78,8 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 constexpr int kEpiWarps = 8;
 constexpr int kGemmThreads = 128 + 32 * kEpiWarps;
 constexpr int kLaunchRegs = kEpiWarps == 16 ? 96 : 168;
-constexpr uint32_t kRegLo = kEpiWarps == 16 ? 32 : 40;
-constexpr uint32_t kRegHi = kEpiWarps == 16 ? 112 : 232;
+constexpr uint32_t kRegLo = kEpiWarps == 16 ? 32 : 56;
+constexpr uint32_t kRegHi = kEpiWarps == 16 ? 112 : 224;
 static_assert(128 * kRegLo + 32 * kEpiWarps * kRegHi <= kGemmThreads * kLaunchRegs, "register split");
 constexpr int kScalePD = 4;   // K-blocks of scale prefetch per epilogue thread
 
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     using S = GemmSmem<BN, STAGES, B_MODE, SD, SPLITK>;
     constexpr int COLS = BN / (kEpiWarps / 4);   // columns per epilogue thread
     constexpr int LW = kEpiWarps == 16 ? 16 : 32; // columns per TMEM load
-    constexpr int LPW = kEpiWarps == 16 ? 1 : 2;  // loads per wait
+    constexpr int LPW = 1;                        // loads per wait
     constexpr int NG = COLS / (LW * LPW);         // waits per K-block
     constexpr int NS = S::NS;
     constexpr int NTB = S::NTB;
