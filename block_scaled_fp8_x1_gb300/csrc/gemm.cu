@@ -387,49 +387,74 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (!ok) continue;
                 tc_fence_after();
                 const float* slot = ring + ss * S::SLOT;
-                if (SD == SD_TMA) {
-                    f = slot[row_local];
-                    if (B_MODE == SCALE_BLOCK) {
-                        const int cb = (int)(n0 >> 7);   // column block of this thread
-                        f *= slot[128 + (p.sb_kb == 1 ? ((cb - ((w.nt * BN) >> 7)) * 4 + (kb & 3)) : (cb & 3))];
+                if constexpr (B_MODE == SCALE_ROW) {
+                    // 16x256b fragments: this thread holds rows g + 8h (h = 0..3) of the warp's
+                    // 32 and columns 8j + 2tq + {0,1}, so it needs 4 row and 32 column scales
+                    // per K-block instead of 1 and 128.
+                    const int g = lane >> 2, tq = lane & 3;
+                    float fr[4];
+                    #pragma unroll
+                    for (int h = 0; h < 4; ++h) fr[h] = slot[quad * 32 + g + 8 * h];
+                    const float* sbv = slot + S::SLOT_A + col_base + 2 * tq;
+                    const uint32_t tb0 = tmem_base + ((uint32_t)(quad * 32) << 16) + ts * BN + col_base;
+                    const uint32_t tb1 = tb0 + (16u << 16);
+                    #pragma unroll
+                    for (int jg = 0; jg < COLS / 32; ++jg) {
+                        uint32_t r0[16], r1[16];   // rows g, g+8 | rows g+16, g+24
+                        tmem_ld_16x256b_x4(tb0 + jg * 32, r0);
+                        tmem_ld_16x256b_x4(tb1 + jg * 32, r1);
+                        tmem_ld_wait(r0);
+                        tmem_ld_wait(r1);
+                        if (jg == COLS / 32 - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[ts]));
+                        }
+                        #pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int j = jg * 4 + jj;
+                            const float2 sc = *reinterpret_cast<const float2*>(sbv + 8 * j);
+                            #pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const uint32_t* r = (h < 2) ? r0 : r1;
+                                const int o = 4 * jj + 2 * (h & 1);
+                                const float2 s2 = __fmul2_rn(make_float2(fr[h], fr[h]), sc);
+                                acc[h * (COLS / 8) + j] = __ffma2_rn(make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 1])),
+                                                                     s2, acc[h * (COLS / 8) + j]);
+                            }
+                        }
                     }
-                }
-                const float2 f2 = make_float2(f, f);
-                const float* sbv = slot + S::SLOT_A + col_base;
-                const uint32_t tbase = tmem_base + t_lane + ts * BN + col_base;
-                // LPW loads of LW columns per wait
-                #pragma unroll
-                for (int g = 0; g < NG; ++g) {
-                    uint32_t r[LPW][LW];
-                    #pragma unroll
-                    for (int h = 0; h < LPW; ++h) tmem_ld_cols(tbase + (g * LPW + h) * LW, r[h]);
-                    #pragma unroll
-                    for (int h = 0; h < LPW; ++h) tmem_ld_wait(r[h]);
-                    if (g == NG - 1) {
-                        // the whole partial is in registers: hand the TMEM buffer back
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[ts]));
-                    }
-                    #pragma unroll
-                    for (int h = 0; h < LPW; ++h) {
-                        const int c0 = (g * LPW + h) * LW;   // first column of these LW
+                } else {
+                                    if (SD == SD_TMA) {
+                        f = slot[row_local];
                         if (B_MODE == SCALE_BLOCK) {
+                            const int cb = (int)(n0 >> 7);   // column block of this thread
+                            f *= slot[128 + (p.sb_kb == 1 ? ((cb - ((w.nt * BN) >> 7)) * 4 + (kb & 3)) : (cb & 3))];
+                        }
+                    }
+                    const float2 f2 = make_float2(f, f);
+                    const uint32_t tbase = tmem_base + t_lane + ts * BN + col_base;
+                    // LPW loads of LW columns per wait
+                    #pragma unroll
+                    for (int g = 0; g < NG; ++g) {
+                        uint32_t r[LPW][LW];
+                        #pragma unroll
+                        for (int h = 0; h < LPW; ++h) tmem_ld_cols(tbase + (g * LPW + h) * LW, r[h]);
+                        #pragma unroll
+                        for (int h = 0; h < LPW; ++h) tmem_ld_wait(r[h]);
+                        if (g == NG - 1) {
+                            // the whole partial is in registers: hand the TMEM buffer back
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[ts]));
+                        }
+                        #pragma unroll
+                        for (int h = 0; h < LPW; ++h) {
+                            const int c0 = (g * LPW + h) * LW;   // first column of these LW
                             #pragma unroll
                             for (int j = 0; j < LW; j += 2)
                                 acc[(c0 + j) / 2] = __ffma2_rn(make_float2(__uint_as_float(r[h][j]), __uint_as_float(r[h][j + 1])),
                                                                f2, acc[(c0 + j) / 2]);
-                        } else {
-                            #pragma unroll
-                            for (int j = 0; j < LW; j += 4) {
-                                const float4 b4 = *reinterpret_cast<const float4*>(sbv + c0 + j);
-                                const float2 s01 = __fmul2_rn(f2, make_float2(b4.x, b4.y));
-                                const float2 s23 = __fmul2_rn(f2, make_float2(b4.z, b4.w));
-                                acc[(c0 + j) / 2] = __ffma2_rn(make_float2(__uint_as_float(r[h][j]), __uint_as_float(r[h][j + 1])),
-                                                               s01, acc[(c0 + j) / 2]);
-                                acc[(c0 + j) / 2 + 1] = __ffma2_rn(make_float2(__uint_as_float(r[h][j + 2]), __uint_as_float(r[h][j + 3])),
-                                                                   s23, acc[(c0 + j) / 2 + 1]);
-                            }
                         }
                     }
                 }
@@ -450,15 +475,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int q = 0; q < COLS / 32; ++q) {
                     if (lane == 0) bulk_wait_read<0>();   // the previous box has left the buffer
                     __syncwarp();
-                    #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int cc = q * 32 + c * 8;    // first of these 8 columns
-                        uint4 v;
-                        v.x = pack_bf16x2(acc[cc / 2 + 0].x, acc[cc / 2 + 0].y);
-                        v.y = pack_bf16x2(acc[cc / 2 + 1].x, acc[cc / 2 + 1].y);
-                        v.z = pack_bf16x2(acc[cc / 2 + 2].x, acc[cc / 2 + 2].y);
-                        v.w = pack_bf16x2(acc[cc / 2 + 3].x, acc[cc / 2 + 3].y);
-                        st_shared_v4(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), v);
+                    if constexpr (B_MODE == SCALE_ROW) {
+                        // rows g + 8h, columns 8j + 2tq + {0,1}: one BF16 pair per (row, chunk)
+                        const int g = lane >> 2, tq = lane & 3;
+                        #pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const int rl = g + 8 * h;
+                            #pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const float2 v = acc[h * (COLS / 8) + q * 4 + c];
+                                st_shared_b32(buf + rl * 64 + ((c ^ ((rl >> 1) & 3)) << 4) + 4 * tq,
+                                              pack_bf16x2(v.x, v.y));
+                            }
+                        }
+                    } else {
+                        #pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const int cc = q * 32 + c * 8;    // first of these 8 columns
+                            uint4 v;
+                            v.x = pack_bf16x2(acc[cc / 2 + 0].x, acc[cc / 2 + 0].y);
+                            v.y = pack_bf16x2(acc[cc / 2 + 1].x, acc[cc / 2 + 1].y);
+                            v.z = pack_bf16x2(acc[cc / 2 + 2].x, acc[cc / 2 + 2].y);
+                            v.w = pack_bf16x2(acc[cc / 2 + 3].x, acc[cc / 2 + 3].y);
+                            st_shared_v4(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), v);
+                        }
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
