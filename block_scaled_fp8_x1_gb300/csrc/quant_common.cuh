@@ -26,13 +26,57 @@ constexpr float kMinFastScale = 3.3881317890172014e-21f;  // 2^-68
 
 __device__ __forceinline__ bool scale_is_slow(float s) { return s < kMinFastScale; }
 
+// s = fl32(amax / 448).  From amax >= 2^-60 on, by Markstein's correction step with the
+// constant reciprocal RN(1/448): q = RN(amax * RN(1/448)), the residual amax - 448 q is
+// exact in one FMA, and RN(q + residual * RN(1/448)) is the correctly rounded quotient
+// (no intermediate is subnormal there).  Below that, IEEE division.  Every positive BF16
+// amax is checked against IEEE division by the exhaustive device test.
+__device__ __forceinline__ float scale_of_amax(float amax) {
+    constexpr float kR448 = 0x1.24924ap-9f;  // RN(1/448)
+    if (amax < 8.673617379884035e-19f)       // 2^-60
+        return __fdiv_rn(amax, 448.0f);
+    const float q = __fmul_rn(amax, kR448);
+    const float e = __fmaf_rn(-q, 448.0f, amax);
+    return __fmaf_rn(e, kR448, q);
+}
+
 __device__ __forceinline__ GroupScale make_scale(float amax) {
     GroupScale g;
-    g.s = __fdiv_rn(amax, 448.0f);
+    g.s = scale_of_amax(amax);
     g.zero = (g.s == 0.0f);
     g.slow = scale_is_slow(g.s);  // includes zero, which is handled first
     g.r = g.slow ? 0.0f : __frcp_rn(g.s);
     return g;
+}
+
+// Group constants of the branch-free encode: r = RN(1/s), and the sign mask that keeps the
+// sign of x in its code (0 for a zero group, whose codes are all 0x00: there s = r = 0 and
+// the correction step yields +0 for both signed zeros).  Slow groups (0 < s < 2^-68) are
+// flagged and re-encoded by division.
+struct FastScale {
+    float s, r;
+    uint32_t sm;
+    bool slow;
+};
+__device__ __forceinline__ FastScale fast_scale(float amax) {
+    FastScale f;
+    f.s = scale_of_amax(amax);
+    f.slow = f.s > 0.0f && scale_is_slow(f.s);
+    f.r = (f.s == 0.0f || f.slow) ? 0.0f : __frcp_rn(f.s);
+    f.sm = f.s == 0.0f ? 0u : 0x80000000u;
+    return f;
+}
+
+// Branch-free encode of a pair with one group (not slow): the correction step of
+// encode_pair, and the sign of x (under the group's sign mask) selected into the quotient
+// bits in one bitwise select.
+__device__ __forceinline__ uint32_t encode_pair_fast(float2 x, float s, float r, uint32_t sm) {
+    const float2 q = __fmul2_rn(x, make_float2(r, r));
+    const float2 e = __ffma2_rn(q, make_float2(-s, -s), x);
+    const float2 c = __ffma2_rn(e, make_float2(r, r), q);
+    const uint32_t c0 = (__float_as_uint(c.x) & ~sm) | (__float_as_uint(x.x) & sm);
+    const uint32_t c1 = (__float_as_uint(c.y) & ~sm) | (__float_as_uint(x.y) & sm);
+    return e4m3x2(__uint_as_float(c0), __uint_as_float(c1));
 }
 
 // amax of BF16 values given as raw bits, compared as integers (|x| order equals the

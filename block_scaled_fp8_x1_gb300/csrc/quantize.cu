@@ -156,6 +156,13 @@ __device__ __forceinline__ void rows_from_smem(const uint8_t* stage, const Panel
     }
 }
 
+// Codes of four pairs of one group whose scale is too small for the division-free encode
+// (0 < s < 2^-68): IEEE division.  Out of line: it runs only for such groups.
+__device__ __noinline__ uint4 encode4_slow(float2 x0, float2 x1, float2 x2, float2 x3, float s) {
+    return make_uint4(e4m3x2(__fdiv_rn(x0.x, s), __fdiv_rn(x0.y, s)), e4m3x2(__fdiv_rn(x1.x, s), __fdiv_rn(x1.y, s)),
+                      e4m3x2(__fdiv_rn(x2.x, s), __fdiv_rn(x2.y, s)), e4m3x2(__fdiv_rn(x3.x, s), __fdiv_rn(x3.y, s)));
+}
+
 // Input stages of the TMA ring (each a 128x128 BF16 tile; SiLU-mul stages gate and up).
 template <int PRO>
 struct PanelStages {
@@ -171,7 +178,7 @@ struct PanelStages {
 // thread 0 refills that stage, so copies of the next tiles overlap the current one's math.
 // RMSNorm streams the CTA's tiles twice: pass 1 sums squares, pass 2 quantizes.
 template <int PRO, bool ROW_OUT, bool COL_OUT>
-__global__ void __launch_bounds__(256) k_quant_panel(const __grid_constant__ CUtensorMap tmx,
+__global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ CUtensorMap tmx,
                                                      const PanelArgs a) {
     using PS = PanelStages<PRO>;
     constexpr int STAGES = PS::STAGES;
@@ -179,10 +186,7 @@ __global__ void __launch_bounds__(256) k_quant_panel(const __grid_constant__ CUt
     uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_smem_raw) + 127) & ~uintptr_t(127));
     __shared__ __align__(8) uint64_t full_bar[STAGES];
     __shared__ int abort_flag;
-    __shared__ __align__(16) uint32_t s_rowmax[64];     // 128 row maxima (BF16 bits)
-    __shared__ __align__(16) uint32_t s_colmax[8][64];  // per-warp column maxima
-    __shared__ __align__(16) float s_row_s[128], s_row_r[128];
-    __shared__ __align__(16) float s_col_s[128], s_col_r[128];
+    __shared__ __align__(16) uint32_t s_colmax[8][64];  // per-warp column maxima (BF16 bits, pairs)
     __shared__ __align__(16) float s_rstd[128];
     __shared__ __align__(16) F2 s_part[128];
 
@@ -290,89 +294,123 @@ __global__ void __launch_bounds__(256) k_quant_panel(const __grid_constant__ CUt
         const int64_t t = t_begin + item % n;
         uint32_t w[8][4];
         rows_from_smem<PRO>(stages + (item % STAGES) * PS::STAGE_BYTES, a, k0, R0, C0, s_rstd, w);
+        // each BF16 value unpacked once: xr[i][j] = columns (2j, 2j+1) of row i
+        float2 xr[8][4];
+        #pragma unroll
+        for (int i = 0; i < 8; ++i)
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) xr[i][j] = make_float2(bf16_lo(w[i][j]), bf16_hi(w[i][j]));
 
+        // group maxima (exact BF16 values): rows over the 16 lanes of the half-warp,
+        // columns over this warp's 16 rows here and over the 8 warps through shared memory
+        uint32_t pm[4];   // rows (2k, 2k+1) of this half, as BF16 bits
         if (ROW_OUT) {
-            uint32_t pm[4];
             #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t e = 0, o = 0;
+            for (int k = 0; k < 4; ++k) {
+                float m[2];
                 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    e = absmax2(e, w[2 * j][c]);
-                    o = absmax2(o, w[2 * j + 1][c]);
+                for (int e = 0; e < 2; ++e) {
+                    float v = 0.0f;
+                    #pragma unroll
+                    for (int j = 0; j < 4; ++j) v = fmaxf(v, fmaxf(fabsf(xr[2 * k + e][j].x), fabsf(xr[2 * k + e][j].y)));
+                    m[e] = v;
                 }
-                pm[j] = max(e & 0xFFFFu, e >> 16) | (max(o & 0xFFFFu, o >> 16) << 16);
+                pm[k] = (__float_as_uint(m[0]) >> 16) | (__float_as_uint(m[1]) & 0xFFFF0000u);
             }
             #pragma unroll
-            for (int off = 8; off >= 1; off >>= 1) {
+            for (int off = 8; off >= 1; off >>= 1)
                 #pragma unroll
-                for (int j = 0; j < 4; ++j) pm[j] = __vmaxu2(pm[j], __shfl_xor_sync(0xffffffffu, pm[j], off));
-            }
-            if (cl == 0) *reinterpret_cast<uint4*>(&s_rowmax[R0 / 2]) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
+                for (int k = 0; k < 4; ++k) pm[k] = __vmaxu2(pm[k], __shfl_xor_sync(0xffffffffu, pm[k], off));
         }
         if (COL_OUT) {
             uint32_t cm[4];
             #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                uint32_t c = 0;
+                float m0v = 0.0f, m1v = 0.0f;
                 #pragma unroll
-                for (int i = 0; i < 8; ++i) c = absmax2(c, w[i][j]);
-                cm[j] = __vmaxu2(c, __shfl_xor_sync(0xffffffffu, c, 16));
+                for (int i = 0; i < 8; ++i) {
+                    m0v = fmaxf(m0v, fabsf(xr[i][j].x));
+                    m1v = fmaxf(m1v, fabsf(xr[i][j].y));
+                }
+                cm[j] = (__float_as_uint(m0v) >> 16) | (__float_as_uint(m1v) & 0xFFFF0000u);
+                cm[j] = __vmaxu2(cm[j], __shfl_xor_sync(0xffffffffu, cm[j], 16));
             }
             if (half == 0) *reinterpret_cast<uint4*>(&s_colmax[warp][cl * 4]) = make_uint4(cm[0], cm[1], cm[2], cm[3]);
         }
-        __syncthreads();                                  // stage consumed: refill it
+        __syncthreads();                                  // stage consumed, column maxima published
         if (tid == 0 && issued < total) issue(issued++);
-        if (ROW_OUT && tid < 128) {
-            const uint32_t mx = reinterpret_cast<const uint16_t*>(s_rowmax)[tid];
-            const GroupScale g = make_scale(bf16_bits_amax_to_f32(mx));
-            s_row_s[tid] = g.s;
-            s_row_r[tid] = g.r;
-            if (m0 + tid < a.M) a.s[t * a.M + m0 + tid] = g.s;
-        }
-        if (COL_OUT && tid >= 128) {
-            const int c = tid - 128;
-            uint32_t mx = 0;
-            #pragma unroll
-            for (int ww = 0; ww < 8; ++ww) mx = max(mx, (uint32_t)reinterpret_cast<const uint16_t*>(s_colmax[ww])[c]);
-            const GroupScale g = make_scale(bf16_bits_amax_to_f32(mx));
-            s_col_s[c] = g.s;
-            s_col_r[c] = g.r;
-            a.sT[panel * a.K + k0 + c] = g.s;
-        }
-        __syncthreads();
+
         if (ROW_OUT) {
+            // lane cl computes the scale of row (cl & 7) of its half, then every lane takes
+            // the scales of its 8 rows from those lanes
+            const int ri = cl & 7;
+            const uint32_t pw = (ri >> 1) == 0 ? pm[0] : (ri >> 1) == 1 ? pm[1] : (ri >> 1) == 2 ? pm[2] : pm[3];
+            const FastScale fs = fast_scale(bf16_bits_amax_to_f32((ri & 1) ? (pw >> 16) : (pw & 0xFFFFu)));
+            if (cl < 8 && m0 + R0 + ri < a.M) a.s[t * a.M + m0 + R0 + ri] = fs.s;
             #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                GroupScale g;
-                g.s = s_row_s[R0 + i];
-                g.r = s_row_r[R0 + i];
-                g.zero = (g.s == 0.0f);
-                g.slow = scale_is_slow(g.s);
+                const int src = (lane & 16) | i;
+                const float si = __shfl_sync(0xffffffffu, fs.s, src);
+                const float ri_ = __shfl_sync(0xffffffffu, fs.r, src);
+                const uint32_t smi = si == 0.0f ? 0u : 0x80000000u;
                 uint32_t c[4];
                 #pragma unroll
-                for (int j = 0; j < 4; ++j) c[j] = encode_pair(bf16_lo(w[i][j]), bf16_hi(w[i][j]), g);
+                for (int j = 0; j < 4; ++j) c[j] = encode_pair_fast(xr[i][j], si, ri_, smi);
+                if (si > 0.0f && scale_is_slow(si)) {
+                    const uint4 v = encode4_slow(xr[i][0], xr[i][1], xr[i][2], xr[i][3], si);
+                    c[0] = v.x; c[1] = v.y; c[2] = v.z; c[3] = v.w;
+                }
                 const int64_t m = m0 + R0 + i;
                 if (m < a.M) stg_v2(a.q + m * a.K + k0 + C0, c[0] | (c[1] << 16), c[2] | (c[3] << 16));
             }
         }
         if (COL_OUT) {
+            // this half computes the scales of columns C0 + 4*half + {0..3} (from the 8 warps'
+            // maxima) and swaps them with the other half for the remaining four
+            uint32_t mx0 = 0, mx1 = 0;
             #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                GroupScale g;
-                g.s = s_col_s[C0 + j];
-                g.r = s_col_r[C0 + j];
-                g.zero = (g.s == 0.0f);
-                g.slow = scale_is_slow(g.s);
+            for (int ww = 0; ww < 8; ++ww) {
+                const uint2 v = *reinterpret_cast<const uint2*>(&s_colmax[ww][cl * 4 + 2 * half]);
+                mx0 = __vmaxu2(mx0, v.x);
+                mx1 = __vmaxu2(mx1, v.y);
+            }
+            const uint32_t mb[4] = {mx0 & 0xFFFFu, mx0 >> 16, mx1 & 0xFFFFu, mx1 >> 16};
+            float os[4], orr[4];
+            #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const FastScale f = fast_scale(bf16_bits_amax_to_f32(mb[e]));
+                os[e] = f.s;
+                orr[e] = f.r;
+            }
+            if (warp == 0)
+                *reinterpret_cast<float4*>(a.sT + panel * a.K + k0 + C0 + 4 * half) = make_float4(os[0], os[1], os[2], os[3]);
+            float cs[8], cr[8];
+            #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float ts = __shfl_xor_sync(0xffffffffu, os[e], 16);
+                const float tr = __shfl_xor_sync(0xffffffffu, orr[e], 16);
+                cs[e] = half ? ts : os[e];
+                cr[e] = half ? tr : orr[e];
+                cs[4 + e] = half ? os[e] : ts;
+                cr[4 + e] = half ? orr[e] : tr;
+            }
+            #pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+                const int j = cc >> 1;
+                const uint32_t smc = cs[cc] == 0.0f ? 0u : 0x80000000u;
+                float2 x[4];
+                #pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    x[k] = (cc & 1) ? make_float2(xr[2 * k][j].y, xr[2 * k + 1][j].y)
+                                    : make_float2(xr[2 * k][j].x, xr[2 * k + 1][j].x);
                 uint32_t c[4];
                 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t wa = w[2 * i][j >> 1], wb = w[2 * i + 1][j >> 1];
-                    const float xa = (j & 1) ? bf16_hi(wa) : bf16_lo(wa);
-                    const float xb = (j & 1) ? bf16_hi(wb) : bf16_lo(wb);
-                    c[i] = encode_pair(xa, xb, g);
+                for (int k = 0; k < 4; ++k) c[k] = encode_pair_fast(x[k], cs[cc], cr[cc], smc);
+                if (cs[cc] > 0.0f && scale_is_slow(cs[cc])) {
+                    const uint4 v = encode4_slow(x[0], x[1], x[2], x[3], cs[cc]);
+                    c[0] = v.x; c[1] = v.y; c[2] = v.z; c[3] = v.w;
                 }
-                stg_v2(a.qT + (k0 + C0 + j) * a.M + m0 + R0, c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+                stg_v2(a.qT + (k0 + C0 + cc) * a.M + m0 + R0, c[0] | (c[1] << 16), c[2] | (c[3] << 16));
             }
         }
     }
@@ -463,22 +501,38 @@ __global__ void __launch_bounds__(256) k_quant_128x128(const uint16_t* __restric
 }
 
 // ------------------------------------------------------------------------------------
-// Diagnostic: the production encode (reciprocal + correction) against IEEE division for
-// every BF16 group maximum in [amax_lo, amax_hi) and every BF16 x with |x| <= amax (both
-// signs, and both zeros).  Counts mismatching codes; records the first one found.
+// Diagnostic: the production scale (amax / 448 by correction step) and both production
+// encodes (the branching one and the branch-free one with its zero-group sign mask)
+// against IEEE division, for every BF16 group maximum in [amax_lo, amax_hi) and every BF16
+// x with |x| <= amax (both signs, and both zeros).  Counts mismatches; records the first
+// one found (x bits 0xFFFF: the scale itself).
 // ------------------------------------------------------------------------------------
 __global__ void k_debug_encode_check(uint32_t amax_lo, uint32_t amax_hi,
                                      unsigned long long* mismatches, uint32_t* first_bad) {
     unsigned long long bad = 0;
     for (uint32_t ab = amax_lo + blockIdx.x; ab < amax_hi; ab += gridDim.x) {
-        const GroupScale g = make_scale(bf16_bits_amax_to_f32(ab));
+        const float amax = bf16_bits_amax_to_f32(ab);
+        // reference: IEEE division for the scale and for every quotient
+        GroupScale ref;
+        ref.s = __fdiv_rn(amax, 448.0f);
+        ref.zero = (ref.s == 0.0f);
+        ref.slow = true;
+        ref.r = 0.0f;
+        const GroupScale g = make_scale(amax);
+        const FastScale f = fast_scale(amax);
+        if (threadIdx.x == 0 && (g.s != ref.s || f.s != ref.s || (!f.slow && f.s != 0.0f && f.r != __frcp_rn(f.s)))) {
+            ++bad;   // the scale itself (reported with x bits 0xFFFF)
+            atomicCAS(first_bad, 0xFFFFFFFFu, (ab << 16) | 0xFFFFu);
+        }
         // x magnitudes 0 .. ab, both signs: 2*(ab+1) values, two per encode
         for (uint32_t i = threadIdx.x; i <= ab; i += blockDim.x) {
             const float xp = __uint_as_float(i << 16);
             const float xn = __uint_as_float((i | 0x8000u) << 16);
+            const uint32_t want = encode_pair_ieee(xp, xn, ref);
             const uint32_t a = encode_pair(xp, xn, g);
-            const uint32_t b = encode_pair_ieee(xp, xn, g);
-            if (a != b) {
+            const uint32_t b = f.slow ? encode_pair_ieee(xp, xn, ref)
+                                      : encode_pair_fast(make_float2(xp, xn), f.s, f.r, f.sm);
+            if (a != want || b != want) {
                 ++bad;
                 atomicCAS(first_bad, 0xFFFFFFFFu, (ab << 16) | i);
             }
