@@ -49,34 +49,43 @@ __device__ __forceinline__ GroupScale make_scale(float amax) {
     return g;
 }
 
-// Group constants of the branch-free encode: r = RN(1/s), and the sign mask that keeps the
-// sign of x in its code (0 for a zero group, whose codes are all 0x00: there s = r = 0 and
-// the correction step yields +0 for both signed zeros).  Slow groups (0 < s < 2^-68) are
-// flagged and re-encoded by division.
+// Group constants of the branch-free encode.  The encode works on the negated quotient:
+// with nr = -RN(1/s), q' = RN(x nr) = -RN(x/s approx), e = RN(x + q' s) is the exact
+// residual and d = RN(q' + e nr) = -RN(x/s) exactly (round-to-nearest is symmetric), and
+// for x = -0 / +0 it gives +0 / -0.  Converting d and flipping the code's sign bit
+// therefore yields code(x/s) with the sign of zero kept, for two codes per bitwise op.
+// A zero group (s = 0) has nr = 0 and code mask 0, which clears its codes to 0x00.  Slow
+// groups (0 < s < 2^-68) are flagged and re-encoded by division.
 struct FastScale {
-    float s, r;
-    uint32_t sm;
+    float s, nr;       // scale, -RN(1/s)
+    uint32_t keep;     // code mask: 0xFFFFFFFF, or 0 for a zero group
     bool slow;
 };
 __device__ __forceinline__ FastScale fast_scale(float amax) {
     FastScale f;
     f.s = scale_of_amax(amax);
     f.slow = f.s > 0.0f && scale_is_slow(f.s);
-    f.r = (f.s == 0.0f || f.slow) ? 0.0f : __frcp_rn(f.s);
-    f.sm = f.s == 0.0f ? 0u : 0x80000000u;
+    f.nr = (f.s == 0.0f || f.slow) ? 0.0f : -__frcp_rn(f.s);
+    f.keep = f.s == 0.0f ? 0u : 0xFFFFFFFFu;
     return f;
 }
 
-// Branch-free encode of a pair with one group (not slow): the correction step of
-// encode_pair, and the sign of x (under the group's sign mask) selected into the quotient
-// bits in one bitwise select.
-__device__ __forceinline__ uint32_t encode_pair_fast(float2 x, float s, float r, uint32_t sm) {
-    const float2 q = __fmul2_rn(x, make_float2(r, r));
-    const float2 e = __ffma2_rn(q, make_float2(-s, -s), x);
-    const float2 c = __ffma2_rn(e, make_float2(r, r), q);
-    const uint32_t c0 = (__float_as_uint(c.x) & ~sm) | (__float_as_uint(x.x) & sm);
-    const uint32_t c1 = (__float_as_uint(c.y) & ~sm) | (__float_as_uint(x.y) & sm);
-    return e4m3x2(__uint_as_float(c0), __uint_as_float(c1));
+// Negated quotients of a pair under one group (not slow), converted: the codes of
+// -x0/s and -x1/s (bits 0-7 and 8-15); flip_codes() turns them into the codes of x/s.
+__device__ __forceinline__ uint32_t encode_pair_neg(float2 x, float s, float nr) {
+    const float2 qn = __fmul2_rn(x, make_float2(nr, nr));
+    const float2 e = __ffma2_rn(qn, make_float2(s, s), x);
+    const float2 d = __ffma2_rn(e, make_float2(nr, nr), qn);
+    return e4m3x2(d.x, d.y);
+}
+// Four codes (two encode_pair_neg results packed) -> codes of x/s, zero groups cleared.
+__device__ __forceinline__ uint32_t flip_codes(uint32_t lo_pair, uint32_t hi_pair, uint32_t keep) {
+    return ((lo_pair | (hi_pair << 16)) ^ 0x80808080u) & keep;
+}
+
+// Branch-free encode of one pair (for the exhaustive check): codes of x/s in bits 0-15.
+__device__ __forceinline__ uint32_t encode_pair_fast(float2 x, float s, float nr, uint32_t keep) {
+    return flip_codes(encode_pair_neg(x, s, nr), 0u, keep) & 0xFFFFu;
 }
 
 // amax of BF16 values given as raw bits, compared as integers (|x| order equals the

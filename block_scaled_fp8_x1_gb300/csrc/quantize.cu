@@ -294,28 +294,23 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
         const int64_t t = t_begin + item % n;
         uint32_t w[8][4];
         rows_from_smem<PRO>(stages + (item % STAGES) * PS::STAGE_BYTES, a, k0, R0, C0, s_rstd, w);
-        // each BF16 value unpacked once: xr[i][j] = columns (2j, 2j+1) of row i
-        float2 xr[8][4];
-        #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            #pragma unroll
-            for (int j = 0; j < 4; ++j) xr[i][j] = make_float2(bf16_lo(w[i][j]), bf16_hi(w[i][j]));
-
-        // group maxima (exact BF16 values): rows over the 16 lanes of the half-warp,
-        // columns over this warp's 16 rows here and over the 8 warps through shared memory
+        // group maxima (exact BF16 values) on the packed words with the sign bits cleared:
+        // rows over the 16 lanes of the half-warp, columns over this warp's 16 rows here and
+        // over the 8 warps through shared memory
         uint32_t pm[4];   // rows (2k, 2k+1) of this half, as BF16 bits
         if (ROW_OUT) {
             #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                float m[2];
+                uint32_t m2[2];
                 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    float v = 0.0f;
+                    uint32_t v = 0;
                     #pragma unroll
-                    for (int j = 0; j < 4; ++j) v = fmaxf(v, fmaxf(fabsf(xr[2 * k + e][j].x), fabsf(xr[2 * k + e][j].y)));
-                    m[e] = v;
+                    for (int j = 0; j < 4; ++j) v = absmax2(v, w[2 * k + e][j]);
+                    m2[e] = v;
                 }
-                pm[k] = (__float_as_uint(m[0]) >> 16) | (__float_as_uint(m[1]) & 0xFFFF0000u);
+                // per row: max of its two halves; rows 2k (low) and 2k+1 (high) in one word
+                pm[k] = __vmaxu2(__byte_perm(m2[0], m2[1], 0x5410), __byte_perm(m2[0], m2[1], 0x7632));
             }
             #pragma unroll
             for (int off = 8; off >= 1; off >>= 1)
@@ -326,17 +321,19 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
             uint32_t cm[4];
             #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                float m0v = 0.0f, m1v = 0.0f;
+                uint32_t c = 0;
                 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    m0v = fmaxf(m0v, fabsf(xr[i][j].x));
-                    m1v = fmaxf(m1v, fabsf(xr[i][j].y));
-                }
-                cm[j] = (__float_as_uint(m0v) >> 16) | (__float_as_uint(m1v) & 0xFFFF0000u);
-                cm[j] = __vmaxu2(cm[j], __shfl_xor_sync(0xffffffffu, cm[j], 16));
+                for (int i = 0; i < 8; ++i) c = absmax2(c, w[i][j]);
+                cm[j] = __vmaxu2(c, __shfl_xor_sync(0xffffffffu, c, 16));
             }
             if (half == 0) *reinterpret_cast<uint4*>(&s_colmax[warp][cl * 4]) = make_uint4(cm[0], cm[1], cm[2], cm[3]);
         }
+        // each BF16 value unpacked once: xr[i][j] = columns (2j, 2j+1) of row i
+        float2 xr[8][4];
+        #pragma unroll
+        for (int i = 0; i < 8; ++i)
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) xr[i][j] = make_float2(bf16_lo(w[i][j]), bf16_hi(w[i][j]));
         __syncthreads();                                  // stage consumed, column maxima published
         if (tid == 0 && issued < total) issue(issued++);
 
@@ -351,17 +348,19 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
             for (int i = 0; i < 8; ++i) {
                 const int src = (lane & 16) | i;
                 const float si = __shfl_sync(0xffffffffu, fs.s, src);
-                const float ri_ = __shfl_sync(0xffffffffu, fs.r, src);
-                const uint32_t smi = si == 0.0f ? 0u : 0x80000000u;
+                const float nri = __shfl_sync(0xffffffffu, fs.nr, src);
+                const uint32_t keep = si == 0.0f ? 0u : 0xFFFFFFFFu;
                 uint32_t c[4];
                 #pragma unroll
-                for (int j = 0; j < 4; ++j) c[j] = encode_pair_fast(xr[i][j], si, ri_, smi);
+                for (int j = 0; j < 4; ++j) c[j] = encode_pair_neg(xr[i][j], si, nri);
+                uint32_t lo = flip_codes(c[0], c[1], keep), hi = flip_codes(c[2], c[3], keep);
                 if (si > 0.0f && scale_is_slow(si)) {
                     const uint4 v = encode4_slow(xr[i][0], xr[i][1], xr[i][2], xr[i][3], si);
-                    c[0] = v.x; c[1] = v.y; c[2] = v.z; c[3] = v.w;
+                    lo = v.x | (v.y << 16);
+                    hi = v.z | (v.w << 16);
                 }
                 const int64_t m = m0 + R0 + i;
-                if (m < a.M) stg_v2(a.q + m * a.K + k0 + C0, c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+                if (m < a.M) stg_v2(a.q + m * a.K + k0 + C0, lo, hi);
             }
         }
         if (COL_OUT) {
@@ -380,7 +379,7 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
             for (int e = 0; e < 4; ++e) {
                 const FastScale f = fast_scale(bf16_bits_amax_to_f32(mb[e]));
                 os[e] = f.s;
-                orr[e] = f.r;
+                orr[e] = f.nr;
             }
             if (warp == 0)
                 *reinterpret_cast<float4*>(a.sT + panel * a.K + k0 + C0 + 4 * half) = make_float4(os[0], os[1], os[2], os[3]);
@@ -397,7 +396,7 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
             #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
                 const int j = cc >> 1;
-                const uint32_t smc = cs[cc] == 0.0f ? 0u : 0x80000000u;
+                const uint32_t keep = cs[cc] == 0.0f ? 0u : 0xFFFFFFFFu;
                 float2 x[4];
                 #pragma unroll
                 for (int k = 0; k < 4; ++k)
@@ -405,12 +404,14 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
                                     : make_float2(xr[2 * k][j].x, xr[2 * k + 1][j].x);
                 uint32_t c[4];
                 #pragma unroll
-                for (int k = 0; k < 4; ++k) c[k] = encode_pair_fast(x[k], cs[cc], cr[cc], smc);
+                for (int k = 0; k < 4; ++k) c[k] = encode_pair_neg(x[k], cs[cc], cr[cc]);
+                uint32_t lo = flip_codes(c[0], c[1], keep), hi = flip_codes(c[2], c[3], keep);
                 if (cs[cc] > 0.0f && scale_is_slow(cs[cc])) {
                     const uint4 v = encode4_slow(x[0], x[1], x[2], x[3], cs[cc]);
-                    c[0] = v.x; c[1] = v.y; c[2] = v.z; c[3] = v.w;
+                    lo = v.x | (v.y << 16);
+                    hi = v.z | (v.w << 16);
                 }
-                stg_v2(a.qT + (k0 + C0 + cc) * a.M + m0 + R0, c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+                stg_v2(a.qT + (k0 + C0 + cc) * a.M + m0 + R0, lo, hi);
             }
         }
     }
@@ -520,7 +521,7 @@ __global__ void k_debug_encode_check(uint32_t amax_lo, uint32_t amax_hi,
         ref.r = 0.0f;
         const GroupScale g = make_scale(amax);
         const FastScale f = fast_scale(amax);
-        if (threadIdx.x == 0 && (g.s != ref.s || f.s != ref.s || (!f.slow && f.s != 0.0f && f.r != __frcp_rn(f.s)))) {
+        if (threadIdx.x == 0 && (g.s != ref.s || f.s != ref.s || (!f.slow && f.s != 0.0f && -f.nr != __frcp_rn(f.s)))) {
             ++bad;   // the scale itself (reported with x bits 0xFFFF)
             atomicCAS(first_bad, 0xFFFFFFFFu, (ab << 16) | 0xFFFFu);
         }
@@ -531,7 +532,7 @@ __global__ void k_debug_encode_check(uint32_t amax_lo, uint32_t amax_hi,
             const uint32_t want = encode_pair_ieee(xp, xn, ref);
             const uint32_t a = encode_pair(xp, xn, g);
             const uint32_t b = f.slow ? encode_pair_ieee(xp, xn, ref)
-                                      : encode_pair_fast(make_float2(xp, xn), f.s, f.r, f.sm);
+                                      : encode_pair_fast(make_float2(xp, xn), f.s, f.nr, f.keep);
             if (a != want || b != want) {
                 ++bad;
                 atomicCAS(first_bad, 0xFFFFFFFFu, (ab << 16) | i);
