@@ -88,7 +88,7 @@ struct PanelArgs {
     float* s;               // scales s[K/128][M]
     uint8_t* qT;            // 128x1 codes, transposed: qT[K][M]
     float* sT;              // scales sT[M/128][K]
-    int tiles_per_cta;      // 128-column sub-tiles handled by one CTA
+    int tiles_per_cta;      // RMSNorm: 128-column sub-tiles handled by one CTA of a panel's cluster
     uint64_t timeout_ns;    // bound of every wait on a TMA copy
 };
 
@@ -172,7 +172,7 @@ struct PanelStages {
     static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 128;  // + alignment slack
 };
 
-// Each CTA owns one 128-row panel and `tiles_per_cta` consecutive 128-column tiles of it.
+// A CTA works through a sequence of 128x128 tiles (see tile_at below).
 // Thread 0 streams the tiles through a ring of TMA stages in shared memory; all threads
 // pull a tile into registers, and once everyone has it (the first barrier of the tile)
 // thread 0 refills that stage, so copies of the next tiles overlap the current one's math.
@@ -193,13 +193,29 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int half = lane >> 4, cl = lane & 15;
     const int R0 = 16 * warp + 8 * half, C0 = 8 * cl;
-    const int64_t panel = blockIdx.y;
-    const int64_t m0 = panel * 128;
     const int64_t ntiles = a.K / 128;
-    const int64_t t_begin = (int64_t)blockIdx.x * a.tiles_per_cta;
+    // Tile sequence of this CTA.  RMSNorm: tiles [t_begin, t_end) of panel blockIdx.y, its
+    // share of the panel's cluster (streamed twice).  Otherwise persistent: every
+    // gridDim.x-th (panel, tile) pair from blockIdx.x, so the TMA ring runs across tiles
+    // and panels without a cold start per CTA.
+    constexpr bool PERSIST = PRO != PRO_RMSNORM;
+    const int64_t rms_panel = blockIdx.y;
+    const int64_t rms_m0 = rms_panel * 128;
+    const int64_t all_tiles = ((a.M + 127) / 128) * ntiles;
+    const int64_t t_begin = PERSIST ? 0 : (int64_t)blockIdx.x * a.tiles_per_cta;
     const int64_t t_end = (t_begin + a.tiles_per_cta < ntiles) ? t_begin + a.tiles_per_cta : ntiles;
-    const int n = (int)(t_end - t_begin);
+    const int n = PERSIST ? (int)((all_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x) : (int)(t_end - t_begin);
     const int total = (PRO == PRO_RMSNORM) ? 2 * n : n;   // items streamed through the ring
+    auto tile_at = [&](int it, int64_t& pnl, int64_t& tt) {
+        if (PERSIST) {
+            const int64_t id = blockIdx.x + (int64_t)(it % n) * gridDim.x;
+            pnl = id / ntiles;
+            tt = id - pnl * ntiles;
+        } else {
+            pnl = rms_panel;
+            tt = t_begin + it % n;
+        }
+    };
 
     if (tid == 0) {
         for (int st = 0; st < STAGES; ++st) mbar_init(smem_u32(&full_bar[st]), 1);
@@ -210,7 +226,9 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
     __syncthreads();
     auto issue = [&](int item) {
         const int st = item % STAGES;
-        const int64_t k0 = (t_begin + item % n) * 128;
+        int64_t pnl, tt;
+        tile_at(item, pnl, tt);
+        const int64_t k0 = tt * 128, m0 = pnl * 128;
         const uint32_t bar = smem_u32(&full_bar[st]);
         uint8_t* dst = stages + st * PS::STAGE_BYTES;
         mbar_arrive_expect_tx(bar, PS::STAGE_BYTES);
@@ -281,7 +299,7 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
             const float ms = __double2float_rn(sum / (double)a.K);
             const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
             s_rstd[tid] = rstd;
-            const int64_t m = m0 + tid;
+            const int64_t m = rms_m0 + tid;
             if (ok && a.rstd_out && cluster.block_rank() == 0 && m < a.M) a.rstd_out[m] = rstd;
         }
         __syncthreads();
@@ -290,8 +308,9 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
     for (; ok && item < total; ++item) {
         ok = wait_item(item);
         if (!ok) break;
-        const int64_t k0 = (t_begin + item % n) * 128;
-        const int64_t t = t_begin + item % n;
+        int64_t panel, t;
+        tile_at(item, panel, t);
+        const int64_t k0 = t * 128, m0 = panel * 128;
         uint32_t w[8][4];
         rows_from_smem<PRO>(stages + (item % STAGES) * PS::STAGE_BYTES, a, k0, R0, C0, s_rstd, w);
         // group maxima (exact BF16 values) on the packed words with the sign bits cleared:
@@ -595,8 +614,21 @@ static cudaError_t launch_panel_t(const PanelArgs& a, int64_t in_cols, int clust
     if (e != cudaSuccess) return e;
     const int64_t ntiles = a.K / 128;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((ntiles + a.tiles_per_cta - 1) / a.tiles_per_cta),
-                       (unsigned)((a.M + 127) / 128), 1);
+    if (PRO == PRO_RMSNORM) {
+        cfg.gridDim = dim3((unsigned)((ntiles + a.tiles_per_cta - 1) / a.tiles_per_cta),
+                           (unsigned)((a.M + 127) / 128), 1);
+    } else {
+        // persistent: as many CTAs as fit on the GPU at once, at most one per tile
+        static const int resident = [&] {
+            int dev = 0, sms = 0, per_sm = 0;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem);
+            return std::max(1, sms * std::max(1, per_sm));
+        }();
+        const int64_t all_tiles = ((a.M + 127) / 128) * ntiles;
+        cfg.gridDim = dim3((unsigned)std::min<int64_t>(all_tiles, resident), 1, 1);
+    }
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -614,14 +646,12 @@ static cudaError_t launch_panel_t(const PanelArgs& a, int64_t in_cols, int clust
 }
 
 // Column tiles per CTA for the streaming kernels: enough to keep the TMA ring busy.
-static int stream_tiles_per_cta(int64_t ntiles) { return (int)std::min<int64_t>(ntiles, 4); }
 
 // quantize 1x128 with the transposed 128x1 output (dual), or 128x1 alone
 cudaError_t launch_quant_dual(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
                               float* s, uint8_t* qT, float* sT, uint64_t timeout_ns, cudaStream_t st) {
     PanelArgs a = {};
     a.x = x; a.ldx = ldx; a.M = M; a.K = K; a.q = q; a.s = s; a.qT = qT; a.sT = sT;
-    a.tiles_per_cta = stream_tiles_per_cta(K / 128);
     a.timeout_ns = timeout_ns;
     if (q) return launch_panel_t<PRO_COPY, true, true>(a, K, 0, st);
     return launch_panel_t<PRO_COPY, false, true>(a, K, 0, st);
@@ -631,7 +661,6 @@ cudaError_t launch_silu_mul_quant(const uint16_t* gu, int64_t M, int64_t I, uint
                                   uint8_t* qT, float* sT, uint64_t timeout_ns, cudaStream_t st) {
     PanelArgs a = {};
     a.x = gu; a.ldx = 2 * I; a.M = M; a.K = I; a.q = q; a.s = s; a.qT = qT; a.sT = sT;
-    a.tiles_per_cta = stream_tiles_per_cta(I / 128);
     a.timeout_ns = timeout_ns;
     if (qT) return launch_panel_t<PRO_SILU, true, true>(a, 2 * I, 0, st);
     return launch_panel_t<PRO_SILU, true, false>(a, 2 * I, 0, st);
