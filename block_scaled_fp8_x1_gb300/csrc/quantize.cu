@@ -168,7 +168,9 @@ template <int PRO>
 struct PanelStages {
     static constexpr int NIN = (PRO == PRO_SILU) ? 2 : 1;
     static constexpr int STAGE_BYTES = NIN * 128 * 128 * 2;
-    static constexpr int STAGES = (PRO == PRO_SILU) ? 3 : 3;
+    // SiLU-mul stages 64 KB per tile: one stage lets two CTAs share an SM, which hides the
+    // copy latency better than three stages in one CTA (0.186 vs 0.242 ms at 8192x14336)
+    static constexpr int STAGES = (PRO == PRO_SILU) ? 1 : 3;
     static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 128;  // + alignment slack
 };
 
