@@ -116,7 +116,10 @@ constexpr int kDecodeBN = 256;
 int64_t decode_tiles(int64_t M, int64_t N) { return ((M + 127) / 128) * ((N + kDecodeBN - 1) / kDecodeBN); }
 
 // Slices per tile: as many as keep all (tile, slice) items within one wave of CTAs, at
-// most 16, and at least two K-blocks per slice.
+// most 16, and at least two K-blocks per slice.  Problems with a wave of tiles or more are
+// not split: writing and re-reading the FP32 partial sums and the last CTA's serial
+// reduction cost more than the unbalanced last wave (256 x 28672 x 4096: 62 us with two
+// slices, 44 us with one).
 int choose_splits(int64_t tiles, int64_t nkb, int num_sms) {
     if (tiles >= num_sms) return 1;
     int64_t s = num_sms / tiles;
@@ -494,10 +497,11 @@ fp8rl_status fp8rl_gemm_fwd_decode_noalloc(const uint8_t* qx, const float* sx, c
     fp8rl_status e = current_device(&sms);
     if (e != FP8RL_OK) return e;
     const int64_t tiles = decode_tiles(M, N);
-    const int splits = choose_splits(tiles, K / 128, sms);
-    const size_t need = decode_ws_bytes(M, N, K, splits);
     const size_t have = noalloc_scratch_bytes();
-    if (need > have) return FP8RL_ERR_WORKSPACE;
+    // the automatic split, or the largest smaller one whose partial sums fit the array
+    int splits = choose_splits(tiles, K / 128, sms);
+    while (splits > 1 && decode_ws_bytes(M, N, K, splits) > have) --splits;
+    if (decode_ws_bytes(M, N, K, splits) > have) return FP8RL_ERR_WORKSPACE;
     void* scratch = nullptr;
     if (noalloc_scratch(&scratch) != cudaSuccess) return FP8RL_ERR_CUDA;
     // the array keeps the previous call's contents: the arrival counters must start at zero

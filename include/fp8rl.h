@@ -224,14 +224,15 @@ FP8RL_API fp8rl_status fp8rl_gemm_fwd_ex(const uint8_t* qx, const float* sx, con
  * memory: a C/C++ decode loop that links only this library and owns no allocator, or a
  * serving loop that must not allocate between decode steps (allocating and freeing
  * device memory can synchronize the device and stall the loop).
- * Same operands, layouts, result and numerics as fp8rl_gemm_fwd_ex with
- * FP8RL_VARIANT_SPLITK and automatic splits (M <= 256).  Its split-K partial sums and
+ * Same operands, layouts and numerics as fp8rl_gemm_fwd_ex with FP8RL_VARIANT_SPLITK
+ * and automatic splits (M <= 256); the result equals it within the GEMM tolerance (the
+ * split, and with it the summation order, may differ).  Its split-K partial sums and
  * arrival counters live in a fixed scratch array inside the library,
  * fp8rl_gemm_noalloc_scratch_bytes() bytes (32 MiB) per device, reserved on every GPU
  * that loads the library and held until the process exits.
- *   - A problem whose split needs more scratch than that returns FP8RL_ERR_WORKSPACE and
- *     launches nothing (the automatic split keeps at most one CTA wave of 128x256 FP32
- *     partial tiles, under 20 MiB on a 152-SM GPU); M > 256 returns FP8RL_ERR_SHAPE.
+ *   - When the automatic split needs more scratch than that, the largest smaller split
+ *     that fits is used (one slice always fits); M > 256 returns FP8RL_ERR_SHAPE and
+ *     launches nothing.
  *   - The first call on a device looks up the array's device address (with that device
  *     current) and caches it; make that first call before any stream capture.
  *   - Every call on a device shares the array and clears its counters on entry (an

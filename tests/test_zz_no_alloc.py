@@ -30,7 +30,7 @@ def _stream():
 
 
 @pytest.mark.parametrize("M,N,K", [(64, 3584, 3584), (256, 4608, 3584), (7, 1280, 1024),
-                                   (256, 3584, 18944)])
+                                   (256, 3584, 18944), (256, 28672, 4096)])
 def test_noalloc_decode_matches_allocating_entry_point(fp8lib, M, N, K):
     lib = _abi.lib()
     x = synth.normal_bf16((M, K), 1.0, M + N, "cuda")
@@ -49,15 +49,26 @@ def test_noalloc_decode_matches_allocating_entry_point(fp8lib, M, N, K):
     assert fp8lib.check_status() == _abi.FP8RL_OK
 
 
-def test_noalloc_scratch_covers_decode_shapes_and_rejects_large_m(fp8lib):
+def test_noalloc_runs_every_decode_shape_and_rejects_large_m(fp8lib):
     lib = _abi.lib()
     cap = lib.fp8rl_gemm_noalloc_scratch_bytes()
     assert cap == 32 << 20
-    # the automatic split keeps every (tile, slice) item within one wave of CTAs, so the
-    # largest 256-token decode problems need far less scratch than the array holds
+    # every 256-token decode problem of the 7B and 32B layers runs inside the array: with
+    # the automatic split where its partial sums fit, else with a smaller one (zero
+    # operands, so the product is exactly zero)
     for N, K in [(4608, 3584), (3584, 3584), (37888, 3584), (3584, 18944), (7168, 5120),
                  (5120, 5120), (55296, 5120), (5120, 27648)]:
-        assert lib.fp8rl_gemm_workspace_bytes(_abi.FP8RL_OP_FWD, 256, N, K) <= cap
+        qx = torch.zeros((256, K), dtype=torch.uint8, device="cuda")
+        sx = torch.zeros((K // 128, 256), dtype=torch.float32, device="cuda")
+        qw = torch.zeros((N, K), dtype=torch.uint8, device="cuda")
+        sw = torch.zeros((N // 128, K // 128), dtype=torch.float32, device="cuda")
+        y = torch.full((256, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        st = lib.fp8rl_gemm_fwd_decode_noalloc(_p(qx), _p(sx), _p(qw), _p(sw), _p(y), 256, N, K, _stream())
+        assert st == _abi.FP8RL_OK, (N, K, _abi.STATUS_NAMES.get(st, st))
+        torch.cuda.synchronize()
+        assert bool((y == 0).all()), (N, K)
+        del qx, sx, qw, sw, y
     t = torch.zeros(64, dtype=torch.uint8, device="cuda")   # never read: rejected first
     st = lib.fp8rl_gemm_fwd_decode_noalloc(_p(t), _p(t), _p(t), _p(t), _p(t), 257, 128, 128, _stream())
     assert st == _abi.FP8RL_ERR_SHAPE
+    assert fp8lib.check_status() == _abi.FP8RL_OK
