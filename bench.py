@@ -225,6 +225,24 @@ class Step:
     LAUNCHES_PER_STEP = 16
 
 
+def max_over_ranks(ms: float, device) -> float:
+    """The largest of every rank's time (the job ends when its slowest replica does); the
+    time itself with a single rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(work_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the work every replica did, over the slowest replica's time
+    (work units per second)."""
+    return work_per_rank * world / (ms * 1e-3)
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -278,11 +296,7 @@ def run_gpu(args):
     clk = clocks.stop((w0, w1))
     st = ops.check_status()
 
-    ms_step = ms_total / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_total / args.steps, dev)
 
     # ---- end to end: host buffers, copies inside the timed region
     host_in = {n: torch.empty_like(getattr(step, n), device="cpu").pin_memory() for n in step.inputs}
@@ -310,11 +324,7 @@ def run_gpu(args):
         e2e_step()
     e1.record()
     barrier()
-    ms_e2e = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
 
     if rank != 0:
         if world > 1:
@@ -354,7 +364,7 @@ def run_gpu(args):
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 3), "traffic": load_traffic(dominant),
                 "kernel": dominant, "peak_note": f"{peaks['source']} copy bandwidth"}
-    value = step_flops * world / (ms_step * 1e-3) / 1e12
+    value = job_rate(step_flops, world, ms_step) / 1e12
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -365,7 +375,7 @@ def run_gpu(args):
                    "l2": "inputs larger than L2 (X 64 MB, W_gate_up 224 MB, dY_gate_up 448 MB per step)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
-        "e2e": {"value": round(step_flops * world / (ms_e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(job_rate(step_flops, world, ms_e2e) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4)},
         "gpu_launches": Step.LAUNCHES_PER_STEP * args.steps,
         "clocks": clk,
