@@ -61,7 +61,8 @@ def quant_bytes():
     E_x, E_h, E_gu = M_TOK * HID, M_TOK * INTER, M_TOK * 2 * INTER
     dual = lambda E: 2 * E + 2 * E + 2 * 4 * E / 128
     b = {}
-    b["wq_gate_up"] = 2 * E_gu + E_gu + E_gu + 4 * E_gu / 16384   # codes + W^T copy + scales
+    E_wgu = 2 * INTER * HID                                          # W_gate_up elements
+    b["wq_gate_up"] = 2 * E_wgu + E_wgu + E_wgu + 4 * E_wgu / 16384   # codes + W^T copy + scales
     E_w = HID * INTER
     b["wq_down"] = 2 * E_w + E_w + E_w + 4 * E_w / 16384
     b["rmsnorm_quant"] = dual(E_x) + 2 * HID + 4 * M_TOK

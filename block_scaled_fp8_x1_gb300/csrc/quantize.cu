@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(256) k_quant_128x128(const uint16_t* __restric
                                                        float* __restrict__ s,
                                                        uint8_t* __restrict__ qT) {
     __shared__ uint32_t s_wmax[8];
-    __shared__ float s_scale[2];
+    __shared__ FastScale s_fs;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int half = lane >> 4, cl = lane & 15;
     const int R0 = 16 * warp + 8 * half, C0 = 8 * cl;
@@ -485,40 +485,53 @@ __global__ void __launch_bounds__(256) k_quant_128x128(const uint16_t* __restric
         uint32_t m = 0;
         #pragma unroll
         for (int i = 0; i < 8; ++i) m = max(m, s_wmax[i]);
-        const GroupScale g = make_scale(bf16_bits_amax_to_f32(m));
-        s_scale[0] = g.s;
-        s_scale[1] = g.r;
-        s[bn * (K / 128) + bk] = g.s;
+        const FastScale f = fast_scale(bf16_bits_amax_to_f32(m));
+        s_fs = f;
+        s[bn * (K / 128) + bk] = f.s;
     }
     __syncthreads();
-    GroupScale g;
-    g.s = s_scale[0];
-    g.r = s_scale[1];
-    g.zero = (g.s == 0.0f);
-    g.slow = scale_is_slow(g.s);
-    // codes of the 8x8 block, row-major and (if wanted) transposed
+    const FastScale f = s_fs;
+    // codes of the 8x8 block, row-major: rc[i] = row i, columns 0-3 | 4-7
     uint32_t rc[8][2];
     #pragma unroll
     for (int i = 0; i < 8; ++i) {
         uint32_t c[4];
         #pragma unroll
-        for (int j = 0; j < 4; ++j) c[j] = encode_pair(bf16_lo(w[i][j]), bf16_hi(w[i][j]), g);
-        rc[i][0] = c[0] | (c[1] << 16);
-        rc[i][1] = c[2] | (c[3] << 16);
-        stg_v2(q + (n0 + R0 + i) * K + k0 + C0, rc[i][0], rc[i][1]);
+        for (int j = 0; j < 4; ++j) c[j] = encode_pair_neg(make_float2(bf16_lo(w[i][j]), bf16_hi(w[i][j])), f.s, f.nr);
+        rc[i][0] = flip_codes(c[0], c[1], f.keep);
+        rc[i][1] = flip_codes(c[2], c[3], f.keep);
     }
-    if (qT) {
-        // transpose the 8x8 byte block held in rc: byte (i, j) = row i, column j
+    if (f.slow) {   // tiny block scale: divide (whole CTA, rare)
         #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            uint32_t lo = 0, hi = 0;
-            #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                lo |= ((rc[i][j >> 2] >> (8 * (j & 3))) & 0xFFu) << (8 * i);
-                hi |= ((rc[i + 4][j >> 2] >> (8 * (j & 3))) & 0xFFu) << (8 * i);
-            }
-            stg_v2(qT + (k0 + C0 + j) * N + n0 + R0, lo, hi);
+        for (int i = 0; i < 8; ++i) {
+            const uint4 v = encode4_slow(make_float2(bf16_lo(w[i][0]), bf16_hi(w[i][0])),
+                                         make_float2(bf16_lo(w[i][1]), bf16_hi(w[i][1])),
+                                         make_float2(bf16_lo(w[i][2]), bf16_hi(w[i][2])),
+                                         make_float2(bf16_lo(w[i][3]), bf16_hi(w[i][3])), f.s);
+            rc[i][0] = v.x | (v.y << 16);
+            rc[i][1] = v.z | (v.w << 16);
         }
+    }
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) stg_v2(q + (n0 + R0 + i) * K + k0 + C0, rc[i][0], rc[i][1]);
+    if (qT) {
+        // transposed codes: four 4x4 byte transposes (rows 0-3 | 4-7 x columns 0-3 | 4-7)
+        uint32_t ct[8][2];   // ct[j] = column j, rows 0-3 | 4-7
+        #pragma unroll
+        for (int rh = 0; rh < 2; ++rh)
+            #pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                const uint32_t a0 = rc[4 * rh + 0][ch], a1 = rc[4 * rh + 1][ch];
+                const uint32_t a2 = rc[4 * rh + 2][ch], a3 = rc[4 * rh + 3][ch];
+                const uint32_t t0 = __byte_perm(a0, a1, 0x5140), t1 = __byte_perm(a0, a1, 0x7362);
+                const uint32_t t2 = __byte_perm(a2, a3, 0x5140), t3 = __byte_perm(a2, a3, 0x7362);
+                ct[4 * ch + 0][rh] = __byte_perm(t0, t2, 0x5410);
+                ct[4 * ch + 1][rh] = __byte_perm(t0, t2, 0x7632);
+                ct[4 * ch + 2][rh] = __byte_perm(t1, t3, 0x5410);
+                ct[4 * ch + 3][rh] = __byte_perm(t1, t3, 0x7632);
+            }
+        #pragma unroll
+        for (int j = 0; j < 8; ++j) stg_v2(qT + (k0 + C0 + j) * N + n0 + R0, ct[j][0], ct[j][1]);
     }
 }
 
