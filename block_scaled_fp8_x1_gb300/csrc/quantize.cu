@@ -315,9 +315,14 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
         const int64_t k0 = t * 128, m0 = panel * 128;
         uint32_t w[8][4];
         rows_from_smem<PRO>(stages + (item % STAGES) * PS::STAGE_BYTES, a, k0, R0, C0, s_rstd, w);
-        // group maxima (exact BF16 values) on the packed words with the sign bits cleared:
-        // rows over the 16 lanes of the half-warp, columns over this warp's 16 rows here and
-        // over the 8 warps through shared memory
+        // group maxima (exact BF16 values) on the packed words with the sign bits cleared
+        // (once per word): rows over the 16 lanes of the half-warp, columns over this warp's
+        // 16 rows here and over the 8 warps through shared memory
+        uint32_t wa[8][4];
+        #pragma unroll
+        for (int i = 0; i < 8; ++i)
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) wa[i][j] = w[i][j] & 0x7FFF7FFFu;
         uint32_t pm[4];   // rows (2k, 2k+1) of this half, as BF16 bits
         if (ROW_OUT) {
             #pragma unroll
@@ -325,9 +330,8 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
                 uint32_t m2[2];
                 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    uint32_t v = 0;
-                    #pragma unroll
-                    for (int j = 0; j < 4; ++j) v = absmax2(v, w[2 * k + e][j]);
+                    uint32_t v = __vmaxu2(wa[2 * k + e][0], wa[2 * k + e][1]);
+                    v = __vmaxu2(v, __vmaxu2(wa[2 * k + e][2], wa[2 * k + e][3]));
                     m2[e] = v;
                 }
                 // per row: max of its two halves; rows 2k (low) and 2k+1 (high) in one word
@@ -342,9 +346,8 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
             uint32_t cm[4];
             #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                uint32_t c = 0;
-                #pragma unroll
-                for (int i = 0; i < 8; ++i) c = absmax2(c, w[i][j]);
+                uint32_t c = __vmaxu2(__vmaxu2(wa[0][j], wa[1][j]), __vmaxu2(wa[2][j], wa[3][j]));
+                c = __vmaxu2(c, __vmaxu2(__vmaxu2(wa[4][j], wa[5][j]), __vmaxu2(wa[6][j], wa[7][j])));
                 cm[j] = __vmaxu2(c, __shfl_xor_sync(0xffffffffu, c, 16));
             }
             if (half == 0) *reinterpret_cast<uint4*>(&s_colmax[warp][cl * 4]) = make_uint4(cm[0], cm[1], cm[2], cm[3]);
