@@ -130,14 +130,12 @@ int choose_splits(int64_t tiles, int64_t nkb, int num_sms) {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-size_t counter_bytes(int64_t tiles) { return align_up((size_t)tiles * 4, 256); }
-
+// Workspace of the decode form: the FP32 partial sums of every (tile, slice) when the
+// reduction is split, nothing otherwise.
 size_t decode_ws_bytes(int64_t M, int64_t N, int64_t K, int splits) {
-    const int64_t tiles = decode_tiles(M, N);
-    size_t b = counter_bytes(tiles);
-    if (splits > 1) b += (size_t)tiles * splits * kDecodeBN * 128 * sizeof(float);
     (void)K;
-    return b;
+    if (splits <= 1) return 0;
+    return (size_t)decode_tiles(M, N) * splits * kDecodeBN * 128 * sizeof(float);
 }
 
 // 2-D tensor map of the BF16 output C [rows][ld] (ld a multiple of 8) for the GEMM's tile
@@ -236,8 +234,10 @@ fp8rl_status run_decode(const uint8_t* qx, const float* sx, const uint8_t* qw, c
     const int splits = splits_req > 0 ? (int)std::min<int64_t>(splits_req, nkb)
                                       : choose_splits(tiles, nkb, num_sms);
     const size_t need = decode_ws_bytes(M, N, K, splits);
-    if (ws == nullptr || ws_bytes < need) return FP8RL_ERR_WORKSPACE;
-    if (!aligned16(ws)) return FP8RL_ERR_ALIGN;
+    if (need > 0) {
+        if (ws == nullptr || ws_bytes < need) return FP8RL_ERR_WORKSPACE;
+        if (!aligned16(ws)) return FP8RL_ERR_ALIGN;
+    }
     CUtensorMap ta, tb;
     fp8rl_status e = make_tmap(&ta, qx, M, K, K, 128);
     if (e != FP8RL_OK) return e;
@@ -248,8 +248,7 @@ fp8rl_status run_decode(const uint8_t* qx, const float* sx, const uint8_t* qw, c
     p.sa = sx; p.sa_kb = M;
     p.sb = sw; p.sb_kb = 1; p.sb_r = K / 128;
     p.c = y; p.ldc = N;
-    p.counters = reinterpret_cast<unsigned int*>(ws);
-    p.ws = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + counter_bytes(tiles));
+    p.ws = reinterpret_cast<float*>(ws);
     p.splits = splits;
     p.m_tiles = (int)((M + 127) / 128);
     p.n_tiles = (int)((N + kDecodeBN - 1) / kDecodeBN);
@@ -504,8 +503,8 @@ fp8rl_status fp8rl_gemm_fwd_decode_noalloc(const uint8_t* qx, const float* sx, c
     if (decode_ws_bytes(M, N, K, splits) > have) return FP8RL_ERR_WORKSPACE;
     void* scratch = nullptr;
     if (noalloc_scratch(&scratch) != cudaSuccess) return FP8RL_ERR_CUDA;
-    // the array keeps the previous call's contents: the arrival counters must start at zero
-    if (cudaMemsetAsync(scratch, 0, counter_bytes(tiles), stream) != cudaSuccess) return FP8RL_ERR_CUDA;
+    // the array keeps the previous call's partial sums; every slice rewrites its own before
+    // the reduction reads it, so nothing needs clearing
     return run_decode(qx, sx, qw, sw, y, M, N, K, scratch, have, splits, sms, stream);
 }
 

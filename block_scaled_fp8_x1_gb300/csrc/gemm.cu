@@ -191,7 +191,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* drain_bar = sempty_bar + NS;     // [1] MMA completion at exit
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* last_flag = reinterpret_cast<int*>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -211,7 +210,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         mbar_init(smem_u32(drain_bar), 1);
         *abort_flag = 0;
-        *last_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
@@ -523,83 +521,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
             } else {
-                // ---- split-K: FP32 partial of this slice, then the last CTA of the tile sums
-                // the slices in slice order (deterministic) and stores BF16.  Partials are laid
-                // out [tile][slice][BN/4][128 rows][4] so that a warp's float4 accesses cover
-                // 32 consecutive rows: fully coalesced 512-byte transactions.
-                float4* part = reinterpret_cast<float4*>(p.ws) +
-                               ((int64_t)w.tile * p.splits + w.split) * (int64_t)(BN * 32) +
-                               (int64_t)(col_base / 4) * 128 + row_local;
-                #pragma unroll
-                for (int c = 0; c < COLS; c += 4)
-                    __stcg(part + (c / 4) * 128, make_float4(acc[c / 2].x, acc[c / 2].y, acc[c / 2 + 1].x, acc[c / 2 + 1].y));
-                __threadfence();
-                named_bar_sync(1, 32 * kEpiWarps);
-                if (ew == 0 && lane == 0) {
-                    const unsigned prev = atomicAdd(p.counters + w.tile, 1u);
-                    *last_flag = (prev == (unsigned)p.splits - 1) ? 1 : 0;
+                // ---- split-K: this slice's FP32 partial sums; k_splitk_reduce adds the slices
+                // in slice order.  Partials are laid out [tile][slice][BN/4][128 rows][4] so
+                // that a warp's float4 accesses cover 32 consecutive rows: fully coalesced
+                // 512-byte transactions.  Rows past R1 are not needed.
+                if (ok && r1 < p.R1) {
+                    float4* part = reinterpret_cast<float4*>(p.ws) +
+                                   ((int64_t)w.tile * p.splits + w.split) * (int64_t)(BN * 32) +
+                                   (int64_t)(col_base / 4) * 128 + row_local;
+                    #pragma unroll
+                    for (int c = 0; c < COLS; c += 4)
+                        __stcg(part + (c / 4) * 128, make_float4(acc[c / 2].x, acc[c / 2].y, acc[c / 2 + 1].x, acc[c / 2 + 1].y));
                 }
-                named_bar_sync(1, 32 * kEpiWarps);
-                if (*last_flag) {
-                    __threadfence();
-                    const float4* tile_ws = reinterpret_cast<const float4*>(p.ws) +
-                                            (int64_t)w.tile * p.splits * (int64_t)(BN * 32) +
-                                            (int64_t)(col_base / 4) * 128 + row_local;
-                    #pragma unroll 1
-                    for (int c0 = 0; c0 < COLS; c0 += 32) {
-                        float4 sum[8];
-                        #pragma unroll
-                        for (int j = 0; j < 8; ++j) sum[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        // the slices in slice order, two slices' loads in flight
-                        int sp = 0;
-                        #pragma unroll 1
-                        for (; sp + 2 <= p.splits; sp += 2) {
-                            float4 v[2][8];
-                            #pragma unroll
-                            for (int q = 0; q < 2; ++q)
-                                #pragma unroll
-                                for (int j = 0; j < 8; ++j)
-                                    v[q][j] = __ldcg(tile_ws + (int64_t)(sp + q) * (BN * 32) + (c0 / 4 + j) * 128);
-                            #pragma unroll
-                            for (int q = 0; q < 2; ++q)
-                                #pragma unroll
-                                for (int j = 0; j < 8; ++j) {
-                                    sum[j].x += v[q][j].x; sum[j].y += v[q][j].y;
-                                    sum[j].z += v[q][j].z; sum[j].w += v[q][j].w;
-                                }
-                        }
-                        #pragma unroll 1
-                        for (; sp < p.splits; ++sp) {
-                            float4 v[8];
-                            #pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                v[j] = __ldcg(tile_ws + (int64_t)sp * (BN * 32) + (c0 / 4 + j) * 128);
-                            #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                sum[j].x += v[j].x; sum[j].y += v[j].y;
-                                sum[j].z += v[j].z; sum[j].w += v[j].w;
-                            }
-                        }
-                        if (r1 < p.R1 && n0 + c0 < p.R2) {
-                            uint16_t* dst = p.c + r1 * p.ldc + n0 + c0;
-                            #pragma unroll
-                            for (int j = 0; j < 8; j += 2) {
-                                uint4 v;
-                                v.x = pack_bf16x2(sum[j].x, sum[j].y);
-                                v.y = pack_bf16x2(sum[j].z, sum[j].w);
-                                v.z = pack_bf16x2(sum[j + 1].x, sum[j + 1].y);
-                                v.w = pack_bf16x2(sum[j + 1].z, sum[j + 1].w);
-                                *reinterpret_cast<uint4*>(dst + 4 * j) = v;
-                            }
-                        }
-                    }
-                    named_bar_sync(1, 32 * kEpiWarps);
-                    if (ew == 0 && lane == 0) {
-                        p.counters[w.tile] = 0u;  // leave the counter ready for the next call
-                        *last_flag = 0;
-                    }
-                }
-                named_bar_sync(1, 32 * kEpiWarps);
             }
         }
         if (SD == SD_THREAD) cp_async_wait_all();   // own scale copies land before exit
@@ -649,11 +582,65 @@ cudaError_t launch_gemm_tiled(const CUtensorMap& ta, const CUtensorMap& tb, cons
     return launch_t<256, SD_THREAD, SCALE_BLOCK, 4, false>(ta, tb, tb, tb, tc, p, grid, st);
 }
 
+// Split-K reduction of the decode form: each output tile's FP32 slices summed in slice
+// order (deterministic: the same order whatever the timing), rounded to BF16.  One CTA of
+// 128 threads per (tile, 16-column chunk), thread t on row t of the tile, so the whole GPU
+// shares the reduction instead of one CTA per tile.
+constexpr int kSplitBN = 256;
+__global__ void __launch_bounds__(128) k_splitk_reduce(const GemmParams p) {
+    constexpr int CH = kSplitBN / 16;   // chunks per tile
+    const int tile = blockIdx.x / CH, chunk = blockIdx.x - tile * CH;
+    const WorkItem w = work_item(p, tile * p.splits);
+    const int64_t r1 = (int64_t)w.mt * 128 + threadIdx.x;
+    const int64_t c0 = (int64_t)w.nt * kSplitBN + chunk * 16;
+    if (r1 >= p.R1 || c0 >= p.R2) return;
+    const float4* src = reinterpret_cast<const float4*>(p.ws) + (int64_t)tile * p.splits * (kSplitBN * 32) +
+                        (int64_t)chunk * 4 * 128 + threadIdx.x;
+    float4 sum[4];
+    #pragma unroll
+    for (int j = 0; j < 4; ++j) sum[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    int sp = 0;
+    #pragma unroll 1
+    for (; sp + 4 <= p.splits; sp += 4) {   // four slices' loads in flight
+        float4 v[4][4];
+        #pragma unroll
+        for (int q = 0; q < 4; ++q)
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) v[q][j] = __ldcg(src + (int64_t)(sp + q) * (kSplitBN * 32) + j * 128);
+        #pragma unroll
+        for (int q = 0; q < 4; ++q)
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                sum[j].x += v[q][j].x; sum[j].y += v[q][j].y;
+                sum[j].z += v[q][j].z; sum[j].w += v[q][j].w;
+            }
+    }
+    #pragma unroll 1
+    for (; sp < p.splits; ++sp) {
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 v = __ldcg(src + (int64_t)sp * (kSplitBN * 32) + j * 128);
+            sum[j].x += v.x; sum[j].y += v.y; sum[j].z += v.z; sum[j].w += v.w;
+        }
+    }
+    uint4 o0, o1;
+    o0.x = pack_bf16x2(sum[0].x, sum[0].y); o0.y = pack_bf16x2(sum[0].z, sum[0].w);
+    o0.z = pack_bf16x2(sum[1].x, sum[1].y); o0.w = pack_bf16x2(sum[1].z, sum[1].w);
+    o1.x = pack_bf16x2(sum[2].x, sum[2].y); o1.y = pack_bf16x2(sum[2].z, sum[2].w);
+    o1.z = pack_bf16x2(sum[3].x, sum[3].y); o1.w = pack_bf16x2(sum[3].z, sum[3].w);
+    uint16_t* dst = p.c + r1 * p.ldc + c0;
+    *reinterpret_cast<uint4*>(dst) = o0;
+    *reinterpret_cast<uint4*>(dst + 8) = o1;
+}
+
 cudaError_t launch_gemm_splitk(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap* tsa,
                                const CUtensorMap* tsb, const GemmParams& p, int grid, cudaStream_t st) {
     // (the split-K form stores no BF16 boxes: tb stands in for the output map)
-    if (tsa && tsb) return launch_t<256, SD_TMA, SCALE_BLOCK, 4, true>(ta, tb, *tsa, *tsb, tb, p, grid, st);
-    return launch_t<256, SD_THREAD, SCALE_BLOCK, 4, true>(ta, tb, tb, tb, tb, p, grid, st);
+    cudaError_t e = (tsa && tsb) ? launch_t<kSplitBN, SD_TMA, SCALE_BLOCK, 4, true>(ta, tb, *tsa, *tsb, tb, p, grid, st)
+                                 : launch_t<kSplitBN, SD_THREAD, SCALE_BLOCK, 4, true>(ta, tb, tb, tb, tb, p, grid, st);
+    if (e != cudaSuccess || p.splits <= 1) return e;
+    k_splitk_reduce<<<p.m_tiles * p.n_tiles * (kSplitBN / 16), 128, 0, st>>>(p);
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------------------------

@@ -31,7 +31,6 @@ struct GemmParams {
     uint16_t* c;             // c[r1*ldc + r2]
     int64_t ldc;
     float* ws;               // split-K partials [tiles][splits][BN/4][128 rows][4]
-    unsigned int* counters;  // split-K arrival counters [tiles], zero between calls
     int splits;              // reduction slices per output tile (<= 1: none)
     int m_tiles, n_tiles, nkb;
     int num_items;

@@ -9,9 +9,9 @@
 // held until the process exits.
 //
 // The array keeps whatever the last call left in it, and every call on a device uses the
-// same array: the entry point clears the split-K arrival counters at the start of each
-// call, and calls whose kernels overlap on the GPU (different streams, no ordering) race
-// on the array and give wrong results.
+// same array.  Nothing in it needs clearing (each call's slices write their partial sums
+// before its reduction reads them), but calls whose kernels overlap on the GPU (different
+// streams, no ordering) race on the array and give wrong results.
 #include <mutex>
 
 #include "common.cuh"
@@ -19,9 +19,9 @@
 
 namespace fp8rl {
 
-// Arrival counters (one per 128-row output tile, padded to 256 bytes) followed by the
-// FP32 split-K partial tiles: 32 MiB covers every 256-token decode shape whose automatic
-// split needs up to 255 partial 256x128 tiles.
+// FP32 split-K partial tiles: 32 MiB holds 256 partial 128x256 tiles, which covers the
+// automatic split of the 7B and 32B decode shapes up to 256 tokens; a problem that would
+// need more runs with a smaller split.
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

@@ -191,10 +191,10 @@ def gemm_workspace_bytes(op: int, M: int, N: int, K: int) -> int:
 
 
 def workspace(nbytes: int, device: torch.device) -> torch.Tensor:
-    """A zero-initialised byte buffer of at least nbytes, cached per device.
+    """A byte buffer of at least nbytes, cached per device.
 
-    The split-K kernel leaves its arrival counters at zero after every call, so one
-    buffer serves every call issued in stream order on that device."""
+    It holds the decode form's split-K partial sums, which every call writes before it
+    reads them, so one buffer serves every call issued in stream order on that device."""
     key = (device.type, device.index)
     with _ws_lock:
         buf = _ws_cache.get(key)

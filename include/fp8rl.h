@@ -162,13 +162,13 @@ typedef enum { FP8RL_OP_FWD = 0, FP8RL_OP_DGRAD = 1, FP8RL_OP_WGRAD = 2 } fp8rl_
  *   qx : E4M3 [M][K] (1x128), sx : float [K/128][M]
  *   qw : E4M3 [N][K] (128x128), sw : float [N/128][K/128]
  *   y  : BF16 [M][N]
- * Small M (<= 256) takes the decode-shaped form (the same kernel with the reduction split
- * into slices over more CTAs, so that the weights stream through every SM; the slices'
- * FP32 partial sums are added in slice order by the last CTA of each output tile); it needs fp8rl_gemm_workspace_bytes(FP8RL_OP_FWD, M, N, K) bytes of
- * workspace.  The workspace must be zero-filled before its first use; every call that
- * completes leaves its arrival counters at zero again, so one workspace serves calls
- * issued in order on one stream (calls that overlap in time need separate workspaces;
- * after a device error, zero it again).  Larger M needs no workspace (ws may be NULL). */
+ * Small M (<= 256) takes the decode-shaped form: the same kernel with the reduction split
+ * into slices over more CTAs, so that the weights stream through every SM, and a second
+ * kernel that adds the slices' FP32 partial sums in slice order (the result does not
+ * depend on timing).  When it splits, it needs fp8rl_gemm_workspace_bytes(FP8RL_OP_FWD,
+ * M, N, K) bytes of workspace for the partial sums (no initial contents required); calls
+ * that overlap in time need separate workspaces.  A size of 0 (no split, or larger M)
+ * means ws may be NULL. */
 FP8RL_API fp8rl_status fp8rl_gemm_fwd(const uint8_t* qx, const float* sx, const uint8_t* qw,
                             const float* sw, uint16_t* y, int64_t M, int64_t N, int64_t K,
                             void* ws, size_t ws_bytes, fp8rl_stream_t stream);
@@ -226,8 +226,8 @@ FP8RL_API fp8rl_status fp8rl_gemm_fwd_ex(const uint8_t* qx, const float* sx, con
  * device memory can synchronize the device and stall the loop).
  * Same operands, layouts and numerics as fp8rl_gemm_fwd_ex with FP8RL_VARIANT_SPLITK
  * and automatic splits (M <= 256); the result equals it within the GEMM tolerance (the
- * split, and with it the summation order, may differ).  Its split-K partial sums and
- * arrival counters live in a fixed scratch array inside the library,
+ * split, and with it the summation order, may differ).  Its split-K partial sums live in
+ * a fixed scratch array inside the library,
  * fp8rl_gemm_noalloc_scratch_bytes() bytes (32 MiB) per device, reserved on every GPU
  * that loads the library and held until the process exits.
  *   - When the automatic split needs more scratch than that, the largest smaller split
@@ -235,9 +235,10 @@ FP8RL_API fp8rl_status fp8rl_gemm_fwd_ex(const uint8_t* qx, const float* sx, con
  *     launches nothing.
  *   - The first call on a device looks up the array's device address (with that device
  *     current) and caches it; make that first call before any stream capture.
- *   - Every call on a device shares the array and clears its counters on entry (an
- *     asynchronous memset on `stream`); calls whose kernels overlap on the GPU race on the
- *     array and give wrong results, so order them on one stream. */
+ *   - Every call on a device shares the array, which keeps the last call's partial sums
+ *     (each call writes its own before reading them, so nothing needs clearing); calls
+ *     whose kernels overlap on the GPU race on the array and give wrong results, so order
+ *     them on one stream. */
 FP8RL_API fp8rl_status fp8rl_gemm_fwd_decode_noalloc(const uint8_t* qx, const float* sx,
                                                      const uint8_t* qw, const float* sw,
                                                      uint16_t* y, int64_t M, int64_t N,

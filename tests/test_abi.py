@@ -76,10 +76,12 @@ def test_host_side_validation_without_gpu(abi):
 
 def test_workspace_sizes(abi):
     L = abi.lib()
-    # decode form (M <= 256) needs counters at least; tiled form needs none
-    assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 64, 3584, 3584) >= 256
+    # decode form (M <= 256) splitting the reduction needs its partial sums; tiled none
+    assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 64, 3584, 3584) > 0
     assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 8192, 3584, 3584) == 0
     assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_WGRAD, 8192, 3584, 3584) == 0
     opts = abi.GemmOpts(abi.FP8RL_VARIANT_SPLITK, 4, 0)
     need = L.fp8rl_gemm_workspace_bytes_ex(abi.FP8RL_OP_FWD, 256, 3584, 3584, ctypes.byref(opts))
-    assert need == 256 + 28 * 4 * 256 * 128 * 4
+    assert need == 28 * 4 * 256 * 128 * 4
+    one = abi.GemmOpts(abi.FP8RL_VARIANT_SPLITK, 1, 0)
+    assert L.fp8rl_gemm_workspace_bytes_ex(abi.FP8RL_OP_FWD, 256, 3584, 3584, ctypes.byref(one)) == 0
