@@ -75,7 +75,9 @@ __global__ void __launch_bounds__(256) k_quant_1x128(const uint16_t* __restrict_
 // ------------------------------------------------------------------------------------
 // Panel kernel: 128-row panels, 128-column sub-tiles, optional fused producer.
 // ------------------------------------------------------------------------------------
-enum Prologue : int { PRO_COPY = 0, PRO_SILU = 1, PRO_RMSNORM = 2 };
+// PRO_RMSNORM computes the rows' rstd itself (a cluster of CTAs per panel, two passes);
+// PRO_RMSNORM_G reads rstd computed beforehand by k_rms_rstd.
+enum Prologue : int { PRO_COPY = 0, PRO_SILU = 1, PRO_RMSNORM = 2, PRO_RMSNORM_G = 3 };
 
 struct PanelArgs {
     const uint16_t* x;      // COPY / RMSNORM: x[M][ldx];  SILU: gu[M][ldx], ldx = 2*K
@@ -116,10 +118,10 @@ __device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
 // 128x128 BF16 tile row-major (256 bytes per row); SiLU-mul stages the up tile after it.
 template <int PRO>
 __device__ __forceinline__ void rows_from_smem(const uint8_t* stage, const PanelArgs& a, int64_t k0,
-                                               int R0, int C0, const float* s_rstd,
+                                               int R0, int C0, const float* s_rstd, const float (&rg)[8],
                                                uint32_t (&w)[8][4]) {
     float gam[8];
-    if (PRO == PRO_RMSNORM) {
+    if (PRO == PRO_RMSNORM || PRO == PRO_RMSNORM_G) {
         const uint4 gv = ldg_nc_v4(a.gamma + k0 + C0);
         gam[0] = bf16_lo(gv.x); gam[1] = bf16_hi(gv.x);
         gam[2] = bf16_lo(gv.y); gam[3] = bf16_hi(gv.y);
@@ -133,8 +135,8 @@ __device__ __forceinline__ void rows_from_smem(const uint8_t* stage, const Panel
         if (PRO == PRO_COPY) {
             #pragma unroll
             for (int j = 0; j < 4; ++j) w[i][j] = xv[j];
-        } else if (PRO == PRO_RMSNORM) {
-            const float r = s_rstd[R0 + i];
+        } else if (PRO == PRO_RMSNORM || PRO == PRO_RMSNORM_G) {
+            const float r = (PRO == PRO_RMSNORM_G) ? rg[i] : s_rstd[R0 + i];
             #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const float y0 = __fmul_rn(__fmul_rn(bf16_lo(xv[j]), r), gam[2 * j]);
@@ -161,6 +163,42 @@ __device__ __forceinline__ void rows_from_smem(const uint8_t* stage, const Panel
 __device__ __noinline__ uint4 encode4_slow(float2 x0, float2 x1, float2 x2, float2 x3, float s) {
     return make_uint4(e4m3x2(__fdiv_rn(x0.x, s), __fdiv_rn(x0.y, s)), e4m3x2(__fdiv_rn(x1.x, s), __fdiv_rn(x1.y, s)),
                       e4m3x2(__fdiv_rn(x2.x, s), __fdiv_rn(x2.y, s)), e4m3x2(__fdiv_rn(x3.x, s), __fdiv_rn(x3.y, s)));
+}
+
+// rstd of every row for PRO_RMSNORM_G: one warp per row.  The squares are summed in
+// binary32 pairs with the exact two-sum (lane-strided 16-byte chunks, then a fixed
+// shuffle tree), so the total is known to about 2^-44 relative; then
+// rstd = 1 / sqrt(fl32(sum / K) + eps) in IEEE single precision.
+__global__ void __launch_bounds__(256) k_rms_rstd(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                                                  float eps, float* __restrict__ rstd) {
+    const int lane = threadIdx.x & 31;
+    const int64_t m = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (m >= M) return;
+    const uint16_t* row = x + m * K;
+    F2 acc = F2{0.0f, 0.0f};
+    #pragma unroll 4
+    for (int64_t c = (int64_t)lane * 8; c < K; c += 256) {
+        const uint4 v = ldg_nc_v4(row + c);
+        const uint32_t xv[4] = {v.x, v.y, v.z, v.w};
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float x0 = bf16_lo(xv[j]), x1 = bf16_hi(xv[j]);
+            acc = two_sum_acc(acc, __fmul_rn(x0, x0));
+            acc = two_sum_acc(acc, __fmul_rn(x1, x1));
+        }
+    }
+    #pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        F2 o;
+        o.hi = __shfl_xor_sync(0xffffffffu, acc.hi, off);
+        o.lo = __shfl_xor_sync(0xffffffffu, acc.lo, off);
+        acc = f2_add(acc, o);
+    }
+    if (lane == 0) {
+        const double sum = (double)acc.hi + (double)acc.lo;
+        const float ms = __double2float_rn(sum / (double)K);
+        rstd[m] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+    }
 }
 
 // Input stages of the TMA ring (each a 128x128 BF16 tile; SiLU-mul stages gate and up).
@@ -314,7 +352,11 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
         tile_at(item, panel, t);
         const int64_t k0 = t * 128, m0 = panel * 128;
         uint32_t w[8][4];
-        rows_from_smem<PRO>(stages + (item % STAGES) * PS::STAGE_BYTES, a, k0, R0, C0, s_rstd, w);
+        float rg[8];
+        #pragma unroll
+        for (int i = 0; i < 8; ++i)   // rows past M (TMA zero fill) are never stored
+            rg[i] = (PRO == PRO_RMSNORM_G && m0 + R0 + i < a.M) ? __ldg(a.rstd_out + m0 + R0 + i) : 0.0f;
+        rows_from_smem<PRO>(stages + (item % STAGES) * PS::STAGE_BYTES, a, k0, R0, C0, s_rstd, rg, w);
         // group maxima (exact BF16 values) on the packed words with the sign bits cleared
         // (once per word): rows over the 16 lanes of the half-warp, columns over this warp's
         // 16 rows here and over the 8 warps through shared memory
@@ -699,9 +741,19 @@ cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float
     PanelArgs a = {};
     a.x = x; a.ldx = K; a.gamma = gamma; a.eps = eps; a.rstd_out = rstd;
     a.M = M; a.K = K; a.q = q; a.s = s; a.qT = qT; a.sT = sT;
+    a.timeout_ns = timeout_ns;
+    if (rstd) {
+        // rstd into the caller's buffer first, then the persistent quantizer reads it
+        k_rms_rstd<<<(unsigned)((M + 7) / 8), 256, 0, st>>>(x, M, K, eps, rstd);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        if (qT) return launch_panel_t<PRO_RMSNORM_G, true, true>(a, K, 0, st);
+        return launch_panel_t<PRO_RMSNORM_G, true, false>(a, K, 0, st);
+    }
+    // no rstd buffer (the library allocates none): the cluster kernel computes rstd in
+    // shared memory
     const int c = rmsnorm_cluster_size(K);
     a.tiles_per_cta = (int)((K / 128) / c);
-    a.timeout_ns = timeout_ns;
     if (qT) return launch_panel_t<PRO_RMSNORM, true, true>(a, K, c, st);
     return launch_panel_t<PRO_RMSNORM, true, false>(a, K, c, st);
 }

@@ -6,7 +6,9 @@ and the transposed 128x1 copy for WGrad).
 
 RMSNorm: the device sums squares in a different order than the oracle's binary64 loop, so
 rstd may differ in the last place for rare rows.  Check: rstd bit-equal or within 1 ulp;
-then every code and scale bit-exact against the oracle fed the device's rstd.
+then every code and scale bit-exact against the oracle fed the device's rstd.  (With an
+rstd buffer the device computes rstd in a separate kernel first; without one, inside a
+cluster of CTAs per panel: both are covered.)
 
 SiLU-mul: the device evaluates silu(g)*u in binary32 (exp and a fast reciprocal), the
 oracle in binary64; they can round h to different BF16 neighbours only where the binary64
@@ -54,6 +56,32 @@ def test_rmsnorm_quant_rows_only(fp8lib, oracle, M, K):
     x = synth.normal_bf16((M, K), 1.0, 3 * M + K, "cuda")
     gamma = torch.ones(K, dtype=torch.bfloat16, device="cuda")
     check_rmsnorm(fp8lib, oracle, x, gamma, 1e-6, dual=False)
+
+
+@pytest.mark.parametrize("M,K", [(256, 640), (384, 1024), (128, 4096)])
+def test_rmsnorm_quant_without_rstd_buffer(fp8lib, M, K):
+    """Without an rstd buffer the library computes rstd inside a cluster of CTAs per panel
+    (it allocates nothing).  Its codes and scales equal those of the path that writes rstd
+    first, on these seeded inputs (the two sum the squares in different orders, which
+    could move rstd by one ulp only for a row whose mean square sits on a rounding
+    boundary of binary32)."""
+    import ctypes
+
+    from block_scaled_fp8_x1_gb300 import _abi
+    x = synth.normal_bf16((M, K), 1.0, 7 * M + K, "cuda", outlier_channels=2, outlier_scale=30.0)
+    gamma = synth.normal_bf16((K,), 0.1, 4, "cuda").float().add_(1.0).to(torch.bfloat16)
+    q1, s1, qT1, sT1, _ = fp8lib.rmsnorm_quant(x, gamma, 1e-5, dual=True)
+    q2, s2 = torch.empty_like(q1), torch.empty_like(s1)
+    qT2, sT2 = torch.empty_like(qT1), torch.empty_like(sT1)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = _abi.lib().fp8rl_rmsnorm_quant(p(x), p(gamma), ctypes.c_float(1e-5), M, K, p(q2), p(s2), p(qT2),
+                                        p(sT2), None, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == _abi.FP8RL_OK
+    torch.cuda.synchronize()
+    assert torch.equal(q1, q2) and torch.equal(qT1, qT2)
+    assert torch.equal(s1.view(torch.int32), s2.view(torch.int32))
+    assert torch.equal(sT1.view(torch.int32), sT2.view(torch.int32))
+    assert fp8lib.check_status() == _abi.FP8RL_OK
 
 
 def check_silu(fp8lib, oracle, gu, dual):
