@@ -158,6 +158,19 @@ __device__ __forceinline__ void rows_from_smem(const uint8_t* stage, const Panel
     }
 }
 
+// BF16 unpacking that the compiler may not merge with the plain one: the column codes
+// unpack again instead of keeping all 64 unpacked values live from the row codes.
+__device__ __forceinline__ float bf16_lo_v(uint32_t w) {
+    uint32_t r;
+    asm volatile("shl.b32 %0, %1, 16;" : "=r"(r) : "r"(w));
+    return __uint_as_float(r);
+}
+__device__ __forceinline__ float bf16_hi_v(uint32_t w) {
+    uint32_t r;
+    asm volatile("and.b32 %0, %1, 0xFFFF0000;" : "=r"(r) : "r"(w));
+    return __uint_as_float(r);
+}
+
 // Codes of four pairs of one group whose scale is too small for the division-free encode
 // (0 < s < 2^-68): IEEE division.  Out of line: it runs only for such groups.
 __device__ __noinline__ uint4 encode4_slow(float2 x0, float2 x1, float2 x2, float2 x3, float s) {
@@ -358,13 +371,9 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
             rg[i] = (PRO == PRO_RMSNORM_G && m0 + R0 + i < a.M) ? __ldg(a.rstd_out + m0 + R0 + i) : 0.0f;
         rows_from_smem<PRO>(stages + (item % STAGES) * PS::STAGE_BYTES, a, k0, R0, C0, s_rstd, rg, w);
         // group maxima (exact BF16 values) on the packed words with the sign bits cleared
-        // (once per word): rows over the 16 lanes of the half-warp, columns over this warp's
+        // rows over the 16 lanes of the half-warp, columns over this warp's
         // 16 rows here and over the 8 warps through shared memory
-        uint32_t wa[8][4];
-        #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            #pragma unroll
-            for (int j = 0; j < 4; ++j) wa[i][j] = w[i][j] & 0x7FFF7FFFu;
+        auto wa = [&](int i, int j) { return w[i][j] & 0x7FFF7FFFu; };
         uint32_t pm[4];   // rows (2k, 2k+1) of this half, as BF16 bits
         if (ROW_OUT) {
             #pragma unroll
@@ -372,8 +381,8 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
                 uint32_t m2[2];
                 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    uint32_t v = __vmaxu2(wa[2 * k + e][0], wa[2 * k + e][1]);
-                    v = __vmaxu2(v, __vmaxu2(wa[2 * k + e][2], wa[2 * k + e][3]));
+                    uint32_t v = __vmaxu2(wa(2 * k + e, 0), wa(2 * k + e, 1));
+                    v = __vmaxu2(v, __vmaxu2(wa(2 * k + e, 2), wa(2 * k + e, 3)));
                     m2[e] = v;
                 }
                 // per row: max of its two halves; rows 2k (low) and 2k+1 (high) in one word
@@ -388,18 +397,15 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
             uint32_t cm[4];
             #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                uint32_t c = __vmaxu2(__vmaxu2(wa[0][j], wa[1][j]), __vmaxu2(wa[2][j], wa[3][j]));
-                c = __vmaxu2(c, __vmaxu2(__vmaxu2(wa[4][j], wa[5][j]), __vmaxu2(wa[6][j], wa[7][j])));
+                uint32_t c = __vmaxu2(__vmaxu2(wa(0, j), wa(1, j)), __vmaxu2(wa(2, j), wa(3, j)));
+                c = __vmaxu2(c, __vmaxu2(__vmaxu2(wa(4, j), wa(5, j)), __vmaxu2(wa(6, j), wa(7, j))));
                 cm[j] = __vmaxu2(c, __shfl_xor_sync(0xffffffffu, c, 16));
             }
             if (half == 0) *reinterpret_cast<uint4*>(&s_colmax[warp][cl * 4]) = make_uint4(cm[0], cm[1], cm[2], cm[3]);
         }
-        // each BF16 value unpacked once: xr[i][j] = columns (2j, 2j+1) of row i
-        float2 xr[8][4];
-        #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            #pragma unroll
-            for (int j = 0; j < 4; ++j) xr[i][j] = make_float2(bf16_lo(w[i][j]), bf16_hi(w[i][j]));
+        // values are unpacked where they are encoded (once per direction): holding the 64
+        // unpacked floats would double the registers and halve the CTAs per SM
+        auto xrow = [&](int i, int j) { return make_float2(bf16_lo(w[i][j]), bf16_hi(w[i][j])); };
         __syncthreads();                                  // stage consumed, column maxima published
         if (tid == 0 && issued < total) issue(issued++);
 
@@ -418,10 +424,10 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
                 const uint32_t keep = si == 0.0f ? 0u : 0xFFFFFFFFu;
                 uint32_t c[4];
                 #pragma unroll
-                for (int j = 0; j < 4; ++j) c[j] = encode_pair_neg(xr[i][j], si, nri);
+                for (int j = 0; j < 4; ++j) c[j] = encode_pair_neg(xrow(i, j), si, nri);
                 uint32_t lo = flip_codes(c[0], c[1], keep), hi = flip_codes(c[2], c[3], keep);
                 if (si > 0.0f && scale_is_slow(si)) {
-                    const uint4 v = encode4_slow(xr[i][0], xr[i][1], xr[i][2], xr[i][3], si);
+                    const uint4 v = encode4_slow(xrow(i, 0), xrow(i, 1), xrow(i, 2), xrow(i, 3), si);
                     lo = v.x | (v.y << 16);
                     hi = v.z | (v.w << 16);
                 }
@@ -466,8 +472,8 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
                 float2 x[4];
                 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    x[k] = (cc & 1) ? make_float2(xr[2 * k][j].y, xr[2 * k + 1][j].y)
-                                    : make_float2(xr[2 * k][j].x, xr[2 * k + 1][j].x);
+                    x[k] = (cc & 1) ? make_float2(bf16_hi_v(w[2 * k][j]), bf16_hi_v(w[2 * k + 1][j]))
+                                    : make_float2(bf16_lo_v(w[2 * k][j]), bf16_lo_v(w[2 * k + 1][j]));
                 uint32_t c[4];
                 #pragma unroll
                 for (int k = 0; k < 4; ++k) c[k] = encode_pair_neg(x[k], cs[cc], cr[cc]);
