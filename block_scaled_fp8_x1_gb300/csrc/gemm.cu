@@ -71,16 +71,21 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// 4 warps (copies, MMA, two idle) + kEpiWarps epilogue warps, kEpiWarps / 4 per SM
+// 4 warps (copies, MMA, two idle) + epi_warps() epilogue warps, a quarter of them per SM
 // sub-partition (one warp's TMEM loads do not overlap each other, so the read rate grows
-// with the warps).  Register split: warpgroup 0 drops to kRegLo, the epilogue rises to
-// kRegHi, within the kLaunchRegs per thread the CTA is launched with.
-constexpr int kEpiWarps = 8;
-constexpr int kGemmThreads = 128 + 32 * kEpiWarps;
-constexpr int kLaunchRegs = kEpiWarps == 16 ? 96 : 168;
-constexpr uint32_t kRegLo = kEpiWarps == 16 ? 32 : 56;
-constexpr uint32_t kRegHi = kEpiWarps == 16 ? 112 : 224;
-static_assert(128 * kRegLo + 32 * kEpiWarps * kRegHi <= kGemmThreads * kLaunchRegs, "register split");
+// with the warps).  Row-scaled B (WGrad) does a multiply and an FMA per element and gains
+// from 16 warps; the block-scaled forms run faster with 8, which leaves each thread 224
+// registers.  Register split: warpgroup 0 drops to reg_lo(), the epilogue rises to
+// reg_hi(), within the launch_regs() per thread the CTA is launched with.
+__host__ __device__ constexpr int epi_warps(int b_mode) { return b_mode == SCALE_ROW ? 16 : 8; }
+__host__ __device__ constexpr int gemm_threads(int b_mode) { return 128 + 32 * epi_warps(b_mode); }
+__host__ __device__ constexpr int launch_regs(int b_mode) { return epi_warps(b_mode) == 16 ? 96 : 168; }
+__host__ __device__ constexpr uint32_t reg_lo(int b_mode) { return epi_warps(b_mode) == 16 ? 32 : 56; }
+__host__ __device__ constexpr uint32_t reg_hi(int b_mode) { return epi_warps(b_mode) == 16 ? 112 : 224; }
+static_assert(128 * reg_lo(SCALE_ROW) + 32 * epi_warps(SCALE_ROW) * reg_hi(SCALE_ROW) <=
+                  gemm_threads(SCALE_ROW) * launch_regs(SCALE_ROW), "register split");
+static_assert(128 * reg_lo(SCALE_BLOCK) + 32 * epi_warps(SCALE_BLOCK) * reg_hi(SCALE_BLOCK) <=
+                  gemm_threads(SCALE_BLOCK) * launch_regs(SCALE_BLOCK), "register split");
 constexpr int kScalePD = 4;   // K-blocks of scale prefetch per epilogue thread
 
 // How the epilogue gets the per-K-block scales of A's rows and of B's column blocks.
@@ -107,11 +112,11 @@ struct GemmSmem {
     static constexpr int NTB = 512 / BN;                      // TMEM partial-sum buffers
     // SD_THREAD: per epilogue thread, kScalePD slots of its scale words: A row (+ B block)
     static constexpr int SC_WORDS = (B_MODE == SCALE_BLOCK) ? 2 : 1;
-    static constexpr int SC_BYTES = (SD == SD_THREAD) ? kScalePD * SC_WORDS * 32 * kEpiWarps * 4 : 0;
+    static constexpr int SC_BYTES = (SD == SD_THREAD) ? kScalePD * SC_WORDS * 32 * epi_warps(B_MODE) * 4 : 0;
     static constexpr int NBARS = 2 * STAGES + 2 * NTB + 2 * NS + 1;
     // BF16 output staging for the TMA store: one 32 x 32 box per epilogue warp (the split-K
     // form writes FP32 partials straight to global memory instead)
-    static constexpr int STAGE_C_BYTES = SPLITK ? 0 : kEpiWarps * 2048;
+    static constexpr int STAGE_C_BYTES = SPLITK ? 0 : epi_warps(B_MODE) * 2048;
     static constexpr size_t BYTES = 1024 /* alignment slack */ + (size_t)STAGES * (A_BYTES + B_BYTES) +
                                     STAGE_C_BYTES + RING_BYTES + SC_BYTES + NBARS * 8 + 16;
 };
@@ -157,11 +162,12 @@ struct ScaleCursor {
 };
 
 template <int BN, int SD, int B_MODE, int STAGES, bool SPLITK>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(gemm_threads(B_MODE), 1)
     k_gemm_bs(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
               const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
     using S = GemmSmem<BN, STAGES, B_MODE, SD, SPLITK>;
+    constexpr int kEpiWarps = epi_warps(B_MODE);
     constexpr int COLS = BN / (kEpiWarps / 4);   // columns per epilogue thread
     constexpr int LW = kEpiWarps == 16 ? 16 : 32; // columns per TMEM load
     constexpr int LPW = 1;                        // loads per wait
@@ -226,7 +232,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    constexpr uint32_t REG_LO = kRegLo, REG_HI = kRegHi;
+    constexpr uint32_t REG_LO = reg_lo(B_MODE), REG_HI = reg_hi(B_MODE);
     if (warp < 4) {
       warpgroup_reg_dealloc<REG_LO>();
       if (warp == 0) {
@@ -561,7 +567,7 @@ static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const 
     static_assert(smem <= 227 * 1024, "shared memory budget");
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kGemmThreads, smem, st>>>(ta, tb, tsa, tsb, tc, p);
+    kern<<<grid, gemm_threads(B_MODE), smem, st>>>(ta, tb, tsa, tsb, tc, p);
     return cudaGetLastError();
 }
 
@@ -571,8 +577,8 @@ cudaError_t launch_gemm_tiled(const CUtensorMap& ta, const CUtensorMap& tb, cons
     if (b_mode == SCALE_ROW) {
         // WGrad: both operands come from 128x1 quantization, every scale array is TMA-able
         if (!tsa || !tsb) return cudaErrorInvalidValue;
-        if (bn == 128) return launch_t<128, SD_TMA, SCALE_ROW, 6, false>(ta, tb, *tsa, *tsb, tc, p, grid, st);
-        return launch_t<256, SD_TMA, SCALE_ROW, 4, false>(ta, tb, *tsa, *tsb, tc, p, grid, st);
+        if (bn == 128) return launch_t<128, SD_TMA, SCALE_ROW, 5, false>(ta, tb, *tsa, *tsb, tc, p, grid, st);
+        return launch_t<256, SD_TMA, SCALE_ROW, 3, false>(ta, tb, *tsa, *tsb, tc, p, grid, st);
     }
     if (tsa && tsb) {
         if (bn == 128) return launch_t<128, SD_TMA, SCALE_BLOCK, 6, false>(ta, tb, *tsa, *tsb, tc, p, grid, st);
