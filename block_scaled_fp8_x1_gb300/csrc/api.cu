@@ -158,7 +158,7 @@ fp8rl_status make_tmap_out(CUtensorMap* m, uint16_t* base, int64_t rows, int64_t
 // ([column block][K-block] storage) or 4 | column blocks ([K-block][column block]); B's
 // row scales [K-block][R2] always qualify (R2 % 128 == 0).  Returns false when they do not
 // all qualify, in which case the kernel takes the per-thread scale path.
-bool scale_maps(const GemmParams& p, int b_mode, int bn, CUtensorMap* tsa, CUtensorMap* tsb,
+bool scale_maps(const GemmParams& p, int b_mode, int bn, bool splitk, CUtensorMap* tsa, CUtensorMap* tsb,
                 fp8rl_status* err) {
     *err = FP8RL_OK;
     const int64_t nkb = p.Kr / 128;
@@ -170,14 +170,17 @@ bool scale_maps(const GemmParams& p, int b_mode, int bn, CUtensorMap* tsa, CUten
     } else {
         if (p.sb_r != 1 || p.sb_kb % 4 != 0) return false;
     }
-    *err = make_tmap_scales(tsa, p.sa, nkb, p.R1, 128, 1);
+    // boxes of one scale group of K-blocks (all of them when K is shorter): the kernel
+    // fetches a group's scales with one copy per operand
+    const int grp = (int)std::min<int64_t>(nkb, scale_group(b_mode, splitk));
+    *err = make_tmap_scales(tsa, p.sa, nkb, p.R1, 128, grp);
     if (*err != FP8RL_OK) return false;
     if (b_mode == SCALE_ROW)
-        *err = make_tmap_scales(tsb, p.sb, nkb, p.R2, bn, 1);
+        *err = make_tmap_scales(tsb, p.sb, nkb, p.R2, bn, grp);
     else if (p.sb_kb == 1)
         *err = make_tmap_scales(tsb, p.sb, (p.R2 + 127) / 128, nkb, 4, bn / 128);
     else
-        *err = make_tmap_scales(tsb, p.sb, nkb, p.sb_kb, 4, 1);
+        *err = make_tmap_scales(tsb, p.sb, nkb, p.sb_kb, 4, grp);
     return *err == FP8RL_OK;
 }
 
@@ -202,7 +205,7 @@ fp8rl_status run_tiled(const TiledArgs& t, int grid_req, int bn_req, int num_sms
     p.splits = 0;
     CUtensorMap tsa, tsb;
     fp8rl_status e = FP8RL_OK;
-    bool tma_scales = scale_maps(p, t.b_mode, bn, &tsa, &tsb, &e);
+    bool tma_scales = scale_maps(p, t.b_mode, bn, false, &tsa, &tsb, &e);
     if (e != FP8RL_OK) return e;
     if (t.b_mode == SCALE_ROW && !tma_scales) return FP8RL_ERR_INVALID_ARG;
     if (!tma_scales) bn = 256;   // the per-thread scale path is built for 256-wide tiles only
@@ -257,7 +260,7 @@ fp8rl_status run_decode(const uint8_t* qx, const float* sx, const uint8_t* qw, c
     p.timeout_ns = g_timeout_ns.load();
     const int grid = std::max(1, std::min(num_sms, p.num_items));
     CUtensorMap tsa, tsb;
-    const bool tma_scales = scale_maps(p, SCALE_BLOCK, kDecodeBN, &tsa, &tsb, &e);
+    const bool tma_scales = scale_maps(p, SCALE_BLOCK, kDecodeBN, true, &tsa, &tsb, &e);
     if (e != FP8RL_OK) return e;
     return cuda_status(launch_gemm_splitk(ta, tb, tma_scales ? &tsa : nullptr, tma_scales ? &tsb : nullptr, p,
                                           grid, st));

@@ -94,17 +94,18 @@ enum ScaleDelivery {
     SD_THREAD = 1   // each epilogue thread copies its own (any M; B rows still by TMA)
 };
 
-// Shared-memory plan of one CTA.  Scale-ring slot: 128 scales of A (SD_TMA), then the
-// scales of B (BN for SCALE_ROW, a box of at most 8 block scales for SCALE_BLOCK).
+// Shared-memory plan of one CTA.  Scale-ring slot (SD_TMA), one per group of SG K-blocks: A's row scales [K-block of the group][128], then B's scales: [K-block][BN]
+// row scales for SCALE_ROW, or a box of at most 16 block scales for SCALE_BLOCK.
 template <int BN, int STAGES, int B_MODE, int SD, bool SPLITK>
 struct GemmSmem {
     static constexpr int A_BYTES = 128 * 128;                 // one 128x128 E4M3 tile of A
     static constexpr int B_BYTES = BN * 128;                  // one BNx128 E4M3 tile of B
-    static constexpr int NS = 8;                              // scale-ring slots
-    static constexpr int SLOT_A = (SD == SD_TMA) ? 128 : 0;   // floats
-    // (a box of block scales takes at most 8 floats; padded so that every TMA destination
+    static constexpr int SG = scale_group(B_MODE, SPLITK);    // K-blocks per scale group
+    static constexpr int NS = (B_MODE == SCALE_ROW) ? 8 : 4;   // scale-ring slots (groups)
+    static constexpr int SLOT_A = (SD == SD_TMA) ? 128 * SG : 0;   // floats
+    // (a box of block scales takes at most 16 floats; padded so that every TMA destination
     // in the ring starts on a 128-byte boundary, as tensor copies require)
-    static constexpr int SLOT_B = (B_MODE == SCALE_ROW) ? BN : ((SD == SD_TMA) ? 32 : 0);
+    static constexpr int SLOT_B = (B_MODE == SCALE_ROW) ? BN * SG : ((SD == SD_TMA) ? 32 : 0);
     static constexpr int SLOT = SLOT_A + SLOT_B;
     static_assert((SLOT_A * 4) % 128 == 0 && (SLOT * 4) % 128 == 0, "TMA destinations 128-byte aligned");
     static constexpr bool RING = SLOT > 0;
@@ -244,6 +245,8 @@ __global__ void __launch_bounds__(gemm_threads(B_MODE), 1)
             // split-K (decode) streams the weights (B) once: let them leave L2 first
             const uint64_t pol_a = l2_policy_evict_last();
             const uint64_t pol_b = SPLITK ? l2_policy_evict_first() : l2_policy_evict_last();
+            // K-blocks per scale box: the group size, or all of them when K is shorter
+            const int sgrp = p.nkb < S::SG ? p.nkb : S::SG;
             uint32_t it = 0, s_issued = 0;
             bool ok = true;
             for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
@@ -260,30 +263,35 @@ __global__ void __launch_bounds__(gemm_threads(B_MODE), 1)
                     mbar_arrive_expect_tx(fb, S::A_BYTES + S::B_BYTES);
                     tma_load_2d(smem_u32(sA + s * S::A_BYTES), &tmA, fb, kb * 128, m0, pol_a);
                     tma_load_2d(smem_u32(sB + s * S::B_BYTES), &tmB, fb, kb * 128, n0, pol_b);
-                    if (S::RING) {
-                        const uint32_t ss = it % NS;
-                        if (!mbar_wait(smem_u32(&sempty_bar[ss]), ((it / NS) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+                    if (S::RING && (kb == w.kb_begin || kb % S::SG == 0)) {
+                        // first K-block of a scale group: the scales of the whole group
+                        const uint32_t ss = s_issued % NS;
+                        if (!mbar_wait(smem_u32(&sempty_bar[ss]), ((s_issued / NS) & 1) ^ 1, p.timeout_ns, abort_flag)) {
                             ok = false;
                             ++it;   // this K-block's tiles are in flight: drain them below
                             break;
                         }
                         const uint32_t sb = smem_u32(&sfull_bar[ss]);
                         float* slot = ring + ss * S::SLOT;
+                        const int kb0 = kb - kb % S::SG;
+                        const uint32_t a_bytes = (SD == SD_TMA) ? 128u * 4u * (uint32_t)sgrp : 0u;
                         if (B_MODE == SCALE_ROW) {
-                            mbar_arrive_expect_tx(sb, (S::SLOT_A + BN) * 4);
-                            tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, n0, kb, pol_a);
+                            mbar_arrive_expect_tx(sb, a_bytes + (uint32_t)BN * 4u * (uint32_t)sgrp);
+                            tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, n0, kb0, pol_a);
                         } else if (p.sb_kb == 1) {
-                            // block scales stored [column block][K-block]: 4 K-blocks x the
-                            // tile's BN/128 column blocks, from a 4-aligned K-block
-                            mbar_arrive_expect_tx(sb, S::SLOT_A * 4 + 16 * (BN / 128));
+                            // block scales stored [column block][K-block]: 4 K-blocks from a
+                            // 4-aligned one (the box's x is a K-block index: x * 4 bytes must
+                            // be a multiple of 16 whatever the group size) x the tile's
+                            // BN/128 column blocks
+                            mbar_arrive_expect_tx(sb, a_bytes + 16u * (BN / 128));
                             tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, kb & ~3, n0 >> 7, pol_a);
                         } else {
                             // block scales stored [K-block][column block]: 4 column blocks
-                            // from a 4-aligned one
-                            mbar_arrive_expect_tx(sb, S::SLOT_A * 4 + 16);
-                            tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, (n0 >> 7) & ~3, kb, pol_a);
+                            // from a 4-aligned one, for each K-block of the group
+                            mbar_arrive_expect_tx(sb, a_bytes + 16u * (uint32_t)sgrp);
+                            tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, (n0 >> 7) & ~3, kb0, pol_a);
                         }
-                        if (SD == SD_TMA) tma_load_2d(smem_u32(slot), &tmSA, sb, m0, kb, pol_a);
+                        if (SD == SD_TMA) tma_load_2d(smem_u32(slot), &tmSA, sb, m0, kb0, pol_a);
                         ++s_issued;
                     }
                 }
@@ -360,6 +368,7 @@ __global__ void __launch_bounds__(gemm_threads(B_MODE), 1)
                           row_local, col_base);
         }
         uint32_t acc_it = 0;
+        uint32_t g_done = 0;   // scale groups consumed
         bool ok = true;
         for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
             const WorkItem w = work_item(p, item);
@@ -381,11 +390,15 @@ __global__ void __launch_bounds__(gemm_threads(B_MODE), 1)
                               row_local, col_base);
                 }
                 if (!ok) continue;
-                const uint32_t ss = acc_it % NS;
+                const uint32_t gi = S::SG == 1 ? acc_it : g_done;   // scale group index
+                const uint32_t ss = gi % NS;
                 const uint32_t ts = acc_it % NTB;
+                const int q = kb % S::SG;   // this K-block's place in its scale group
+                const bool g_first = kb == w.kb_begin || q == 0;
+                const bool g_last = kb + 1 == w.kb_end || q == S::SG - 1;
                 bool got = true;
-                if (S::RING)
-                    got = mbar_wait(smem_u32(&sfull_bar[ss]), (acc_it / NS) & 1, p.timeout_ns, abort_flag);
+                if (S::RING && g_first)
+                    got = mbar_wait(smem_u32(&sfull_bar[ss]), (gi / NS) & 1, p.timeout_ns, abort_flag);
                 got = got && mbar_wait(smem_u32(&tfull_bar[ts]), (acc_it / NTB) & 1, p.timeout_ns, abort_flag);
                 ok = __all_sync(0xffffffffu, got);
                 if (!ok) continue;
@@ -398,8 +411,8 @@ __global__ void __launch_bounds__(gemm_threads(B_MODE), 1)
                     const int g = lane >> 2, tq = lane & 3;
                     float fr[4];
                     #pragma unroll
-                    for (int h = 0; h < 4; ++h) fr[h] = slot[quad * 32 + g + 8 * h];
-                    const float* sbv = slot + S::SLOT_A + col_base + 2 * tq;
+                    for (int h = 0; h < 4; ++h) fr[h] = slot[q * 128 + quad * 32 + g + 8 * h];
+                    const float* sbv = slot + S::SLOT_A + q * BN + col_base + 2 * tq;
                     const uint32_t tb0 = tmem_base + ((uint32_t)(quad * 32) << 16) + ts * BN + col_base;
                     const uint32_t tb1 = tb0 + (16u << 16);
                     #pragma unroll
@@ -430,10 +443,10 @@ __global__ void __launch_bounds__(gemm_threads(B_MODE), 1)
                     }
                 } else {
                                     if (SD == SD_TMA) {
-                        f = slot[row_local];
+                        f = slot[q * 128 + row_local];
                         if (B_MODE == SCALE_BLOCK) {
                             const int cb = (int)(n0 >> 7);   // column block of this thread
-                            f *= slot[128 + (p.sb_kb == 1 ? ((cb - ((w.nt * BN) >> 7)) * 4 + (kb & 3)) : (cb & 3))];
+                            f *= slot[S::SLOT_A + (p.sb_kb == 1 ? ((cb - ((w.nt * BN) >> 7)) * 4 + (kb & 3)) : (q * 4 + (cb & 3)))];
                         }
                     }
                     const float2 f2 = make_float2(f, f);
@@ -462,9 +475,10 @@ __global__ void __launch_bounds__(gemm_threads(B_MODE), 1)
                         }
                     }
                 }
-                if (S::RING) {
+                if (S::RING && g_last) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&sempty_bar[ss]));
+                    if (S::SG > 1) ++g_done;
                 }
             }
 

@@ -22,6 +22,17 @@ enum ScaleMode : int {
     SCALE_BLOCK = 1   // one scale per 128-row block:      s[(row/128)*s_r + kb*s_kb]
 };
 
+// K-blocks whose scales the GEMM's copy warp fetches with one TMA copy per operand (one
+// scale-ring slot and one barrier round trip per group): 4 for the tiled block-scaled
+// form; 1 for row-scaled B (WGrad, whose per-K-block slots measured faster) and for the
+// split-K form (short K slices).  Groups start at K-block multiples of the group size, so
+// a box of block scales stored [column block][K-block] lines up with them; a work item's
+// first and last groups may be partial.  Scale tensor maps use boxes of
+// min(group, K-blocks) K-blocks.
+__host__ __device__ constexpr int scale_group(int b_mode, bool splitk) {
+    return (b_mode == SCALE_ROW || splitk) ? 1 : 4;
+}
+
 struct GemmParams {
     int64_t R1, R2, Kr;      // C is R1 x R2; reduction length Kr (multiple of 128)
     const float* sa;         // scales of A, one per row: sa[kb*sa_kb + r1]
@@ -37,10 +48,10 @@ struct GemmParams {
     uint64_t timeout_ns;
 };
 
-// Scale tensor maps (FP32, one K-block per box row): tsa over A's row scales
-// [K-block][R1], box 128 x 1; tsb over B's scales, box BN x 1 for row scales [K-block][R2],
-// 4 x BN/128 for block scales stored [column block][K-block] (sb_kb == 1), 4 x 1 for block
-// scales stored [K-block][column block].  With both maps the scales travel by TMA; when
+// Scale tensor maps (FP32; g = min(scale_group(), K-blocks) K-blocks per box): tsa over A's
+// row scales [K-block][R1], box 128 x g; tsb over B's scales, box BN x g for row scales
+// [K-block][R2], 4 x BN/128 for block scales stored [column block][K-block] (sb_kb == 1),
+// 4 x g for block scales stored [K-block][column block].  With both maps the scales travel by TMA; when
 // either is null (strides that are not multiples of 16 bytes) each epilogue thread copies
 // its own.  B row scales (WGrad) always need both maps.
 // tc: tensor map of C (BF16 [R1][ldc], box 32 x 32, 64-byte swizzle) for the tile stores.
