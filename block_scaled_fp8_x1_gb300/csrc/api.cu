@@ -347,7 +347,7 @@ fp8rl_status fp8rl_quantize_128x128(const uint16_t* w, int64_t N, int64_t K, int
     if (qT && !aligned16(qT)) return FP8RL_ERR_ALIGN;
     fp8rl_status e = current_device(nullptr);
     if (e != FP8RL_OK) return e;
-    return cuda_status(launch_quant_128x128(w, N, K, ldw, q, s, qT, stream));
+    return cuda_status(launch_quant_128x128(w, N, K, ldw, q, s, qT, g_timeout_ns.load(), stream));
 }
 
 fp8rl_status fp8rl_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M,

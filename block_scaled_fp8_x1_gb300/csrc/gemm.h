@@ -74,7 +74,7 @@ cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float
                                  float* rstd, uint64_t timeout_ns, cudaStream_t st);
 fp8rl_status read_and_clear_quant_status();
 cudaError_t launch_quant_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
-                                 float* s, uint8_t* qT, cudaStream_t st);
+                                 float* s, uint8_t* qT, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_debug_e4m3(const float* in, uint8_t* out, int64_t n, cudaStream_t st);
 cudaError_t launch_debug_encode_check(uint32_t amax_lo, uint32_t amax_hi,
                                       unsigned long long* mismatches, uint32_t* first_bad,

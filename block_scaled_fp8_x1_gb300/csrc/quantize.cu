@@ -502,87 +502,141 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
 
 // ------------------------------------------------------------------------------------
 // 128x128 weight blocks (+ optional transposed copy with the same scale).
+// Persistent: each CTA takes every gridDim.x-th block.  Thread 0 streams the blocks through
+// a ring of TMA stages (one 128x128 BF16 tile each); all threads pull their 8x8 sub-block
+// into registers, and once everyone has it (the barrier that also publishes the warps'
+// maxima) thread 0 refills that stage, so the copies of the next blocks overlap this
+// block's encode and stores.
 // ------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_quant_128x128(const uint16_t* __restrict__ w_in,
-                                                       int64_t N, int64_t K, int64_t ldw,
-                                                       uint8_t* __restrict__ q,
-                                                       float* __restrict__ s,
-                                                       uint8_t* __restrict__ qT) {
-    __shared__ uint32_t s_wmax[8];
-    __shared__ FastScale s_fs;
+struct W128Args {
+    int64_t N, K;
+    uint8_t* q;
+    float* s;
+    uint8_t* qT;
+    uint64_t timeout_ns;
+};
+constexpr int kW128Stages = 3;
+constexpr int kW128StageBytes = 128 * 128 * 2;
+constexpr size_t kW128Smem = (size_t)kW128Stages * kW128StageBytes + 128;   // + alignment slack
+
+__global__ void __launch_bounds__(256, 2) k_quant_128x128(const __grid_constant__ CUtensorMap tmw,
+                                                          const W128Args a) {
+    extern __shared__ uint8_t w_smem_raw[];
+    uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(w_smem_raw) + 127) & ~uintptr_t(127));
+    __shared__ __align__(8) uint64_t full_bar[kW128Stages];
+    __shared__ int abort_flag;
+    __shared__ uint32_t s_wmax[2][8];   // per-warp maxima, double-buffered across blocks
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int half = lane >> 4, cl = lane & 15;
     const int R0 = 16 * warp + 8 * half, C0 = 8 * cl;
-    const int64_t bk = blockIdx.x, bn = blockIdx.y;
-    const int64_t n0 = bn * 128, k0 = bk * 128;
+    const int64_t nbk = a.K / 128;
+    const int64_t blocks = (a.N / 128) * nbk;
+    const int n = (int)((blocks - blockIdx.x + gridDim.x - 1) / gridDim.x);   // blocks of this CTA
 
-    uint32_t w[8][4];
-    uint4 v[8];
-    #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = ldg_nc_v4(w_in + (n0 + R0 + i) * ldw + k0 + C0);
-    uint32_t mx = 0;
-    #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        w[i][0] = v[i].x; w[i][1] = v[i].y; w[i][2] = v[i].z; w[i][3] = v[i].w;
-        #pragma unroll
-        for (int j = 0; j < 4; ++j) mx = absmax2(mx, w[i][j]);
-    }
-    mx = max(mx & 0xFFFFu, mx >> 16);
-    #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0) s_wmax[warp] = mx;
-    __syncthreads();
     if (tid == 0) {
-        uint32_t m = 0;
-        #pragma unroll
-        for (int i = 0; i < 8; ++i) m = max(m, s_wmax[i]);
-        const FastScale f = fast_scale(bf16_bits_amax_to_f32(m));
-        s_fs = f;
-        s[bn * (K / 128) + bk] = f.s;
+        for (int st = 0; st < kW128Stages; ++st) mbar_init(smem_u32(&full_bar[st]), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmw);
     }
     __syncthreads();
-    const FastScale f = s_fs;
-    // codes of the 8x8 block, row-major: rc[i] = row i, columns 0-3 | 4-7
-    uint32_t rc[8][2];
-    #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint32_t c[4];
-        #pragma unroll
-        for (int j = 0; j < 4; ++j) c[j] = encode_pair_neg(make_float2(bf16_lo(w[i][j]), bf16_hi(w[i][j])), f.s, f.nr);
-        rc[i][0] = flip_codes(c[0], c[1], f.keep);
-        rc[i][1] = flip_codes(c[2], c[3], f.keep);
-    }
-    if (f.slow) {   // tiny block scale: divide (whole CTA, rare)
+    auto issue = [&](int item) {
+        const int st = item % kW128Stages;
+        const int64_t id = blockIdx.x + (int64_t)item * gridDim.x;
+        const int64_t bn = id / nbk, bk = id - bn * nbk;
+        const uint32_t bar = smem_u32(&full_bar[st]);
+        mbar_arrive_expect_tx(bar, kW128StageBytes);
+        tma_load_2d(smem_u32(stages + st * kW128StageBytes), &tmw, bar, (int)(bk * 128), (int)(bn * 128), 0);
+    };
+    int issued = 0;
+    if (tid == 0)
+        for (; issued < kW128Stages && issued < n; ++issued) issue(issued);
+
+    int done = n;   // blocks processed (fewer only after a wait gave up)
+    for (int item = 0; item < n; ++item) {
+        // every thread waits for the block; the decision to stop is made block-wide
+        const bool got = mbar_wait(smem_u32(&full_bar[item % kW128Stages]), (item / kW128Stages) & 1,
+                                   a.timeout_ns, &abort_flag);
+        if (__syncthreads_or(got ? 0 : 1)) {
+            done = item;
+            break;
+        }
+        const int64_t id = blockIdx.x + (int64_t)item * gridDim.x;
+        const int64_t bn = id / nbk, bk = id - bn * nbk;
+        const int64_t n0 = bn * 128, k0 = bk * 128;
+        const uint8_t* stage = stages + (item % kW128Stages) * kW128StageBytes;
+
+        uint32_t w[8][4];
+        uint32_t mx = 0;
         #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint4 v = encode4_slow(make_float2(bf16_lo(w[i][0]), bf16_hi(w[i][0])),
-                                         make_float2(bf16_lo(w[i][1]), bf16_hi(w[i][1])),
-                                         make_float2(bf16_lo(w[i][2]), bf16_hi(w[i][2])),
-                                         make_float2(bf16_lo(w[i][3]), bf16_hi(w[i][3])), f.s);
-            rc[i][0] = v.x | (v.y << 16);
-            rc[i][1] = v.z | (v.w << 16);
+            const uint4 v = *reinterpret_cast<const uint4*>(stage + (R0 + i) * 256 + C0 * 2);
+            w[i][0] = v.x; w[i][1] = v.y; w[i][2] = v.z; w[i][3] = v.w;
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) mx = absmax2(mx, w[i][j]);
+        }
+        mx = max(mx & 0xFFFFu, mx >> 16);
+        #pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (lane == 0) s_wmax[item & 1][warp] = mx;
+        __syncthreads();                              // stage consumed, maxima published
+        if (tid == 0 && issued < n) issue(issued++);
+        uint32_t m = 0;
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) m = max(m, s_wmax[item & 1][i]);
+        const FastScale f = fast_scale(bf16_bits_amax_to_f32(m));
+        if (tid == 0) a.s[bn * nbk + bk] = f.s;
+        const int64_t N = a.N, K = a.K;
+        uint8_t* const q = a.q;
+        uint8_t* const qT = a.qT;
+        // codes of the 8x8 block, row-major: rc[i] = row i, columns 0-3 | 4-7
+        uint32_t rc[8][2];
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t c[4];
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) c[j] = encode_pair_neg(make_float2(bf16_lo(w[i][j]), bf16_hi(w[i][j])), f.s, f.nr);
+            rc[i][0] = flip_codes(c[0], c[1], f.keep);
+            rc[i][1] = flip_codes(c[2], c[3], f.keep);
+        }
+        if (f.slow) {   // tiny block scale: divide (whole CTA, rare)
+            #pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint4 v = encode4_slow(make_float2(bf16_lo(w[i][0]), bf16_hi(w[i][0])),
+                                             make_float2(bf16_lo(w[i][1]), bf16_hi(w[i][1])),
+                                             make_float2(bf16_lo(w[i][2]), bf16_hi(w[i][2])),
+                                             make_float2(bf16_lo(w[i][3]), bf16_hi(w[i][3])), f.s);
+                rc[i][0] = v.x | (v.y << 16);
+                rc[i][1] = v.z | (v.w << 16);
+            }
+        }
+        #pragma unroll
+        for (int i = 0; i < 8; ++i) stg_v2(q + (n0 + R0 + i) * K + k0 + C0, rc[i][0], rc[i][1]);
+        if (qT) {
+            // transposed codes: four 4x4 byte transposes (rows 0-3 | 4-7 x columns 0-3 | 4-7)
+            uint32_t ct[8][2];   // ct[j] = column j, rows 0-3 | 4-7
+            #pragma unroll
+            for (int rh = 0; rh < 2; ++rh)
+                #pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    const uint32_t a0 = rc[4 * rh + 0][ch], a1 = rc[4 * rh + 1][ch];
+                    const uint32_t a2 = rc[4 * rh + 2][ch], a3 = rc[4 * rh + 3][ch];
+                    const uint32_t t0 = __byte_perm(a0, a1, 0x5140), t1 = __byte_perm(a0, a1, 0x7362);
+                    const uint32_t t2 = __byte_perm(a2, a3, 0x5140), t3 = __byte_perm(a2, a3, 0x7362);
+                    ct[4 * ch + 0][rh] = __byte_perm(t0, t2, 0x5410);
+                    ct[4 * ch + 1][rh] = __byte_perm(t0, t2, 0x7632);
+                    ct[4 * ch + 2][rh] = __byte_perm(t1, t3, 0x5410);
+                    ct[4 * ch + 3][rh] = __byte_perm(t1, t3, 0x7632);
+                }
+            #pragma unroll
+            for (int j = 0; j < 8; ++j) stg_v2(qT + (k0 + C0 + j) * N + n0 + R0, ct[j][0], ct[j][1]);
         }
     }
-    #pragma unroll
-    for (int i = 0; i < 8; ++i) stg_v2(q + (n0 + R0 + i) * K + k0 + C0, rc[i][0], rc[i][1]);
-    if (qT) {
-        // transposed codes: four 4x4 byte transposes (rows 0-3 | 4-7 x columns 0-3 | 4-7)
-        uint32_t ct[8][2];   // ct[j] = column j, rows 0-3 | 4-7
-        #pragma unroll
-        for (int rh = 0; rh < 2; ++rh)
-            #pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                const uint32_t a0 = rc[4 * rh + 0][ch], a1 = rc[4 * rh + 1][ch];
-                const uint32_t a2 = rc[4 * rh + 2][ch], a3 = rc[4 * rh + 3][ch];
-                const uint32_t t0 = __byte_perm(a0, a1, 0x5140), t1 = __byte_perm(a0, a1, 0x7362);
-                const uint32_t t2 = __byte_perm(a2, a3, 0x5140), t3 = __byte_perm(a2, a3, 0x7362);
-                ct[4 * ch + 0][rh] = __byte_perm(t0, t2, 0x5410);
-                ct[4 * ch + 1][rh] = __byte_perm(t0, t2, 0x7632);
-                ct[4 * ch + 2][rh] = __byte_perm(t1, t3, 0x5410);
-                ct[4 * ch + 3][rh] = __byte_perm(t1, t3, 0x7632);
-            }
-        #pragma unroll
-        for (int j = 0; j < 8; ++j) stg_v2(qT + (k0 + C0 + j) * N + n0 + R0, ct[j][0], ct[j][1]);
+    // After a wait gave up: the copies already issued land before the CTA exits.
+    if (tid == 0 && done < issued) {
+        volatile int no_abort = 0;
+        for (int j = done; j < issued; ++j)
+            mbar_wait(smem_u32(&full_bar[j % kW128Stages]), (j / kW128Stages) & 1, a.timeout_ns, &no_abort);
     }
 }
 
@@ -765,9 +819,23 @@ cudaError_t launch_rmsnorm_quant(const uint16_t* x, const uint16_t* gamma, float
 }
 
 cudaError_t launch_quant_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
-                                 float* s, uint8_t* qT, cudaStream_t st) {
-    dim3 grid((unsigned)(K / 128), (unsigned)(N / 128), 1);
-    k_quant_128x128<<<grid, 256, 0, st>>>(w, N, K, ldw, q, s, qT);
+                                 float* s, uint8_t* qT, uint64_t timeout_ns, cudaStream_t st) {
+    CUtensorMap tm;
+    cudaError_t e = tmap_bf16(&tm, w, N, K, ldw);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_quant_128x128, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kW128Smem);
+    if (e != cudaSuccess) return e;
+    // persistent: as many CTAs as fit on the GPU at once, at most one per block
+    static const int resident = [] {
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quant_128x128, 256, kW128Smem);
+        return std::max(1, sms * std::max(1, per_sm));
+    }();
+    const int64_t blocks = (N / 128) * (K / 128);
+    W128Args a = {N, K, q, s, qT, timeout_ns};
+    k_quant_128x128<<<(unsigned)std::min<int64_t>(blocks, resident), 256, kW128Smem, st>>>(tm, a);
     return cudaGetLastError();
 }
 
