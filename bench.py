@@ -286,10 +286,14 @@ def run_gpu(args):
     barrier()
     w1 = time.time()
     ms_total = t0.elapsed_time(t1)
-    # per-kernel durations from events between launches (separate pass, same work)
+    # per-kernel durations from events between launches (separate pass, same work).  Each
+    # pass starts on an idle device: a short device-side spin ahead of the first mark lets
+    # the host queue the whole step first, so no mark interval holds host launch time.
     per = {}
     for _ in range(args.steps):
         marks = []
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(4_000_000)   # about 2 ms at 2 GHz
         step.run(marks)
         torch.cuda.synchronize()
         for (_, a), (name, b) in zip(marks[:-1], marks[1:]):
