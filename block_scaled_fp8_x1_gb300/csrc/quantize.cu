@@ -34,6 +34,9 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
 __device__ __forceinline__ void stg_v2(void* p, uint32_t a, uint32_t b) {
     asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }
+__device__ __forceinline__ void stg_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
 
 // ------------------------------------------------------------------------------------
 // 1x128 quantization of rows, any M.  16 threads per group (8 BF16 each), groups ordered
@@ -610,8 +613,20 @@ __global__ void __launch_bounds__(256, 2) k_quant_128x128(const __grid_constant_
                 rc[i][1] = v.z | (v.w << 16);
             }
         }
+        // 16-byte stores: lanes cl and cl^1 hold the two 8-byte halves of a 16-byte row
+        // piece.  For each row pair the even lane stores the even row and the odd lane the
+        // odd one, each after swapping the other row's half with its partner.
+        const bool odd = cl & 1;
         #pragma unroll
-        for (int i = 0; i < 8; ++i) stg_v2(q + (n0 + R0 + i) * K + k0 + C0, rc[i][0], rc[i][1]);
+        for (int pr = 0; pr < 4; ++pr) {
+            const uint32_t g0 = __shfl_xor_sync(0xffffffffu, odd ? rc[2 * pr][0] : rc[2 * pr + 1][0], 1);
+            const uint32_t g1 = __shfl_xor_sync(0xffffffffu, odd ? rc[2 * pr][1] : rc[2 * pr + 1][1], 1);
+            const uint32_t o0 = odd ? rc[2 * pr + 1][0] : rc[2 * pr][0];
+            const uint32_t o1 = odd ? rc[2 * pr + 1][1] : rc[2 * pr][1];
+            const int i = 2 * pr + (odd ? 1 : 0);
+            if (odd) stg_v4(q + (n0 + R0 + i) * K + k0 + C0 - 8, g0, g1, o0, o1);
+            else     stg_v4(q + (n0 + R0 + i) * K + k0 + C0, o0, o1, g0, g1);
+        }
         if (qT) {
             // transposed codes: four 4x4 byte transposes (rows 0-3 | 4-7 x columns 0-3 | 4-7)
             uint32_t ct[8][2];   // ct[j] = column j, rows 0-3 | 4-7
@@ -628,8 +643,19 @@ __global__ void __launch_bounds__(256, 2) k_quant_128x128(const __grid_constant_
                     ct[4 * ch + 2][rh] = __byte_perm(t1, t3, 0x5410);
                     ct[4 * ch + 3][rh] = __byte_perm(t1, t3, 0x7632);
                 }
+            // 16-byte stores: lanes l and l^16 (rows R0 and R0 + 8 of W) hold the two halves
+            // of a 16-byte piece of each W^T row; half 0 stores the even W^T rows, half 1
+            // the odd ones.
             #pragma unroll
-            for (int j = 0; j < 8; ++j) stg_v2(qT + (k0 + C0 + j) * N + n0 + R0, ct[j][0], ct[j][1]);
+            for (int pr = 0; pr < 4; ++pr) {
+                const uint32_t g0 = __shfl_xor_sync(0xffffffffu, half ? ct[2 * pr][0] : ct[2 * pr + 1][0], 16);
+                const uint32_t g1 = __shfl_xor_sync(0xffffffffu, half ? ct[2 * pr][1] : ct[2 * pr + 1][1], 16);
+                const uint32_t o0 = half ? ct[2 * pr + 1][0] : ct[2 * pr][0];
+                const uint32_t o1 = half ? ct[2 * pr + 1][1] : ct[2 * pr][1];
+                const int j = 2 * pr + half;
+                if (half) stg_v4(qT + (k0 + C0 + j) * N + n0 + R0 - 8, g0, g1, o0, o1);
+                else      stg_v4(qT + (k0 + C0 + j) * N + n0 + R0, o0, o1, g0, g1);
+            }
         }
     }
     // After a wait gave up: the copies already issued land before the CTA exits.
