@@ -94,8 +94,9 @@ enum ScaleDelivery {
     SD_THREAD = 1   // each epilogue thread copies its own (any M; B rows still by TMA)
 };
 
-// Shared-memory plan of one CTA.  Scale-ring slot (SD_TMA), one per group of SG K-blocks: A's row scales [K-block of the group][128], then B's scales: [K-block][BN]
-// row scales for SCALE_ROW, or a box of at most 16 block scales for SCALE_BLOCK.
+// Shared-memory plan of one CTA.  Scale-ring slot (SD_TMA), one per group of SG K-blocks:
+// A's row scales [K-block of the group][128], then B's scales: [K-block][BN] row scales
+// for SCALE_ROW, or a box of at most 16 block scales for SCALE_BLOCK.
 template <int BN, int STAGES, int B_MODE, int SD, bool SPLITK>
 struct GemmSmem {
     static constexpr int A_BYTES = 128 * 128;                 // one 128x128 E4M3 tile of A
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(gemm_threads(B_MODE), 1)
                         }
                     }
                 } else {
-                                    if (SD == SD_TMA) {
+                    if (SD == SD_TMA) {
                         f = slot[q * 128 + row_local];
                         if (B_MODE == SCALE_BLOCK) {
                             const int cb = (int)(n0 >> 7);   // column block of this thread
