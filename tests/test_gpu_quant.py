@@ -107,6 +107,24 @@ def test_quantize_128x128_strided_and_zero_block(fp8lib, oracle):
     assert f32(s)[0, 0] == 0.0
 
 
+def test_quantize_128x128_tiny_blocks_in_a_long_sequence(fp8lib, oracle):
+    """512 blocks over at most 304 persistent CTAs, so CTAs run a second block. Two blocks
+    have amax small enough that their scale is below 2^-68 (the exact-division fallback),
+    one of them with BF16 denormals."""
+    N, K = 2048, 4096
+    w = synth.normal_bf16((N, K), 0.02, 17, "cuda")
+    w[3 * 128:4 * 128, 5 * 128:6 * 128] *= 2.0 ** -90           # amax ~2^-96: scale ~2^-105
+    w[10 * 128:11 * 128, 20 * 128:21 * 128] = 0.0
+    w[10 * 128 + 7, 20 * 128 + 9] = 2.0 ** -130                 # BF16 denormal, alone in its block
+    w[10 * 128 + 100, 20 * 128 + 1] = -(2.0 ** -131)
+    q, s, qT = fp8lib.quantize_128x128(w)
+    qr, sr, qTr = oracle.quantize_128x128(bits16(w))
+    assert_same_u8(u8(q), qr, "q")
+    assert_same_bits_f32(f32(s), sr, "s")
+    assert_same_u8(u8(qT), qTr, "qT")
+    assert 0.0 < f32(s)[3, 5] < 2.0 ** -68 and 0.0 < f32(s)[10, 20] < 2.0 ** -68
+
+
 def test_device_encoder_exhaustive(fp8lib, oracle):
     """The device E4M3 conversion equals the oracle's encoder on every finite binary32."""
     chunk = 1 << 28
