@@ -153,3 +153,35 @@ def test_zero_group_and_denormal_amax(oracle):
     quotient = np.float32(-(2.0 ** -131)) / s[1, 1]          # IEEE binary32 division
     assert q[1, 129] == oracle.e4m3_encode(np.array([quotient], np.float32))[0]
     assert np.all(q[1, 130:] == 0)
+
+
+def test_quotient_is_the_ieee_binary32_division_in_the_normal_range(oracle):
+    """Every code is the E4M3 rounding of the correctly rounded binary32 quotient x / s,
+    not of x times a rounded reciprocal: random groups whose maxima are not powers of two
+    (so s is not one either), spread over 2^-20 .. 2^20.  The reference is numpy's IEEE
+    binary32 division and torch's float8_e4m3fn cast, two routines the oracle does not use."""
+    rng = np.random.default_rng(5)
+    R, C = 256, 1024
+    sig = 2.0 ** rng.uniform(-20, 20, size=(R, 1))
+    x = (rng.standard_normal((R, C)) * sig).astype(np.float32)
+    xb = bf16_bits(x)
+    xf = oracle.bf16_to_f32(xb).astype(np.float32)
+    q, s = oracle.quantize_1x128(xb)
+    g = xf.reshape(R, C // 128, 128)
+    amax = np.abs(g).max(axis=2)
+    s_ref = amax / np.float32(448.0)                      # binary32 division
+    assert s_ref.dtype == np.float32
+    assert np.array_equal(s.T.view(np.uint32), s_ref.view(np.uint32))
+    # almost no scale is a power of two, so a reciprocal product differs somewhere
+    mant = s_ref.view(np.uint32) & 0x7FFFFF
+    assert np.mean(mant != 0) > 0.99
+    v = g / s_ref[:, :, None]                             # binary32 division, per element
+    assert v.dtype == np.float32
+    v = np.clip(v, -448.0, 448.0).reshape(R, C)
+    ref = torch.from_numpy(np.ascontiguousarray(v)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    bad = q != ref
+    assert not bad.any(), f"{int(bad.sum())} codes differ, first at {np.argwhere(bad)[0]}"
+    # the reciprocal form really differs on these inputs (so this test can tell them apart)
+    v_rcp = np.clip((g * (np.float32(1.0) / s_ref)[:, :, None]).reshape(R, C), -448.0, 448.0)
+    rcp = torch.from_numpy(np.ascontiguousarray(v_rcp)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert (rcp != ref).any()
