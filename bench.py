@@ -1,21 +1,24 @@
 """Benchmark of the unified-precision FP8 linear layer on one GB300 (or N replicas).
 
-One step = one pass of the whole hot path over the Llama-3.1-8B MLP at training shape
-(8192 tokens, hidden 4096, intermediate 14336) plus a 256-token rollout decode through the
-same FP8 weights ("Technical summary: Jet-RL": rollout and training forward share one
-quantization flow; master weights stay BF16 and are re-quantized each step):
+One step = one pass of the whole hot path over a Qwen2.5-32B-shaped transformer layer at
+16384 tokens (hidden 5120; qkv 7168x5120, o 5120x5120, gate_up 55296x5120, down
+5120x27648), forward, DGrad and WGrad of all four linears with their quantizers
+("Technical summary: Jet-RL": rollout and training forward share one quantization flow;
+master weights stay BF16 and are re-quantized each step; DGrad and WGrad run in FP8):
 
-  weight refresh   quantize_128x128(W_gate_up), quantize_128x128(W_down)  (+ W^T copies)
-  forward          rmsnorm_quant(X) -> gemm_fwd(gate_up) -> silu_mul_quant -> gemm_fwd(down)
-  backward down    quantize_1x128 dual(dY_down) -> gemm_dgrad -> gemm_wgrad
-  backward gate_up quantize_1x128 dual(dY_gate_up) -> gemm_dgrad -> gemm_wgrad
-  rollout decode   quantize_1x128(X_dec) -> gemm_fwd(gate_up, M=256) -> silu_mul_quant
-                   -> gemm_fwd(down, M=256)
+  weight refresh   quantize_128x128(W) for qkv, o, gate_up, down  (+ W^T copies)
+  forward          rmsnorm_quant(X_attn) -> gemm_fwd(qkv)
+                   quantize_1x128 dual(attention output) -> gemm_fwd(o)
+                   rmsnorm_quant(X_mlp) -> gemm_fwd(gate_up) -> silu_mul_quant -> gemm_fwd(down)
+  backward         for each linear: quantize_1x128 dual(dY) -> gemm_dgrad -> gemm_wgrad
 
 value = GEMM FLOPs of the step / device time of the step (TFLOP/s), inputs resident in HBM
 and larger than L2.  e2e = the same with the step's inputs copied from pinned host memory
 and its results copied back inside the timed region.  Per-kernel CUDA-event times give the
-quantizers' GB/s and the roofline of the dominant kernel.
+quantizers' GB/s and the roofline of the dominant kernel.  Two more workloads are reported
+beside it: the Llama-3.1-8B MLP training step at 8192 tokens, and the rollout decode
+linears of Qwen2.5-7B at 64, 128 and 256 tokens (CUDA-graph replays over weight copies
+larger than L2).
 
 `--impl reference` times the CPU oracle (test infrastructure, unchanged) on the host cores
 on a bounded sample of the same step and reports the same metric.
@@ -37,51 +40,73 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "FP8 block-scaled GEMM TFLOP/s & % FP8 peak; quantize GB/s vs HBM peak"
-M_TOK, HID, INTER, M_DEC = 8192, 4096, 14336, 256
-WORKLOAD = ("Llama-3.1-8B MLP layer: training step at 8192 tokens (fwd + DGrad + WGrad, "
-            "weight refresh) + 256-token rollout decode")
-FP8_PER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor throughput ratio on GB300
+FP8_PER_BF16 = 2.0       # nominal dense FP8 / BF16 tensor throughput ratio on GB300
+FP8_NOMINAL_TFLOPS = 4500.0
+
+# Qwen2.5-32B-shaped layer at 16384 tokens (the headline step)
+M32, H32 = 16384, 5120
+LIN32 = {"qkv": (7168, 5120), "o": (5120, 5120), "gate_up": (55296, 5120), "down": (5120, 27648)}
+WORKLOAD = ("Qwen2.5-32B layer at 16384 tokens: qkv 7168x5120, o 5120x5120, gate_up "
+            "55296x5120, down 5120x27648; fwd + DGrad + WGrad of all four with their "
+            "quantizers and the weight refresh")
+# Llama-3.1-8B MLP at 8192 tokens (reported beside it)
+M_TOK, HID, INTER = 8192, 4096, 14336
+# Qwen2.5-7B decode linears (reported beside it)
+DEC7B = {"qkv": (4608, 3584), "o": (3584, 3584), "gate_up": (37888, 3584), "down": (3584, 18944)}
+DEC_M = (64, 128, 256)
 
 
-def gemm_flops():
-    f = {}
-    f["fwd_gate_up"] = 2.0 * M_TOK * 2 * INTER * HID
-    f["fwd_down"] = 2.0 * M_TOK * HID * INTER
-    f["dgrad_down"] = f["fwd_down"]
-    f["wgrad_down"] = f["fwd_down"]
-    f["dgrad_gate_up"] = f["fwd_gate_up"]
-    f["wgrad_gate_up"] = f["fwd_gate_up"]
-    f["decode_gate_up"] = 2.0 * M_DEC * 2 * INTER * HID
-    f["decode_down"] = 2.0 * M_DEC * HID * INTER
-    return f
+def dual_bytes(E):
+    """BF16 in, 1x128 and 128x1 codes and scales out."""
+    return 2 * E + 2 * E + 2 * 4 * E / 128
 
 
-def quant_bytes():
-    """Algorithmic HBM bytes per launch of each quantizer: BF16 in, codes and FP32 scales out
-    (two code sets for the dual outputs), SiLU-mul reads gate and up."""
-    E_x, E_h, E_gu = M_TOK * HID, M_TOK * INTER, M_TOK * 2 * INTER
-    dual = lambda E: 2 * E + 2 * E + 2 * 4 * E / 128
-    b = {}
-    E_wgu = 2 * INTER * HID                                          # W_gate_up elements
-    b["wq_gate_up"] = 2 * E_wgu + E_wgu + E_wgu + 4 * E_wgu / 16384   # codes + W^T copy + scales
-    E_w = HID * INTER
-    b["wq_down"] = 2 * E_w + E_w + E_w + 4 * E_w / 16384
-    b["rmsnorm_quant"] = dual(E_x) + 2 * HID + 4 * M_TOK
-    b["silu_mul_quant"] = 2 * 2 * E_h + E_h + E_h + 2 * 4 * E_h / 128
-    b["dq_dy_down"] = dual(E_x)
-    b["dq_dy_gate_up"] = dual(E_gu)
-    b["decode_quant"] = 2 * M_DEC * HID + M_DEC * HID + 4 * M_DEC * HID / 128
-    b["decode_silu"] = 2 * 2 * M_DEC * INTER + M_DEC * INTER + 4 * M_DEC * INTER / 128
-    return b
+def wq_bytes(E):
+    """BF16 weight in, codes + W^T copy + block scales out."""
+    return 2 * E + E + E + 4 * E / 16384
 
 
-def decode_bytes():
-    """HBM bytes of a decode-shaped GEMM: the FP8 weight stream, its scales, the BF16
-    activations and the BF16 output (the activations are quantized by the kernel before)."""
-    d = {}
-    for name, N, K in (("decode_gate_up", 2 * INTER, HID), ("decode_down", HID, INTER)):
-        d[name] = N * K + 4 * (N // 128) * (K // 128) + M_DEC * K + 4 * M_DEC * K / 128 + 2 * M_DEC * N
-    return d
+def silu_bytes(M, I):
+    return 2 * 2 * M * I + M * I + M * I + 2 * 4 * M * I / 128
+
+
+def rms_bytes(M, K):
+    return dual_bytes(M * K) + 2 * K + 4 * M
+
+
+def layer32_work():
+    """(GEMM FLOPs per launch name, algorithmic HBM bytes per quantizer launch name)."""
+    f, b = {}, {}
+    M = M32
+    for name, (N, K) in LIN32.items():
+        fl = 2.0 * M * N * K
+        f[f"fwd_{name}"] = f[f"dgrad_{name}"] = f[f"wgrad_{name}"] = fl
+        b[f"wq_{name}"] = wq_bytes(N * K)
+        b[f"dq_dy_{name}"] = dual_bytes(M * N)
+    b["rmsnorm_quant_attn"] = rms_bytes(M, H32)
+    b["dq_attn_out"] = dual_bytes(M * H32)
+    b["rmsnorm_quant_mlp"] = rms_bytes(M, H32)
+    b["silu_mul_quant"] = silu_bytes(M, LIN32["down"][1])
+    return f, b
+
+
+def mlp8_work():
+    f, b = {}, {}
+    f["fwd_gate_up"] = f["dgrad_gate_up"] = f["wgrad_gate_up"] = 2.0 * M_TOK * 2 * INTER * HID
+    f["fwd_down"] = f["dgrad_down"] = f["wgrad_down"] = 2.0 * M_TOK * HID * INTER
+    b["wq_gate_up"] = wq_bytes(2 * INTER * HID)
+    b["wq_down"] = wq_bytes(HID * INTER)
+    b["rmsnorm_quant"] = rms_bytes(M_TOK, HID)
+    b["silu_mul_quant"] = silu_bytes(M_TOK, INTER)
+    b["dq_dy_down"] = dual_bytes(M_TOK * HID)
+    b["dq_dy_gate_up"] = dual_bytes(M_TOK * 2 * INTER)
+    return f, b
+
+
+def decode_work(M, N, K):
+    """(FLOPs, algorithmic HBM bytes) of one decode-shaped linear: the FP8 weight stream and
+    its block scales, the BF16 activations in, the BF16 output."""
+    return 2.0 * M * N * K, N * K + 4 * (N // 128) * (K // 128) + 2 * M * K + 2 * M * N
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -170,8 +195,81 @@ def measured_peaks():
 
 # ----------------------------------------------------------------------------- GPU arm
 
-class Step:
-    """All buffers of one step, resident on the device, and the launches in order."""
+class _Marks:
+    """Optional CUDA events after each launch (for the per-kernel split)."""
+
+    def __init__(self, torch, marks):
+        self.torch, self.marks = torch, marks
+
+    def __call__(self, name):
+        if self.marks is not None:
+            e = self.torch.cuda.Event(enable_timing=True)
+            e.record()
+            self.marks.append((name, e))
+
+
+class Layer32Step:
+    """Qwen2.5-32B-shaped layer at 16384 tokens: all buffers resident on the device and the
+    launches of one step in order."""
+
+    LAUNCHES_PER_STEP = 26   # 4 weight, 2x2 RMSNorm, 1 dual, 4 fwd, 1 SiLU-mul, 4x3 backward
+
+    def __init__(self, dev):
+        import torch
+        from block_scaled_fp8_x1_gb300 import _abi, ops, synth
+        self.torch, self.ops, self._abi = torch, ops, _abi
+        w = synth.QWEN32B_LAYER_M16384
+        lins = {l.name: l for l in w.linears}
+        self.x_attn = synth.activation(w, M32, H32, 0, dev)
+        self.attn_out = synth.activation(w, M32, H32, 1, dev)
+        self.x_mlp = synth.activation(w, M32, H32, 2, dev)
+        self.gamma = torch.ones(H32, dtype=torch.bfloat16, device=dev)
+        self.w = {n: synth.weight(w, lins[n], 10 + i, dev) for i, n in enumerate(LIN32)}
+        self.dy = {n: synth.gradient(w, M32, LIN32[n][0], 20 + i, dev) for i, n in enumerate(LIN32)}
+        self.eps = 1e-5
+        self.inputs = ["x_attn", "attn_out", "x_mlp", "gamma"] + [f"w.{n}" for n in LIN32] + \
+                      [f"dy.{n}" for n in LIN32]
+        self.outputs = {}
+
+    def tensor(self, name):
+        if "." in name:
+            d, k = name.split(".")
+            return getattr(self, d)[k]
+        return getattr(self, name)
+
+    def run(self, marks=None):
+        ops, V = self.ops, self._abi
+        mark = _Marks(self.torch, marks)
+        mark("start")
+        qw = {}
+        for n in LIN32:
+            qw[n] = ops.quantize_128x128(self.w[n]); mark(f"wq_{n}")
+        acts = {}
+        q, s, qT, sT, _ = ops.rmsnorm_quant(self.x_attn, self.gamma, self.eps); mark("rmsnorm_quant_attn")
+        acts["qkv"] = (q, s, qT, sT)
+        qkv = ops.gemm_fwd(q, s, qw["qkv"][0], qw["qkv"][1], variant=V.FP8RL_VARIANT_TILED); mark("fwd_qkv")
+        q, s, qT, sT = ops.quantize_1x128(self.attn_out, dual=True); mark("dq_attn_out")
+        acts["o"] = (q, s, qT, sT)
+        o = ops.gemm_fwd(q, s, qw["o"][0], qw["o"][1], variant=V.FP8RL_VARIANT_TILED); mark("fwd_o")
+        q, s, qT, sT, _ = ops.rmsnorm_quant(self.x_mlp, self.gamma, self.eps); mark("rmsnorm_quant_mlp")
+        acts["gate_up"] = (q, s, qT, sT)
+        gu = ops.gemm_fwd(q, s, qw["gate_up"][0], qw["gate_up"][1], variant=V.FP8RL_VARIANT_TILED); mark("fwd_gate_up")
+        acts["down"] = ops.silu_mul_quant(gu); mark("silu_mul_quant")
+        q, s = acts["down"][0], acts["down"][1]
+        y = ops.gemm_fwd(q, s, qw["down"][0], qw["down"][1], variant=V.FP8RL_VARIANT_TILED); mark("fwd_down")
+        out = {"qkv": qkv, "o": o, "y": y}
+        for n in ("down", "gate_up", "o", "qkv"):
+            qd, sd, qdT, sdT = ops.quantize_1x128(self.dy[n], dual=True); mark(f"dq_dy_{n}")
+            out[f"dx_{n}"] = ops.gemm_dgrad(qd, sd, qw[n][2], qw[n][1]); mark(f"dgrad_{n}")
+            out[f"dw_{n}"] = ops.gemm_wgrad(qdT, sdT, acts[n][2], acts[n][3]); mark(f"wgrad_{n}")
+        self.outputs = out
+        return out
+
+
+class Mlp8Step:
+    """Llama-3.1-8B MLP training step at 8192 tokens (forward, DGrad, WGrad, weight refresh)."""
+
+    LAUNCHES_PER_STEP = 14
 
     def __init__(self, dev):
         import torch
@@ -186,23 +284,11 @@ class Step:
         self.w_d = synth.weight(w, down, 2, dev)
         self.dy_d = synth.gradient(wb, M_TOK, HID, 3, dev)
         self.dy_gu = synth.gradient(wb, M_TOK, 2 * INTER, 4, dev)
-        self.x_dec = synth.activation(synth.QWEN7B_DECODE, M_DEC, HID, 5, dev)
         self.eps = w.extra["eps"]
-        self.dev = dev
-        self.inputs = ["x", "gamma", "w_gu", "w_d", "dy_d", "dy_gu", "x_dec"]
-        self.outputs = {}
 
     def run(self, marks=None):
-        """Launch the step; if `marks` is a list, append (name, event) after each launch."""
         ops, V = self.ops, self._abi
-        torch = self.torch
-
-        def mark(name):
-            if marks is not None:
-                e = torch.cuda.Event(enable_timing=True)
-                e.record()
-                marks.append((name, e))
-
+        mark = _Marks(self.torch, marks)
         mark("start")
         q_gu, s_gu, qT_gu = ops.quantize_128x128(self.w_gu); mark("wq_gate_up")
         q_d, s_d, qT_d = ops.quantize_128x128(self.w_d); mark("wq_down")
@@ -216,17 +302,109 @@ class Step:
         qg, sg, qgT, sgT = ops.quantize_1x128(self.dy_gu, dual=True); mark("dq_dy_gate_up")
         dx = ops.gemm_dgrad(qg, sg, qT_gu, s_gu); mark("dgrad_gate_up")
         dw_gu = ops.gemm_wgrad(qgT, sgT, qxT, sxT); mark("wgrad_gate_up")
-        qxd, sxd = ops.quantize_1x128(self.x_dec); mark("decode_quant")
-        gud = ops.gemm_fwd(qxd, sxd, q_gu, s_gu); mark("decode_gate_up")
-        qhd, shd, _, _ = ops.silu_mul_quant(gud, dual=False); mark("decode_silu")
-        yd = ops.gemm_fwd(qhd, shd, q_d, s_d); mark("decode_down")
-        # results read back by the end-to-end leg; dH stays on the device (it feeds the
-        # SiLU-mul backward, which lies outside this path)
-        self.keep = dh
-        self.outputs = {"y": y, "dx": dx, "dw_gu": dw_gu, "dw_d": dw_d, "y_dec": yd}
-        return self.outputs
+        return {"y": y, "dh": dh, "dx": dx, "dw_gu": dw_gu, "dw_d": dw_d}
 
-    LAUNCHES_PER_STEP = 16
+
+def time_steps(step, steps, torch):
+    """(ms per step over `steps` back-to-back steps, {kernel: [ms, ...]} from a second pass
+    with an event after every launch)."""
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        step.run()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    return ms
+
+
+def per_kernel(step, passes, torch):
+    """Per-launch durations from events between launches.  Each pass starts on an idle
+    device: a short device-side spin ahead of the first mark lets the host queue the whole
+    step first, so that no interval holds host launch time."""
+    per = {}
+    for _ in range(passes):
+        marks = []
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(8_000_000)   # about 4 ms at 2 GHz
+        step.run(marks)
+        torch.cuda.synchronize()
+        for (_, a), (name, b) in zip(marks[:-1], marks[1:]):
+            per.setdefault(name, []).append(a.elapsed_time(b))
+    return {k: statistics.mean(v) for k, v in per.items()}
+
+
+def kernel_table(per_ms, flops, qbytes, fp8_peak, hbm):
+    kern = {}
+    for name, ms in per_ms.items():
+        e = {"ms": round(ms, 4)}
+        if name in flops:
+            tf = flops[name] / (ms * 1e-3) / 1e12
+            e.update({"TFLOP/s": round(tf, 1), "frac_fp8_peak": round(tf / fp8_peak, 3)})
+        elif name in qbytes:
+            gbs = qbytes[name] / (ms * 1e-3) / 1e9
+            e.update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)})
+        kern[name] = e
+    return kern
+
+
+def decode_table(dev, fp8_peak, hbm, reps=40):
+    """Qwen2.5-7B decode linears at M in {64, 128, 256}: activation quantization plus the
+    decode GEMM per call, timed as CUDA-graph replays of `reps` calls that cycle through
+    weight copies larger than L2 in total, so every call streams its weights from HBM.
+    Returns {"<linear>_m<M>": {...}} with the roofline fraction max(FLOP/peak, bytes/HBM)
+    / time."""
+    import torch
+    from block_scaled_fp8_x1_gb300 import _abi, ops, synth
+    w = synth.QWEN7B_DECODE
+    lins = {l.name: l for l in w.linears}
+    rows = {}
+    for li, (name, (N, K)) in enumerate(DEC7B.items()):
+        wq = ops.quantize_128x128(synth.weight(w, lins[name], 30 + li, dev), transpose=False)
+        ncopy = max(2, -(-(512 << 20) // (N * K)))
+        copies = [(wq[0].clone(), wq[1].clone()) for _ in range(ncopy)]
+        del wq
+        for M in DEC_M:
+            x = synth.activation(w, M, K, 40 + li, dev)
+            # the workspace cache is filled before capture
+            ops.workspace(ops.gemm_workspace_bytes(_abi.FP8RL_OP_FWD, M, N, K), x.device)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+            def call(i):
+                qx, sx = ops.quantize_1x128(x)
+                ops.gemm_fwd(qx, sx, copies[i % ncopy][0], copies[i % ncopy][1], out=y)
+
+            for i in range(3):
+                call(i)
+            torch.cuda.synchronize()
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s):
+                    for i in range(reps):
+                        call(i)
+            torch.cuda.synchronize()
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(5):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (5 * reps)
+            fl, by = decode_work(M, N, K)
+            roof_us = max(fl / (fp8_peak * 1e12), by / (hbm * 1e9)) * 1e6
+            rows[f"{name}_m{M}"] = {"M": M, "N": N, "K": K, "us": round(us, 2),
+                                    "GB/s": round(by / (us * 1e-6) / 1e9, 1),
+                                    "TFLOP/s": round(fl / (us * 1e-6) / 1e12, 1),
+                                    "roofline_us": round(roof_us, 2),
+                                    "frac_roofline": round(roof_us / us, 3)}
+            del g, x, y
+        del copies
+        torch.cuda.empty_cache()
+    return rows
 
 
 def max_over_ranks(ms: float, device) -> float:
@@ -262,8 +440,13 @@ def run_gpu(args):
     build_library()
     ops.init(local)
 
-    step = Step(dev)
-    flops = gemm_flops()
+    peaks = measured_peaks()
+    # kernels are timed inside a sub-second region: the burst rate is their ceiling
+    fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
+    hbm = peaks["hbm_gbs"]
+
+    step = Layer32Step(dev)
+    flops, qbytes = layer32_work()
     step_flops = sum(flops.values())
 
     def barrier():
@@ -275,49 +458,32 @@ def run_gpu(args):
         step.run()
     barrier()
 
-    # ---- device-resident timed region: whole steps, then per-kernel split
+    # ---- device-resident timed region: whole steps
     clocks = ClockSampler(local)
     clocks.start()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
     barrier()
     w0 = time.time()
-    t0.record()
-    for _ in range(args.steps):
-        step.run()
-    t1.record()
+    ms_total = time_steps(step, args.steps, torch)
     barrier()
     w1 = time.time()
-    ms_total = t0.elapsed_time(t1)
-    # per-kernel durations from events between launches (separate pass, same work).  Each
-    # pass starts on an idle device: a short device-side spin ahead of the first mark lets
-    # the host queue the whole step first, so no mark interval holds host launch time.
-    per = {}
-    for _ in range(args.steps):
-        marks = []
-        if hasattr(torch.cuda, "_sleep"):
-            torch.cuda._sleep(4_000_000)   # about 2 ms at 2 GHz
-        step.run(marks)
-        torch.cuda.synchronize()
-        for (_, a), (name, b) in zip(marks[:-1], marks[1:]):
-            per.setdefault(name, []).append(a.elapsed_time(b))
     clk = clocks.stop((w0, w1))
+    ms_step = max_over_ranks(ms_total, dev)
+    # per-kernel split (separate passes, same work)
+    per = per_kernel(step, max(3, min(args.steps, 10)), torch)
     st = ops.check_status()
-
-    ms_step = max_over_ranks(ms_total / args.steps, dev)
 
     # ---- end to end: host buffers, copies inside the timed region.  Every step uploads
     # its inputs from pinned host memory and downloads its results; the copies run on two
     # copy streams and overlap the neighbouring steps' compute (two device input sets,
     # ordered by events), as a training loop that feeds the GPU would.
-    host_in = {n: torch.empty_like(getattr(step, n), device="cpu").pin_memory() for n in step.inputs}
+    host_in = {n: torch.empty_like(step.tensor(n), device="cpu").pin_memory() for n in step.inputs}
     for n in step.inputs:
-        host_in[n].copy_(getattr(step, n))
+        host_in[n].copy_(step.tensor(n))
     outs = step.run()
     host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in outs.items()}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-    sets = [step, Step(dev)]                      # device input sets, used alternately
+    sets = [step, Layer32Step(dev)]               # device input sets, used alternately
     comp = torch.cuda.current_stream()
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     uploaded = [torch.cuda.Event(), torch.cuda.Event()]
@@ -326,11 +492,11 @@ def run_gpu(args):
         e.record(comp)
 
     def upload(i):
-        st = sets[i % 2]
+        sset = sets[i % 2]
         up.wait_event(computed[i % 2])            # the set's previous step is done with it
         with torch.cuda.stream(up):
-            for n in st.inputs:
-                getattr(st, n).copy_(host_in[n], non_blocking=True)
+            for n in sset.inputs:
+                sset.tensor(n).copy_(host_in[n], non_blocking=True)
         uploaded[i % 2].record(up)
 
     def compute_and_download(i):
@@ -362,64 +528,72 @@ def run_gpu(args):
     e1.record(comp)
     barrier()
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    del sets, host_in, host_out, outs
+    step.outputs = {}
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
-    peaks = measured_peaks()
-    fp8_peak_sustained = peaks["bf16_tflops_sustained"] * FP8_PER_BF16
-    kern = {}
-    qb = quant_bytes()
-    db = decode_bytes()
-    for name, v in per.items():
-        ms = statistics.mean(v)
-        e = {"ms": round(ms, 4)}
-        if name in db:
-            gbs = db[name] / (ms * 1e-3) / 1e9
-            e.update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3),
-                      "TFLOP/s": round(flops[name] / (ms * 1e-3) / 1e12, 1)})
-        elif name in flops:
-            tf = flops[name] / (ms * 1e-3) / 1e12
-            e.update({"TFLOP/s": round(tf, 1), "frac_fp8_peak": round(tf / fp8_peak_sustained, 3)})
-        elif name in qb:
-            gbs = qb[name] / (ms * 1e-3) / 1e9
-            e.update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 3)})
-        kern[name] = e
+    kern = kernel_table(per, flops, qbytes, fp8_peak, hbm)
     dominant = max(kern, key=lambda n: kern[n]["ms"])
     dom_ms = kern[dominant]["ms"]
-    if dominant in flops and dominant not in db:
+    if dominant in flops:
         achieved = flops[dominant] / (dom_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak_sustained, 1),
-                "unit": "TFLOP/s", "frac": round(achieved / fp8_peak_sustained, 3),
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 3),
                 "traffic": load_traffic(dominant), "kernel": dominant,
-                "peak_note": f"{peaks['source']} sustained bf16 x {FP8_PER_BF16} (nominal FP8/BF16 ratio)"}
+                "frac_of_nominal_4500": round(achieved / FP8_NOMINAL_TFLOPS, 3),
+                "peak_note": f"{peaks['source']} burst bf16 {peaks['bf16_tflops']} x {FP8_PER_BF16} "
+                             f"(nominal FP8/BF16 ratio); kernels timed in a sub-second region"}
     else:
-        nbytes = qb.get(dominant, db.get(dominant, 0.0))
-        achieved = nbytes / (dom_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 3), "traffic": load_traffic(dominant),
+        achieved = qbytes[dominant] / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 3), "traffic": load_traffic(dominant),
                 "kernel": dominant, "peak_note": f"{peaks['source']} copy bandwidth"}
     value = job_rate(step_flops, world, ms_step) / 1e12
+
+    # ---- beside the headline: the 8B MLP step and the 7B decode linears (rank 0 only)
+    extra = {}
+    if not args.no_extra:
+        torch.cuda.empty_cache()
+        s8 = Mlp8Step(dev)
+        f8, b8 = mlp8_work()
+        for _ in range(3):
+            s8.run()
+        torch.cuda.synchronize()
+        ms8 = time_steps(s8, args.steps, torch)
+        k8 = kernel_table(per_kernel(s8, 5, torch), f8, b8, fp8_peak, hbm)
+        extra["llama8b_mlp_step"] = {
+            "workload": "Llama-3.1-8B MLP training step at 8192 tokens (gate_up 28672x4096, "
+                        "down 4096x14336; fwd + DGrad + WGrad, weight refresh)",
+            "ms_per_step": round(ms8, 4), "TFLOP/s": round(sum(f8.values()) / (ms8 * 1e-3) / 1e12, 1),
+            "kernels": k8}
+        del s8
+        torch.cuda.empty_cache()
+        extra["qwen7b_decode"] = decode_table(dev, fp8_peak, hbm)
+
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8_e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens": M_TOK, "hidden": HID, "intermediate": INTER,
-                   "decode_tokens": M_DEC, "gemm_flops_per_step": step_flops,
-                   "l2": "inputs larger than L2 (X 64 MB, W_gate_up 224 MB, dY_gate_up 448 MB per step)",
+        "config": {"workload": WORKLOAD, "tokens": M32, "hidden": H32,
+                   "linears": {k: list(v) for k, v in LIN32.items()},
+                   "gemm_flops_per_step": step_flops,
+                   "l2": "inputs larger than L2 (X 168 MB each, W_gate_up 566 MB, dY_gate_up 1.8 GB per step)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
         "e2e": {"value": round(job_rate(step_flops, world, ms_e2e) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4),
                 "copies": "every step's inputs up from pinned host memory and results down, on two copy streams overlapping the neighbouring steps' compute"},
-        "gpu_launches": Step.LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": Layer32Step.LAUNCHES_PER_STEP * args.steps,
         "clocks": clk,
         "kernels": kern,
         "device_status": st,
     }
+    line.update(extra)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line), flush=True)
@@ -456,9 +630,10 @@ def load_traffic(kernel: str):
 # ----------------------------------------------------------------------------- oracle arm
 
 def oracle_step_estimate(rows: int, n_samp: int):
-    """Time the CPU oracle on a bounded sample of every kernel of the step (quantizers on
-    `rows` token rows, GEMMs on `n_samp` output elements) and extrapolate each to its full
-    size.  Returns (estimated seconds for one full step, threads, sample description)."""
+    """Time the CPU oracle on a bounded sample of every kernel of the 32B layer step
+    (quantizers on `rows` token rows or weight rows, GEMMs on `n_samp` output elements) and
+    extrapolate each to its full size.  Returns (estimated seconds for one full step,
+    threads, sample description)."""
     import numpy as np
     import torch
 
@@ -466,50 +641,58 @@ def oracle_step_estimate(rows: int, n_samp: int):
     from block_scaled_fp8_x1_gb300 import synth
 
     threads = oracle.threads()
-    w = synth.LLAMA8B_MLP_M8192
+    w = synth.QWEN32B_LAYER_M16384
+    lins = {l.name: l for l in w.linears}
     rng = np.random.default_rng(0)
 
     def bits(t):
         return t.contiguous().view(torch.int16).numpy().view(np.uint16)
-
-    x = bits(synth.activation(w, rows, HID, 0))
-    gu = bits(synth.normal_bf16((rows, 2 * INTER), 2.0, 9))
-    wq_rows = 128
-    wgu = bits(synth.weight(w, w.linears[0], 1)[:wq_rows])
-    est = 0.0
-    parts = []
 
     def timed(fn):
         t = time.perf_counter()
         out = fn()
         return time.perf_counter() - t, out
 
-    # quantizers (sampled rows, scaled by full rows / sampled rows)
-    t, _ = timed(lambda: oracle.quantize_128x128(wgu))
-    est += t * (2 * INTER + HID) / wq_rows
-    t, r = timed(lambda: oracle.rmsnorm_quant(x, np.full(HID, 0x3F80, np.uint16), 1e-5))
-    est += t * M_TOK / rows
+    est = 0.0
+    x = bits(synth.activation(w, rows, H32, 0))
+    gamma = np.full(H32, 0x3F80, np.uint16)
+    # weight refresh: 128 weight rows of each linear, scaled by its rows
+    for n, (N, K) in LIN32.items():
+        wb = bits(synth.normal_bf16((128, K), w.weight_std, 7))
+        t, _ = timed(lambda: oracle.quantize_128x128(wb))
+        est += t * N / 128
+    # two RMSNorm dual quantizers, the attention-output dual quantizer
+    t, r = timed(lambda: oracle.rmsnorm_quant(x, gamma, 1e-5))
+    est += 2 * t * M32 / rows
+    t, _ = timed(lambda: (oracle.quantize_1x128(x), oracle.quantize_128x1(x)))
+    est += t * M32 / rows
+    # SiLU-mul on the gate_up output, then its dual quantization
+    I = LIN32["down"][1]
+    gu = bits(synth.normal_bf16((rows, 2 * I), 2.0, 9))
     t, h = timed(lambda: oracle.silu_mul(gu))
     t2, _ = timed(lambda: (oracle.quantize_1x128(h[0]), oracle.quantize_128x1(h[0])))
-    est += (t + t2) * M_TOK / rows
+    est += (t + t2) * M32 / rows
+    # dual quantization of every dY, per element of the sampled activation rows
     t, _ = timed(lambda: (oracle.quantize_1x128(x), oracle.quantize_128x1(x)))
-    est += t * M_TOK / rows * (1 + 2 * INTER / HID)        # dY_down and dY_gate_up
-    parts.append(f"quantizers on {rows} rows")
+    est += t * M32 / rows * sum(N for N, _ in LIN32.values()) / H32
+    parts = [f"quantizers on {rows} token rows / 128 weight rows"]
     # GEMMs: sampled output elements, scaled by outputs / samples
     qx, sx = r[0], r[1]
-    qw, sw, _ = oracle.quantize_128x128(bits(synth.weight(w, w.linears[0], 1)[:256]))
+    qw, sw, _ = oracle.quantize_128x128(bits(synth.weight(w, lins["qkv"], 1)[:256]))
     i1 = rng.integers(0, rows, n_samp)
     i2 = rng.integers(0, 256, n_samp)
     t, _ = timed(lambda: oracle.gemm_sampled(qx, sx, qw, sw, "fwd", i1, i2))
-    per_flop = t / (2.0 * HID * n_samp)
-    est += per_flop * sum(gemm_flops().values())
-    parts.append(f"{n_samp} GEMM outputs (K={HID}) extrapolated per FLOP")
+    per_flop = t / (2.0 * H32 * n_samp)
+    f, _ = layer32_work()
+    est += per_flop * sum(f.values())
+    parts.append(f"{n_samp} GEMM outputs (K={H32}) extrapolated per FLOP")
     return est, threads, "; ".join(parts)
 
 
 def cpu_baseline():
-    est, threads, sample = oracle_step_estimate(rows=1024, n_samp=4096)
-    flops = sum(gemm_flops().values())
+    est, threads, sample = oracle_step_estimate(rows=512, n_samp=4096)
+    f, _ = layer32_work()
+    flops = sum(f.values())
     return {"value": round(flops / est / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle", "sample": sample + f"; full step extrapolated to {est:.1f} s",
             "ms_per_step_extrapolated": round(est * 1e3, 1)}
@@ -531,7 +714,8 @@ def run_reference(args):
         ests.append(e)
     wall = time.perf_counter() - t0
     est = statistics.median(ests)
-    flops = sum(gemm_flops().values())
+    f, _ = layer32_work()
+    flops = sum(f.values())
     value = flops / est / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
@@ -539,8 +723,8 @@ def run_reference(args):
         "ms_per_step": round(est * 1e3, 1), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64 (oracle: binary64 block sums, binary32 quantizers)",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens": M_TOK, "hidden": HID, "intermediate": INTER,
-                   "decode_tokens": M_DEC},
+        "config": {"workload": WORKLOAD, "tokens": M32, "hidden": H32,
+                   "linears": {k: list(v) for k, v in LIN32.items()}},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads,
                          "kind": "oracle", "sample": sample + f"; {args.steps} samples in {wall:.1f} s"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -630,6 +814,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the 8B MLP step and the 7B decode table beside the headline")
     ap.add_argument("--kernel", default=None,
                     help="run one kernel form alone (for profiling): gemm_fwd, gemm_dgrad, "
                          "gemm_wgrad, gemm_decode, rmsnorm_quant, silu_mul_quant, quant_dual, "

@@ -500,9 +500,10 @@ fp8rl_status fp8rl_gemm_fwd_decode_noalloc(const uint8_t* qx, const float* sx, c
     if (e != FP8RL_OK) return e;
     const int64_t tiles = decode_tiles(M, N);
     const size_t have = noalloc_scratch_bytes();
-    // the automatic split, or the largest smaller one whose partial sums fit the array
-    int splits = choose_splits(tiles, K / 128, sms);
-    while (splits > 1 && decode_ws_bytes(M, N, K, splits) > have) --splits;
+    // The automatic split keeps tiles x slices <= SMs, so the partial sums never exceed
+    // SMs x 128 KiB (19 MiB at 152 SMs): they fit the 32 MiB array on any GPU with up to
+    // 256 SMs.  A larger GPU would be refused here rather than overrun the array.
+    const int splits = choose_splits(tiles, K / 128, sms);
     if (decode_ws_bytes(M, N, K, splits) > have) return FP8RL_ERR_WORKSPACE;
     void* scratch = nullptr;
     if (noalloc_scratch(&scratch) != cudaSuccess) return FP8RL_ERR_CUDA;

@@ -644,6 +644,14 @@ __global__ void __launch_bounds__(128) k_splitk_reduce(const GemmParams p) {
             sum[j].x += v.x; sum[j].y += v.y; sum[j].z += v.z; sum[j].w += v.w;
         }
     }
+    // A slice whose bounded wait ran out stored no partial sums, so its slot may hold
+    // another call's: once a timeout is on record (until fp8rl_check_status clears it)
+    // the result is NaN rather than plausible but wrong values.
+    if (*reinterpret_cast<volatile unsigned int*>(&g_device_status) == FP8RL_ERR_DEVICE_TIMEOUT) {
+        const float qnan = __uint_as_float(0x7FC00000u);
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) sum[j] = make_float4(qnan, qnan, qnan, qnan);
+    }
     uint4 o0, o1;
     o0.x = pack_bf16x2(sum[0].x, sum[0].y); o0.y = pack_bf16x2(sum[0].z, sum[0].w);
     o0.z = pack_bf16x2(sum[1].x, sum[1].y); o0.w = pack_bf16x2(sum[1].z, sum[1].w);

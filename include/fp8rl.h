@@ -100,7 +100,10 @@ FP8RL_API fp8rl_status fp8rl_init(int device);
 FP8RL_API void fp8rl_set_wait_timeout_ns(uint64_t ns);
 
 /* Waits for `stream`, then reads and clears the current device's status word.
- * Returns FP8RL_OK or the first device-side error recorded since the last check. */
+ * Returns FP8RL_OK or the first device-side error recorded since the last check.
+ * FP8RL_ERR_DEVICE_TIMEOUT means that the outputs of the GEMM calls made since the
+ * previous check are not valid: a CTA whose wait ran out skips its stores (the split-K
+ * reduction writes NaN instead once a timeout is on record). */
 FP8RL_API fp8rl_status fp8rl_check_status(fp8rl_stream_t stream);
 
 /* ----------------------------------------------------------------------------------------
@@ -230,11 +233,13 @@ FP8RL_API fp8rl_status fp8rl_gemm_fwd_ex(const uint8_t* qx, const float* sx, con
  * a fixed scratch array inside the library,
  * fp8rl_gemm_noalloc_scratch_bytes() bytes (32 MiB) per device, reserved on every GPU
  * that loads the library and held until the process exits.
- *   - When the automatic split needs more scratch than that, the largest smaller split
- *     that fits is used (one slice always fits); M > 256 returns FP8RL_ERR_SHAPE and
- *     launches nothing.
- *   - The first call on a device looks up the array's device address (with that device
- *     current) and caches it; make that first call before any stream capture.
+ *   - The automatic split keeps at most one (tile, slice) pair per SM, so the partial
+ *     sums take at most SMs x 128 KiB (19 MiB on a 152-SM GB300); a GPU where they would
+ *     not fit gets FP8RL_ERR_WORKSPACE.  M > 256 returns FP8RL_ERR_SHAPE.  Neither
+ *     launches anything.
+ *   - The first call in each CUDA context of a device looks up the array's device
+ *     address (with that device current) and caches it; make that first call before any
+ *     stream capture.
  *   - Every call on a device shares the array, which keeps the last call's partial sums
  *     (each call writes its own before reading them, so nothing needs clearing); calls
  *     whose kernels overlap on the GPU race on the array and give wrong results, so order
