@@ -745,19 +745,22 @@ def run_kernel(args):
     k = args.kernel
     if k.startswith("gemm"):
         M, N, K = dims
+        var = {"auto": _abi.FP8RL_VARIANT_AUTO, "tiled": _abi.FP8RL_VARIANT_TILED,
+               "pair": _abi.FP8RL_VARIANT_PAIR}[args.variant]
         if k == "gemm_wgrad":
             a = ops.quantize_128x1(synth.normal_bf16((M, N), 1e-3, 1, dev))
             b = ops.quantize_128x1(synth.normal_bf16((M, K), 1.0, 2, dev))
-            fn = lambda: ops.gemm_wgrad(a[0], a[1], b[0], b[1])
+            fn = lambda: ops.gemm_wgrad(a[0], a[1], b[0], b[1], variant=var, epi_warps=args.epi)
         else:
             lhs_cols = N if k == "gemm_dgrad" else K
             qa, sa = ops.quantize_1x128(synth.normal_bf16((M, lhs_cols), 1.0, 1, dev))
             if k == "gemm_dgrad":
                 _, sw, qwT = ops.quantize_128x128(synth.normal_bf16((N, K), 0.02, 2, dev))
-                fn = lambda: ops.gemm_dgrad(qa, sa, qwT, sw)
+                fn = lambda: ops.gemm_dgrad(qa, sa, qwT, sw, variant=var, epi_warps=args.epi)
             else:
                 qw, sw, _ = ops.quantize_128x128(synth.normal_bf16((N, K), 0.02, 2, dev), transpose=False)
-                var = _abi.FP8RL_VARIANT_SPLITK if k == "gemm_decode" else _abi.FP8RL_VARIANT_TILED
+                if k == "gemm_decode":
+                    var = _abi.FP8RL_VARIANT_SPLITK
                 # decode streams each layer's weights once: cycle through copies that together
                 # exceed L2 so that back-to-back launches read HBM, not L2
                 ncopy = max(1, -(-(256 << 20) // (N * K))) if k == "gemm_decode" else 1
@@ -767,7 +770,8 @@ def run_kernel(args):
                 def fn():
                     w_q, w_s = ws[it[0] % len(ws)]
                     it[0] += 1
-                    return ops.gemm_fwd(qa, sa, w_q, w_s, variant=var, tile_n=args.tile_n)
+                    return ops.gemm_fwd(qa, sa, w_q, w_s, variant=var, tile_n=args.tile_n,
+                                        epi_warps=args.epi)
         work, unit = 2.0 * M * N * K, "TFLOP/s"
     else:
         M, K = dims
@@ -823,6 +827,9 @@ def main():
     ap.add_argument("--shape", default=None, help="M,N,K (GEMMs) or M,K (quantizers)")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--tile-n", type=int, default=0, help="tiled forward GEMM tile width (128/256)")
+    ap.add_argument("--variant", default="auto", choices=["auto", "tiled", "pair"],
+                    help="GEMM form for --kernel gemm_fwd/gemm_dgrad/gemm_wgrad")
+    ap.add_argument("--epi", type=int, default=0, help="paired form: epilogue warps per CTA (8/16)")
     args = ap.parse_args()
     if args.kernel:
         run_kernel(args)

@@ -33,7 +33,7 @@ FP8RL_ERR_DEVICE_TIMEOUT = 7
 FP8RL_ERR_DEVICE_BOUNDS = 8
 
 FP8RL_OP_FWD, FP8RL_OP_DGRAD, FP8RL_OP_WGRAD = 0, 1, 2
-FP8RL_VARIANT_AUTO, FP8RL_VARIANT_TILED, FP8RL_VARIANT_SPLITK = 0, 1, 2
+FP8RL_VARIANT_AUTO, FP8RL_VARIANT_TILED, FP8RL_VARIANT_SPLITK, FP8RL_VARIANT_PAIR = 0, 1, 2, 3
 
 
 class Fp8rlError(RuntimeError):
@@ -46,7 +46,7 @@ class Fp8rlError(RuntimeError):
 
 class GemmOpts(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("splits", ctypes.c_int), ("grid", ctypes.c_int),
-                ("tile_n", ctypes.c_int)]
+                ("tile_n", ctypes.c_int), ("epi_warps", ctypes.c_int)]
 
 
 P = ctypes.c_void_p
@@ -74,6 +74,10 @@ SIGNATURES = {
                                                         ctypes.POINTER(GemmOpts)]),
     "fp8rl_gemm_fwd_ex": (ST, [P, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t,
                                ctypes.POINTER(GemmOpts), STREAM]),
+    "fp8rl_gemm_dgrad_ex": (ST, [P, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t,
+                                 ctypes.POINTER(GemmOpts), STREAM]),
+    "fp8rl_gemm_wgrad_ex": (ST, [P, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t,
+                                 ctypes.POINTER(GemmOpts), STREAM]),
     "fp8rl_gemm_fwd_decode_noalloc": (ST, [P, P, P, P, P, I64, I64, I64, STREAM]),
     "fp8rl_gemm_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "fp8rl_debug_e4m3_encode": (ST, [P, P, I64, STREAM]),

@@ -171,7 +171,11 @@ typedef enum { FP8RL_OP_FWD = 0, FP8RL_OP_DGRAD = 1, FP8RL_OP_WGRAD = 2 } fp8rl_
  * depend on timing).  When it splits, it needs fp8rl_gemm_workspace_bytes(FP8RL_OP_FWD,
  * M, N, K) bytes of workspace for the partial sums (no initial contents required); calls
  * that overlap in time need separate workspaces.  A size of 0 (no split, or larger M)
- * means ws may be NULL. */
+ * means ws may be NULL.
+ * Larger M takes the one-SM tiled form (FP8RL_VARIANT_TILED); the paired-SM form
+ * (FP8RL_VARIANT_PAIR) is available on request when every scale array can be moved by TMA:
+ * M % 4 == 0 and (K/128) % 4 == 0 for the forward GEMM, M % 4 == 0 and (K/128) % 4 == 0
+ * on the weight's block-scale rows for DGrad, always for WGrad. */
 FP8RL_API fp8rl_status fp8rl_gemm_fwd(const uint8_t* qx, const float* sx, const uint8_t* qw,
                             const float* sw, uint16_t* y, int64_t M, int64_t N, int64_t K,
                             void* ws, size_t ws_bytes, fp8rl_stream_t stream);
@@ -199,17 +203,23 @@ FP8RL_API size_t fp8rl_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_
 
 /* Explicit kernel choice, for tests and benchmarks. */
 typedef enum {
-    FP8RL_VARIANT_AUTO = 0,   /* what fp8rl_gemm_fwd picks */
-    FP8RL_VARIANT_TILED = 1,  /* persistent 128 x BN tiles over (M, N) */
-    FP8RL_VARIANT_SPLITK = 2  /* decode-shaped: the reduction of each 128x256 output tile
-                                 is split over `splits` CTAs (M <= 256) */
+    FP8RL_VARIANT_AUTO = 0,   /* what fp8rl_gemm_fwd / _dgrad / _wgrad pick */
+    FP8RL_VARIANT_TILED = 1,  /* one SM per output tile: persistent 128 x BN tiles */
+    FP8RL_VARIANT_SPLITK = 2, /* decode-shaped: the reduction of each 128x256 output tile
+                                 is split over `splits` CTAs (forward only, M <= 256) */
+    FP8RL_VARIANT_PAIR = 3    /* two SMs per output tile: persistent 256 x 128 tiles on
+                                 clusters of two CTAs (M = 256 tensor-core MMAs); needs
+                                 scale arrays whose rows are multiples of 16 bytes (the
+                                 rule under fp8rl_gemm_fwd), else FP8RL_ERR_SHAPE */
 } fp8rl_variant;
 
 typedef struct {
-    int variant;  /* fp8rl_variant */
-    int splits;   /* SPLITK: number of reduction slices (0 = choose); ignored otherwise */
-    int grid;     /* TILED: persistent CTAs (0 = one per SM); ignored otherwise */
-    int tile_n;   /* TILED: output tile width, 128 or 256 (0 = choose); ignored otherwise */
+    int variant;    /* fp8rl_variant */
+    int splits;     /* SPLITK: number of reduction slices (0 = choose); ignored otherwise */
+    int grid;       /* TILED: persistent CTAs (0 = one per SM); PAIR: persistent clusters
+                       (0 = one per two SMs); ignored otherwise */
+    int tile_n;     /* TILED: output tile width, 128 or 256 (0 = choose); ignored otherwise */
+    int epi_warps;  /* PAIR: epilogue warps per CTA, 8 or 16 (0 = choose); ignored otherwise */
 } fp8rl_gemm_opts;
 
 /* Workspace bytes fp8rl_gemm_fwd_ex needs with these options (opts may be NULL = AUTO). */
@@ -221,6 +231,17 @@ FP8RL_API fp8rl_status fp8rl_gemm_fwd_ex(const uint8_t* qx, const float* sx, con
                                const float* sw, uint16_t* y, int64_t M, int64_t N,
                                int64_t K, void* ws, size_t ws_bytes,
                                const fp8rl_gemm_opts* opts, fp8rl_stream_t stream);
+
+/* fp8rl_gemm_dgrad / fp8rl_gemm_wgrad with an explicit variant (AUTO, TILED or PAIR);
+ * opts may be NULL (= AUTO). */
+FP8RL_API fp8rl_status fp8rl_gemm_dgrad_ex(const uint8_t* qdy, const float* sdy, const uint8_t* qwT,
+                                 const float* sw, uint16_t* dx, int64_t M, int64_t N,
+                                 int64_t K, void* ws, size_t ws_bytes,
+                                 const fp8rl_gemm_opts* opts, fp8rl_stream_t stream);
+FP8RL_API fp8rl_status fp8rl_gemm_wgrad_ex(const uint8_t* qdyT, const float* sdyT, const uint8_t* qxT,
+                                 const float* sxT, uint16_t* dw, int64_t M, int64_t N,
+                                 int64_t K, void* ws, size_t ws_bytes,
+                                 const fp8rl_gemm_opts* opts, fp8rl_stream_t stream);
 
 /* Decode-shaped forward GEMM that allocates nothing and takes no workspace.  It has no
  * counterpart in the scheme's pages; it exists for callers that cannot provide device

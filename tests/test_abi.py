@@ -64,6 +64,10 @@ def test_host_side_validation_without_gpu(abi):
     assert L.fp8rl_rmsnorm_quant(fake, fake, ctypes.c_float(-1.0), 4, 128, fake, fake, null, null, null, null) == abi.FP8RL_ERR_INVALID_ARG
     opts = abi.GemmOpts(7, 0, 0)
     assert L.fp8rl_gemm_fwd_ex(fake, fake, fake, fake, fake, 4, 128, 128, null, 0, ctypes.byref(opts), null) == abi.FP8RL_ERR_INVALID_ARG
+    # DGrad / WGrad take AUTO, TILED or PAIR; the split-K form is forward-only
+    splitk = abi.GemmOpts(abi.FP8RL_VARIANT_SPLITK, 0, 0)
+    assert L.fp8rl_gemm_dgrad_ex(fake, fake, fake, fake, fake, 4, 128, 128, null, 0, ctypes.byref(splitk), null) == abi.FP8RL_ERR_INVALID_ARG
+    assert L.fp8rl_gemm_wgrad_ex(fake, fake, fake, fake, fake, 128, 128, 128, null, 0, ctypes.byref(opts), null) == abi.FP8RL_ERR_INVALID_ARG
     # alignment (16 bytes for every device pointer)
     assert L.fp8rl_quantize_1x128(odd, 4, 128, 128, fake, fake, null, null, null) == abi.FP8RL_ERR_ALIGN
     assert L.fp8rl_quantize_1x128(fake, 4, 128, 132, fake, fake, null, null, null) == abi.FP8RL_ERR_ALIGN

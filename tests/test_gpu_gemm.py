@@ -59,7 +59,8 @@ def test_fwd_auto_matches_forms(fp8lib, oracle):
     M, N, K = 192, 768, 2048
     qx, sx, qw, sw, _ = fwd_operands(fp8lib, oracle, M, N, K, 99)
     y_ref = oracle.gemm(u8(qx), f32(sx), u8(qw), f32(sw), "fwd")
-    for v in (_abi.FP8RL_VARIANT_AUTO, _abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK):
+    for v in (_abi.FP8RL_VARIANT_AUTO, _abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK,
+              _abi.FP8RL_VARIANT_PAIR):
         gemm_tolerance_check(bits16(fp8lib.gemm_fwd(qx, sx, qw, sw, variant=v)), y_ref, f"variant {v}")
 
 
@@ -106,7 +107,7 @@ def test_exactly_representable_gemm(fp8lib, oracle):
     qw, sw, _ = fp8lib.quantize_128x128(wt)
     assert torch.all(sx == 1.0) and torch.all(sw == 1.0)
     exact = x @ w.T
-    for v in (_abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK):
+    for v in (_abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK, _abi.FP8RL_VARIANT_PAIR):
         y = bits16(fp8lib.gemm_fwd(qx, sx, qw, sw, variant=v))
         yf = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
         assert np.all(np.abs(yf - exact) <= np.abs(exact) * 2.0 ** -8 + 1e-30)
@@ -121,15 +122,79 @@ def test_scaling_law_on_device(fp8lib, oracle):
     qw, sw, _ = fp8lib.quantize_128x128(w)
     qx2, sx2 = fp8lib.quantize_1x128((x.float() * 8.0).to(torch.bfloat16))
     qw2, sw2, _ = fp8lib.quantize_128x128((w.float() * 0.25).to(torch.bfloat16))
-    for v in (_abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK):
+    for v in (_abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK, _abi.FP8RL_VARIANT_PAIR):
         y = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=v).float()
         y2 = fp8lib.gemm_fwd(qx2, sx2, qw2, sw2, variant=v).float()
         assert torch.equal(y2, y * 2.0)
 
 
-def test_tiled_deterministic_and_grid_independent(fp8lib, oracle):
+@pytest.mark.parametrize("variant", [_abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_PAIR])
+def test_tiled_deterministic_and_grid_independent(fp8lib, oracle, variant):
+    """Both persistent forms against the oracle, with a full grid and with a few CTAs (or
+    clusters) that each walk many tiles; the two runs give the same bytes."""
     M, N, K = 640, 1536, 1024
     qx, sx, qw, sw, _ = fwd_operands(fp8lib, oracle, M, N, K, 3)
-    y1 = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_TILED)
-    y2 = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_TILED, grid=7)
+    ref = oracle.gemm(u8(qx), f32(sx), u8(qw), f32(sw), "fwd")
+    y1 = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=variant)
+    y2 = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=variant, grid=7)
+    gemm_tolerance_check(bits16(y1), ref, f"variant {variant}, full grid")
+    gemm_tolerance_check(bits16(y2), ref, f"variant {variant}, grid 7")
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+# ------------------------------------------------------------------ paired-SM form
+# 256 x 128 output tiles on clusters of two CTAs.  Row counts that are not multiples of
+# 256 leave the second CTA of the last pair partly or wholly outside A (TMA zero fill,
+# clipped stores); grid = clusters, so small grids make each cluster walk many tiles.
+
+@pytest.mark.parametrize("M,N,K", [(256, 128, 512), (128, 256, 512), (300, 384, 512),
+                                   (1000, 1280, 1024), (132, 128, 2048), (520, 640, 1536)])
+@pytest.mark.parametrize("epi", [8, 16])
+def test_fwd_pair(fp8lib, oracle, M, N, K, epi):
+    qx, sx, qw, sw, _ = fwd_operands(fp8lib, oracle, M, N, K, M + N + K + epi)
+    ref = oracle.gemm(u8(qx), f32(sx), u8(qw), f32(sw), "fwd")
+    for grid in (0, 2):
+        y = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_PAIR, epi_warps=epi, grid=grid)
+        gemm_tolerance_check(bits16(y), ref, f"pair fwd {M}x{N}x{K} epi {epi} grid {grid}")
+    assert fp8lib.check_status() == _abi.FP8RL_OK
+
+
+# (512, 640, 512): 5 K-blocks, the last scale group of each tile partial
+@pytest.mark.parametrize("M,N,K", [(128, 256, 512), (300, 384, 1024), (512, 640, 512),
+                                   (768, 1024, 2048)])
+def test_dgrad_pair(fp8lib, oracle, M, N, K):
+    dy = synth.normal_bf16((M, N), 1e-3, M + 31, "cuda")
+    w = synth.normal_bf16((N, K), 0.02, K + 35, "cuda")
+    qdy, sdy = fp8lib.quantize_1x128(dy)
+    _, sw, qwT = fp8lib.quantize_128x128(w)
+    ref = oracle.gemm(u8(qdy), f32(sdy), u8(qwT), f32(sw), "dgrad")
+    for v, grid in ((_abi.FP8RL_VARIANT_PAIR, 0), (_abi.FP8RL_VARIANT_PAIR, 3), (_abi.FP8RL_VARIANT_TILED, 0)):
+        dx = fp8lib.gemm_dgrad(qdy, sdy, qwT, sw, variant=v, grid=grid)
+        gemm_tolerance_check(bits16(dx), ref, f"dgrad {M}x{N}x{K} variant {v} grid {grid}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 512), (1024, 256, 768),
+                                   (384, 640, 1152)])
+@pytest.mark.parametrize("epi", [8, 16])
+def test_wgrad_pair(fp8lib, oracle, M, N, K, epi):
+    dy = synth.normal_bf16((M, N), 1e-3, M + 41 + epi, "cuda")
+    x = synth.normal_bf16((M, K), 1.0, K + 43, "cuda", outlier_channels=2, outlier_scale=30.0)
+    qdyT, sdyT = fp8lib.quantize_128x1(dy)
+    qxT, sxT = fp8lib.quantize_128x1(x)
+    ref = oracle.gemm(u8(qdyT), f32(sdyT), u8(qxT), f32(sxT), "wgrad")
+    for grid in (0, 2):
+        dw = fp8lib.gemm_wgrad(qdyT, sdyT, qxT, sxT, variant=_abi.FP8RL_VARIANT_PAIR, epi_warps=epi, grid=grid)
+        gemm_tolerance_check(bits16(dw), ref, f"pair wgrad {M}x{N}x{K} epi {epi} grid {grid}")
+    dw = fp8lib.gemm_wgrad(qdyT, sdyT, qxT, sxT, variant=_abi.FP8RL_VARIANT_TILED)
+    gemm_tolerance_check(bits16(dw), ref, f"one-SM wgrad {M}x{N}x{K}")
+
+
+def test_pair_refuses_scales_it_cannot_copy(fp8lib, oracle):
+    """PAIR needs TMA-able scale rows; AUTO then takes the one-SM form."""
+    M, N, K = 256, 256, 640      # 5 K-blocks: rows of 5 block scales are not 16-byte multiples
+    qx, sx, qw, sw, _ = fwd_operands(fp8lib, oracle, M, N, K, 77)
+    with pytest.raises(_abi.Fp8rlError) as e:
+        fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_PAIR)
+    assert e.value.status == _abi.FP8RL_ERR_SHAPE
+    ref = oracle.gemm(u8(qx), f32(sx), u8(qw), f32(sw), "fwd")
+    gemm_tolerance_check(bits16(fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_AUTO)), ref, "auto")
