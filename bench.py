@@ -350,8 +350,8 @@ def kernel_table(per_ms, flops, qbytes, fp8_peak, hbm):
 
 
 def decode_table(dev, fp8_peak, hbm, reps=40):
-    """Qwen2.5-7B decode linears at M in {64, 128, 256}: activation quantization plus the
-    decode GEMM per call, timed as CUDA-graph replays of `reps` calls that cycle through
+    """Qwen2.5-7B decode linears at M in {64, 128, 256}: the fused linear (activation
+    quantization, then the decode GEMM) per call, timed as CUDA-graph replays of `reps` calls that cycle through
     weight copies larger than L2 in total, so every call streams its weights from HBM.
     Returns {"<linear>_m<M>": {...}} with the roofline fraction max(FLOP/peak, bytes/HBM)
     / time."""
@@ -367,13 +367,11 @@ def decode_table(dev, fp8_peak, hbm, reps=40):
         del wq
         for M in DEC_M:
             x = synth.activation(w, M, K, 40 + li, dev)
-            # the workspace cache is filled before capture
-            ops.workspace(ops.gemm_workspace_bytes(_abi.FP8RL_OP_FWD, M, N, K), x.device)
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
 
             def call(i):
-                qx, sx = ops.quantize_1x128(x)
-                ops.gemm_fwd(qx, sx, copies[i % ncopy][0], copies[i % ncopy][1], out=y)
+                # the fused linear: 1x128 quantization of x, then the decode GEMM overlapping it
+                ops.linear_fwd(x, copies[i % ncopy][0], copies[i % ncopy][1], out=y)
 
             for i in range(3):
                 call(i)

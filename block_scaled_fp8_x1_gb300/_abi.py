@@ -34,6 +34,7 @@ FP8RL_ERR_DEVICE_BOUNDS = 8
 
 FP8RL_OP_FWD, FP8RL_OP_DGRAD, FP8RL_OP_WGRAD = 0, 1, 2
 FP8RL_VARIANT_AUTO, FP8RL_VARIANT_TILED, FP8RL_VARIANT_SPLITK, FP8RL_VARIANT_PAIR = 0, 1, 2, 3
+FP8RL_VARIANT_DECODE = 4
 
 
 class Fp8rlError(RuntimeError):
@@ -78,6 +79,7 @@ SIGNATURES = {
                                  ctypes.POINTER(GemmOpts), STREAM]),
     "fp8rl_gemm_wgrad_ex": (ST, [P, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t,
                                  ctypes.POINTER(GemmOpts), STREAM]),
+    "fp8rl_linear_fwd": (ST, [P, I64, I64, I64, P, P, I64, P, P, P, P, ctypes.c_size_t, STREAM]),
     "fp8rl_gemm_fwd_decode_noalloc": (ST, [P, P, P, P, P, I64, I64, I64, STREAM]),
     "fp8rl_gemm_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "fp8rl_debug_e4m3_encode": (ST, [P, P, I64, STREAM]),

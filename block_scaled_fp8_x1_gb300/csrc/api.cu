@@ -314,6 +314,83 @@ fp8rl_status run_decode(const uint8_t* qx, const float* sx, const uint8_t* qw, c
                                           grid, st));
 }
 
+// Whether the automatic choice takes the decode form with the weights on the MMA's M side
+// (else the split-K form with the tokens there).  Measured on the 7B decode shapes:
+// up to 64 tokens it is the faster form; at 128 tokens it is for the narrow layers (qkv,
+// o: 12.8 against 16.6 us) but not for gate_up (38 against 30 us), whose 296 weight tiles
+// each re-read a 128-token activation tile as large as themselves; at 256 tokens the
+// split-K form wins on every layer.
+bool decode_swapped_auto(int64_t M, int64_t N) { return M <= 64 || (M <= 128 && N <= 8192); }
+
+// Decode form with the weights on the MMA's M side (decode.cu).  Cluster size (split of
+// the reduction): the one that minimises waves x K-blocks per CTA, with one K-block of cost
+// for the cluster reduction, among the sizes whose clusters fit on the GPU at once.
+struct DecodeChoice {
+    int cached = 0;
+    int max_clusters[9] = {};
+};
+DecodeChoice g_dec_choice[kMaxDevices][4];
+std::mutex g_dec_mu;
+
+int decode_splits(int64_t M, int64_t tiles, int64_t nkb) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int mp = decode_mp((int)M);
+    const int cls = mp == 32 ? 0 : (mp == 64 ? 1 : (mp == 128 ? 2 : 3));
+    int maxc[9];
+    {
+        std::lock_guard<std::mutex> lk(g_dec_mu);
+        DecodeChoice& c = g_dec_choice[dev < kMaxDevices ? dev : 0][cls];
+        if (!c.cached) {
+            for (int sz = 1; sz <= 8; ++sz) c.max_clusters[sz] = decode_max_clusters((int)M, sz);
+            c.cached = 1;
+        }
+        for (int sz = 1; sz <= 8; ++sz) maxc[sz] = c.max_clusters[sz];
+    }
+    int best = 1;
+    double best_cost = 1e30;
+    for (int sz = 1; sz <= 8 && sz <= nkb; ++sz) {
+        if (maxc[sz] <= 0) continue;
+        // the busiest CTA's K-blocks: S = 1 runs persistent CTAs (one pipeline across their
+        // tiles, one fill); S > 1 one wave per maxc[sz] clusters, each wave paying a pipeline
+        // fill and the cluster reduction
+        const int64_t waves = (tiles + maxc[sz] - 1) / maxc[sz];
+        const double cost = sz == 1 ? (double)(waves * nkb) + 2.0
+                                    : (double)waves * ((double)((nkb + sz - 1) / sz) + 3.0);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = sz;
+        }
+    }
+    return best;
+}
+
+fp8rl_status run_decode_swap(const uint8_t* qx, const float* sx, const uint8_t* qw, const float* sw,
+                             uint16_t* y, int64_t M, int64_t N, int64_t K, int splits_req, cudaStream_t st) {
+    const int64_t nkb = K / 128;
+    const int64_t tiles = N / 128;
+    const int splits = splits_req > 0 ? (int)std::min<int64_t>(std::min(splits_req, 8), nkb)
+                                      : decode_splits(M, tiles, nkb);
+    CUtensorMap tw, tx;
+    fp8rl_status e = make_tmap(&tw, qw, N, K, K, 128);
+    if (e != FP8RL_OK) return e;
+    e = make_tmap(&tx, qx, M, K, K, decode_mp((int)M));
+    if (e != FP8RL_OK) return e;
+    DecodeParams p = {};
+    p.M = (int)M;
+    p.nkb = (int)nkb;
+    p.tiles = (int)tiles;
+    p.sx = sx; p.sx_kb = M;
+    p.sw = sw; p.sw_r = nkb;
+    p.y = y; p.ldy = N;
+    p.timeout_ns = g_timeout_ns.load();
+    // one cluster per tile when the reduction is split; else persistent CTAs, one per SM
+    int sms = 0;
+    current_device(&sms);
+    const int grid = splits > 1 ? (int)tiles : (int)std::min<int64_t>(tiles, std::max(sms, 1));
+    return cuda_status(launch_decode(tw, tx, p, grid, splits, st));
+}
+
 }  // namespace
 
 // ====================================================================================
@@ -352,7 +429,10 @@ fp8rl_status fp8rl_check_status(fp8rl_stream_t stream) {
     const fp8rl_status g = read_and_clear_device_status(stream);  // synchronizes the stream
     const fp8rl_status q = read_and_clear_quant_status();
     const fp8rl_status pr = read_and_clear_pair_status();
-    return g != FP8RL_OK ? g : (pr != FP8RL_OK ? pr : q);
+    const fp8rl_status dc = read_and_clear_decode_status();
+    if (g != FP8RL_OK) return g;
+    if (pr != FP8RL_OK) return pr;
+    return dc != FP8RL_OK ? dc : q;
 }
 
 // ---------------------------------------------------------------- quantizers
@@ -441,8 +521,9 @@ size_t fp8rl_gemm_workspace_bytes_ex(int op, int64_t M, int64_t N, int64_t K,
                                      const fp8rl_gemm_opts* opts) {
     if (op != FP8RL_OP_FWD || M <= 0 || N <= 0 || K <= 0 || K % 128 != 0) return 0;
     const int variant = opts ? opts->variant : FP8RL_VARIANT_AUTO;
-    const bool decode = variant == FP8RL_VARIANT_SPLITK || (variant == FP8RL_VARIANT_AUTO && M <= 256);
-    if (!decode || M > 256) return 0;
+    // only the split-K form uses one
+    if (M > 256 || !(variant == FP8RL_VARIANT_SPLITK || (variant == FP8RL_VARIANT_AUTO && !decode_swapped_auto(M, N))))
+        return 0;
     int sms = 0;
     if (current_device(&sms) != FP8RL_OK) sms = 148;
     const int64_t tiles = decode_tiles(M, N), nkb = K / 128;
@@ -457,18 +538,21 @@ fp8rl_status fp8rl_gemm_fwd_ex(const uint8_t* qx, const float* sx, const uint8_t
                                fp8rl_stream_t stream) {
     if (M < 0 || N < 0 || K <= 0) return FP8RL_ERR_INVALID_ARG;
     const int variant = opts ? opts->variant : FP8RL_VARIANT_AUTO;
-    if (variant < FP8RL_VARIANT_AUTO || variant > FP8RL_VARIANT_PAIR) return FP8RL_ERR_INVALID_ARG;
+    if (variant < FP8RL_VARIANT_AUTO || variant > FP8RL_VARIANT_DECODE) return FP8RL_ERR_INVALID_ARG;
     if (K % 128 != 0 || N % 128 != 0) return FP8RL_ERR_SHAPE;
     if (M == 0 || N == 0) return FP8RL_OK;
     if (!qx || !sx || !qw || !sw || !y) return FP8RL_ERR_INVALID_ARG;
     if (!aligned16(qx) || !aligned16(sx) || !aligned16(qw) || !aligned16(sw) || !aligned16(y))
         return FP8RL_ERR_ALIGN;
-    const bool decode = variant == FP8RL_VARIANT_SPLITK || (variant == FP8RL_VARIANT_AUTO && M <= 256);
-    if (decode && M > 256) return FP8RL_ERR_SHAPE;
+    const bool swapped = variant == FP8RL_VARIANT_DECODE || (variant == FP8RL_VARIANT_AUTO && decode_swapped_auto(M, N));
+    const bool splitk = variant == FP8RL_VARIANT_SPLITK || (variant == FP8RL_VARIANT_AUTO && !swapped && M <= 256);
+    if ((swapped || splitk) && M > 256) return FP8RL_ERR_SHAPE;
     int sms = 0;
     fp8rl_status e = current_device(&sms);
     if (e != FP8RL_OK) return e;
-    if (decode)
+    if (swapped)
+        return run_decode_swap(qx, sx, qw, sw, y, M, N, K, opts ? opts->splits : 0, stream);
+    if (splitk)
         return run_decode(qx, sx, qw, sw, y, M, N, K, ws, ws_bytes, opts ? opts->splits : 0, sms, stream);
     TiledArgs t;
     t.A = qx; t.sa = sx; t.sa_kb = M;
@@ -548,6 +632,35 @@ fp8rl_status fp8rl_gemm_wgrad_ex(const uint8_t* qdyT, const float* sdyT, const u
     t.c = dw; t.ldc = K;
     t.R1 = N; t.R2 = K; t.Kr = M;
     return run_gemm(t, opts, sms, stream);
+}
+
+// ---------------------------------------------------------------- fused linear
+
+fp8rl_status fp8rl_linear_fwd(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const uint8_t* qw,
+                              const float* sw, int64_t N, uint8_t* qx, float* sx, uint16_t* y,
+                              void* ws, size_t ws_bytes, fp8rl_stream_t stream) {
+    if (M < 0 || N < 0 || K <= 0 || ldx < K) return FP8RL_ERR_INVALID_ARG;
+    if (K % 128 != 0 || N % 128 != 0) return FP8RL_ERR_SHAPE;
+    if (M == 0 || N == 0) return FP8RL_OK;
+    if (!x || !qw || !sw || !qx || !sx || !y) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(qw) || !aligned16(sw) || !aligned16(qx) || !aligned16(sx) ||
+        !aligned16(y) || (ldx * 2) % 16 != 0)
+        return FP8RL_ERR_ALIGN;
+    int sms = 0;
+    fp8rl_status e = current_device(&sms);
+    if (e != FP8RL_OK) return e;
+    e = cuda_status(launch_quant_1x128(x, M, K, ldx, qx, sx, sms, stream));
+    if (e != FP8RL_OK) return e;
+    if (decode_swapped_auto(M, N))
+        return run_decode_swap(qx, sx, qw, sw, y, M, N, K, 0, stream);
+    if (M <= 256)
+        return run_decode(qx, sx, qw, sw, y, M, N, K, ws, ws_bytes, 0, sms, stream);
+    TiledArgs t;
+    t.A = qx; t.sa = sx; t.sa_kb = M;
+    t.B = qw; t.sb = sw; t.sb_kb = 1; t.sb_r = K / 128; t.b_mode = SCALE_BLOCK;
+    t.c = y; t.ldc = N;
+    t.R1 = M; t.R2 = N; t.Kr = K;
+    return run_gemm(t, nullptr, sms, stream);
 }
 
 // ---------------------------------------------------------------- no-allocation decode

@@ -71,6 +71,29 @@ cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const
                              int epi_warps, int clusters, cudaStream_t st);
 fp8rl_status read_and_clear_pair_status();
 
+// decode.cu: decode-shaped forward GEMM (M <= 256 tokens), weights on the MMA's M side,
+// split-K reduced inside a cluster of `splits` CTAs (1..8) through distributed shared
+// memory.  tw: weight codes [N][K] with 128 x 128-byte boxes; tx: activation codes [M][K]
+// with boxes of decode_mp(M) rows x 128 bytes.  grid_clusters: p.tiles when splits > 1
+// (one tile per cluster), any count up to p.tiles when splits == 1 (persistent CTAs).
+struct DecodeParams {
+    int M;                   // tokens, 1..256
+    int nkb;                 // K / 128
+    int tiles;               // N / 128
+    const float* sx;         // activation scales sx[kb * sx_kb + m]
+    int64_t sx_kb;
+    const float* sw;         // weight block scales sw[(n / 128) * sw_r + kb]
+    int64_t sw_r;
+    uint16_t* y;             // y[m * ldy + n]
+    int64_t ldy;
+    uint64_t timeout_ns;
+};
+int decode_mp(int M);
+int decode_max_clusters(int M, int splits);
+cudaError_t launch_decode(const CUtensorMap& tw, const CUtensorMap& tx, const DecodeParams& p, int grid_clusters,
+                          int splits, cudaStream_t st);
+fp8rl_status read_and_clear_decode_status();
+
 // quantize.cu
 cudaError_t launch_quant_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
                                float* s, int num_sms, cudaStream_t st);

@@ -221,14 +221,11 @@ def gemm_fwd(qx, sx, qw, sw, out=None, variant: int = _abi.FP8RL_VARIANT_AUTO, s
     N = qw.shape[0]
     dev = qx.device
     y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    decode = variant == _abi.FP8RL_VARIANT_SPLITK or (
-        variant == _abi.FP8RL_VARIANT_AUTO and M <= 256)
     opts = GemmOpts(int(variant), int(splits), int(grid), int(tile_n), int(epi_warps))
-    wsb = None
-    if decode:
-        need = int(lib().fp8rl_gemm_workspace_bytes_ex(_abi.FP8RL_OP_FWD, M, N, K,
-                                                       ctypes.byref(opts)))
-        wsb = ws if ws is not None else workspace(need, dev)
+    wsb = ws
+    need = int(lib().fp8rl_gemm_workspace_bytes_ex(_abi.FP8RL_OP_FWD, M, N, K, ctypes.byref(opts)))
+    if need > 0 and wsb is None:
+        wsb = workspace(need, dev)
     check(lib().fp8rl_gemm_fwd_ex(_ptr(qx), _ptr(sx), _ptr(qw), _ptr(sw), _ptr(y), M, N, K,
                                   _ptr(wsb), wsb.numel() if wsb is not None else 0,
                                   ctypes.byref(opts), _stream(dev)), "fp8rl_gemm_fwd_ex")
@@ -261,3 +258,28 @@ def gemm_wgrad(qdyT, sdyT, qxT, sxT, out=None, variant: int = _abi.FP8RL_VARIANT
     check(lib().fp8rl_gemm_wgrad_ex(_ptr(qdyT), _ptr(sdyT), _ptr(qxT), _ptr(sxT), _ptr(dw), M, N,
                                     K, None, 0, ctypes.byref(opts), _stream(dev)), "fp8rl_gemm_wgrad_ex")
     return dw
+
+
+def linear_fwd(x: torch.Tensor, qw, sw, out=None):
+    """One linear layer from the BF16 activation: x bf16 [M,K] is quantized 1x128 (returned
+    as qx u8 [M,K], sx f32 [K/128,M]) and y = X W^T bf16 [M,N] computed from it; for
+    M <= 256 the GEMM overlaps the quantizer.  Returns (y, qx, sx)."""
+    _require(x, torch.bfloat16, "x")
+    _require(qw, torch.uint8, "codes W", x.device)
+    _require(sw, torch.float32, "scales W", x.device)
+    _contig(qw, "codes W")
+    _contig(sw, "scales W")
+    if x.stride(1) != 1:
+        raise ValueError("x: rows must be contiguous")
+    M, K = x.shape
+    N = qw.shape[0]
+    dev = x.device
+    qx = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    sx = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    need = gemm_workspace_bytes(_abi.FP8RL_OP_FWD, M, N, K)
+    wsb = workspace(need, dev) if need > 0 else None
+    check(lib().fp8rl_linear_fwd(_ptr(x), M, K, x.stride(0), _ptr(qw), _ptr(sw), N, _ptr(qx),
+                                 _ptr(sx), _ptr(y), _ptr(wsb), wsb.numel() if wsb is not None else 0,
+                                 _stream(dev)), "fp8rl_linear_fwd")
+    return y, qx, sx

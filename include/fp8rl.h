@@ -165,13 +165,15 @@ typedef enum { FP8RL_OP_FWD = 0, FP8RL_OP_DGRAD = 1, FP8RL_OP_WGRAD = 2 } fp8rl_
  *   qx : E4M3 [M][K] (1x128), sx : float [K/128][M]
  *   qw : E4M3 [N][K] (128x128), sw : float [N/128][K/128]
  *   y  : BF16 [M][N]
- * Small M (<= 256) takes the decode-shaped form: the same kernel with the reduction split
- * into slices over more CTAs, so that the weights stream through every SM, and a second
- * kernel that adds the slices' FP32 partial sums in slice order (the result does not
- * depend on timing).  When it splits, it needs fp8rl_gemm_workspace_bytes(FP8RL_OP_FWD,
- * M, N, K) bytes of workspace for the partial sums (no initial contents required); calls
- * that overlap in time need separate workspaces.  A size of 0 (no split, or larger M)
- * means ws may be NULL.
+ * Small M takes a decode-shaped form.  Up to 64 tokens (and up to 128 when N <= 8192),
+ * FP8RL_VARIANT_DECODE: each CTA streams 128 weight rows of one reduction slice, and the
+ * slices of a tile are added in rank order inside a cluster (the result does not depend
+ * on timing); no workspace.  Otherwise up to 256 tokens, FP8RL_VARIANT_SPLITK: tokens on
+ * the tensor core's M side, the reduction split over CTAs whose FP32 partial sums a
+ * second kernel adds in slice order;
+ * it needs fp8rl_gemm_workspace_bytes(FP8RL_OP_FWD, M, N, K) bytes of workspace (no
+ * initial contents required; calls that overlap in time need separate workspaces).  A
+ * size of 0 means ws may be NULL.
  * Larger M takes the one-SM tiled form (FP8RL_VARIANT_TILED); the paired-SM form
  * (FP8RL_VARIANT_PAIR) is available on request when every scale array can be moved by TMA:
  * M % 4 == 0 and (K/128) % 4 == 0 for the forward GEMM, M % 4 == 0 and (K/128) % 4 == 0
@@ -207,10 +209,15 @@ typedef enum {
     FP8RL_VARIANT_TILED = 1,  /* one SM per output tile: persistent 128 x BN tiles */
     FP8RL_VARIANT_SPLITK = 2, /* decode-shaped: the reduction of each 128x256 output tile
                                  is split over `splits` CTAs (forward only, M <= 256) */
-    FP8RL_VARIANT_PAIR = 3    /* two SMs per output tile: persistent 256 x 128 tiles on
+    FP8RL_VARIANT_PAIR = 3,   /* two SMs per output tile: persistent 256 x 128 tiles on
                                  clusters of two CTAs (M = 256 tensor-core MMAs); needs
                                  scale arrays whose rows are multiples of 16 bytes (the
                                  rule under fp8rl_gemm_fwd), else FP8RL_ERR_SHAPE */
+    FP8RL_VARIANT_DECODE = 4  /* forward only, M <= 256: weights on the MMA's M side (one
+                                 CTA per 128 weight rows and reduction slice), the
+                                 reduction split over a cluster of `splits` CTAs (1..8, 0 =
+                                 choose) and summed in the cluster's shared memory in rank
+                                 order; no workspace */
 } fp8rl_variant;
 
 typedef struct {
@@ -242,6 +249,16 @@ FP8RL_API fp8rl_status fp8rl_gemm_wgrad_ex(const uint8_t* qdyT, const float* sdy
                                  const float* sxT, uint16_t* dw, int64_t M, int64_t N,
                                  int64_t K, void* ws, size_t ws_bytes,
                                  const fp8rl_gemm_opts* opts, fp8rl_stream_t stream);
+
+/* One linear layer from the BF16 activation ("Core architecture": rollout and the
+ * training forward pass run the same FP8 linear): x is quantized 1x128 into qx / sx
+ * (exactly fp8rl_quantize_1x128), then Y = X W^T with the form fp8rl_gemm_fwd picks.
+ *   x : BF16 [M][ldx];  qw, sw, y, ws as for fp8rl_gemm_fwd;  qx : E4M3 [M][K] and
+ *   sx : float [K/128][M] receive the quantized activation (caller-owned). */
+FP8RL_API fp8rl_status fp8rl_linear_fwd(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                                        const uint8_t* qw, const float* sw, int64_t N,
+                                        uint8_t* qx, float* sx, uint16_t* y, void* ws,
+                                        size_t ws_bytes, fp8rl_stream_t stream);
 
 /* Decode-shaped forward GEMM that allocates nothing and takes no workspace.  It has no
  * counterpart in the scheme's pages; it exists for callers that cannot provide device

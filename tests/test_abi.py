@@ -81,7 +81,13 @@ def test_host_side_validation_without_gpu(abi):
 def test_workspace_sizes(abi):
     L = abi.lib()
     # decode form (M <= 256) splitting the reduction needs its partial sums; tiled none
-    assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 64, 3584, 3584) > 0
+    # the automatic decode form for up to 64 tokens (128 for N <= 8192) reduces inside a
+    # cluster: no workspace; the split-K form (otherwise up to 256 tokens) keeps its partial
+    # sums in one
+    assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 64, 37888, 3584) == 0
+    assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 128, 3584, 3584) == 0
+    assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 128, 8320, 3584) > 0
+    assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 256, 3584, 3584) > 0
     assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 8192, 3584, 3584) == 0
     assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_WGRAD, 8192, 3584, 3584) == 0
     opts = abi.GemmOpts(abi.FP8RL_VARIANT_SPLITK, 4, 0)

@@ -54,13 +54,46 @@ def test_fwd_decode(fp8lib, oracle, M, splits):
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
 
 
+# decode form with the weights on the MMA's M side: token counts around every padding class
+# (32/64/128/256), cluster sizes from one CTA to one K-block per CTA
+@pytest.mark.parametrize("M", [1, 5, 31, 32, 33, 64, 100, 128, 129, 200, 256])
+@pytest.mark.parametrize("splits", [0, 1, 3, 8])
+def test_fwd_decode_swapped(fp8lib, oracle, M, splits):
+    N, K = 1280, 1024
+    qx, sx, qw, sw, _ = fwd_operands(fp8lib, oracle, M, N, K, 11 * M + splits)
+    y_ref = oracle.gemm(u8(qx), f32(sx), u8(qw), f32(sw), "fwd")
+    y = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_DECODE, splits=splits)
+    gemm_tolerance_check(bits16(y), y_ref, f"decode (swapped) M={M} splits={splits}")
+    y2 = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_DECODE, splits=splits)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    assert fp8lib.check_status() == _abi.FP8RL_OK
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 1280, 3584), (256, 768, 2048), (17, 2048, 512), (300, 512, 1024)])
+def test_linear_fwd_quantizes_and_multiplies(fp8lib, oracle, M, N, K):
+    """The fused linear: its activation codes and scales are the oracle's 1x128 quantization
+    bit for bit, and its output is within the GEMM bound of the oracle's result from them
+    (the GEMM overlapping the quantizer for M <= 256)."""
+    x = synth.normal_bf16((M, K), 1.0, M + K + 5, "cuda", outlier_channels=3, outlier_scale=30.0)
+    w = synth.normal_bf16((N, K), 0.02, N + 7, "cuda")
+    qw, sw, _ = fp8lib.quantize_128x128(w, transpose=False)
+    for rep in range(2):
+        y, qx, sx = fp8lib.linear_fwd(x, qw, sw)
+        qxr, sxr = oracle.quantize_1x128(bits16(x))
+        assert_same_u8(u8(qx), qxr, "qx")
+        assert_same_bits_f32(f32(sx), sxr, "sx")
+        y_ref = oracle.gemm(qxr, sxr, u8(qw), f32(sw), "fwd")
+        gemm_tolerance_check(bits16(y), y_ref, f"linear {M}x{N}x{K} rep {rep}")
+    assert fp8lib.check_status() == _abi.FP8RL_OK
+
+
 def test_fwd_auto_matches_forms(fp8lib, oracle):
     """AUTO picks the decode form for M <= 256; both forms obey the same bound."""
     M, N, K = 192, 768, 2048
     qx, sx, qw, sw, _ = fwd_operands(fp8lib, oracle, M, N, K, 99)
     y_ref = oracle.gemm(u8(qx), f32(sx), u8(qw), f32(sw), "fwd")
     for v in (_abi.FP8RL_VARIANT_AUTO, _abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK,
-              _abi.FP8RL_VARIANT_PAIR):
+              _abi.FP8RL_VARIANT_PAIR, _abi.FP8RL_VARIANT_DECODE):
         gemm_tolerance_check(bits16(fp8lib.gemm_fwd(qx, sx, qw, sw, variant=v)), y_ref, f"variant {v}")
 
 
@@ -107,7 +140,8 @@ def test_exactly_representable_gemm(fp8lib, oracle):
     qw, sw, _ = fp8lib.quantize_128x128(wt)
     assert torch.all(sx == 1.0) and torch.all(sw == 1.0)
     exact = x @ w.T
-    for v in (_abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK, _abi.FP8RL_VARIANT_PAIR):
+    for v in (_abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK, _abi.FP8RL_VARIANT_PAIR,
+              _abi.FP8RL_VARIANT_DECODE):
         y = bits16(fp8lib.gemm_fwd(qx, sx, qw, sw, variant=v))
         yf = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
         assert np.all(np.abs(yf - exact) <= np.abs(exact) * 2.0 ** -8 + 1e-30)
@@ -122,7 +156,8 @@ def test_scaling_law_on_device(fp8lib, oracle):
     qw, sw, _ = fp8lib.quantize_128x128(w)
     qx2, sx2 = fp8lib.quantize_1x128((x.float() * 8.0).to(torch.bfloat16))
     qw2, sw2, _ = fp8lib.quantize_128x128((w.float() * 0.25).to(torch.bfloat16))
-    for v in (_abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK, _abi.FP8RL_VARIANT_PAIR):
+    for v in (_abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK, _abi.FP8RL_VARIANT_PAIR,
+              _abi.FP8RL_VARIANT_DECODE):
         y = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=v).float()
         y2 = fp8lib.gemm_fwd(qx2, sx2, qw2, sw2, variant=v).float()
         assert torch.equal(y2, y * 2.0)
