@@ -41,7 +41,9 @@ def check_rmsnorm(fp8lib, oracle, x, gamma, eps, dual):
     return int((diff != 0).sum())
 
 
-@pytest.mark.parametrize("M,K", [(128, 128), (256, 640), (384, 1024), (128, 4096), (256, 5120)])
+# 6272 = 49 x 128 K-blocks: the cluster form splits a panel 7 ways
+@pytest.mark.parametrize("M,K", [(128, 128), (256, 640), (384, 1024), (128, 4096), (256, 5120),
+                                 (128, 6144), (256, 6272)])
 def test_rmsnorm_quant_dual(fp8lib, oracle, M, K):
     x = synth.normal_bf16((M, K), 1.0, M + K, "cuda", outlier_channels=max(1, K // 1000),
                           outlier_scale=30.0)
@@ -58,7 +60,7 @@ def test_rmsnorm_quant_rows_only(fp8lib, oracle, M, K):
     check_rmsnorm(fp8lib, oracle, x, gamma, 1e-6, dual=False)
 
 
-@pytest.mark.parametrize("M,K", [(256, 640), (384, 1024), (128, 4096)])
+@pytest.mark.parametrize("M,K", [(256, 640), (384, 1024), (128, 4096), (256, 6272)])
 def test_rmsnorm_quant_without_rstd_buffer(fp8lib, M, K):
     """Without an rstd buffer the library computes rstd inside a cluster of CTAs per panel
     (it allocates nothing).  Its codes and scales equal those of the path that writes rstd
