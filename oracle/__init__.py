@@ -67,6 +67,8 @@ def _load():
             "orc_quantize_128x128": (None, [P, I64, I64, I64, P, I64, P, P]),
             "orc_rmsnorm": (None, [P, P, ctypes.c_float, I64, I64, P, P, P]),
             "orc_silu_mul": (I64, [P, I64, I64, P, P]),
+            "orc_silu_mul_bwd": (I64, [P, P, I64, I64, P, P]),
+            "orc_rmsnorm_bwd": (None, [P, P, P, P, I64, I64, P, P, P]),
             "orc_gemm": (None, [P, I64, P, I64, P, I64, P, I64, I64, I64, I64, I64, I64, P]),
             "orc_gemm_sampled": (None, [P, I64, P, I64, P, I64, P, I64, I64, I64, I64, P, P,
                                         I64, P]),
@@ -208,6 +210,46 @@ def silu_mul(gu_bf16: np.ndarray):
     alt = np.empty((M, I), dtype=np.uint16)
     n = _load().orc_silu_mul(_p(gu), M, I, _p(h), _p(alt))
     return h, alt, int(n)
+
+
+def silu_mul_bwd(gu_bf16: np.ndarray, dh_bf16: np.ndarray):
+    """SiLU-mul backward: GU[M, 2I] (the forward's gate | up) and dH[M, I] ->
+    (dGU uint16 [M, 2I] = [dg | du] as BF16, alt uint16 [M, 2I], n_flagged).
+
+    ``alt`` differs from ``dGU`` only where the binary64 value lies within 2^-16 relative of
+    a BF16 rounding midpoint; there it holds the other BF16 neighbour."""
+    gu = _c(gu_bf16, np.uint16)
+    dh = _c(dh_bf16, np.uint16)
+    M, I2 = gu.shape
+    I = I2 // 2
+    assert dh.shape == (M, I)
+    dgu = np.empty((M, 2 * I), dtype=np.uint16)
+    alt = np.empty((M, 2 * I), dtype=np.uint16)
+    n = _load().orc_silu_mul_bwd(_p(gu), _p(dh), M, I, _p(dgu), _p(alt))
+    return dgu, alt, int(n)
+
+
+def silu_mul_bwd_quant(gu_bf16, dh_bf16):
+    """SiLU-mul backward, then the dual quantization of dGU: (q, s, qT, sT, dgu, alt)."""
+    dgu, alt, _ = silu_mul_bwd(gu_bf16, dh_bf16)
+    q, s = quantize_1x128(dgu)
+    qT, sT = quantize_128x1(dgu) if dgu.shape[0] % 128 == 0 else (None, None)
+    return q, s, qT, sT, dgu, alt
+
+
+def rmsnorm_bwd(x_bf16, gamma_bf16, rstd, dy_bf16):
+    """RMSNorm backward from the forward's rstd: (dx uint16 [M,K], mag float64 [M,K],
+    dgamma float64 [K]); mag = |r*gamma*dy| + |r^3*x*S/K| per element."""
+    x = _c(x_bf16, np.uint16)
+    g = _c(gamma_bf16, np.uint16)
+    r = _c(rstd, np.float32)
+    dy = _c(dy_bf16, np.uint16)
+    M, K = x.shape
+    dx = np.empty((M, K), dtype=np.uint16)
+    mag = np.empty((M, K), dtype=np.float64)
+    dgamma = np.empty(K, dtype=np.float64)
+    _load().orc_rmsnorm_bwd(_p(x), _p(g), _p(r), _p(dy), M, K, _p(dx), _p(mag), _p(dgamma))
+    return dx, mag, dgamma
 
 
 def rmsnorm_quant(x_bf16, gamma_bf16, eps, rstd_in=None):

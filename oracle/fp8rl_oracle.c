@@ -27,6 +27,13 @@
  *       IEEE single, y = bf16_rne((x*rstd)*gamma) in IEEE single; y is rounded to BF16
  *       before it is quantized.
  *   R6  SiLU-mul: h = bf16_rne(silu(g)*u) evaluated in binary64, g = first I columns.
+ *   R7  SiLU-mul backward (the chain rule of R6): with s = 1/(1+exp(-g)),
+ *       dg = dh*u*s*(1 + g*(1-s)) and du = dh*g*s in binary64, each rounded to BF16 (the
+ *       gradient between operators is BF16); [dg | du] is then quantized as a gradient.
+ *   R8  RMSNorm backward (the chain rule of R5 through rstd, the BF16 rounding of y taken
+ *       as the identity): with r the forward's rstd and S = sum_k dy_k*gamma_k*x_k,
+ *       dx_j = r*gamma_j*dy_j - r^3*x_j*S/K in binary64, rounded to BF16;
+ *       dgamma_k = sum_m dy_mk*x_mk*r_m in binary64.
  *
  * Every routine is written as the plain definition: scalar loops, no blocking or fusion.
  * Independent groups are spread over OpenMP threads only to make big inputs finish.
@@ -322,6 +329,92 @@ ORC_API int64_t orc_silu_mul(const uint16_t* gu, int64_t M, int64_t I, uint16_t*
         }
     }
     return flagged;
+}
+
+/* ---------------------------------------------------------------- SiLU-mul backward (R7) */
+
+/* The two BF16 neighbours of v: the one v rounds to is `b`; returns the other. */
+static uint16_t other_bf16_neighbour(double v, uint16_t b) {
+    double a = fabs(v);
+    int e;
+    frexp(a, &e);
+    e -= 1;
+    if (e < -126) e = -126;
+    double ulp = ldexp(1.0, e - 7);
+    double lo = floor(a / ulp) * ulp, hi = lo + ulp;
+    double bv = fabs((double)orc_bf16_to_f32(b));
+    double other = (bv == lo) ? hi : lo;
+    return orc_f64_to_bf16(v < 0 ? -other : other);
+}
+
+/* gu[M, 2I] holds the forward's g = gu[:, :I] and u = gu[:, I:]; dh[M, I] is the gradient
+ * of h.  dgu[M, 2I] receives dg in columns [0, I) and du in [I, 2I), each bf16_rne of a
+ * binary64 evaluation.  alt[M, 2I] (nullable) receives the other BF16 neighbour where the
+ * binary64 value lies within 2^-16 relative of a BF16 midpoint, else a copy.  Returns the
+ * count of such near-midpoint elements. */
+ORC_API int64_t orc_silu_mul_bwd(const uint16_t* gu, const uint16_t* dh, int64_t M, int64_t I,
+                                 uint16_t* dgu, uint16_t* alt) {
+    int64_t flagged = 0;
+    #pragma omp parallel for schedule(static) num_threads(g_threads) reduction(+ : flagged)
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t i = 0; i < I; ++i) {
+            double g = (double)orc_bf16_to_f32(gu[m * 2 * I + i]);
+            double u = (double)orc_bf16_to_f32(gu[m * 2 * I + I + i]);
+            double d = (double)orc_bf16_to_f32(dh[m * I + i]);
+            double sg = 1.0 / (1.0 + exp(-g));
+            double dg = d * u * sg * (1.0 + g * (1.0 - sg));
+            double du = d * (g * sg);
+            double v[2] = {dg, du};
+            int64_t col[2] = {i, I + i};
+            for (int h = 0; h < 2; ++h) {
+                uint16_t b = orc_f64_to_bf16(v[h]);
+                dgu[m * 2 * I + col[h]] = b;
+                if (alt) {
+                    alt[m * 2 * I + col[h]] = b;
+                    if (near_bf16_midpoint(v[h], ldexp(1.0, -16))) {
+                        alt[m * 2 * I + col[h]] = other_bf16_neighbour(v[h], b);
+                        flagged += 1;
+                    }
+                }
+            }
+        }
+    }
+    return flagged;
+}
+
+/* ---------------------------------------------------------------- RMSNorm backward (R8) */
+
+/* x[M,K], gamma[K], rstd[M] (the forward's), dy[M,K] -> dx[M,K] = bf16_rne of the binary64
+ * value; mag[M,K] (nullable) receives |r*gamma*dy| + |r^3*x*S/K| (the size of the two terms,
+ * for error bounds); dgamma[K] (nullable) receives sum_m dy*x*r in binary64. */
+ORC_API void orc_rmsnorm_bwd(const uint16_t* x, const uint16_t* gamma, const float* rstd,
+                             const uint16_t* dy, int64_t M, int64_t K, uint16_t* dx,
+                             double* mag, double* dgamma) {
+    #pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t m = 0; m < M; ++m) {
+        double r = (double)rstd[m];
+        double S = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+            S += (double)orc_bf16_to_f32(dy[m * K + k]) * (double)orc_bf16_to_f32(gamma[k]) *
+                 (double)orc_bf16_to_f32(x[m * K + k]);
+        for (int64_t k = 0; k < K; ++k) {
+            double xv = (double)orc_bf16_to_f32(x[m * K + k]);
+            double t1 = r * (double)orc_bf16_to_f32(gamma[k]) * (double)orc_bf16_to_f32(dy[m * K + k]);
+            double t2 = r * r * r * xv * S / (double)K;
+            dx[m * K + k] = orc_f64_to_bf16(t1 - t2);
+            if (mag) mag[m * K + k] = fabs(t1) + fabs(t2);
+        }
+    }
+    if (dgamma) {
+        #pragma omp parallel for schedule(static) num_threads(g_threads)
+        for (int64_t k = 0; k < K; ++k) {
+            double acc = 0.0;
+            for (int64_t m = 0; m < M; ++m)
+                acc += (double)orc_bf16_to_f32(dy[m * K + k]) * (double)orc_bf16_to_f32(x[m * K + k]) *
+                       (double)rstd[m];
+            dgamma[k] = acc;
+        }
+    }
 }
 
 /* ---------------------------------------------------------------- block-scaled GEMM (R4) */
