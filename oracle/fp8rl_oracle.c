@@ -349,9 +349,11 @@ static uint16_t other_bf16_neighbour(double v, uint16_t b) {
 
 /* gu[M, 2I] holds the forward's g = gu[:, :I] and u = gu[:, I:]; dh[M, I] is the gradient
  * of h.  dgu[M, 2I] receives dg in columns [0, I) and du in [I, 2I), each bf16_rne of a
- * binary64 evaluation.  alt[M, 2I] (nullable) receives the other BF16 neighbour where the
- * binary64 value lies within 2^-16 relative of a BF16 midpoint, else a copy.  Returns the
- * count of such near-midpoint elements. */
+ * binary64 evaluation.  alt[M, 2I] (nullable) receives the other BF16 neighbour where a
+ * binary32 evaluation may round either way, else a copy: where the binary64 value lies
+ * within 2^-16 of a BF16 midpoint, relative to the size of the terms it is made of (dg =
+ * dh*u*s + dh*u*s*g*(1-s) cancels near g = -1.28, where silu' = 0).  Returns the count of
+ * such near-midpoint elements. */
 ORC_API int64_t orc_silu_mul_bwd(const uint16_t* gu, const uint16_t* dh, int64_t M, int64_t I,
                                  uint16_t* dgu, uint16_t* alt) {
     int64_t flagged = 0;
@@ -365,13 +367,15 @@ ORC_API int64_t orc_silu_mul_bwd(const uint16_t* gu, const uint16_t* dh, int64_t
             double dg = d * u * sg * (1.0 + g * (1.0 - sg));
             double du = d * (g * sg);
             double v[2] = {dg, du};
+            /* size of the terms, relative to the value: 1 for the product du */
+            double cond[2] = {dg != 0.0 ? fabs(d * u * sg) * (1.0 + fabs(g * (1.0 - sg))) / fabs(dg) : 1.0, 1.0};
             int64_t col[2] = {i, I + i};
             for (int h = 0; h < 2; ++h) {
                 uint16_t b = orc_f64_to_bf16(v[h]);
                 dgu[m * 2 * I + col[h]] = b;
                 if (alt) {
                     alt[m * 2 * I + col[h]] = b;
-                    if (near_bf16_midpoint(v[h], ldexp(1.0, -16))) {
+                    if (near_bf16_midpoint(v[h], ldexp(1.0, -16) * cond[h])) {
                         alt[m * 2 * I + col[h]] = other_bf16_neighbour(v[h], b);
                         flagged += 1;
                     }
