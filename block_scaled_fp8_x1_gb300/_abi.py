@@ -67,6 +67,9 @@ SIGNATURES = {
     "fp8rl_quantize_128x128": (ST, [P, I64, I64, I64, P, P, P, STREAM]),
     "fp8rl_rmsnorm_quant": (ST, [P, P, ctypes.c_float, I64, I64, P, P, P, P, P, STREAM]),
     "fp8rl_silu_mul_quant": (ST, [P, I64, I64, P, P, P, P, STREAM]),
+    "fp8rl_silu_mul_bwd_quant": (ST, [P, P, I64, I64, P, P, P, P, STREAM]),
+    "fp8rl_rmsnorm_bwd": (ST, [P, P, P, P, I64, I64, P, P, P, ctypes.c_size_t, STREAM]),
+    "fp8rl_rmsnorm_bwd_workspace_bytes": (ctypes.c_size_t, [I64, I64]),
     "fp8rl_gemm_fwd": (ST, [P, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t, STREAM]),
     "fp8rl_gemm_dgrad": (ST, [P, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t, STREAM]),
     "fp8rl_gemm_wgrad": (ST, [P, P, P, P, P, I64, I64, I64, P, ctypes.c_size_t, STREAM]),

@@ -511,6 +511,56 @@ fp8rl_status fp8rl_silu_mul_quant(const uint16_t* gu, int64_t M, int64_t I, uint
     return cuda_status(launch_silu_mul_quant(gu, M, I, q, s, qT, sT, g_timeout_ns.load(), stream));
 }
 
+// ---------------------------------------------------------------- backward steps
+
+fp8rl_status fp8rl_silu_mul_bwd_quant(const uint16_t* gu, const uint16_t* dh, int64_t M, int64_t I,
+                                      uint8_t* q, float* s, uint8_t* qT, float* sT,
+                                      fp8rl_stream_t stream) {
+    if (M < 0 || I <= 0) return FP8RL_ERR_INVALID_ARG;
+    if ((qT == nullptr) != (sT == nullptr)) return FP8RL_ERR_INVALID_ARG;
+    if (I % 128 != 0) return FP8RL_ERR_SHAPE;
+    if (qT && M % 128 != 0) return FP8RL_ERR_SHAPE;
+    if (M == 0) return FP8RL_OK;
+    if (!gu || !dh || !q || !s) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(gu) || !aligned16(dh) || !aligned16(q) || !aligned16(s)) return FP8RL_ERR_ALIGN;
+    if (qT && (!aligned16(qT) || !aligned16(sT))) return FP8RL_ERR_ALIGN;
+    fp8rl_status e = current_device(nullptr);
+    if (e != FP8RL_OK) return e;
+    return cuda_status(launch_silu_mul_bwd_quant(gu, dh, M, I, q, s, qT, sT, g_timeout_ns.load(), stream));
+}
+
+size_t fp8rl_rmsnorm_bwd_workspace_bytes(int64_t M, int64_t K) {
+    if (M <= 0 || K <= 0) return 0;
+    int sms = 0;
+    if (current_device(&sms) != FP8RL_OK) sms = 148;
+    return (size_t)rmsnorm_bwd_blocks(M, sms) * (size_t)K * sizeof(float);
+}
+
+fp8rl_status fp8rl_rmsnorm_bwd(const uint16_t* x, const uint16_t* gamma, const float* rstd,
+                               const uint16_t* dy, int64_t M, int64_t K, uint16_t* dx,
+                               float* dgamma, void* ws, size_t ws_bytes, fp8rl_stream_t stream) {
+    if (M < 0 || K <= 0) return FP8RL_ERR_INVALID_ARG;
+    if (K % 128 != 0 || K > 8192) return FP8RL_ERR_SHAPE;
+    if (M == 0) {
+        if (dgamma) return cuda_status(cudaMemsetAsync(dgamma, 0, (size_t)K * sizeof(float), stream));
+        return FP8RL_OK;
+    }
+    if (!x || !gamma || !rstd || !dy || !dx) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(rstd) || !aligned16(dy) || !aligned16(dx))
+        return FP8RL_ERR_ALIGN;
+    int sms = 0;
+    fp8rl_status e = current_device(&sms);
+    if (e != FP8RL_OK) return e;
+    const int nblocks = rmsnorm_bwd_blocks(M, sms);
+    if (dgamma) {
+        if (!aligned16(dgamma)) return FP8RL_ERR_ALIGN;
+        if (!ws || ws_bytes < (size_t)nblocks * (size_t)K * sizeof(float)) return FP8RL_ERR_WORKSPACE;
+        if (!aligned16(ws)) return FP8RL_ERR_ALIGN;
+    }
+    return cuda_status(launch_rmsnorm_bwd(x, gamma, rstd, dy, M, K, dx, dgamma, reinterpret_cast<float*>(ws),
+                                          nblocks, stream));
+}
+
 // ---------------------------------------------------------------- GEMMs
 
 size_t fp8rl_gemm_workspace_bytes(int op, int64_t M, int64_t N, int64_t K) {

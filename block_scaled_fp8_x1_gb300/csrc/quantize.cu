@@ -80,10 +80,14 @@ __global__ void __launch_bounds__(256) k_quant_1x128(const uint16_t* __restrict_
 // ------------------------------------------------------------------------------------
 // PRO_RMSNORM computes the rows' rstd itself (a cluster of CTAs per panel, two passes);
 // PRO_RMSNORM_G reads rstd computed beforehand by k_rms_rstd.
-enum Prologue : int { PRO_COPY = 0, PRO_SILU = 1, PRO_RMSNORM = 2, PRO_RMSNORM_G = 3 };
+// PRO_SILU_BWD quantizes the gradient of the gate_up output, [dg | du], from the forward's
+// gate / up tiles and the gradient of h (a second tensor map).
+enum Prologue : int { PRO_COPY = 0, PRO_SILU = 1, PRO_RMSNORM = 2, PRO_RMSNORM_G = 3, PRO_SILU_BWD = 5 };
 
 struct PanelArgs {
-    const uint16_t* x;      // COPY / RMSNORM: x[M][ldx];  SILU: gu[M][ldx], ldx = 2*K
+    const uint16_t* x;      // COPY / RMSNORM: x[M][ldx];  SILU: gu[M][ldx], ldx = 2*K;
+                            // SILU_BWD: gu[M][ldx], ldx = K (K = 2I quantized columns)
+    const uint16_t* x2;     // SILU_BWD: dh[M][K/2]
     int64_t ldx;
     const uint16_t* gamma;  // RMSNORM: gamma[K]
     float eps;
@@ -145,6 +149,29 @@ __device__ __forceinline__ void rows_from_smem(const uint8_t* stage, const Panel
                 const float y0 = __fmul_rn(__fmul_rn(bf16_lo(xv[j]), r), gam[2 * j]);
                 const float y1 = __fmul_rn(__fmul_rn(bf16_hi(xv[j]), r), gam[2 * j + 1]);
                 w[i][j] = pack_bf16x2(y0, y1);
+            }
+        } else if (PRO == PRO_SILU_BWD) {
+            // stage: gate tile, up tile, tile of dh.  Columns [0, I) of the output are
+            // dg = dh*u*s*(1 + g*(1 - s)), columns [I, 2I) are du = dh*g*s, s = sigmoid(g)
+            const uint4 u = *reinterpret_cast<const uint4*>(stage + 128 * 256 + (R0 + i) * 256 + C0 * 2);
+            const uint4 d = *reinterpret_cast<const uint4*>(stage + 2 * 128 * 256 + (R0 + i) * 256 + C0 * 2);
+            const uint32_t uv[4] = {u.x, u.y, u.z, u.w};
+            const uint32_t dv[4] = {d.x, d.y, d.z, d.w};
+            const bool part_u = k0 >= a.K / 2;
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float o[2];
+                #pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float g = e ? bf16_hi(xv[j]) : bf16_lo(xv[j]);
+                    const float uu = e ? bf16_hi(uv[j]) : bf16_lo(uv[j]);
+                    const float dd = e ? bf16_hi(dv[j]) : bf16_lo(dv[j]);
+                    const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
+                    o[e] = part_u ? __fmul_rn(dd, __fmul_rn(g, sg))
+                                  : __fmul_rn(__fmul_rn(__fmul_rn(dd, uu), sg),
+                                              __fmaf_rn(g, __fsub_rn(1.0f, sg), 1.0f));
+                }
+                w[i][j] = pack_bf16x2(o[0], o[1]);
             }
         } else {  // SILU: h = bf16(silu(g) * u), silu(g) = g / (1 + exp(-g))
             const uint4 u = *reinterpret_cast<const uint4*>(stage + 128 * 256 + (R0 + i) * 256 + C0 * 2);
@@ -220,11 +247,11 @@ __global__ void __launch_bounds__(256) k_rms_rstd(const uint16_t* __restrict__ x
 // Input stages of the TMA ring (each a 128x128 BF16 tile; SiLU-mul stages gate and up).
 template <int PRO>
 struct PanelStages {
-    static constexpr int NIN = (PRO == PRO_SILU) ? 2 : 1;
+    static constexpr int NIN = (PRO == PRO_SILU) ? 2 : (PRO == PRO_SILU_BWD ? 3 : 1);
     static constexpr int STAGE_BYTES = NIN * 128 * 128 * 2;
     // SiLU-mul stages 64 KB per tile: one stage lets two CTAs share an SM, which hides the
     // copy latency better than three stages in one CTA (0.186 vs 0.242 ms at 8192x14336)
-    static constexpr int STAGES = (PRO == PRO_SILU) ? 1 : 3;
+    static constexpr int STAGES = (PRO == PRO_SILU || PRO == PRO_SILU_BWD) ? 1 : 3;
     static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 128;  // + alignment slack
 };
 
@@ -235,6 +262,7 @@ struct PanelStages {
 // RMSNorm streams the CTA's tiles twice: pass 1 sums squares, pass 2 quantizes.
 template <int PRO, bool ROW_OUT, bool COL_OUT>
 __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ CUtensorMap tmx,
+                                                     const __grid_constant__ CUtensorMap tmy,
                                                      const PanelArgs a) {
     using PS = PanelStages<PRO>;
     constexpr int STAGES = PS::STAGES;
@@ -267,6 +295,9 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
             const int64_t id = blockIdx.x + (int64_t)(it % n) * gridDim.x;
             pnl = id / ntiles;
             tt = id - pnl * ntiles;
+            // SiLU-mul backward: the dg and du tiles of one column block are neighbours in
+            // the order, so the second reads its gate and dh tiles from L2
+            if (PRO == PRO_SILU_BWD) tt = (tt & 1) ? ntiles / 2 + (tt >> 1) : (tt >> 1);
         } else {
             pnl = rms_panel;
             tt = t_begin + it % n;
@@ -278,6 +309,7 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
         abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmx);
+        if (PRO == PRO_SILU_BWD) tma_prefetch_desc(&tmy);
     }
     __syncthreads();
     auto issue = [&](int item) {
@@ -288,8 +320,18 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
         const uint32_t bar = smem_u32(&full_bar[st]);
         uint8_t* dst = stages + st * PS::STAGE_BYTES;
         mbar_arrive_expect_tx(bar, PS::STAGE_BYTES);
-        tma_load_2d(smem_u32(dst), &tmx, bar, (int)k0, (int)m0, 0);
-        if (PRO == PRO_SILU) tma_load_2d(smem_u32(dst + 128 * 128 * 2), &tmx, bar, (int)(a.K + k0), (int)m0, 0);
+        if (PRO == PRO_SILU_BWD) {
+            // output column tile k0 is dg (k0 < I) or du (k0 >= I) of source column block j0:
+            // the gate tile, the up tile and the tile of dh of that block
+            const int64_t half_k = a.K / 2;
+            const int64_t j0 = k0 < half_k ? k0 : k0 - half_k;
+            tma_load_2d(smem_u32(dst), &tmx, bar, (int)j0, (int)m0, 0);
+            tma_load_2d(smem_u32(dst + 128 * 128 * 2), &tmx, bar, (int)(half_k + j0), (int)m0, 0);
+            tma_load_2d(smem_u32(dst + 2 * 128 * 128 * 2), &tmy, bar, (int)j0, (int)m0, 0);
+        } else {
+            tma_load_2d(smem_u32(dst), &tmx, bar, (int)k0, (int)m0, 0);
+            if (PRO == PRO_SILU) tma_load_2d(smem_u32(dst + 128 * 128 * 2), &tmx, bar, (int)(a.K + k0), (int)m0, 0);
+        }
     };
     int issued = 0;
     if (tid == 0)
@@ -751,9 +793,15 @@ static cudaError_t tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int
 
 template <int PRO, bool ROW_OUT, bool COL_OUT>
 static cudaError_t launch_panel_t(const PanelArgs& a, int64_t in_cols, int cluster, cudaStream_t st) {
-    CUtensorMap tm;
+    CUtensorMap tm, tm2;
     cudaError_t e = tmap_bf16(&tm, a.x, a.M, in_cols, a.ldx);
     if (e != cudaSuccess) return e;
+    if (PRO == PRO_SILU_BWD) {
+        e = tmap_bf16(&tm2, a.x2, a.M, a.K / 2, a.K / 2);
+        if (e != cudaSuccess) return e;
+    } else {
+        tm2 = tm;   // unused
+    }
     auto kern = k_quant_panel<PRO, ROW_OUT, COL_OUT>;
     constexpr size_t smem = PanelStages<PRO>::SMEM;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -788,7 +836,7 @@ static cudaError_t launch_panel_t(const PanelArgs& a, int64_t in_cols, int clust
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kern, tm, a);
+    return cudaLaunchKernelEx(&cfg, kern, tm, tm2, a);
 }
 
 // Column tiles per CTA for the streaming kernels: enough to keep the TMA ring busy.
@@ -810,6 +858,16 @@ cudaError_t launch_silu_mul_quant(const uint16_t* gu, int64_t M, int64_t I, uint
     a.timeout_ns = timeout_ns;
     if (qT) return launch_panel_t<PRO_SILU, true, true>(a, 2 * I, 0, st);
     return launch_panel_t<PRO_SILU, true, false>(a, 2 * I, 0, st);
+}
+
+// SiLU-mul backward -> dual quantization of the gate_up output's gradient [dg | du]
+cudaError_t launch_silu_mul_bwd_quant(const uint16_t* gu, const uint16_t* dh, int64_t M, int64_t I, uint8_t* q,
+                                      float* s, uint8_t* qT, float* sT, uint64_t timeout_ns, cudaStream_t st) {
+    PanelArgs a = {};
+    a.x = gu; a.ldx = 2 * I; a.x2 = dh; a.M = M; a.K = 2 * I; a.q = q; a.s = s; a.qT = qT; a.sT = sT;
+    a.timeout_ns = timeout_ns;
+    if (qT) return launch_panel_t<PRO_SILU_BWD, true, true>(a, 2 * I, 0, st);
+    return launch_panel_t<PRO_SILU_BWD, true, false>(a, 2 * I, 0, st);
 }
 
 // Number of CTAs that split one 128-row panel of an RMSNorm along K: the largest divisor

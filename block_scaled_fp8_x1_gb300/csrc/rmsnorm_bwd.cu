@@ -1,0 +1,169 @@
+// rmsnorm_bwd.cu -- RMSNorm backward from the forward's saved rstd.
+//
+// "Technical summary: Jet-RL", section "Quantization Scheme": gradients between operators
+// stay BF16.  The forward is y = (x * r) * gamma with r = rstd = 1/sqrt(mean(x^2) + eps)
+// (its BF16 rounding passed straight through), so by the chain rule, with
+// S = sum_k dy_k * gamma_k * x_k over the row,
+//     dx_j     = r * gamma_j * dy_j - r^3 * x_j * S / K          (rounded to BF16)
+//     dgamma_k = sum_m dy_mk * x_mk * r_m                          (FP32)
+//
+// k_rms_bwd: each CTA takes a block of rows; thread t holds columns 8t + 2048 i of a row
+// (16-byte loads), the row's S is reduced over the CTA in a fixed order, dx is written as
+// BF16, and the thread's share of dgamma is accumulated over the CTA's rows with a
+// compensated (two-sum) FP32 pair.  The per-CTA partials go to a workspace that
+// k_rms_bwd_colsum adds in block order, so the result does not depend on timing.
+#include "common.cuh"
+#include "gemm.h"
+
+namespace fp8rl {
+
+namespace {
+
+constexpr int kBwdThreads = 256;
+constexpr int kBwdChunk = 8 * kBwdThreads;   // columns per pass of the CTA over a row
+
+__device__ __forceinline__ uint4 ldg_v4(const uint16_t* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ float lo16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// (hi, lo) += v with the exact two-sum.
+__device__ __forceinline__ void two_sum_add(float& hi, float& lo, float v) {
+    const float s = __fadd_rn(hi, v);
+    const float bp = __fsub_rn(s, hi);
+    const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(v, bp));
+    hi = s;
+    lo = __fadd_rn(lo, e);
+}
+
+}  // namespace
+
+template <int NCH>
+__global__ void __launch_bounds__(kBwdThreads) k_rms_bwd(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma,
+                                                         const float* __restrict__ rstd, const uint16_t* __restrict__ dy,
+                                                         int64_t M, int64_t K, uint16_t* __restrict__ dx,
+                                                         float* __restrict__ ws) {
+    __shared__ float s_part[2][kBwdThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t rows = (M + gridDim.x - 1) / gridDim.x;
+    const int64_t m_begin = (int64_t)blockIdx.x * rows;
+    const int64_t m_end = m_begin + rows < M ? m_begin + rows : M;
+
+    float gam[NCH][8];
+    bool valid[NCH];
+    #pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const int64_t c = (int64_t)i * kBwdChunk + 8 * tid;
+        valid[i] = c < K;
+        const uint4 g = valid[i] ? ldg_v4(gamma + c) : make_uint4(0, 0, 0, 0);
+        const uint32_t gv[4] = {g.x, g.y, g.z, g.w};
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            gam[i][2 * j] = lo16(gv[j]);
+            gam[i][2 * j + 1] = hi16(gv[j]);
+        }
+    }
+    float dg_hi[NCH][8], dg_lo[NCH][8];
+    #pragma unroll
+    for (int i = 0; i < NCH; ++i)
+        #pragma unroll
+        for (int j = 0; j < 8; ++j) dg_hi[i][j] = dg_lo[i][j] = 0.0f;
+
+    int par = 0;
+    for (int64_t m = m_begin; m < m_end; ++m, par ^= 1) {
+        float xv[NCH][8], dv[NCH][8];
+        float part = 0.0f;
+        #pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+            const int64_t c = (int64_t)i * kBwdChunk + 8 * tid;
+            const uint4 a = valid[i] ? ldg_v4(x + m * K + c) : make_uint4(0, 0, 0, 0);
+            const uint4 b = valid[i] ? ldg_v4(dy + m * K + c) : make_uint4(0, 0, 0, 0);
+            const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+            const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                xv[i][2 * j] = lo16(av[j]);
+                xv[i][2 * j + 1] = hi16(av[j]);
+                dv[i][2 * j] = lo16(bv[j]);
+                dv[i][2 * j + 1] = hi16(bv[j]);
+            }
+            #pragma unroll
+            for (int j = 0; j < 8; ++j) part = __fmaf_rn(__fmul_rn(dv[i][j], gam[i][j]), xv[i][j], part);
+        }
+        // S over the row: a fixed shuffle tree in each warp, then the warps in order
+        #pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, off));
+        if (lane == 0) s_part[par][warp] = part;
+        __syncthreads();
+        float S = 0.0f;
+        #pragma unroll
+        for (int w = 0; w < kBwdThreads / 32; ++w) S = __fadd_rn(S, s_part[par][w]);
+        const float r = __ldg(rstd + m);
+        const float coef = __fdiv_rn(__fmul_rn(__fmul_rn(__fmul_rn(r, r), r), S), (float)K);
+        #pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+            if (!valid[i]) continue;
+            const int64_t c = (int64_t)i * kBwdChunk + 8 * tid;
+            uint32_t o[4];
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float d0 = __fsub_rn(__fmul_rn(__fmul_rn(r, gam[i][2 * j]), dv[i][2 * j]), __fmul_rn(coef, xv[i][2 * j]));
+                const float d1 = __fsub_rn(__fmul_rn(__fmul_rn(r, gam[i][2 * j + 1]), dv[i][2 * j + 1]),
+                                           __fmul_rn(coef, xv[i][2 * j + 1]));
+                o[j] = pack_bf16x2(d0, d1);
+            }
+            *reinterpret_cast<uint4*>(dx + m * K + c) = make_uint4(o[0], o[1], o[2], o[3]);
+            if (ws) {
+                #pragma unroll
+                for (int j = 0; j < 8; ++j) two_sum_add(dg_hi[i][j], dg_lo[i][j], __fmul_rn(__fmul_rn(dv[i][j], xv[i][j]), r));
+            }
+        }
+    }
+    if (ws) {
+        #pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+            if (!valid[i]) continue;
+            const int64_t c = (int64_t)i * kBwdChunk + 8 * tid;
+            float* dst = ws + (int64_t)blockIdx.x * K + c;
+            #pragma unroll
+            for (int j = 0; j < 8; ++j) dst[j] = __fadd_rn(dg_hi[i][j], dg_lo[i][j]);
+        }
+    }
+}
+
+// dgamma[k] = sum over the row blocks of their partials, in block order (compensated).
+__global__ void __launch_bounds__(256) k_rms_bwd_colsum(const float* __restrict__ ws, int nblocks, int64_t K,
+                                                        float* __restrict__ dgamma) {
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= K) return;
+    float hi = 0.0f, lo = 0.0f;
+    for (int b = 0; b < nblocks; ++b) two_sum_add(hi, lo, ws[(int64_t)b * K + k]);
+    dgamma[k] = __fadd_rn(hi, lo);
+}
+
+// Row blocks of the backward: two CTAs per SM, at most one per row.
+int rmsnorm_bwd_blocks(int64_t M, int num_sms) {
+    const int64_t b = 2 * (int64_t)(num_sms > 0 ? num_sms : 148);
+    return (int)(M < b ? (M > 0 ? M : 1) : b);
+}
+
+cudaError_t launch_rmsnorm_bwd(const uint16_t* x, const uint16_t* gamma, const float* rstd, const uint16_t* dy,
+                               int64_t M, int64_t K, uint16_t* dx, float* dgamma, float* ws, int nblocks,
+                               cudaStream_t st) {
+    const int nch = (int)((K + kBwdChunk - 1) / kBwdChunk);
+    float* part = dgamma ? ws : nullptr;
+    switch (nch) {
+        case 1: k_rms_bwd<1><<<nblocks, kBwdThreads, 0, st>>>(x, gamma, rstd, dy, M, K, dx, part); break;
+        case 2: k_rms_bwd<2><<<nblocks, kBwdThreads, 0, st>>>(x, gamma, rstd, dy, M, K, dx, part); break;
+        case 3: k_rms_bwd<3><<<nblocks, kBwdThreads, 0, st>>>(x, gamma, rstd, dy, M, K, dx, part); break;
+        case 4: k_rms_bwd<4><<<nblocks, kBwdThreads, 0, st>>>(x, gamma, rstd, dy, M, K, dx, part); break;
+        default: return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || !dgamma) return e;
+    k_rms_bwd_colsum<<<(unsigned)((K + 255) / 256), 256, 0, st>>>(ws, nblocks, K, dgamma);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8rl

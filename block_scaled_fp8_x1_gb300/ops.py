@@ -180,6 +180,52 @@ def silu_mul_quant(gu: torch.Tensor, dual: bool = True):
     return q, s, qT, sT
 
 
+# ------------------------------------------------------------------ backward steps
+
+def silu_mul_bwd_quant(gu: torch.Tensor, dh: torch.Tensor, dual: bool = True):
+    """Gradient of the gate_up output from the forward's gu bf16 [M, 2I] and dh bf16 [M, I],
+    quantized: (q [M,2I], s [2I/128,M], qT [2I,M] or None, sT [M/128,2I] or None)."""
+    _require(gu, torch.bfloat16, "gu")
+    _require(dh, torch.bfloat16, "dh", gu.device)
+    _contig(gu, "gu")
+    _contig(dh, "dh")
+    M, I2 = gu.shape
+    if dh.shape != (M, I2 // 2):
+        raise ValueError(f"dh: expected {(M, I2 // 2)}, got {tuple(dh.shape)}")
+    dev = gu.device
+    q = torch.empty((M, I2), dtype=torch.uint8, device=dev)
+    s = torch.empty((I2 // 128, M), dtype=torch.float32, device=dev)
+    qT = sT = None
+    if dual:
+        qT = torch.empty((I2, M), dtype=torch.uint8, device=dev)
+        sT = torch.empty((M // 128, I2), dtype=torch.float32, device=dev)
+    check(lib().fp8rl_silu_mul_bwd_quant(_ptr(gu), _ptr(dh), M, I2 // 2, _ptr(q), _ptr(s), _ptr(qT),
+                                         _ptr(sT), _stream(dev)), "fp8rl_silu_mul_bwd_quant")
+    return q, s, qT, sT
+
+
+def rmsnorm_bwd(x: torch.Tensor, gamma: torch.Tensor, rstd: torch.Tensor, dy: torch.Tensor,
+                with_dgamma: bool = True):
+    """RMSNorm backward from the forward's rstd: (dx bf16 [M,K], dgamma f32 [K] or None)."""
+    _require(x, torch.bfloat16, "x")
+    _require(gamma, torch.bfloat16, "gamma", x.device)
+    _require(rstd, torch.float32, "rstd", x.device)
+    _require(dy, torch.bfloat16, "dy", x.device)
+    for t, n in ((x, "x"), (gamma, "gamma"), (rstd, "rstd"), (dy, "dy")):
+        _contig(t, n)
+    M, K = x.shape
+    dev = x.device
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    dgamma = ws = None
+    if with_dgamma:
+        dgamma = torch.empty((K,), dtype=torch.float32, device=dev)
+        ws = workspace(int(lib().fp8rl_rmsnorm_bwd_workspace_bytes(M, K)), dev)
+    check(lib().fp8rl_rmsnorm_bwd(_ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dy), M, K, _ptr(dx),
+                                  _ptr(dgamma), _ptr(ws), ws.numel() if ws is not None else 0,
+                                  _stream(dev)), "fp8rl_rmsnorm_bwd")
+    return dx, dgamma
+
+
 # ------------------------------------------------------------------ GEMMs
 
 _ws_lock = threading.Lock()

@@ -153,6 +153,37 @@ FP8RL_API fp8rl_status fp8rl_silu_mul_quant(const uint16_t* gu, int64_t M, int64
                                   float* s, uint8_t* qT, float* sT, fp8rl_stream_t stream);
 
 /* ----------------------------------------------------------------------------------------
+ * Backward operators either side of the gradient quantizer ("Quantization Scheme":
+ * gradients between operators stay BF16; DGrad and WGrad consume quantized gradients).
+ * -------------------------------------------------------------------------------------- */
+
+/* Fused SiLU-mul backward -> quantize: the gradient of the gate_up output from the forward's
+ * gate_up output and the gradient of h (the down projection's DGrad output):
+ *   gu : BF16 [M][2*I] (gate = columns [0, I), up = [I, 2I));  dh : BF16 [M][I]
+ *   with s = sigmoid(g):  dg = bf16(dh*u*s*(1 + g*(1 - s))),  du = bf16(dh*g*s)
+ *   evaluated in FP32; dgu = [dg | du] ([M][2I]) is quantized 1x128 along its 2I columns
+ *   (q [M][2I], s [2I/128][M], the DGrad operand) and, if qT/sT are set (M % 128 == 0),
+ *   128x1 transposed (qT [2I][M], sT [M/128][2I], the WGrad operand).  dgu itself is not
+ *   stored.  I % 128 == 0. */
+FP8RL_API fp8rl_status fp8rl_silu_mul_bwd_quant(const uint16_t* gu, const uint16_t* dh, int64_t M,
+                                                int64_t I, uint8_t* q, float* s, uint8_t* qT,
+                                                float* sT, fp8rl_stream_t stream);
+
+/* RMSNorm backward from the forward's saved rstd (fp8rl_rmsnorm_quant's rstd output):
+ *   x : BF16 [M][K];  gamma : BF16 [K];  rstd : float [M];  dy : BF16 [M][K] (the gradient
+ *   of the normalised output)
+ *   dx[m,j]   = bf16( r*gamma_j*dy_j - r^3*x_j*S/K ),  S = sum_k dy_k*gamma_k*x_k   (FP32)
+ *   dgamma[k] = sum_m dy[m,k]*x[m,k]*r_m   (FP32; nullable: then ws is unused)
+ * K % 128 == 0 and K <= 8192, else FP8RL_ERR_SHAPE.  dgamma needs
+ * fp8rl_rmsnorm_bwd_workspace_bytes(M, K) bytes of workspace (no initial contents); the
+ * sums run in a fixed order, so repeated calls give the same bits. */
+FP8RL_API fp8rl_status fp8rl_rmsnorm_bwd(const uint16_t* x, const uint16_t* gamma, const float* rstd,
+                                         const uint16_t* dy, int64_t M, int64_t K, uint16_t* dx,
+                                         float* dgamma, void* ws, size_t ws_bytes,
+                                         fp8rl_stream_t stream);
+FP8RL_API size_t fp8rl_rmsnorm_bwd_workspace_bytes(int64_t M, int64_t K);
+
+/* ----------------------------------------------------------------------------------------
  * Block-scaled FP8 GEMMs ("Quantization Scheme": forward, DGrad and WGrad in FP8).
  * Output element = bf16_rne( sum_kb sA(kb,row) * sB(kb,col) * sum_{k in kb} a*b ), with
  * the inner block sum in FP32 on the tensor cores and the outer sum in FP32 registers.

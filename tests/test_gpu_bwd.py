@@ -1,0 +1,99 @@
+"""The backward operators either side of the gradient quantizer, on the GPU vs the oracle.
+
+"Technical summary: Jet-RL", section "Quantization Scheme": gradients between operators
+stay BF16 and DGrad / WGrad run on gradients quantized 1x128 and 128x1.
+
+SiLU-mul backward -> quantize: the device evaluates dg, du in binary32 (exp and a fast
+reciprocal), the oracle in binary64; they can round to different BF16 neighbours only where
+the oracle flags an element as near a BF16 midpoint (relative to the size of its terms).
+Groups without such elements must be bit-exact in codes and scales; groups with them must
+equal the oracle's quantization of one of the choices.
+
+RMSNorm backward: dx within one BF16 rounding of the oracle's binary64 value plus binary32
+evaluation error, |dx - ref| <= 2^-8 (|r gamma dy| + |r^3 x S / K|); dgamma within
+2^-12 sum_m |dy x r| (binary32 sums of up to 16384 rows, compensated); repeat calls give
+identical bits.
+"""
+import numpy as np
+import pytest
+import torch
+
+from block_scaled_fp8_x1_gb300 import _abi, synth
+from parity import bits16, f32, silu_group_matches, u8
+
+pytestmark = pytest.mark.gpu
+
+
+def check_silu_bwd(fp8lib, oracle, gu, dh, dual):
+    q, s, qT, sT = fp8lib.silu_mul_bwd_quant(gu, dh, dual=dual)
+    dgu, alt, nflag = oracle.silu_mul_bwd(bits16(gu), bits16(dh))
+    qr, sr = oracle.quantize_1x128(dgu)
+    qg, sg = u8(q), f32(s)
+    M, C = dgu.shape
+    n_inexact = 0
+    for m in range(M):
+        for b in range(C // 128):
+            sl = slice(b * 128, (b + 1) * 128)
+            if np.array_equal(qg[m, sl], qr[m, sl]) and sg[b, m].view(np.uint32) == sr[b, m].view(np.uint32):
+                continue
+            n_inexact += 1
+            assert silu_group_matches(oracle, qg[m, sl], sg[b, m], dgu[m, sl], alt[m, sl]), (m, b)
+    if dual:
+        qTr, sTr = oracle.quantize_128x1(dgu)
+        qTg, sTg = u8(qT), f32(sT)
+        for c in range(C):
+            for b in range(M // 128):
+                sl = slice(b * 128, (b + 1) * 128)
+                if np.array_equal(qTg[c, sl], qTr[c, sl]) and sTg[b, c].view(np.uint32) == sTr[b, c].view(np.uint32):
+                    continue
+                n_inexact += 1
+                assert silu_group_matches(oracle, qTg[c, sl], sTg[b, c], dgu[sl, c], alt[sl, c]), (c, b)
+    return n_inexact, nflag
+
+
+@pytest.mark.parametrize("M,I", [(128, 128), (256, 384), (384, 1024)])
+def test_silu_mul_bwd_quant_dual(fp8lib, oracle, M, I):
+    gu = synth.normal_bf16((M, 2 * I), 2.0, 5 * M + I, "cuda")
+    dh = synth.normal_bf16((M, I), 1e-3, 3 * M + I, "cuda")
+    gu[0, :I] = 0.0                  # g = 0: dg = dh*u/2, du = 0 (a zero group of du)
+    gu[1, :I] = 30.0                 # saturated sigmoid
+    dh[2] = 0.0                      # zero gradient row
+    gu[3, :I] = -1.28125             # next to the root of silu' (dg cancels)
+    n_inexact, nflag = check_silu_bwd(fp8lib, oracle, gu, dh, dual=True)
+    assert n_inexact <= 2 * nflag
+    assert fp8lib.check_status() == _abi.FP8RL_OK
+
+
+def test_silu_mul_bwd_quant_rows_only_ragged(fp8lib, oracle):
+    gu = synth.normal_bf16((77, 2 * 256), 1.5, 8, "cuda")
+    dh = synth.normal_bf16((77, 256), 1e-2, 9, "cuda")
+    check_silu_bwd(fp8lib, oracle, gu, dh, dual=False)
+
+
+@pytest.mark.parametrize("M,K", [(128, 128), (300, 640), (1000, 4096), (257, 5120), (64, 8192)])
+def test_rmsnorm_bwd(fp8lib, oracle, M, K):
+    x = synth.normal_bf16((M, K), 1.0, M + K, "cuda", outlier_channels=max(1, K // 1000), outlier_scale=30.0)
+    x[1] = 0.0                       # zero row
+    x[2] = 1.5                       # constant row
+    gamma = synth.normal_bf16((K,), 0.1, 6, "cuda").float().add_(1.0).to(torch.bfloat16)
+    dy = synth.normal_bf16((M, K), 1e-3, 2 * M + K, "cuda")
+    _, _, _, _, rstd = fp8lib.rmsnorm_quant(x, gamma, 1e-5, dual=False)
+    dx, dgamma = fp8lib.rmsnorm_bwd(x, gamma, rstd, dy)
+    xr, gr, dyr, rr = bits16(x), bits16(gamma), bits16(dy), f32(rstd)
+    dx_ref, mag, dg_ref = oracle.rmsnorm_bwd(xr, gr, rr, dyr)
+    got = (bits16(dx).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ref = (dx_ref.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    # ref is the BF16 rounding of the binary64 value: one more BF16 rounding allowed
+    bad = np.abs(got - ref) > 2.0 ** -8 * mag + 2.0 ** -8 * np.abs(ref) + 1e-30
+    assert not bad.any(), f"{int(bad.sum())} dx outside the bound, first at {np.argwhere(bad)[0]}"
+    def b2f(b):
+        return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    absum = np.sum(np.abs(b2f(dyr) * b2f(xr) * rr.astype(np.float64)[:, None]), axis=0)
+    dg = f32(dgamma).astype(np.float64)
+    assert np.all(np.abs(dg - dg_ref) <= 2.0 ** -12 * absum + 1e-30)
+    dx2, dgamma2 = fp8lib.rmsnorm_bwd(x, gamma, rstd, dy)
+    assert torch.equal(dx.view(torch.int16), dx2.view(torch.int16))
+    assert torch.equal(dgamma.view(torch.int32), dgamma2.view(torch.int32))
+    dx3, none = fp8lib.rmsnorm_bwd(x, gamma, rstd, dy, with_dgamma=False)
+    assert none is None and torch.equal(dx.view(torch.int16), dx3.view(torch.int16))
+    assert fp8lib.check_status() == _abi.FP8RL_OK
