@@ -68,6 +68,7 @@ def _load():
             "orc_rmsnorm": (None, [P, P, ctypes.c_float, I64, I64, P, P, P]),
             "orc_silu_mul": (I64, [P, I64, I64, P, P]),
             "orc_silu_mul_bwd": (I64, [P, P, I64, I64, P, P]),
+            "orc_requant_128x1": (None, [P, P, I64, I64, P, P]),
             "orc_rmsnorm_bwd": (None, [P, P, P, P, I64, I64, P, P, P]),
             "orc_gemm": (None, [P, I64, P, I64, P, I64, P, I64, I64, I64, I64, I64, I64, P]),
             "orc_gemm_sampled": (None, [P, I64, P, I64, P, I64, P, I64, I64, I64, I64, P, P,
@@ -210,6 +211,19 @@ def silu_mul(gu_bf16: np.ndarray):
     alt = np.empty((M, I), dtype=np.uint16)
     n = _load().orc_silu_mul(_p(gu), M, I, _p(h), _p(alt))
     return h, alt, int(n)
+
+
+def requant_128x1(q: np.ndarray, s: np.ndarray):
+    """From X's 1x128 codes q[M,K] and scales s[K/128,M]: the 128x1 quantization of the
+    dequantized values fl32(decode(q)*s), transposed: (qT uint8 [K,M], sT float32 [M/128,K])."""
+    qq = _c(q, np.uint8)
+    ss = _c(s, np.float32)
+    M, K = qq.shape
+    assert M % 128 == 0 and K % 128 == 0 and ss.shape == (K // 128, M)
+    qT = np.empty((K, M), dtype=np.uint8)
+    sT = np.empty((M // 128, K), dtype=np.float32)
+    _load().orc_requant_128x1(_p(qq), _p(ss), M, K, _p(qT), _p(sT))
+    return qT, sT
 
 
 def silu_mul_bwd(gu_bf16: np.ndarray, dh_bf16: np.ndarray):

@@ -30,6 +30,9 @@
  *   R7  SiLU-mul backward (the chain rule of R6): with s = 1/(1+exp(-g)),
  *       dg = dh*u*s*(1 + g*(1-s)) and du = dh*g*s in binary64, each rounded to BF16 (the
  *       gradient between operators is BF16); [dg | du] is then quantized as a gradient.
+ *   R9  WGrad operand from the saved FP8 activation (the memory-saving variant): the
+ *       1x128 codes and scales of X are dequantized, x^ = fl32(decode(q) * s) in IEEE
+ *       single precision, and x^ is quantized 128x1 (R2, R3) along the token dimension.
  *   R8  RMSNorm backward (the chain rule of R5 through rstd, the BF16 rounding of y taken
  *       as the identity): with r the forward's rstd and S = sum_k dy_k*gamma_k*x_k,
  *       dx_j = r*gamma_j*dy_j - r^3*x_j*S/K in binary64, rounded to BF16;
@@ -329,6 +332,27 @@ ORC_API int64_t orc_silu_mul(const uint16_t* gu, int64_t M, int64_t I, uint16_t*
         }
     }
     return flagged;
+}
+
+/* ---------------------------------------------------------------- requantization (R9) */
+
+/* From the 1x128 codes q[M][K] and scales s[K/128][M] of X: the 128x1 quantization of the
+ * dequantized x^ = fl32(decode(q) * s), transposed like orc_quantize_128x1: codes
+ * qT[k*M + m], scales sT[(m/128)*K + k].  M % 128 == 0, K % 128 == 0. */
+ORC_API void orc_requant_128x1(const uint8_t* q, const float* s, int64_t M, int64_t K, uint8_t* qT,
+                               float* sT) {
+    int64_t nmb = M / 128;
+    #pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t k = 0; k < K; ++k) {
+        float buf[128];
+        for (int64_t mb = 0; mb < nmb; ++mb) {
+            for (int i = 0; i < 128; ++i) {
+                int64_t m = mb * 128 + i;
+                buf[i] = (float)orc_e4m3_decode(q[m * K + k]) * s[(k / 128) * M + m];
+            }
+            quant_group(buf, 128, 1, qT + k * M + mb * 128, 1, &sT[mb * K + k]);
+        }
+    }
 }
 
 /* ---------------------------------------------------------------- SiLU-mul backward (R7) */

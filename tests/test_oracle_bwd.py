@@ -133,3 +133,34 @@ def test_rmsnorm_bwd_special_rows(oracle):
     assert np.all(f64(dx[1]) == f64(bf16(np.full(K, r[1] * 0.5))))
     # +-1 row with dy = 1: S = sum(x) = 0, so dx = r * dy
     assert np.all(f64(dx[2]) == f64(bf16(np.full(K, r[2]))))
+
+
+def test_requant_128x1_is_the_128x1_quantization_of_the_dequantized_values(oracle):
+    """The WGrad operand from the saved FP8: decode(q)*s in binary32 (numpy), then the
+    128x1 quantization of those binary32 values (the already pinned group quantizer, and
+    numpy's binary32 division with torch's E4M3 cast for the codes)."""
+    rng = np.random.default_rng(14)
+    M, K = 256, 384
+    x = rng.standard_normal((M, K)) * np.exp(rng.uniform(-3, 3, (1, K)))
+    q, s = oracle.quantize_1x128(bf16(x))
+    qT, sT = oracle.requant_128x1(q, s)
+    xhat = (oracle.e4m3_decode(q).astype(np.float32) *
+            np.repeat(s.T, 128, axis=1).astype(np.float32))          # [M, K] binary32
+    assert xhat.dtype == np.float32
+    g = xhat.reshape(M // 128, 128, K)
+    amax = np.abs(g).max(axis=1)                                     # [M/128, K]
+    s_ref = amax / np.float32(448.0)
+    assert np.array_equal(sT.view(np.uint32), s_ref.view(np.uint32))
+    v = np.clip(g / s_ref[:, None, :], -448.0, 448.0)                # binary32 division
+    codes = torch.from_numpy(np.ascontiguousarray(v)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ref = codes.transpose(2, 0, 1).reshape(K, M)                     # qT[k, m]
+    assert np.array_equal(qT, ref)
+    # a group whose values are exactly E4M3 grid points times a power of two is unchanged
+    # by the round trip: requantizing the exactly representable 1x128 groups of the
+    # transpose returns the same codes
+    z = np.zeros((128, 128))
+    z[:, 0] = 448.0 * 2.0 ** -3
+    z[5, 1] = -3.0
+    qz, sz = oracle.quantize_1x128(bf16(z))
+    qTz, sTz = oracle.requant_128x1(qz, sz)
+    assert sTz[0, 0] == np.float32(2.0 ** -3) and np.all(qTz[0] == 0x7E)
