@@ -215,7 +215,8 @@ def silu_mul(gu_bf16: np.ndarray):
 
 def requant_128x1(q: np.ndarray, s: np.ndarray):
     """From X's 1x128 codes q[M,K] and scales s[K/128,M]: the 128x1 quantization of the
-    dequantized values fl32(decode(q)*s), transposed: (qT uint8 [K,M], sT float32 [M/128,K])."""
+    dequantized BF16 values bf16(fl32(decode(q)*s)), transposed: (qT uint8 [K,M],
+    sT float32 [M/128,K])."""
     qq = _c(q, np.uint8)
     ss = _c(s, np.float32)
     M, K = qq.shape

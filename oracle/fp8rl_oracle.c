@@ -31,8 +31,9 @@
  *       dg = dh*u*s*(1 + g*(1-s)) and du = dh*g*s in binary64, each rounded to BF16 (the
  *       gradient between operators is BF16); [dg | du] is then quantized as a gradient.
  *   R9  WGrad operand from the saved FP8 activation (the memory-saving variant): the
- *       1x128 codes and scales of X are dequantized, x^ = fl32(decode(q) * s) in IEEE
- *       single precision, and x^ is quantized 128x1 (R2, R3) along the token dimension.
+ *       1x128 codes and scales of X are dequantized back to the BF16 activation,
+ *       x^ = bf16_rne(fl32(decode(q) * s)), and x^ is quantized 128x1 (R2, R3) along the
+ *       token dimension, as the BF16 path quantizes X itself.
  *   R8  RMSNorm backward (the chain rule of R5 through rstd, the BF16 rounding of y taken
  *       as the identity): with r the forward's rstd and S = sum_k dy_k*gamma_k*x_k,
  *       dx_j = r*gamma_j*dy_j - r^3*x_j*S/K in binary64, rounded to BF16;
@@ -337,8 +338,8 @@ ORC_API int64_t orc_silu_mul(const uint16_t* gu, int64_t M, int64_t I, uint16_t*
 /* ---------------------------------------------------------------- requantization (R9) */
 
 /* From the 1x128 codes q[M][K] and scales s[K/128][M] of X: the 128x1 quantization of the
- * dequantized x^ = fl32(decode(q) * s), transposed like orc_quantize_128x1: codes
- * qT[k*M + m], scales sT[(m/128)*K + k].  M % 128 == 0, K % 128 == 0. */
+ * dequantized x^ = bf16_rne(fl32(decode(q) * s)), transposed like orc_quantize_128x1:
+ * codes qT[k*M + m], scales sT[(m/128)*K + k].  M % 128 == 0, K % 128 == 0. */
 ORC_API void orc_requant_128x1(const uint8_t* q, const float* s, int64_t M, int64_t K, uint8_t* qT,
                                float* sT) {
     int64_t nmb = M / 128;
@@ -348,7 +349,8 @@ ORC_API void orc_requant_128x1(const uint8_t* q, const float* s, int64_t M, int6
         for (int64_t mb = 0; mb < nmb; ++mb) {
             for (int i = 0; i < 128; ++i) {
                 int64_t m = mb * 128 + i;
-                buf[i] = (float)orc_e4m3_decode(q[m * K + k]) * s[(k / 128) * M + m];
+                float v = (float)orc_e4m3_decode(q[m * K + k]) * s[(k / 128) * M + m];
+                buf[i] = orc_bf16_to_f32(orc_f32_to_bf16(v));
             }
             quant_group(buf, 128, 1, qT + k * M + mb * 128, 1, &sT[mb * K + k]);
         }

@@ -136,9 +136,9 @@ def test_rmsnorm_bwd_special_rows(oracle):
 
 
 def test_requant_128x1_is_the_128x1_quantization_of_the_dequantized_values(oracle):
-    """The WGrad operand from the saved FP8: decode(q)*s in binary32 (numpy), then the
-    128x1 quantization of those binary32 values (the already pinned group quantizer, and
-    numpy's binary32 division with torch's E4M3 cast for the codes)."""
+    """The WGrad operand from the saved FP8: decode(q)*s in binary32 (numpy), rounded to
+    BF16 (torch), then the 128x1 quantization of those values (numpy's binary32 division
+    and torch's E4M3 cast for the codes)."""
     rng = np.random.default_rng(14)
     M, K = 256, 384
     x = rng.standard_normal((M, K)) * np.exp(rng.uniform(-3, 3, (1, K)))
@@ -147,6 +147,7 @@ def test_requant_128x1_is_the_128x1_quantization_of_the_dequantized_values(oracl
     xhat = (oracle.e4m3_decode(q).astype(np.float32) *
             np.repeat(s.T, 128, axis=1).astype(np.float32))          # [M, K] binary32
     assert xhat.dtype == np.float32
+    xhat = torch.from_numpy(xhat).to(torch.bfloat16).to(torch.float32).numpy()   # BF16 RNE
     g = xhat.reshape(M // 128, 128, K)
     amax = np.abs(g).max(axis=1)                                     # [M/128, K]
     s_ref = amax / np.float32(448.0)
