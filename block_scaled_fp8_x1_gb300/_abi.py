@@ -64,6 +64,7 @@ SIGNATURES = {
     "fp8rl_check_status": (ST, [STREAM]),
     "fp8rl_quantize_1x128": (ST, [P, I64, I64, I64, P, P, P, P, STREAM]),
     "fp8rl_quantize_128x1": (ST, [P, I64, I64, I64, P, P, STREAM]),
+    "fp8rl_requantize_128x1": (ST, [P, P, I64, I64, P, P, STREAM]),
     "fp8rl_quantize_128x128": (ST, [P, I64, I64, I64, P, P, P, STREAM]),
     "fp8rl_rmsnorm_quant": (ST, [P, P, ctypes.c_float, I64, I64, P, P, P, P, P, STREAM]),
     "fp8rl_silu_mul_quant": (ST, [P, I64, I64, P, P, P, P, STREAM]),

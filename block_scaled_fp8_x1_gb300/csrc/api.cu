@@ -466,6 +466,18 @@ fp8rl_status fp8rl_quantize_128x1(const uint16_t* x, int64_t M, int64_t K, int64
     return cuda_status(launch_quant_dual(x, M, K, ldx, nullptr, nullptr, qT, sT, g_timeout_ns.load(), stream));
 }
 
+fp8rl_status fp8rl_requantize_128x1(const uint8_t* q, const float* s, int64_t M, int64_t K,
+                                    uint8_t* qT, float* sT, fp8rl_stream_t stream) {
+    if (M < 0 || K <= 0) return FP8RL_ERR_INVALID_ARG;
+    if (K % 128 != 0 || M % 128 != 0) return FP8RL_ERR_SHAPE;
+    if (M == 0) return FP8RL_OK;
+    if (!q || !s || !qT || !sT) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(s) || !aligned16(qT) || !aligned16(sT)) return FP8RL_ERR_ALIGN;
+    fp8rl_status e = current_device(nullptr);
+    if (e != FP8RL_OK) return e;
+    return cuda_status(launch_requant_128x1(q, s, M, K, qT, sT, g_timeout_ns.load(), stream));
+}
+
 fp8rl_status fp8rl_quantize_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw,
                                     uint8_t* q, float* s, uint8_t* qT, fp8rl_stream_t stream) {
     if (N < 0 || K <= 0 || ldw < K) return FP8RL_ERR_INVALID_ARG;

@@ -110,6 +110,8 @@ cudaError_t launch_rmsnorm_bwd(const uint16_t* x, const uint16_t* gamma, const f
                                int64_t M, int64_t K, uint16_t* dx, float* dgamma, float* ws, int nblocks,
                                cudaStream_t st);
 int rmsnorm_bwd_blocks(int64_t M, int num_sms);
+cudaError_t launch_requant_128x1(const uint8_t* q, const float* s, int64_t M, int64_t K, uint8_t* qT, float* sT,
+                                 uint64_t timeout_ns, cudaStream_t st);
 fp8rl_status read_and_clear_quant_status();
 cudaError_t launch_quant_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
                                  float* s, uint8_t* qT, uint64_t timeout_ns, cudaStream_t st);

@@ -81,13 +81,17 @@ __global__ void __launch_bounds__(256) k_quant_1x128(const uint16_t* __restrict_
 // PRO_RMSNORM computes the rows' rstd itself (a cluster of CTAs per panel, two passes);
 // PRO_RMSNORM_G reads rstd computed beforehand by k_rms_rstd.
 // PRO_SILU_BWD quantizes the gradient of the gate_up output, [dg | du], from the forward's
-// gate / up tiles and the gradient of h (a second tensor map).
-enum Prologue : int { PRO_COPY = 0, PRO_SILU = 1, PRO_RMSNORM = 2, PRO_RMSNORM_G = 3, PRO_SILU_BWD = 5 };
+// gate / up tiles and the gradient of h (a second tensor map).  PRO_DEQUANT rebuilds the
+// BF16 activation from its saved 1x128 codes and row scales (the stage holds a 128x128
+// code tile and the tile's 128 row scales) for the 128x1 WGrad operand.
+enum Prologue : int { PRO_COPY = 0, PRO_SILU = 1, PRO_RMSNORM = 2, PRO_RMSNORM_G = 3, PRO_SILU_BWD = 5,
+                      PRO_DEQUANT = 6 };
 
 struct PanelArgs {
     const uint16_t* x;      // COPY / RMSNORM: x[M][ldx];  SILU: gu[M][ldx], ldx = 2*K;
                             // SILU_BWD: gu[M][ldx], ldx = K (K = 2I quantized columns)
     const uint16_t* x2;     // SILU_BWD: dh[M][K/2]
+    const float* xs;        // DEQUANT: the codes' scales xs[K/128][M] (x holds the codes)
     int64_t ldx;
     const uint16_t* gamma;  // RMSNORM: gamma[K]
     float eps;
@@ -137,6 +141,28 @@ __device__ __forceinline__ void rows_from_smem(const uint8_t* stage, const Panel
     }
     #pragma unroll
     for (int i = 0; i < 8; ++i) {
+        if (PRO == PRO_DEQUANT) {
+            // x^ = bf16(fl32(decode(code) * s_row)); decode from the format: sign, 4-bit
+            // exponent (bias 7), 3-bit mantissa, subnormal steps of 2^-9
+            const uint2 c8 = *reinterpret_cast<const uint2*>(stage + (R0 + i) * 128 + C0);
+            const float sr = *reinterpret_cast<const float*>(stage + 128 * 128 + 4 * (R0 + i));
+            const uint32_t cw[2] = {c8.x, c8.y};
+            #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float o[2];
+                #pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const uint32_t b = (cw[j >> 1] >> (8 * (2 * (j & 1) + e))) & 0xFFu;
+                    const uint32_t ex = (b >> 3) & 0xFu, mt = b & 7u;
+                    float mag = ex ? __uint_as_float(((ex + 120u) << 23) | (mt << 20))
+                                   : __fmul_rn((float)mt, 0.001953125f);
+                    mag = (b & 0x80u) ? -mag : mag;
+                    o[e] = __fmul_rn(mag, sr);
+                }
+                w[i][j] = pack_bf16x2(o[0], o[1]);
+            }
+            continue;
+        }
         const uint4 v = *reinterpret_cast<const uint4*>(stage + (R0 + i) * 256 + C0 * 2);
         const uint32_t xv[4] = {v.x, v.y, v.z, v.w};
         if (PRO == PRO_COPY) {
@@ -248,7 +274,8 @@ __global__ void __launch_bounds__(256) k_rms_rstd(const uint16_t* __restrict__ x
 template <int PRO>
 struct PanelStages {
     static constexpr int NIN = (PRO == PRO_SILU) ? 2 : (PRO == PRO_SILU_BWD ? 3 : 1);
-    static constexpr int STAGE_BYTES = NIN * 128 * 128 * 2;
+    // DEQUANT: a 128x128 code tile and its 128 row scales
+    static constexpr int STAGE_BYTES = PRO == PRO_DEQUANT ? 128 * 128 + 128 * 4 : NIN * 128 * 128 * 2;
     // SiLU-mul stages 64 KB per tile: one stage lets two CTAs share an SM, which hides the
     // copy latency better than three stages in one CTA (0.186 vs 0.242 ms at 8192x14336)
     static constexpr int STAGES = (PRO == PRO_SILU || PRO == PRO_SILU_BWD) ? 1 : 3;
@@ -320,7 +347,12 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
         const uint32_t bar = smem_u32(&full_bar[st]);
         uint8_t* dst = stages + st * PS::STAGE_BYTES;
         mbar_arrive_expect_tx(bar, PS::STAGE_BYTES);
-        if (PRO == PRO_SILU_BWD) {
+        if (PRO == PRO_DEQUANT) {
+            // the code tile and the 128 row scales of its column block (one bulk copy:
+            // 512 bytes at a 16-byte-aligned offset, since M is a multiple of 128)
+            tma_load_2d(smem_u32(dst), &tmx, bar, (int)k0, (int)m0, 0);
+            bulk_load_1d(smem_u32(dst + 128 * 128), a.xs + tt * a.M + m0, 128 * 4, bar);
+        } else if (PRO == PRO_SILU_BWD) {
             // output column tile k0 is dg (k0 < I) or du (k0 >= I) of source column block j0:
             // the gate tile, the up tile and the tile of dh of that block
             const int64_t half_k = a.K / 2;
@@ -791,10 +823,24 @@ static cudaError_t tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 2-D tensor map of a code matrix [rows][cols] bytes (rows contiguous), 128x128 boxes.
+static cudaError_t tmap_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols};
+    cuuint32_t box[2] = {128u, 128u};
+    cuuint32_t es[2] = {1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int PRO, bool ROW_OUT, bool COL_OUT>
 static cudaError_t launch_panel_t(const PanelArgs& a, int64_t in_cols, int cluster, cudaStream_t st) {
     CUtensorMap tm, tm2;
-    cudaError_t e = tmap_bf16(&tm, a.x, a.M, in_cols, a.ldx);
+    cudaError_t e = PRO == PRO_DEQUANT ? tmap_u8(&tm, a.x, a.M, in_cols) : tmap_bf16(&tm, a.x, a.M, in_cols, a.ldx);
     if (e != cudaSuccess) return e;
     if (PRO == PRO_SILU_BWD) {
         e = tmap_bf16(&tm2, a.x2, a.M, a.K / 2, a.K / 2);
@@ -868,6 +914,15 @@ cudaError_t launch_silu_mul_bwd_quant(const uint16_t* gu, const uint16_t* dh, in
     a.timeout_ns = timeout_ns;
     if (qT) return launch_panel_t<PRO_SILU_BWD, true, true>(a, 2 * I, 0, st);
     return launch_panel_t<PRO_SILU_BWD, true, false>(a, 2 * I, 0, st);
+}
+
+// 128x1 WGrad operand rebuilt from the saved 1x128 codes and scales of X
+cudaError_t launch_requant_128x1(const uint8_t* q, const float* s, int64_t M, int64_t K, uint8_t* qT, float* sT,
+                                 uint64_t timeout_ns, cudaStream_t st) {
+    PanelArgs a = {};
+    a.x = reinterpret_cast<const uint16_t*>(q); a.ldx = K; a.xs = s; a.M = M; a.K = K; a.qT = qT; a.sT = sT;
+    a.timeout_ns = timeout_ns;
+    return launch_panel_t<PRO_DEQUANT, false, true>(a, K, 0, st);
 }
 
 // Number of CTAs that split one 128-row panel of an RMSNorm along K: the largest divisor

@@ -126,6 +126,22 @@ def quantize_128x1(x: torch.Tensor):
     return qT, sT
 
 
+def requantize_128x1(q: torch.Tensor, s: torch.Tensor):
+    """From a saved 1x128 quantization (q u8 [M,K], s f32 [K/128,M]): the 128x1 WGrad operand
+    of the dequantized BF16 activation, transposed: (qT u8 [K,M], sT f32 [M/128,K])."""
+    _require(q, torch.uint8, "q")
+    _require(s, torch.float32, "s", q.device)
+    _contig(q, "q")
+    _contig(s, "s")
+    M, K = q.shape
+    dev = q.device
+    qT = torch.empty((K, M), dtype=torch.uint8, device=dev)
+    sT = torch.empty((M // 128, K), dtype=torch.float32, device=dev)
+    check(lib().fp8rl_requantize_128x1(_ptr(q), _ptr(s), M, K, _ptr(qT), _ptr(sT), _stream(dev)),
+          "fp8rl_requantize_128x1")
+    return qT, sT
+
+
 def quantize_128x128(w: torch.Tensor, transpose: bool = True):
     """w bf16 [N,K] -> (q u8 [N,K], s f32 [N/128,K/128], qT u8 [K,N] or None)."""
     _require(w, torch.bfloat16, "w")

@@ -125,6 +125,16 @@ FP8RL_API fp8rl_status fp8rl_quantize_1x128(const uint16_t* x, int64_t M, int64_
 FP8RL_API fp8rl_status fp8rl_quantize_128x1(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
                                   uint8_t* qT, float* sT, fp8rl_stream_t stream);
 
+/* 128x1 WGrad operand rebuilt from a saved 1x128 quantization (the memory-saving variant of
+ * "Quantization Scheme": the activation saved for the backward pass is its FP8 form).
+ *   q : E4M3 [M][K], s : float [K/128][M]  (an fp8rl_quantize_1x128 output)
+ *   x^ = bf16_rne( fl32(decode(q) * s) ) is quantized 128x1 along M, transposed:
+ *   qT : E4M3 [K][M], sT : float [M/128][K].  M % 128 == 0, K % 128 == 0.
+ * The result differs from fp8rl_quantize_128x1 of the original BF16 X by the 1x128
+ * rounding error it starts from. */
+FP8RL_API fp8rl_status fp8rl_requantize_128x1(const uint8_t* q, const float* s, int64_t M, int64_t K,
+                                              uint8_t* qT, float* sT, fp8rl_stream_t stream);
+
 /* Weight quantization, 128x128 blocks (re-run from the BF16 master weights after each
  * optimizer step: "Core architecture", master weights stay BF16).
  *   w : BF16 [N][ldw];  q : E4M3 [N][K];  s : float [N/128][K/128]
