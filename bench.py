@@ -349,6 +349,55 @@ def kernel_table(per_ms, flops, qbytes, fp8_peak, hbm):
     return kern
 
 
+def backward_ops_table(dev, hbm, reps=10):
+    """The operators either side of the gradient quantizer at the 32B layer's sizes (16384
+    tokens): SiLU-mul backward into the dual-quantized gate_up gradient, RMSNorm backward,
+    and the 128x1 WGrad operand re-quantized from a saved 1x128 activation.  Algorithmic
+    HBM bytes per launch; times from CUDA events over `reps` back-to-back launches."""
+    import torch
+    from block_scaled_fp8_x1_gb300 import ops, synth
+    M, H, I = M32, H32, LIN32["down"][1]
+    rows = {}
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    gu = synth.normal_bf16((M, 2 * I), 2.0, 101, dev)
+    dh = synth.normal_bf16((M, I), 1e-3, 102, dev)
+    ms = timed(lambda: ops.silu_mul_bwd_quant(gu, dh))
+    by = 2 * M * 2 * I + 2 * M * I + 2 * M * 2 * I + 8 * M * 2 * I / 128
+    rows["silu_mul_bwd_quant"] = {"shape": [M, I], "ms": round(ms, 4), "GB/s": round(by / ms / 1e6, 1),
+                                  "frac_hbm": round(by / ms / 1e6 / hbm, 3)}
+    del gu, dh
+    x = synth.normal_bf16((M, H), 1.0, 103, dev)
+    dy = synth.normal_bf16((M, H), 1e-3, 104, dev)
+    g = torch.ones(H, dtype=torch.bfloat16, device=dev)
+    _, _, _, _, rstd = ops.rmsnorm_quant(x, g, 1e-5, dual=False)
+    ms = timed(lambda: ops.rmsnorm_bwd(x, g, rstd, dy))
+    by = 2 * 2 * M * H + 2 * M * H + 4 * M + 2 * H + 4 * H
+    rows["rmsnorm_bwd"] = {"shape": [M, H], "ms": round(ms, 4), "GB/s": round(by / ms / 1e6, 1),
+                           "frac_hbm": round(by / ms / 1e6 / hbm, 3)}
+    for K in (H, I):
+        xk = synth.normal_bf16((M, K), 1.0, 105, dev)
+        q, sc = ops.quantize_1x128(xk)
+        del xk
+        ms = timed(lambda: ops.requantize_128x1(q, sc))
+        by = 2 * M * K + 8 * M * K / 128
+        rows[f"requantize_128x1_k{K}"] = {"shape": [M, K], "ms": round(ms, 4), "GB/s": round(by / ms / 1e6, 1),
+                                          "frac_hbm": round(by / ms / 1e6 / hbm, 3)}
+        del q, sc
+    torch.cuda.empty_cache()
+    return rows
+
+
 def decode_table(dev, fp8_peak, hbm, reps=40):
     """Qwen2.5-7B decode linears at M in {64, 128, 256}: the fused linear (activation
     quantization, then the decode GEMM) per call, timed as CUDA-graph replays of `reps` calls that cycle through
@@ -571,6 +620,7 @@ def run_gpu(args):
         del s8
         torch.cuda.empty_cache()
         extra["qwen7b_decode"] = decode_table(dev, fp8_peak, hbm)
+        extra["backward_ops_32b"] = backward_ops_table(dev, hbm)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -744,7 +794,7 @@ def run_kernel(args):
     if k.startswith("gemm"):
         M, N, K = dims
         var = {"auto": _abi.FP8RL_VARIANT_AUTO, "tiled": _abi.FP8RL_VARIANT_TILED,
-               "pair": _abi.FP8RL_VARIANT_PAIR}[args.variant]
+               "pair": _abi.FP8RL_VARIANT_PAIR, "decode": _abi.FP8RL_VARIANT_DECODE}[args.variant]
         if k == "gemm_wgrad":
             a = ops.quantize_128x1(synth.normal_bf16((M, N), 1e-3, 1, dev))
             b = ops.quantize_128x1(synth.normal_bf16((M, K), 1.0, 2, dev))
@@ -758,7 +808,7 @@ def run_kernel(args):
             else:
                 qw, sw, _ = ops.quantize_128x128(synth.normal_bf16((N, K), 0.02, 2, dev), transpose=False)
                 if k == "gemm_decode":
-                    var = _abi.FP8RL_VARIANT_SPLITK
+                    var = _abi.FP8RL_VARIANT_DECODE if args.variant == "decode" else _abi.FP8RL_VARIANT_SPLITK
                 # decode streams each layer's weights once: cycle through copies that together
                 # exceed L2 so that back-to-back launches read HBM, not L2
                 ncopy = max(1, -(-(256 << 20) // (N * K))) if k == "gemm_decode" else 1
@@ -825,8 +875,9 @@ def main():
     ap.add_argument("--shape", default=None, help="M,N,K (GEMMs) or M,K (quantizers)")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--tile-n", type=int, default=0, help="tiled forward GEMM tile width (128/256)")
-    ap.add_argument("--variant", default="auto", choices=["auto", "tiled", "pair"],
-                    help="GEMM form for --kernel gemm_fwd/gemm_dgrad/gemm_wgrad")
+    ap.add_argument("--variant", default="auto", choices=["auto", "tiled", "pair", "decode"],
+                    help="GEMM form for --kernel gemm_fwd/gemm_dgrad/gemm_wgrad; gemm_decode: "
+                         "decode (weights on the MMA's M side) or the split-K form (default)")
     ap.add_argument("--epi", type=int, default=0, help="paired form: epilogue warps per CTA (8/16)")
     args = ap.parse_args()
     if args.kernel:
