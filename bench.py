@@ -247,16 +247,16 @@ class Layer32Step:
         acts = {}
         q, s, qT, sT, _ = ops.rmsnorm_quant(self.x_attn, self.gamma, self.eps); mark("rmsnorm_quant_attn")
         acts["qkv"] = (q, s, qT, sT)
-        qkv = ops.gemm_fwd(q, s, qw["qkv"][0], qw["qkv"][1], variant=V.FP8RL_VARIANT_TILED); mark("fwd_qkv")
+        qkv = ops.gemm_fwd(q, s, qw["qkv"][0], qw["qkv"][1]); mark("fwd_qkv")
         q, s, qT, sT = ops.quantize_1x128(self.attn_out, dual=True); mark("dq_attn_out")
         acts["o"] = (q, s, qT, sT)
-        o = ops.gemm_fwd(q, s, qw["o"][0], qw["o"][1], variant=V.FP8RL_VARIANT_TILED); mark("fwd_o")
+        o = ops.gemm_fwd(q, s, qw["o"][0], qw["o"][1]); mark("fwd_o")
         q, s, qT, sT, _ = ops.rmsnorm_quant(self.x_mlp, self.gamma, self.eps); mark("rmsnorm_quant_mlp")
         acts["gate_up"] = (q, s, qT, sT)
-        gu = ops.gemm_fwd(q, s, qw["gate_up"][0], qw["gate_up"][1], variant=V.FP8RL_VARIANT_TILED); mark("fwd_gate_up")
+        gu = ops.gemm_fwd(q, s, qw["gate_up"][0], qw["gate_up"][1]); mark("fwd_gate_up")
         acts["down"] = ops.silu_mul_quant(gu); mark("silu_mul_quant")
         q, s = acts["down"][0], acts["down"][1]
-        y = ops.gemm_fwd(q, s, qw["down"][0], qw["down"][1], variant=V.FP8RL_VARIANT_TILED); mark("fwd_down")
+        y = ops.gemm_fwd(q, s, qw["down"][0], qw["down"][1]); mark("fwd_down")
         out = {"qkv": qkv, "o": o, "y": y}
         for n in ("down", "gate_up", "o", "qkv"):
             qd, sd, qdT, sdT = ops.quantize_1x128(self.dy[n], dual=True); mark(f"dq_dy_{n}")
@@ -293,9 +293,9 @@ class Mlp8Step:
         q_gu, s_gu, qT_gu = ops.quantize_128x128(self.w_gu); mark("wq_gate_up")
         q_d, s_d, qT_d = ops.quantize_128x128(self.w_d); mark("wq_down")
         qx, sx, qxT, sxT, rstd = ops.rmsnorm_quant(self.x, self.gamma, self.eps); mark("rmsnorm_quant")
-        gu = ops.gemm_fwd(qx, sx, q_gu, s_gu, variant=V.FP8RL_VARIANT_TILED); mark("fwd_gate_up")
+        gu = ops.gemm_fwd(qx, sx, q_gu, s_gu); mark("fwd_gate_up")
         qh, sh, qhT, shT = ops.silu_mul_quant(gu); mark("silu_mul_quant")
-        y = ops.gemm_fwd(qh, sh, q_d, s_d, variant=V.FP8RL_VARIANT_TILED); mark("fwd_down")
+        y = ops.gemm_fwd(qh, sh, q_d, s_d); mark("fwd_down")
         qdy, sdy, qdyT, sdyT = ops.quantize_1x128(self.dy_d, dual=True); mark("dq_dy_down")
         dh = ops.gemm_dgrad(qdy, sdy, qT_d, s_d); mark("dgrad_down")
         dw_d = ops.gemm_wgrad(qdyT, sdyT, qhT, shT); mark("wgrad_down")
@@ -798,13 +798,13 @@ def run_kernel(args):
         if k == "gemm_wgrad":
             a = ops.quantize_128x1(synth.normal_bf16((M, N), 1e-3, 1, dev))
             b = ops.quantize_128x1(synth.normal_bf16((M, K), 1.0, 2, dev))
-            fn = lambda: ops.gemm_wgrad(a[0], a[1], b[0], b[1], variant=var, epi_warps=args.epi)
+            fn = lambda: ops.gemm_wgrad(a[0], a[1], b[0], b[1], variant=var, epi_warps=args.epi, tile_n=args.tile_n)
         else:
             lhs_cols = N if k == "gemm_dgrad" else K
             qa, sa = ops.quantize_1x128(synth.normal_bf16((M, lhs_cols), 1.0, 1, dev))
             if k == "gemm_dgrad":
                 _, sw, qwT = ops.quantize_128x128(synth.normal_bf16((N, K), 0.02, 2, dev))
-                fn = lambda: ops.gemm_dgrad(qa, sa, qwT, sw, variant=var, epi_warps=args.epi)
+                fn = lambda: ops.gemm_dgrad(qa, sa, qwT, sw, variant=var, epi_warps=args.epi, tile_n=args.tile_n)
             else:
                 qw, sw, _ = ops.quantize_128x128(synth.normal_bf16((N, K), 0.02, 2, dev), transpose=False)
                 if k == "gemm_decode":
@@ -874,7 +874,7 @@ def main():
                          "quant_128x128")
     ap.add_argument("--shape", default=None, help="M,N,K (GEMMs) or M,K (quantizers)")
     ap.add_argument("--reps", type=int, default=3)
-    ap.add_argument("--tile-n", type=int, default=0, help="tiled forward GEMM tile width (128/256)")
+    ap.add_argument("--tile-n", type=int, default=0, help="GEMM tile width (128/256) of the tiled or paired form")
     ap.add_argument("--variant", default="auto", choices=["auto", "tiled", "pair", "decode"],
                     help="GEMM form for --kernel gemm_fwd/gemm_dgrad/gemm_wgrad; gemm_decode: "
                          "decode (weights on the MMA's M side) or the split-K form (default)")

@@ -195,9 +195,11 @@ int tiled_bn(int req) { return req == 128 ? 128 : 256; }
 
 fp8rl_status run_tiled(const TiledArgs& t, int grid_req, int bn_req, int num_sms, cudaStream_t st);
 
-// Paired-SM form (gemm_pair.cu): 256 x 128 tiles on clusters of two CTAs.  Returns
-// FP8RL_ERR_SHAPE, launching nothing, when a scale array cannot be moved by TMA.
-fp8rl_status run_pair(const TiledArgs& t, int clusters_req, int epi_req, int num_sms, cudaStream_t st) {
+// Paired-SM form (gemm_pair.cu): 256 x pn tiles (pn = 128 or 256) on clusters of two
+// CTAs.  Returns FP8RL_ERR_SHAPE, launching nothing, when a scale array cannot be moved by
+// TMA.
+fp8rl_status run_pair(const TiledArgs& t, int clusters_req, int epi_req, int pn_req, int num_sms, cudaStream_t st) {
+    const int pn = pn_req == 128 ? 128 : 256;
     GemmParams p = {};
     p.R1 = t.R1; p.R2 = t.R2; p.Kr = t.Kr;
     p.sa = t.sa; p.sa_kb = t.sa_kb;
@@ -206,14 +208,14 @@ fp8rl_status run_pair(const TiledArgs& t, int clusters_req, int epi_req, int num
     p.splits = 0;
     CUtensorMap tsa, tsb;
     fp8rl_status e = FP8RL_OK;
-    if (!scale_maps(p, t.b_mode, 128, false, &tsa, &tsb, &e)) return e != FP8RL_OK ? e : FP8RL_ERR_SHAPE;
+    if (!scale_maps(p, t.b_mode, pn, false, &tsa, &tsb, &e)) return e != FP8RL_OK ? e : FP8RL_ERR_SHAPE;
     if (t.ldc % 8 != 0) return FP8RL_ERR_ALIGN;
     CUtensorMap ta, tb, tc;
     if ((e = make_tmap(&ta, t.A, t.R1, t.Kr, t.Kr, 128)) != FP8RL_OK) return e;
-    if ((e = make_tmap(&tb, t.B, t.R2, t.Kr, t.Kr, 64)) != FP8RL_OK) return e;
+    if ((e = make_tmap(&tb, t.B, t.R2, t.Kr, t.Kr, pn / 2)) != FP8RL_OK) return e;
     if ((e = make_tmap_out(&tc, t.c, t.R1, t.R2, t.ldc)) != FP8RL_OK) return e;
     p.m_tiles = (int)((t.R1 + 127) / 128);
-    p.n_tiles = (int)((t.R2 + 127) / 128);
+    p.n_tiles = (int)((t.R2 + pn - 1) / pn);
     p.nkb = (int)(t.Kr / 128);
     const int items = ((p.m_tiles + 1) / 2) * p.n_tiles;
     p.num_items = items;
@@ -221,7 +223,7 @@ fp8rl_status run_pair(const TiledArgs& t, int clusters_req, int epi_req, int num
     int clusters = clusters_req > 0 ? clusters_req : num_sms / 2;
     clusters = std::max(1, std::min(clusters, items));
     const int epi = epi_req == 8 || epi_req == 16 ? epi_req : 8;
-    return cuda_status(launch_gemm_pair(ta, tb, tsa, tsb, tc, p, t.b_mode, epi, clusters, st));
+    return cuda_status(launch_gemm_pair(ta, tb, tsa, tsb, tc, p, t.b_mode, epi, pn, clusters, st));
 }
 
 // Whether every scale array of the problem can be moved by TMA (the paired form's need).
@@ -233,13 +235,21 @@ bool pair_eligible(const TiledArgs& t) {
     return t.sb_r == 1 && t.sb_kb % 4 == 0;
 }
 
-// The tiled forms: PAIR on request, else TILED.  AUTO takes the one-SM form: on the
-// training shapes of the 8B and 32B layers it measured 5-20% faster than the pairs (both
-// are bound by the same TMEM round trip, and the pairs pay for more synchronisation).
+// The tiled forms: PAIR or TILED on request.  AUTO takes 256 x 256 pair tiles for the
+// block-scaled GEMMs (forward, DGrad) when their scales can travel by TMA and the tiles
+// fill every pair of SMs at least once: per SM the tensor pipe then reads 32 KB of
+// operands per K-block instead of 48 KB, and on the 32B layer's forward and DGrad shapes
+// that measured 3-10% faster than the one-SM form.  WGrad (a scale per row of both
+// operands: a multiply and an FMA per element in the epilogue) stays on the one-SM form
+// with 16 epilogue warps, which measured 3-8% faster than the pairs there.
 fp8rl_status run_gemm(const TiledArgs& t, const fp8rl_gemm_opts* opts, int num_sms, cudaStream_t st) {
     const int variant = opts ? opts->variant : FP8RL_VARIANT_AUTO;
     if (variant == FP8RL_VARIANT_PAIR)
-        return pair_eligible(t) ? run_pair(t, opts->grid, opts->epi_warps, num_sms, st) : FP8RL_ERR_SHAPE;
+        return pair_eligible(t) ? run_pair(t, opts->grid, opts->epi_warps, opts->tile_n, num_sms, st) : FP8RL_ERR_SHAPE;
+    if (variant == FP8RL_VARIANT_AUTO && t.b_mode == SCALE_BLOCK && pair_eligible(t)) {
+        const int64_t pair_tiles = ((t.R1 + 255) / 256) * ((t.R2 + 255) / 256);
+        if (pair_tiles >= num_sms / 2) return run_pair(t, opts ? opts->grid : 0, 8, 256, num_sms, st);
+    }
     return run_tiled(t, opts ? opts->grid : 0, opts ? opts->tile_n : 0, num_sms, st);
 }
 

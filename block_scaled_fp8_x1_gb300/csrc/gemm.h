@@ -62,13 +62,14 @@ cudaError_t launch_gemm_splitk(const CUtensorMap& ta, const CUtensorMap& tb, con
                                const CUtensorMap* tsb, const GemmParams& p, int grid, cudaStream_t st);
 cudaError_t launch_debug_wait_timeout(uint64_t timeout_ns, cudaStream_t st);
 
-// gemm_pair.cu: the same GEMM on clusters of two CTAs (256 x 128 tiles, M = 256 MMAs).
-// ta: A map with 128 x 128-byte boxes; tb: B map with 64 x 128-byte boxes; tsa, tsb: the
-// scale maps of scale_maps() for a tile width of 128; tc: the BF16 output map.
-// p.m_tiles / p.n_tiles count 128-row / 128-column tiles; `clusters` persistent pairs.
+// gemm_pair.cu: the same GEMM on clusters of two CTAs (256 x pn tiles, M = 256 MMAs,
+// pn = 128 or 256).  ta: A map with 128 x 128-byte boxes; tb: B map with pn/2 x 128-byte
+// boxes; tsa, tsb: the scale maps of scale_maps() for a tile width of pn; tc: the BF16
+// output map.  p.m_tiles / p.n_tiles count 128-row / pn-column tiles; `clusters`
+// persistent pairs.
 cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                              const CUtensorMap& tsb, const CUtensorMap& tc, const GemmParams& p, int b_mode,
-                             int epi_warps, int clusters, cudaStream_t st);
+                             int epi_warps, int pn, int clusters, cudaStream_t st);
 fp8rl_status read_and_clear_pair_status();
 
 // decode.cu: decode-shaped forward GEMM (M <= 256 tokens), weights on the MMA's M side,

@@ -39,8 +39,9 @@ namespace fp8rl {
 
 namespace {
 
-constexpr int kPairN = 128;     // output columns of a pair tile
-constexpr int kPairBufs = 4;    // TMEM partial-sum buffers of 128 columns per CTA
+// A pair tile is 256 rows x PN columns (PN = 128 or 256); each CTA's TMEM holds 512/PN
+// partial-sum buffers of PN columns.
+__host__ __device__ constexpr int pair_bufs(int pn) { return 512 / pn; }
 
 __device__ __forceinline__ uint32_t cluster_id_x() {
     uint32_t r;
@@ -57,7 +58,7 @@ __device__ __forceinline__ uint32_t num_clusters_x() {
 // over the column tiles, so the clusters running at the same time reuse A and B through L2.
 struct PairTile {
     int mp;   // pair-row tile (256 rows)
-    int nt;   // column tile (128 columns)
+    int nt;   // column tile (PN columns)
 };
 
 __device__ __forceinline__ PairTile pair_tile(int m_pairs, int n_tiles, int item) {
@@ -83,32 +84,42 @@ static_assert(128 * pair_reg_lo(8) + 256 * pair_reg_hi(8) <= pair_threads(8) * p
 static_assert(128 * pair_reg_lo(16) + 512 * pair_reg_hi(16) <= pair_threads(16) * pair_launch_regs(16), "split");
 
 // Shared-memory plan of one CTA of the pair.
-template <int B_MODE, int STAGES>
+// BF16 output staging: each epilogue warp owns this many 2 KB boxes (32 x 32 BF16) and
+// cycles through them, so one box's TMA store overlaps the filling of the next.
+__host__ __device__ constexpr int pair_boxes(int epi) { return epi == 16 ? 1 : 2; }
+
+template <int B_MODE, int EPI, int STAGES, int PN>
 struct PairSmem {
     static constexpr int A_BYTES = 128 * 128;            // this CTA's 128 rows of A, one K-block
-    static constexpr int B_BYTES = (kPairN / 2) * 128;   // this CTA's half of B's rows
+    static constexpr int B_BYTES = (PN / 2) * 128;       // this CTA's half of B's rows
     static constexpr int SG = scale_group(B_MODE, false);
     static constexpr int NS = (B_MODE == SCALE_ROW) ? 8 : 4;   // scale-ring slots (groups)
     static constexpr int SLOT_A = 128 * SG;                    // floats
-    // B's scales: kPairN row scales per K-block, or a box of at most 16 block scales
+    // B's scales: PN row scales per K-block, or a box of at most 16 block scales
     // (padded so that every TMA destination starts on a 128-byte boundary)
-    static constexpr int SLOT_B = (B_MODE == SCALE_ROW) ? kPairN * SG : 32;
+    static constexpr int SLOT_B = (B_MODE == SCALE_ROW) ? PN * SG : 32;
     static constexpr int SLOT = SLOT_A + SLOT_B;
     static_assert((SLOT_A * 4) % 128 == 0 && (SLOT * 4) % 128 == 0, "TMA destinations 128-byte aligned");
     static constexpr int RING_BYTES = NS * SLOT * 4;
-    static constexpr int STAGE_C_BYTES = 128 * kPairN * 2;    // the CTA's BF16 tile, 32x32 boxes
-    static constexpr int NBARS = 2 * STAGES + 2 * kPairBufs + 2 * NS + 1;
+    static constexpr int STAGE_C_BYTES = EPI * pair_boxes(EPI) * 2048;   // [warp][box][32x32 BF16]
+    static constexpr int NBARS = 2 * STAGES + 2 * pair_bufs(PN) + 2 * NS + 1;
     static constexpr size_t BYTES = 1024 + (size_t)STAGES * (A_BYTES + B_BYTES) + STAGE_C_BYTES + RING_BYTES +
                                     NBARS * 8 + 16;
 };
 
-template <int B_MODE, int EPI, int STAGES>
+template <int B_MODE, int EPI, int STAGES, int PN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                 const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-    using S = PairSmem<B_MODE, STAGES>;
-    constexpr int COLS = kPairN / (EPI / 4);        // columns per epilogue thread: 64 or 32
+    using S = PairSmem<B_MODE, EPI, STAGES, PN>;
+    constexpr int kPairN = PN;
+    constexpr int kPairBufs = pair_bufs(PN);
+    constexpr int COLS = kPairN / (EPI / 4);        // columns per epilogue thread: 32 .. 128
+    // TMEM loads of 32 columns, LPW of them per wait: the partial and the accumulators of
+    // one thread stay within its registers
+    constexpr int LPW = EPI == 16 ? 1 : 2;
+    constexpr int NG = COLS / (32 * LPW);
     constexpr int NS = S::NS;
     constexpr uint32_t TMEM_COLS = 512;
     constexpr uint32_t IDESC = idesc_e4m3_f32(256, kPairN);
@@ -118,13 +129,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * S::A_BYTES;
-    uint8_t* stage_c = sB + STAGES * S::B_BYTES;                          // [32x32 box][2 KB]
+    uint8_t* stage_c = sB + STAGES * S::B_BYTES;                          // [warp][box][2 KB]
     float* ring = reinterpret_cast<float*>(stage_c + S::STAGE_C_BYTES);   // [NS][SLOT]
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ring) + S::RING_BYTES);
     uint64_t* full_bar = bars;                       // [STAGES] copies of both CTAs -> MMA (leader's)
     uint64_t* empty_bar = bars + STAGES;             // [STAGES] MMA -> copies (each CTA's own)
-    uint64_t* tfull_bar = bars + 2 * STAGES;         // [4] MMA -> epilogue (each CTA's own)
-    uint64_t* tempty_bar = tfull_bar + kPairBufs;    // [4] both epilogues -> MMA (leader's)
+    uint64_t* tfull_bar = bars + 2 * STAGES;         // [bufs] MMA -> epilogue (each CTA's own)
+    uint64_t* tempty_bar = tfull_bar + kPairBufs;    // [bufs] both epilogues -> MMA (leader's)
     uint64_t* sfull_bar = tempty_bar + kPairBufs;    // [NS] scale copies -> epilogue
     uint64_t* sempty_bar = sfull_bar + NS;           // [NS] epilogue -> scale copies
     uint64_t* drain_bar = sempty_bar + NS;           // [1] MMA completion at exit (leader)
@@ -214,8 +225,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
                                 tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, n0, kb, pol);
                             } else if (p.sb_kb == 1) {
                                 // block scales stored [column block][K-block]: 4 K-blocks of the
-                                // tile's one column block (x, a K-block index, is a multiple of 4)
-                                mbar_arrive_expect_tx(sb, a_bytes + 16u);
+                                // tile's PN/128 column blocks (x, a K-block index, is a multiple of 4)
+                                mbar_arrive_expect_tx(sb, a_bytes + 16u * (kPairN / 128));
                                 tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, kb, n0 >> 7, pol);
                             } else {
                                 // block scales stored [K-block][column block]: 4 column blocks
@@ -288,7 +299,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
         const int row_local = quad * 32 + lane;
         const uint32_t t_lane = (uint32_t)(quad * 32) << 16;
         const uint32_t tempty0 = mapa_shared(smem_u32(tempty_bar), 0);   // the leader's
-        uint32_t acc_it = 0, g_done = 0;
+        constexpr int NBX = pair_boxes(EPI);
+        uint32_t acc_it = 0, g_done = 0, box_it = 0;
         bool ok = true;
         for (int item = cid; ok && item < num_items; item += ncl) {
             const PairTile t = pair_tile(m_pairs, p.n_tiles, item);
@@ -311,42 +323,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
                 tc_fence_after();
                 const float* slot = ring + ss * S::SLOT;
                 const uint32_t tb = tmem_base + t_lane + ts * kPairN + col_base;
-                uint32_t r[COLS / 32][32];
-                #pragma unroll
-                for (int h = 0; h < COLS / 32; ++h) tmem_ld_32x32b_x32(tb + h * 32, r[h]);
-                #pragma unroll
-                for (int h = 0; h < COLS / 32; ++h) tmem_ld_wait(r[h]);
-                // the whole partial is in registers: hand the buffer back to the leader
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(tempty0 + 8 * ts);
                 const float fa = slot[q * 128 + row_local];
-                if constexpr (B_MODE == SCALE_ROW) {
-                    const float* sbv = slot + S::SLOT_A + q * kPairN + col_base;
-                    const float2 fa2 = make_float2(fa, fa);
+                float2 f2 = make_float2(fa, fa);
+                if constexpr (B_MODE != SCALE_ROW) {
+                    // the block scale of B for this thread's 128-column block
+                    const int cb = (t.nt * kPairN + col_base) >> 7;
+                    const float fb = (p.sb_kb == 1) ? slot[S::SLOT_A + (cb - ((t.nt * kPairN) >> 7)) * 4 + (kb & 3)]
+                                                    : slot[S::SLOT_A + q * 4 + (cb & 3)];
+                    f2 = make_float2(fa * fb, fa * fb);
+                }
+                const float* sbv = slot + S::SLOT_A + q * kPairN + col_base;   // B row scales (WGrad)
+                #pragma unroll
+                for (int g = 0; g < NG; ++g) {
+                    uint32_t r[LPW][32];
                     #pragma unroll
-                    for (int h = 0; h < COLS / 32; ++h) {
-                        #pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            const float4 sc = *reinterpret_cast<const float4*>(sbv + h * 32 + j);
-                            const float2 s01 = __fmul2_rn(fa2, make_float2(sc.x, sc.y));
-                            const float2 s23 = __fmul2_rn(fa2, make_float2(sc.z, sc.w));
-                            const int c = (h * 32 + j) / 2;
-                            acc[c] = __ffma2_rn(make_float2(__uint_as_float(r[h][j]), __uint_as_float(r[h][j + 1])), s01, acc[c]);
-                            acc[c + 1] = __ffma2_rn(make_float2(__uint_as_float(r[h][j + 2]), __uint_as_float(r[h][j + 3])), s23, acc[c + 1]);
+                    for (int h = 0; h < LPW; ++h) tmem_ld_32x32b_x32(tb + (g * LPW + h) * 32, r[h]);
+                    #pragma unroll
+                    for (int h = 0; h < LPW; ++h) tmem_ld_wait(r[h]);
+                    if (g == NG - 1) {
+                        // the whole partial is in registers: hand the buffer back to the leader
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(tempty0 + 8 * ts);
+                    }
+                    #pragma unroll
+                    for (int h = 0; h < LPW; ++h) {
+                        const int c0 = (g * LPW + h) * 32;   // first of these 32 columns
+                        if constexpr (B_MODE == SCALE_ROW) {
+                            #pragma unroll
+                            for (int j = 0; j < 32; j += 4) {
+                                const float4 sc = *reinterpret_cast<const float4*>(sbv + c0 + j);
+                                const float2 s01 = __fmul2_rn(f2, make_float2(sc.x, sc.y));
+                                const float2 s23 = __fmul2_rn(f2, make_float2(sc.z, sc.w));
+                                const int c = (c0 + j) / 2;
+                                acc[c] = __ffma2_rn(make_float2(__uint_as_float(r[h][j]), __uint_as_float(r[h][j + 1])), s01, acc[c]);
+                                acc[c + 1] = __ffma2_rn(make_float2(__uint_as_float(r[h][j + 2]), __uint_as_float(r[h][j + 3])), s23, acc[c + 1]);
+                            }
+                        } else {
+                            #pragma unroll
+                            for (int j = 0; j < 32; j += 2)
+                                acc[(c0 + j) / 2] = __ffma2_rn(make_float2(__uint_as_float(r[h][j]), __uint_as_float(r[h][j + 1])),
+                                                               f2, acc[(c0 + j) / 2]);
                         }
                     }
-                } else {
-                    const float fb = (p.sb_kb == 1) ? slot[S::SLOT_A + (kb & 3)]
-                                                    : slot[S::SLOT_A + q * 4 + ((t.nt * kPairN) >> 7 & 3)];
-                    const float f = fa * fb;
-                    const float2 f2 = make_float2(f, f);
-                    #pragma unroll
-                    for (int h = 0; h < COLS / 32; ++h)
-                        #pragma unroll
-                        for (int j = 0; j < 32; j += 2)
-                            acc[(h * 32 + j) / 2] = __ffma2_rn(make_float2(__uint_as_float(r[h][j]), __uint_as_float(r[h][j + 1])),
-                                                               f2, acc[(h * 32 + j) / 2]);
                 }
                 if (g_last) {
                     __syncwarp();
@@ -356,16 +375,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
             }
             if (!ok) break;
 
-            // ---- the warp's 32 rows x COLS columns go out as 32 x 32 BF16 boxes, each in
-            // its own 2 KB of the staging area (64-byte swizzle: the 16-byte chunk c of row
-            // r sits at chunk c ^ ((r >> 1) & 3)), written by TMA, which clips rows and
-            // columns outside C.  The previous tile's boxes have left the buffers first.
-            if (lane == 0) bulk_wait_read<0>();
-            __syncwarp();
+            // ---- the warp's 32 rows x COLS columns go out as 32 x 32 BF16 boxes, staged in
+            // the warp's own 2 KB buffers in turn (64-byte swizzle: the 16-byte chunk c of row
+            // r sits at chunk c ^ ((r >> 1) & 3)) and written by TMA, which clips rows and
+            // columns outside C.  One bulk group per box: before a buffer is refilled, the
+            // store that last read it has finished reading.
             const int y0 = t.mp * 256 + (int)rank * 128 + quad * 32;
             #pragma unroll
-            for (int b = 0; b < COLS / 32; ++b) {
-                const uint32_t buf = smem_u32(stage_c + (ew * (COLS / 32) + b) * 2048);
+            for (int b = 0; b < COLS / 32; ++b, ++box_it) {
+                const uint32_t buf = smem_u32(stage_c + (ew * NBX + (int)(box_it % NBX)) * 2048);
+                if (lane == 0) bulk_wait_read<NBX - 1>();
+                __syncwarp();
                 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int cc = b * 32 + c * 8;    // first of these 8 columns
@@ -376,16 +396,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
                     v.w = pack_bf16x2(acc[cc / 2 + 3].x, acc[cc / 2 + 3].y);
                     st_shared_v4(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), v);
                 }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0 && y0 < p.R1) {
-                #pragma unroll
-                for (int b = 0; b < COLS / 32; ++b) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
                     const int x = t.nt * kPairN + col_base + b * 32;
-                    if (x < p.R2) tma_store_2d(&tmC, smem_u32(stage_c + (ew * (COLS / 32) + b) * 2048), x, y0);
+                    if (y0 < p.R1 && x < p.R2) tma_store_2d(&tmC, buf, x, y0);
+                    bulk_commit();
                 }
-                bulk_commit();
             }
         }
         if (lane == 0) bulk_wait_all();   // tile stores complete before exit
@@ -401,12 +418,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
     }
 }
 
-template <int B_MODE, int EPI, int STAGES>
+template <int B_MODE, int EPI, int STAGES, int PN>
 cudaError_t launch_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                           const CUtensorMap& tsb, const CUtensorMap& tc, const GemmParams& p, int clusters,
                           cudaStream_t st) {
-    auto kern = k_gemm_pair<B_MODE, EPI, STAGES>;
-    constexpr size_t smem = PairSmem<B_MODE, STAGES>::BYTES;
+    auto kern = k_gemm_pair<B_MODE, EPI, STAGES, PN>;
+    constexpr size_t smem = PairSmem<B_MODE, EPI, STAGES, PN>::BYTES;
     static_assert(smem <= 227 * 1024, "shared memory budget");
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -417,18 +434,27 @@ cudaError_t launch_pair_t(const CUtensorMap& ta, const CUtensorMap& tb, const CU
 }  // namespace
 
 // Launch contract (checked by the caller): A's tensor map has 128 x 128-byte boxes, B's
-// 64 x 128-byte boxes; tsa is A's row-scale map with boxes of 128 x min(4 or 1, K-blocks);
-// tsb B's scale map as for the one-SM kernel with a tile width of 128; tc the BF16 output
-// map (32 x 32 boxes).  p.m_tiles counts 128-row tiles, p.n_tiles 128-column tiles.
+// pn/2 x 128-byte boxes; tsa is A's row-scale map with boxes of 128 x min(4 or 1,
+// K-blocks); tsb B's scale map as for the one-SM kernel with a tile width of pn; tc the
+// BF16 output map (32 x 32 boxes).  p.m_tiles counts 128-row tiles, p.n_tiles pn-column
+// tiles.  pn is 128 or 256.
 cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                              const CUtensorMap& tsb, const CUtensorMap& tc, const GemmParams& p, int b_mode,
-                             int epi_warps, int clusters, cudaStream_t st) {
-    if (b_mode == SCALE_ROW) {
-        if (epi_warps == 8) return launch_pair_t<SCALE_ROW, 8, 7>(ta, tb, tsa, tsb, tc, p, clusters, st);
-        return launch_pair_t<SCALE_ROW, 16, 7>(ta, tb, tsa, tsb, tc, p, clusters, st);
+                             int epi_warps, int pn, int clusters, cudaStream_t st) {
+    if (pn == 256) {
+        if (b_mode == SCALE_ROW) {
+            if (epi_warps == 8) return launch_pair_t<SCALE_ROW, 8, 5, 256>(ta, tb, tsa, tsb, tc, p, clusters, st);
+            return launch_pair_t<SCALE_ROW, 16, 5, 256>(ta, tb, tsa, tsb, tc, p, clusters, st);
+        }
+        if (epi_warps == 16) return launch_pair_t<SCALE_BLOCK, 16, 5, 256>(ta, tb, tsa, tsb, tc, p, clusters, st);
+        return launch_pair_t<SCALE_BLOCK, 8, 5, 256>(ta, tb, tsa, tsb, tc, p, clusters, st);
     }
-    if (epi_warps == 16) return launch_pair_t<SCALE_BLOCK, 16, 7>(ta, tb, tsa, tsb, tc, p, clusters, st);
-    return launch_pair_t<SCALE_BLOCK, 8, 7>(ta, tb, tsa, tsb, tc, p, clusters, st);
+    if (b_mode == SCALE_ROW) {
+        if (epi_warps == 8) return launch_pair_t<SCALE_ROW, 8, 7, 128>(ta, tb, tsa, tsb, tc, p, clusters, st);
+        return launch_pair_t<SCALE_ROW, 16, 7, 128>(ta, tb, tsa, tsb, tc, p, clusters, st);
+    }
+    if (epi_warps == 16) return launch_pair_t<SCALE_BLOCK, 16, 7, 128>(ta, tb, tsa, tsb, tc, p, clusters, st);
+    return launch_pair_t<SCALE_BLOCK, 8, 7, 128>(ta, tb, tsa, tsb, tc, p, clusters, st);
 }
 
 // Reads and clears this translation unit's device status word (the pair kernel's bounded

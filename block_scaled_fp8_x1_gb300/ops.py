@@ -295,28 +295,28 @@ def gemm_fwd(qx, sx, qw, sw, out=None, variant: int = _abi.FP8RL_VARIANT_AUTO, s
 
 
 def gemm_dgrad(qdy, sdy, qwT, sw, out=None, variant: int = _abi.FP8RL_VARIANT_AUTO,
-               grid: int = 0, epi_warps: int = 0):
+               grid: int = 0, epi_warps: int = 0, tile_n: int = 0):
     """dX = dY W: qdy [M,N], sdy [N/128,M], qwT [K,N], sw [N/128,K/128] -> dx bf16 [M,K]."""
     _check_gemm_inputs(qdy, sdy, qwT, sw)
     M, N = qdy.shape
     K = qwT.shape[0]
     dev = qdy.device
     dx = out if out is not None else torch.empty((M, K), dtype=torch.bfloat16, device=dev)
-    opts = GemmOpts(int(variant), 0, int(grid), 0, int(epi_warps))
+    opts = GemmOpts(int(variant), 0, int(grid), int(tile_n), int(epi_warps))
     check(lib().fp8rl_gemm_dgrad_ex(_ptr(qdy), _ptr(sdy), _ptr(qwT), _ptr(sw), _ptr(dx), M, N, K,
                                     None, 0, ctypes.byref(opts), _stream(dev)), "fp8rl_gemm_dgrad_ex")
     return dx
 
 
 def gemm_wgrad(qdyT, sdyT, qxT, sxT, out=None, variant: int = _abi.FP8RL_VARIANT_AUTO,
-               grid: int = 0, epi_warps: int = 0):
+               grid: int = 0, epi_warps: int = 0, tile_n: int = 0):
     """dW = dY^T X: qdyT [N,M], sdyT [M/128,N], qxT [K,M], sxT [M/128,K] -> dw bf16 [N,K]."""
     _check_gemm_inputs(qdyT, sdyT, qxT, sxT)
     N, M = qdyT.shape
     K = qxT.shape[0]
     dev = qdyT.device
     dw = out if out is not None else torch.empty((N, K), dtype=torch.bfloat16, device=dev)
-    opts = GemmOpts(int(variant), 0, int(grid), 0, int(epi_warps))
+    opts = GemmOpts(int(variant), 0, int(grid), int(tile_n), int(epi_warps))
     check(lib().fp8rl_gemm_wgrad_ex(_ptr(qdyT), _ptr(sdyT), _ptr(qxT), _ptr(sxT), _ptr(dw), M, N,
                                     K, None, 0, ctypes.byref(opts), _stream(dev)), "fp8rl_gemm_wgrad_ex")
     return dw

@@ -215,10 +215,11 @@ typedef enum { FP8RL_OP_FWD = 0, FP8RL_OP_DGRAD = 1, FP8RL_OP_WGRAD = 2 } fp8rl_
  * it needs fp8rl_gemm_workspace_bytes(FP8RL_OP_FWD, M, N, K) bytes of workspace (no
  * initial contents required; calls that overlap in time need separate workspaces).  A
  * size of 0 means ws may be NULL.
- * Larger M takes the one-SM tiled form (FP8RL_VARIANT_TILED); the paired-SM form
- * (FP8RL_VARIANT_PAIR) is available on request when every scale array can be moved by TMA:
- * M % 4 == 0 and (K/128) % 4 == 0 for the forward GEMM, M % 4 == 0 and (K/128) % 4 == 0
- * on the weight's block-scale rows for DGrad, always for WGrad. */
+ * Larger M takes the paired-SM form (FP8RL_VARIANT_PAIR, 256 x 256 tiles) when every
+ * scale array can be moved by TMA -- M % 4 == 0 and (K/128) % 4 == 0 for the forward GEMM,
+ * M % 4 == 0 and (K/128) % 4 == 0 on the weight's block-scale rows for DGrad -- and its
+ * tiles cover every pair of SMs at least once; otherwise the one-SM tiled form
+ * (FP8RL_VARIANT_TILED).  WGrad takes the one-SM form (PAIR on request). */
 FP8RL_API fp8rl_status fp8rl_gemm_fwd(const uint8_t* qx, const float* sx, const uint8_t* qw,
                             const float* sw, uint16_t* y, int64_t M, int64_t N, int64_t K,
                             void* ws, size_t ws_bytes, fp8rl_stream_t stream);
@@ -250,8 +251,9 @@ typedef enum {
     FP8RL_VARIANT_TILED = 1,  /* one SM per output tile: persistent 128 x BN tiles */
     FP8RL_VARIANT_SPLITK = 2, /* decode-shaped: the reduction of each 128x256 output tile
                                  is split over `splits` CTAs (forward only, M <= 256) */
-    FP8RL_VARIANT_PAIR = 3,   /* two SMs per output tile: persistent 256 x 128 tiles on
-                                 clusters of two CTAs (M = 256 tensor-core MMAs); needs
+    FP8RL_VARIANT_PAIR = 3,   /* two SMs per output tile: persistent 256 x 256 (or, with
+                                 tile_n = 128, 256 x 128) tiles on clusters of two CTAs
+                                 (M = 256 tensor-core MMAs); needs
                                  scale arrays whose rows are multiples of 16 bytes (the
                                  rule under fp8rl_gemm_fwd), else FP8RL_ERR_SHAPE */
     FP8RL_VARIANT_DECODE = 4  /* forward only, M <= 256: weights on the MMA's M side (one
@@ -266,7 +268,8 @@ typedef struct {
     int splits;     /* SPLITK: number of reduction slices (0 = choose); ignored otherwise */
     int grid;       /* TILED: persistent CTAs (0 = one per SM); PAIR: persistent clusters
                        (0 = one per two SMs); ignored otherwise */
-    int tile_n;     /* TILED: output tile width, 128 or 256 (0 = choose); ignored otherwise */
+    int tile_n;     /* TILED: output tile width, 128 or 256 (0 = choose); PAIR: the pair
+                       tile's width, 128 or 256 (0 = 256); ignored otherwise */
     int epi_warps;  /* PAIR: epilogue warps per CTA, 8 or 16 (0 = choose); ignored otherwise */
 } fp8rl_gemm_opts;
 

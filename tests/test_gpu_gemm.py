@@ -178,19 +178,22 @@ def test_tiled_deterministic_and_grid_independent(fp8lib, oracle, variant):
 
 
 # ------------------------------------------------------------------ paired-SM form
-# 256 x 128 output tiles on clusters of two CTAs.  Row counts that are not multiples of
-# 256 leave the second CTA of the last pair partly or wholly outside A (TMA zero fill,
-# clipped stores); grid = clusters, so small grids make each cluster walk many tiles.
+# 256 x 128 and 256 x 256 output tiles on clusters of two CTAs.  Row counts that are not
+# multiples of 256 leave the second CTA of the last pair partly or wholly outside A, and
+# column counts that are not multiples of the tile width leave B's second half partly or
+# wholly outside B (TMA zero fill, clipped stores); grid = clusters, so small grids make
+# each cluster walk many tiles.
 
 @pytest.mark.parametrize("M,N,K", [(256, 128, 512), (128, 256, 512), (300, 384, 512),
                                    (1000, 1280, 1024), (132, 128, 2048), (520, 640, 1536)])
 @pytest.mark.parametrize("epi", [8, 16])
-def test_fwd_pair(fp8lib, oracle, M, N, K, epi):
+@pytest.mark.parametrize("pn", [128, 256])
+def test_fwd_pair(fp8lib, oracle, M, N, K, epi, pn):
     qx, sx, qw, sw, _ = fwd_operands(fp8lib, oracle, M, N, K, M + N + K + epi)
     ref = oracle.gemm(u8(qx), f32(sx), u8(qw), f32(sw), "fwd")
     for grid in (0, 2):
-        y = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_PAIR, epi_warps=epi, grid=grid)
-        gemm_tolerance_check(bits16(y), ref, f"pair fwd {M}x{N}x{K} epi {epi} grid {grid}")
+        y = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_PAIR, epi_warps=epi, grid=grid, tile_n=pn)
+        gemm_tolerance_check(bits16(y), ref, f"pair fwd {M}x{N}x{K} epi {epi} grid {grid} tile {pn}")
     assert fp8lib.check_status() == _abi.FP8RL_OK
 
 
@@ -203,23 +206,27 @@ def test_dgrad_pair(fp8lib, oracle, M, N, K):
     qdy, sdy = fp8lib.quantize_1x128(dy)
     _, sw, qwT = fp8lib.quantize_128x128(w)
     ref = oracle.gemm(u8(qdy), f32(sdy), u8(qwT), f32(sw), "dgrad")
-    for v, grid in ((_abi.FP8RL_VARIANT_PAIR, 0), (_abi.FP8RL_VARIANT_PAIR, 3), (_abi.FP8RL_VARIANT_TILED, 0)):
-        dx = fp8lib.gemm_dgrad(qdy, sdy, qwT, sw, variant=v, grid=grid)
-        gemm_tolerance_check(bits16(dx), ref, f"dgrad {M}x{N}x{K} variant {v} grid {grid}")
+    for v, grid, pn in ((_abi.FP8RL_VARIANT_PAIR, 0, 128), (_abi.FP8RL_VARIANT_PAIR, 3, 128),
+                        (_abi.FP8RL_VARIANT_PAIR, 0, 256), (_abi.FP8RL_VARIANT_PAIR, 3, 256),
+                        (_abi.FP8RL_VARIANT_TILED, 0, 0)):
+        dx = fp8lib.gemm_dgrad(qdy, sdy, qwT, sw, variant=v, grid=grid, tile_n=pn)
+        gemm_tolerance_check(bits16(dx), ref, f"dgrad {M}x{N}x{K} variant {v} grid {grid} tile {pn}")
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 512), (1024, 256, 768),
                                    (384, 640, 1152)])
 @pytest.mark.parametrize("epi", [8, 16])
-def test_wgrad_pair(fp8lib, oracle, M, N, K, epi):
+@pytest.mark.parametrize("pn", [128, 256])
+def test_wgrad_pair(fp8lib, oracle, M, N, K, epi, pn):
     dy = synth.normal_bf16((M, N), 1e-3, M + 41 + epi, "cuda")
     x = synth.normal_bf16((M, K), 1.0, K + 43, "cuda", outlier_channels=2, outlier_scale=30.0)
     qdyT, sdyT = fp8lib.quantize_128x1(dy)
     qxT, sxT = fp8lib.quantize_128x1(x)
     ref = oracle.gemm(u8(qdyT), f32(sdyT), u8(qxT), f32(sxT), "wgrad")
     for grid in (0, 2):
-        dw = fp8lib.gemm_wgrad(qdyT, sdyT, qxT, sxT, variant=_abi.FP8RL_VARIANT_PAIR, epi_warps=epi, grid=grid)
-        gemm_tolerance_check(bits16(dw), ref, f"pair wgrad {M}x{N}x{K} epi {epi} grid {grid}")
+        dw = fp8lib.gemm_wgrad(qdyT, sdyT, qxT, sxT, variant=_abi.FP8RL_VARIANT_PAIR, epi_warps=epi, grid=grid,
+                               tile_n=pn)
+        gemm_tolerance_check(bits16(dw), ref, f"pair wgrad {M}x{N}x{K} epi {epi} grid {grid} tile {pn}")
     dw = fp8lib.gemm_wgrad(qdyT, sdyT, qxT, sxT, variant=_abi.FP8RL_VARIANT_TILED)
     gemm_tolerance_check(bits16(dw), ref, f"one-SM wgrad {M}x{N}x{K}")
 
