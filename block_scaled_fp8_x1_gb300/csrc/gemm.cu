@@ -10,7 +10,7 @@
 //           P_kb = sum_{k in block kb} A[r1, k] * B[r2, k]      (E4M3 x E4M3, FP32)
 // with A [R1, Kr] and B [R2, Kr] stored K-major (reduction dimension contiguous).
 //
-// Structure (one CTA of 640 threads per SM, persistent over work items):
+// Structure (one CTA of 384 threads per SM, persistent over work items):
 //   warp 0      copies (lane 0): TMA loads of the 128x128 A tile and the BNx128 B tile of
 //               each K-block into a STAGES-deep shared-memory ring (128-byte swizzle); when
 //               B has one scale per row (WGrad), also that K-block's BN scales of B into an
@@ -20,11 +20,12 @@
 //               block), so the tensor pipe runs up to 512/BN - 1 blocks ahead of the
 //               epilogue.
 //   warps 2-3   idle (they complete warpgroup 0, whose registers go to the epilogue).
-//   warps 4-19  epilogue, four warps per TMEM lane quadrant, each owning 32 rows x BN/4
+//   warps 4-11  epilogue, two warps per TMEM lane quadrant, each owning 32 rows x BN/2
 //               columns: per K-block, load the FP32 partial from TMEM, release the buffer,
 //               and promote it into FP32 registers with the block's scales ("per-block
-//               scale promotion"); the row scales of A (and the block scales of B) are read
-//               from global memory a few K-blocks ahead.  Finally round to BF16 and store,
+//               scale promotion"); the scales arrive in the scale ring (or, when they
+//               cannot travel by TMA, each thread copies its own a few K-blocks ahead).
+//               Finally round to BF16 and store,
 //               or, in the split-K form, store FP32 partials and let the last CTA of a tile
 //               sum them in split order (deterministic, no spin-wait).
 // Every mbarrier wait is bounded; on timeout the CTA records FP8RL_ERR_DEVICE_TIMEOUT,
@@ -72,20 +73,17 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 }
 
 // 4 warps (copies, MMA, two idle) + epi_warps() epilogue warps, a quarter of them per SM
-// sub-partition (one warp's TMEM loads do not overlap each other, so the read rate grows
-// with the warps).  Row-scaled B (WGrad) does a multiply and an FMA per element and gains
-// from 16 warps; the block-scaled forms run faster with 8, which leaves each thread 224
-// registers.  Register split: warpgroup 0 drops to reg_lo(), the epilogue rises to
-// reg_hi(), within the launch_regs() per thread the CTA is launched with.
-__host__ __device__ constexpr int epi_warps(int b_mode) { return b_mode == SCALE_ROW ? 16 : 8; }
+// sub-partition.  With 8 the epilogue threads get 224 registers: room for a 128-column
+// accumulator and a partial in flight.  (16 warps of 112 registers measured no faster for
+// the row-scaled form and 25% more instructions.)  Register split: warpgroup 0 drops to
+// reg_lo(), the epilogue rises to reg_hi(), within the launch_regs() per thread the CTA is
+// launched with.
+__host__ __device__ constexpr int epi_warps(int) { return 8; }
 __host__ __device__ constexpr int gemm_threads(int b_mode) { return 128 + 32 * epi_warps(b_mode); }
-__host__ __device__ constexpr int launch_regs(int b_mode) { return epi_warps(b_mode) == 16 ? 96 : 168; }
-__host__ __device__ constexpr uint32_t reg_lo(int b_mode) { return epi_warps(b_mode) == 16 ? 32 : 56; }
-__host__ __device__ constexpr uint32_t reg_hi(int b_mode) { return epi_warps(b_mode) == 16 ? 112 : 224; }
-static_assert(128 * reg_lo(SCALE_ROW) + 32 * epi_warps(SCALE_ROW) * reg_hi(SCALE_ROW) <=
-                  gemm_threads(SCALE_ROW) * launch_regs(SCALE_ROW), "register split");
-static_assert(128 * reg_lo(SCALE_BLOCK) + 32 * epi_warps(SCALE_BLOCK) * reg_hi(SCALE_BLOCK) <=
-                  gemm_threads(SCALE_BLOCK) * launch_regs(SCALE_BLOCK), "register split");
+__host__ __device__ constexpr int launch_regs(int) { return 168; }
+__host__ __device__ constexpr uint32_t reg_lo(int) { return 56; }
+__host__ __device__ constexpr uint32_t reg_hi(int) { return 224; }
+static_assert(128 * reg_lo(0) + 32 * epi_warps(0) * reg_hi(0) <= gemm_threads(0) * launch_regs(0), "register split");
 constexpr int kScalePD = 4;   // K-blocks of scale prefetch per epilogue thread
 
 // How the epilogue gets the per-K-block scales of A's rows and of B's column blocks.
@@ -408,39 +406,52 @@ __global__ void __launch_bounds__(gemm_threads(B_MODE), 1)
                 if constexpr (B_MODE == SCALE_ROW) {
                     // 16x256b fragments: this thread holds rows g + 8h (h = 0..3) of the warp's
                     // 32 and columns 8j + 2tq + {0,1}, so it needs 4 row and 32 column scales
-                    // per K-block instead of 1 and 128.
+                    // per K-block instead of 1 and 128 (read with shared-space loads).
                     const int g = lane >> 2, tq = lane & 3;
                     float fr[4];
+                    const uint32_t fra = smem_u32(slot) + 4u * (uint32_t)(q * 128 + quad * 32 + g);
                     #pragma unroll
-                    for (int h = 0; h < 4; ++h) fr[h] = slot[q * 128 + quad * 32 + g + 8 * h];
-                    const float* sbv = slot + S::SLOT_A + q * BN + col_base + 2 * tq;
+                    for (int h = 0; h < 4; ++h)
+                        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(fr[h]) : "r"(fra + 32u * h));
+                    const uint32_t sba = smem_u32(slot) + 4u * (uint32_t)(S::SLOT_A + q * BN + col_base + 2 * tq);
                     const uint32_t tb0 = tmem_base + ((uint32_t)(quad * 32) << 16) + ts * BN + col_base;
                     const uint32_t tb1 = tb0 + (16u << 16);
+                    // parts of 16 rows x 32 columns, the next part's TMEM load in flight
+                    // while this one is promoted
+                    constexpr int NP = 2 * (COLS / 32);
+                    uint32_t ra[16], rb[16];
+                    float2 sc[4];
+                    tmem_ld_16x256b_x4(tb0, ra);
+                    tmem_ld_wait(ra);
                     #pragma unroll
-                    for (int jg = 0; jg < COLS / 32; ++jg) {
-                        uint32_t r0[16], r1[16];   // rows g, g+8 | rows g+16, g+24
-                        tmem_ld_16x256b_x4(tb0 + jg * 32, r0);
-                        tmem_ld_16x256b_x4(tb1 + jg * 32, r1);
-                        tmem_ld_wait(r0);
-                        tmem_ld_wait(r1);
-                        if (jg == COLS / 32 - 1) {
+                    for (int pp = 0; pp < NP; ++pp) {
+                        const int jq = pp >> 1, hh = pp & 1;
+                        uint32_t (&cur)[16] = (pp & 1) ? rb : ra;
+                        uint32_t (&nxt)[16] = (pp & 1) ? ra : rb;
+                        if (pp + 1 < NP) {
+                            tmem_ld_16x256b_x4((((pp + 1) & 1) ? tb1 : tb0) + ((pp + 1) >> 1) * 32, nxt);
+                        } else {
                             tc_fence_before();
                             __syncwarp();
                             if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[ts]));
                         }
+                        if (hh == 0) {
+                            #pragma unroll
+                            for (int jj = 0; jj < 4; ++jj)
+                                asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(sc[jj].x), "=f"(sc[jj].y) : "r"(sba + 32u * (jq * 4 + jj)));
+                        }
                         #pragma unroll
                         for (int jj = 0; jj < 4; ++jj) {
-                            const int j = jg * 4 + jj;
-                            const float2 sc = *reinterpret_cast<const float2*>(sbv + 8 * j);
                             #pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                const uint32_t* r = (h < 2) ? r0 : r1;
-                                const int o = 4 * jj + 2 * (h & 1);
-                                const float2 s2 = __fmul2_rn(make_float2(fr[h], fr[h]), sc);
-                                acc[h * (COLS / 8) + j] = __ffma2_rn(make_float2(__uint_as_float(r[o]), __uint_as_float(r[o + 1])),
-                                                                     s2, acc[h * (COLS / 8) + j]);
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const int h = 2 * hh + h2;
+                                const int o = 4 * jj + 2 * h2;
+                                const float2 s2 = __fmul2_rn(make_float2(fr[h], fr[h]), sc[jj]);
+                                acc[h * (COLS / 8) + jq * 4 + jj] = __ffma2_rn(make_float2(__uint_as_float(cur[o]), __uint_as_float(cur[o + 1])),
+                                                                               s2, acc[h * (COLS / 8) + jq * 4 + jj]);
                             }
                         }
+                        if (pp + 1 < NP) tmem_ld_wait(nxt);
                     }
                 } else {
                     if (SD == SD_TMA) {
