@@ -35,6 +35,7 @@ FP8RL_ERR_DEVICE_BOUNDS = 8
 FP8RL_OP_FWD, FP8RL_OP_DGRAD, FP8RL_OP_WGRAD = 0, 1, 2
 FP8RL_VARIANT_AUTO, FP8RL_VARIANT_TILED, FP8RL_VARIANT_SPLITK, FP8RL_VARIANT_PAIR = 0, 1, 2, 3
 FP8RL_VARIANT_DECODE = 4
+FP8RL_VARIANT_MULTICAST = 5
 
 
 class Fp8rlError(RuntimeError):

@@ -226,6 +226,34 @@ fp8rl_status run_pair(const TiledArgs& t, int clusters_req, int epi_req, int pn_
     return cuda_status(launch_gemm_pair(ta, tb, tsa, tsb, tc, p, t.b_mode, epi, pn, clusters, st));
 }
 
+// Multicast form (gemm_mc.cu): 128 x 256 one-SM tiles, two CTAs of a cluster on vertically
+// adjacent tiles sharing each B tile.  Needs TMA-able scales (FP8RL_ERR_SHAPE otherwise).
+fp8rl_status run_mc(const TiledArgs& t, int clusters_req, int num_sms, cudaStream_t st) {
+    constexpr int bn = 256;
+    GemmParams p = {};
+    p.R1 = t.R1; p.R2 = t.R2; p.Kr = t.Kr;
+    p.sa = t.sa; p.sa_kb = t.sa_kb;
+    p.sb = t.sb; p.sb_kb = t.sb_kb; p.sb_r = t.sb_r;
+    p.c = t.c; p.ldc = t.ldc;
+    p.splits = 0;
+    CUtensorMap tsa, tsb;
+    fp8rl_status e = FP8RL_OK;
+    if (!scale_maps(p, t.b_mode, bn, false, &tsa, &tsb, &e)) return e != FP8RL_OK ? e : FP8RL_ERR_SHAPE;
+    if (t.ldc % 8 != 0) return FP8RL_ERR_ALIGN;
+    CUtensorMap ta, tb, tc;
+    if ((e = make_tmap(&ta, t.A, t.R1, t.Kr, t.Kr, 128)) != FP8RL_OK) return e;
+    if ((e = make_tmap(&tb, t.B, t.R2, t.Kr, t.Kr, bn / 2)) != FP8RL_OK) return e;
+    if ((e = make_tmap_out(&tc, t.c, t.R1, t.R2, t.ldc)) != FP8RL_OK) return e;
+    p.m_tiles = (int)((t.R1 + 127) / 128);
+    p.n_tiles = (int)((t.R2 + bn - 1) / bn);
+    p.nkb = (int)(t.Kr / 128);
+    p.num_items = ((p.m_tiles + 1) / 2) * p.n_tiles;
+    p.timeout_ns = g_timeout_ns.load();
+    int clusters = clusters_req > 0 ? clusters_req : num_sms / 2;
+    clusters = std::max(1, std::min(clusters, p.num_items));
+    return cuda_status(launch_gemm_mc(ta, tb, tsa, tsb, tc, p, t.b_mode, clusters, st));
+}
+
 // Whether every scale array of the problem can be moved by TMA (the paired form's need).
 bool pair_eligible(const TiledArgs& t) {
     const int64_t nkb = t.Kr / 128;
@@ -246,6 +274,8 @@ fp8rl_status run_gemm(const TiledArgs& t, const fp8rl_gemm_opts* opts, int num_s
     const int variant = opts ? opts->variant : FP8RL_VARIANT_AUTO;
     if (variant == FP8RL_VARIANT_PAIR)
         return pair_eligible(t) ? run_pair(t, opts->grid, opts->epi_warps, opts->tile_n, num_sms, st) : FP8RL_ERR_SHAPE;
+    if (variant == FP8RL_VARIANT_MULTICAST)
+        return pair_eligible(t) ? run_mc(t, opts->grid, num_sms, st) : FP8RL_ERR_SHAPE;
     if (variant == FP8RL_VARIANT_AUTO && t.b_mode == SCALE_BLOCK && pair_eligible(t)) {
         const int64_t pair_tiles = ((t.R1 + 255) / 256) * ((t.R2 + 255) / 256);
         if (pair_tiles >= num_sms / 2) return run_pair(t, opts ? opts->grid : 0, 8, 256, num_sms, st);
@@ -440,8 +470,10 @@ fp8rl_status fp8rl_check_status(fp8rl_stream_t stream) {
     const fp8rl_status q = read_and_clear_quant_status();
     const fp8rl_status pr = read_and_clear_pair_status();
     const fp8rl_status dc = read_and_clear_decode_status();
+    const fp8rl_status mc = read_and_clear_mc_status();
     if (g != FP8RL_OK) return g;
     if (pr != FP8RL_OK) return pr;
+    if (mc != FP8RL_OK) return mc;
     return dc != FP8RL_OK ? dc : q;
 }
 
@@ -610,7 +642,7 @@ fp8rl_status fp8rl_gemm_fwd_ex(const uint8_t* qx, const float* sx, const uint8_t
                                fp8rl_stream_t stream) {
     if (M < 0 || N < 0 || K <= 0) return FP8RL_ERR_INVALID_ARG;
     const int variant = opts ? opts->variant : FP8RL_VARIANT_AUTO;
-    if (variant < FP8RL_VARIANT_AUTO || variant > FP8RL_VARIANT_DECODE) return FP8RL_ERR_INVALID_ARG;
+    if (variant < FP8RL_VARIANT_AUTO || variant > FP8RL_VARIANT_MULTICAST) return FP8RL_ERR_INVALID_ARG;
     if (K % 128 != 0 || N % 128 != 0) return FP8RL_ERR_SHAPE;
     if (M == 0 || N == 0) return FP8RL_OK;
     if (!qx || !sx || !qw || !sw || !y) return FP8RL_ERR_INVALID_ARG;
@@ -646,6 +678,12 @@ fp8rl_status fp8rl_gemm_dgrad(const uint8_t* qdy, const float* sdy, const uint8_
     return fp8rl_gemm_dgrad_ex(qdy, sdy, qwT, sw, dx, M, N, K, ws, ws_bytes, nullptr, stream);
 }
 
+// The forms DGrad and WGrad take: AUTO, TILED, PAIR, MULTICAST (not the decode-shaped ones).
+static bool training_variant(int v) {
+    return v == FP8RL_VARIANT_AUTO || v == FP8RL_VARIANT_TILED || v == FP8RL_VARIANT_PAIR ||
+           v == FP8RL_VARIANT_MULTICAST;
+}
+
 fp8rl_status fp8rl_gemm_dgrad_ex(const uint8_t* qdy, const float* sdy, const uint8_t* qwT,
                                  const float* sw, uint16_t* dx, int64_t M, int64_t N, int64_t K,
                                  void* ws, size_t ws_bytes, const fp8rl_gemm_opts* opts,
@@ -653,9 +691,7 @@ fp8rl_status fp8rl_gemm_dgrad_ex(const uint8_t* qdy, const float* sdy, const uin
     (void)ws;
     (void)ws_bytes;
     if (M < 0 || N < 0 || K <= 0) return FP8RL_ERR_INVALID_ARG;
-    if (opts && (opts->variant < FP8RL_VARIANT_AUTO || opts->variant > FP8RL_VARIANT_PAIR ||
-                 opts->variant == FP8RL_VARIANT_SPLITK))
-        return FP8RL_ERR_INVALID_ARG;
+    if (opts && !training_variant(opts->variant)) return FP8RL_ERR_INVALID_ARG;
     if (K % 128 != 0 || N % 128 != 0) return FP8RL_ERR_SHAPE;
     if (M == 0) return FP8RL_OK;
     if (N == 0) return FP8RL_ERR_SHAPE;
@@ -686,9 +722,7 @@ fp8rl_status fp8rl_gemm_wgrad_ex(const uint8_t* qdyT, const float* sdyT, const u
     (void)ws;
     (void)ws_bytes;
     if (M < 0 || N < 0 || K <= 0) return FP8RL_ERR_INVALID_ARG;
-    if (opts && (opts->variant < FP8RL_VARIANT_AUTO || opts->variant > FP8RL_VARIANT_PAIR ||
-                 opts->variant == FP8RL_VARIANT_SPLITK))
-        return FP8RL_ERR_INVALID_ARG;
+    if (opts && !training_variant(opts->variant)) return FP8RL_ERR_INVALID_ARG;
     if (K % 128 != 0 || N % 128 != 0 || M % 128 != 0) return FP8RL_ERR_SHAPE;
     if (N == 0) return FP8RL_OK;
     if (!qdyT || !sdyT || !qxT || !sxT || !dw) return FP8RL_ERR_INVALID_ARG;

@@ -72,6 +72,15 @@ cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const
                              int epi_warps, int pn, int clusters, cudaStream_t st);
 fp8rl_status read_and_clear_pair_status();
 
+// gemm_mc.cu: the one-SM kernel on clusters of two CTAs along M that share each B tile by
+// TMA multicast (this GPU's memory only).  As launch_gemm_tiled with BN = 256 and both scale
+// maps, except: tb has 128-row boxes (half a tile), p.num_items counts pairs of m-tiles x
+// n-tiles, `clusters` persistent pairs.
+cudaError_t launch_gemm_mc(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                           const CUtensorMap& tsb, const CUtensorMap& tc, const GemmParams& p, int b_mode,
+                           int clusters, cudaStream_t st);
+fp8rl_status read_and_clear_mc_status();
+
 // decode.cu: decode-shaped forward GEMM (M <= 256 tokens), weights on the MMA's M side,
 // split-K reduced inside a cluster of `splits` CTAs (1..8) through distributed shared
 // memory.  tw: weight codes [N][K] with 128 x 128-byte boxes; tx: activation codes [M][K]

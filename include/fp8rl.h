@@ -256,18 +256,23 @@ typedef enum {
                                  (M = 256 tensor-core MMAs); needs
                                  scale arrays whose rows are multiples of 16 bytes (the
                                  rule under fp8rl_gemm_fwd), else FP8RL_ERR_SHAPE */
-    FP8RL_VARIANT_DECODE = 4  /* forward only, M <= 256: weights on the MMA's M side (one
+    FP8RL_VARIANT_DECODE = 4, /* forward only, M <= 256: weights on the MMA's M side (one
                                  CTA per 128 weight rows and reduction slice), the
                                  reduction split over a cluster of `splits` CTAs (1..8, 0 =
                                  choose) and summed in the cluster's shared memory in rank
                                  order; no workspace */
+    FP8RL_VARIANT_MULTICAST = 5 /* the TILED form's 128 x 256 tiles on clusters of two CTAs
+                                 (vertically adjacent tiles) that share each B tile: every
+                                 CTA copies half of it with a TMA multicast into both CTAs;
+                                 the same scale-array rule as PAIR (FP8RL_ERR_SHAPE
+                                 otherwise); this GPU's memory only */
 } fp8rl_variant;
 
 typedef struct {
     int variant;    /* fp8rl_variant */
     int splits;     /* SPLITK: number of reduction slices (0 = choose); ignored otherwise */
-    int grid;       /* TILED: persistent CTAs (0 = one per SM); PAIR: persistent clusters
-                       (0 = one per two SMs); ignored otherwise */
+    int grid;       /* TILED: persistent CTAs (0 = one per SM); PAIR, MULTICAST: persistent
+                       clusters of two (0 = one per two SMs); ignored otherwise */
     int tile_n;     /* TILED: output tile width, 128 or 256 (0 = choose); PAIR: the pair
                        tile's width, 128 or 256 (0 = 256); ignored otherwise */
     int epi_warps;  /* PAIR: epilogue warps per CTA, 8 or 16 (0 = choose); ignored otherwise */
@@ -283,7 +288,8 @@ FP8RL_API fp8rl_status fp8rl_gemm_fwd_ex(const uint8_t* qx, const float* sx, con
                                int64_t K, void* ws, size_t ws_bytes,
                                const fp8rl_gemm_opts* opts, fp8rl_stream_t stream);
 
-/* fp8rl_gemm_dgrad / fp8rl_gemm_wgrad with an explicit variant (AUTO, TILED or PAIR);
+/* fp8rl_gemm_dgrad / fp8rl_gemm_wgrad with an explicit variant (AUTO, TILED, PAIR or
+ * MULTICAST);
  * opts may be NULL (= AUTO). */
 FP8RL_API fp8rl_status fp8rl_gemm_dgrad_ex(const uint8_t* qdy, const float* sdy, const uint8_t* qwT,
                                  const float* sw, uint16_t* dx, int64_t M, int64_t N,

@@ -93,7 +93,7 @@ def test_fwd_auto_matches_forms(fp8lib, oracle):
     qx, sx, qw, sw, _ = fwd_operands(fp8lib, oracle, M, N, K, 99)
     y_ref = oracle.gemm(u8(qx), f32(sx), u8(qw), f32(sw), "fwd")
     for v in (_abi.FP8RL_VARIANT_AUTO, _abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK,
-              _abi.FP8RL_VARIANT_PAIR, _abi.FP8RL_VARIANT_DECODE):
+              _abi.FP8RL_VARIANT_PAIR, _abi.FP8RL_VARIANT_DECODE, _abi.FP8RL_VARIANT_MULTICAST):
         gemm_tolerance_check(bits16(fp8lib.gemm_fwd(qx, sx, qw, sw, variant=v)), y_ref, f"variant {v}")
 
 
@@ -141,7 +141,7 @@ def test_exactly_representable_gemm(fp8lib, oracle):
     assert torch.all(sx == 1.0) and torch.all(sw == 1.0)
     exact = x @ w.T
     for v in (_abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK, _abi.FP8RL_VARIANT_PAIR,
-              _abi.FP8RL_VARIANT_DECODE):
+              _abi.FP8RL_VARIANT_DECODE, _abi.FP8RL_VARIANT_MULTICAST):
         y = bits16(fp8lib.gemm_fwd(qx, sx, qw, sw, variant=v))
         yf = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
         assert np.all(np.abs(yf - exact) <= np.abs(exact) * 2.0 ** -8 + 1e-30)
@@ -157,13 +157,14 @@ def test_scaling_law_on_device(fp8lib, oracle):
     qx2, sx2 = fp8lib.quantize_1x128((x.float() * 8.0).to(torch.bfloat16))
     qw2, sw2, _ = fp8lib.quantize_128x128((w.float() * 0.25).to(torch.bfloat16))
     for v in (_abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_SPLITK, _abi.FP8RL_VARIANT_PAIR,
-              _abi.FP8RL_VARIANT_DECODE):
+              _abi.FP8RL_VARIANT_DECODE, _abi.FP8RL_VARIANT_MULTICAST):
         y = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=v).float()
         y2 = fp8lib.gemm_fwd(qx2, sx2, qw2, sw2, variant=v).float()
         assert torch.equal(y2, y * 2.0)
 
 
-@pytest.mark.parametrize("variant", [_abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_PAIR])
+@pytest.mark.parametrize("variant", [_abi.FP8RL_VARIANT_TILED, _abi.FP8RL_VARIANT_PAIR,
+                                     _abi.FP8RL_VARIANT_MULTICAST])
 def test_tiled_deterministic_and_grid_independent(fp8lib, oracle, variant):
     """Both persistent forms against the oracle, with a full grid and with a few CTAs (or
     clusters) that each walk many tiles; the two runs give the same bytes."""
@@ -229,6 +230,59 @@ def test_wgrad_pair(fp8lib, oracle, M, N, K, epi, pn):
         gemm_tolerance_check(bits16(dw), ref, f"pair wgrad {M}x{N}x{K} epi {epi} grid {grid} tile {pn}")
     dw = fp8lib.gemm_wgrad(qdyT, sdyT, qxT, sxT, variant=_abi.FP8RL_VARIANT_TILED)
     gemm_tolerance_check(bits16(dw), ref, f"one-SM wgrad {M}x{N}x{K}")
+
+
+# ------------------------------------------------------------------ multicast form
+# Clusters of two CTAs on vertically adjacent 128 x 256 tiles share each B tile (each CTA
+# copies half of it into both).  Odd m-tile counts leave the second CTA of the last pair
+# wholly outside A (zero fill, clipped stores); N not a multiple of 256 leaves the second
+# half of the last B tile outside B; grid = clusters.
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 512), (384, 384, 512), (300, 1280, 1024),
+                                   (132, 128, 2048), (1000, 768, 1536)])
+def test_fwd_multicast(fp8lib, oracle, M, N, K):
+    qx, sx, qw, sw, _ = fwd_operands(fp8lib, oracle, M, N, K, 3 * M + N + K)
+    ref = oracle.gemm(u8(qx), f32(sx), u8(qw), f32(sw), "fwd")
+    for grid in (0, 1, 3):
+        y = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_MULTICAST, grid=grid)
+        gemm_tolerance_check(bits16(y), ref, f"multicast fwd {M}x{N}x{K} grid {grid}")
+    assert fp8lib.check_status() == _abi.FP8RL_OK
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 512), (300, 384, 1024), (512, 640, 512)])
+def test_dgrad_multicast(fp8lib, oracle, M, N, K):
+    dy = synth.normal_bf16((M, N), 1e-3, M + 61, "cuda")
+    w = synth.normal_bf16((N, K), 0.02, K + 65, "cuda")
+    qdy, sdy = fp8lib.quantize_1x128(dy)
+    _, sw, qwT = fp8lib.quantize_128x128(w)
+    ref = oracle.gemm(u8(qdy), f32(sdy), u8(qwT), f32(sw), "dgrad")
+    for grid in (0, 2):
+        dx = fp8lib.gemm_dgrad(qdy, sdy, qwT, sw, variant=_abi.FP8RL_VARIANT_MULTICAST, grid=grid)
+        gemm_tolerance_check(bits16(dx), ref, f"multicast dgrad {M}x{N}x{K} grid {grid}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (256, 384, 512), (1024, 384, 768),
+                                   (384, 640, 1152)])
+def test_wgrad_multicast(fp8lib, oracle, M, N, K):
+    dy = synth.normal_bf16((M, N), 1e-3, M + 71, "cuda")
+    x = synth.normal_bf16((M, K), 1.0, K + 73, "cuda", outlier_channels=2, outlier_scale=30.0)
+    qdyT, sdyT = fp8lib.quantize_128x1(dy)
+    qxT, sxT = fp8lib.quantize_128x1(x)
+    ref = oracle.gemm(u8(qdyT), f32(sdyT), u8(qxT), f32(sxT), "wgrad")
+    for grid in (0, 2):
+        dw = fp8lib.gemm_wgrad(qdyT, sdyT, qxT, sxT, variant=_abi.FP8RL_VARIANT_MULTICAST, grid=grid)
+        gemm_tolerance_check(bits16(dw), ref, f"multicast wgrad {M}x{N}x{K} grid {grid}")
+    assert fp8lib.check_status() == _abi.FP8RL_OK
+
+
+def test_multicast_same_bytes_as_one_sm_form(fp8lib, oracle):
+    """The multicast form changes only where B's bytes come from: the same partial sums in
+    the same order, so the same BF16 output bytes as the one-SM form."""
+    M, N, K = 640, 1536, 1024
+    qx, sx, qw, sw, _ = fwd_operands(fp8lib, oracle, M, N, K, 17)
+    y1 = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_TILED)
+    y2 = fp8lib.gemm_fwd(qx, sx, qw, sw, variant=_abi.FP8RL_VARIANT_MULTICAST)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
 
 
 def test_pair_refuses_scales_it_cannot_copy(fp8lib, oracle):
