@@ -649,7 +649,8 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-GEMM_SOURCES = ("block_scaled_fp8_x1_gb300/csrc/gemm.cu", "block_scaled_fp8_x1_gb300/csrc/common.cuh",
+GEMM_SOURCES = ("block_scaled_fp8_x1_gb300/csrc/gemm.cu", "block_scaled_fp8_x1_gb300/csrc/gemm_tiled.cuh",
+                "block_scaled_fp8_x1_gb300/csrc/gemm_pair.cu", "block_scaled_fp8_x1_gb300/csrc/common.cuh",
                 "block_scaled_fp8_x1_gb300/csrc/gemm.h")
 
 

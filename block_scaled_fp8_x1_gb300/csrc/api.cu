@@ -219,6 +219,7 @@ fp8rl_status run_pair(const TiledArgs& t, int clusters_req, int epi_req, int pn_
     p.nkb = (int)(t.Kr / 128);
     const int items = ((p.m_tiles + 1) / 2) * p.n_tiles;
     p.num_items = items;
+    choose_raster((p.m_tiles + 1) / 2, p.n_tiles, 256 * t.Kr, (int64_t)pn * t.Kr, &p.group, &p.raster_n);
     p.timeout_ns = g_timeout_ns.load();
     int clusters = clusters_req > 0 ? clusters_req : num_sms / 2;
     clusters = std::max(1, std::min(clusters, items));
@@ -248,6 +249,7 @@ fp8rl_status run_mc(const TiledArgs& t, int clusters_req, int num_sms, cudaStrea
     p.n_tiles = (int)((t.R2 + bn - 1) / bn);
     p.nkb = (int)(t.Kr / 128);
     p.num_items = ((p.m_tiles + 1) / 2) * p.n_tiles;
+    choose_raster((p.m_tiles + 1) / 2, p.n_tiles, 256 * t.Kr, (int64_t)bn * t.Kr, &p.group, &p.raster_n);
     p.timeout_ns = g_timeout_ns.load();
     int clusters = clusters_req > 0 ? clusters_req : num_sms / 2;
     clusters = std::max(1, std::min(clusters, p.num_items));
@@ -306,6 +308,7 @@ fp8rl_status run_tiled(const TiledArgs& t, int grid_req, int bn_req, int num_sms
     p.n_tiles = (int)((t.R2 + bn - 1) / bn);
     p.nkb = (int)(t.Kr / 128);
     p.num_items = p.m_tiles * p.n_tiles;
+    choose_raster(p.m_tiles, p.n_tiles, 128 * t.Kr, (int64_t)bn * t.Kr, &p.group, &p.raster_n);
     p.timeout_ns = g_timeout_ns.load();
     int grid = grid_req > 0 ? grid_req : num_sms;
     grid = std::max(1, std::min(grid, p.num_items));
@@ -345,6 +348,8 @@ fp8rl_status run_decode(const uint8_t* qx, const float* sx, const uint8_t* qw, c
     p.n_tiles = (int)((N + kDecodeBN - 1) / kDecodeBN);
     p.nkb = (int)nkb;
     p.num_items = (int)(tiles * splits);
+    p.group = p.m_tiles;   // at most two row tiles: every weight tile streams once
+    p.raster_n = 0;
     p.timeout_ns = g_timeout_ns.load();
     const int grid = std::max(1, std::min(num_sms, p.num_items));
     CUtensorMap tsa, tsb;

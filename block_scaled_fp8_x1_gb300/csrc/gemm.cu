@@ -7,11 +7,33 @@
 // gradients), per 128x128 block (weights) and, for WGrad, per 128x1 group.
 #include "gemm_tiled.cuh"
 
+#include <algorithm>
+
 namespace fp8rl {
 
 // ------------------------------------------------------------------------------------
 // Host side
 // ------------------------------------------------------------------------------------
+
+// Tile order of the persistent GEMMs (raster_tile in gemm.h): the operand whose panel the
+// running CTAs share is held to kRasterPanelBytes, small enough to stay in L2 next to the
+// tiles of the other operand streaming past; of the two orientations, the one whose panels
+// make the fewest HBM reads of A and B together.
+constexpr int64_t kRasterPanelBytes = 48ll << 20;
+
+void choose_raster(int64_t m_units, int64_t n_units, int64_t a_unit_bytes, int64_t b_unit_bytes, int* group,
+                   int* raster_n) {
+    m_units = std::max<int64_t>(m_units, 1);
+    n_units = std::max<int64_t>(n_units, 1);
+    const int64_t gm = std::min(m_units, std::max<int64_t>(1, kRasterPanelBytes / std::max<int64_t>(a_unit_bytes, 1)));
+    const int64_t gn = std::min(n_units, std::max<int64_t>(1, kRasterPanelBytes / std::max<int64_t>(b_unit_bytes, 1)));
+    const double a = (double)m_units * (double)a_unit_bytes, b = (double)n_units * (double)b_unit_bytes;
+    const double reads_m = a + b * (double)((m_units + gm - 1) / gm);   // B once per row group
+    const double reads_n = b + a * (double)((n_units + gn - 1) / gn);   // A once per column group
+    *raster_n = reads_n < reads_m ? 1 : 0;
+    *group = (int)(*raster_n ? gn : gm);
+}
+
 
 template <int BN, int SD, int B_MODE, int STAGES, bool SPLITK>
 static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,

@@ -45,8 +45,35 @@ struct GemmParams {
     int splits;              // reduction slices per output tile (<= 1: none)
     int m_tiles, n_tiles, nkb;
     int num_items;
+    int group;               // tile order (see raster_tile): units per group
+    int raster_n;            // 0: groups of row units sweep the column tiles; 1: the converse
     uint64_t timeout_ns;
 };
+
+// Tile order of the persistent GEMMs.  Output tiles are numbered in groups: with
+// raster_n == 0 a group is `group` consecutive row units (128-row tiles, or pairs of them)
+// and its tiles are numbered row unit first, then column tile, so the CTAs running at the
+// same time share the group's rows of A from L2 while the column tiles of B stream past;
+// raster_n == 1 is the same with the roles of rows and columns exchanged.  The host picks
+// the orientation and size that read the operands from HBM the fewest times.
+__host__ __device__ inline void raster_tile(int tile, int m_units, int n_units, int group, int raster_n, int* m,
+                                            int* n) {
+    const int g_units = raster_n ? n_units : m_units;   // the grouped dimension
+    const int s_units = raster_n ? m_units : n_units;   // the swept one
+    const int per_group = group * s_units;
+    const int g = tile / per_group;
+    const int first = g * group;
+    const int gs = (group < g_units - first) ? group : g_units - first;
+    const int r = tile - g * per_group;
+    const int a = first + r % gs, b = r / gs;
+    *m = raster_n ? b : a;
+    *n = raster_n ? a : b;
+}
+
+// The group of raster_tile for an m_units x n_units grid of tiles whose row unit holds
+// a_unit_bytes of A and column tile b_unit_bytes of B (each across the whole reduction).
+void choose_raster(int64_t m_units, int64_t n_units, int64_t a_unit_bytes, int64_t b_unit_bytes, int* group,
+                   int* raster_n);
 
 // Scale tensor maps (FP32; g = min(scale_group(), K-blocks) K-blocks per box): tsa over A's
 // row scales [K-block][R1], box 128 x g; tsb over B's scales, box BN x g for row scales

@@ -54,23 +54,16 @@ __device__ __forceinline__ uint32_t num_clusters_x() {
     return r;
 }
 
-// Pair tiles in a grouped order: kGroup pair-rows (256 rows of C each) share each sweep
-// over the column tiles, so the clusters running at the same time reuse A and B through L2.
+// Pair tiles (pair-rows of 256 rows of C x column tiles) in the grouped order of
+// raster_tile, so the clusters running at the same time reuse A and B through L2.
 struct PairTile {
     int mp;   // pair-row tile (256 rows)
     int nt;   // column tile (PN columns)
 };
 
-__device__ __forceinline__ PairTile pair_tile(int m_pairs, int n_tiles, int item) {
-    constexpr int kGroup = 8;
-    const int per_group = kGroup * n_tiles;
-    const int g = item / per_group;
-    const int first = g * kGroup;
-    const int gm = min(kGroup, m_pairs - first);
-    const int r = item - g * per_group;
+__device__ __forceinline__ PairTile pair_tile(const GemmParams& p, int m_pairs, int item) {
     PairTile t;
-    t.mp = first + r % gm;
-    t.nt = r / gm;
+    raster_tile(item, m_pairs, p.n_tiles, p.group, p.raster_n, &t.mp, &t.nt);
     return t;
 }
 
@@ -194,7 +187,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
             uint32_t it = 0, s_issued = 0;
             bool ok = true;
             for (int item = cid; ok && item < num_items; item += ncl) {
-                const PairTile t = pair_tile(m_pairs, p.n_tiles, item);
+                const PairTile t = pair_tile(p, m_pairs, item);
                 const int m0 = t.mp * 256 + (int)rank * 128;            // this CTA's rows of A
                 const int n0 = t.nt * kPairN;                           // the tile's first column
                 const int nb = n0 + (int)rank * (kPairN / 2);           // this CTA's rows of B
@@ -303,7 +296,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
         uint32_t acc_it = 0, g_done = 0, box_it = 0;
         bool ok = true;
         for (int item = cid; ok && item < num_items; item += ncl) {
-            const PairTile t = pair_tile(m_pairs, p.n_tiles, item);
+            const PairTile t = pair_tile(p, m_pairs, item);
             float2 acc[COLS / 2];
             #pragma unroll
             for (int c = 0; c < COLS / 2; ++c) acc[c] = make_float2(0.0f, 0.0f);

@@ -51,8 +51,8 @@ struct WorkItem {
 };
 
 // Items are (output tile, reduction slice) pairs; slices of one tile are adjacent items.
-// Tiles follow a grouped order: GROUP m-tiles share each sweep over the n-tiles, so the
-// CTAs running at the same time reuse the same A rows and B columns through L2.
+// Tiles follow the grouped order of raster_tile (p.group, p.raster_n), so the CTAs running
+// at the same time reuse the same A rows and B columns through L2.
 // With clusters of CM CTAs along M (CM = 2: the multicast form), an item is a group of CM
 // vertically adjacent tiles, and CTA `rank` of the cluster takes m-tile CM * group + rank
 // (past the last m-tile its rows are TMA zero fill and its stores are clipped).
@@ -65,15 +65,10 @@ __device__ __forceinline__ WorkItem work_item(const GemmParams& p, int item, int
     const int splits = p.splits > 1 ? p.splits : 1;
     w.tile = item / splits;
     w.split = item - w.tile * splits;
-    constexpr int GROUP = 16 / CM;
-    const int m_groups = (p.m_tiles + CM - 1) / CM;
-    const int per_group = GROUP * p.n_tiles;
-    const int g = w.tile / per_group;
-    const int first_m = g * GROUP;
-    const int gm = min(GROUP, m_groups - first_m);
-    const int r = w.tile - g * per_group;
-    w.mt = (first_m + r % gm) * CM + rank;
-    w.nt = r / gm;
+    int mu, nt;
+    raster_tile(w.tile, (p.m_tiles + CM - 1) / CM, p.n_tiles, p.group, p.raster_n, &mu, &nt);
+    w.mt = mu * CM + rank;
+    w.nt = nt;
     w.kb_begin = (int)(((int64_t)w.split * p.nkb) / splits);
     w.kb_end = (int)(((int64_t)(w.split + 1) * p.nkb) / splits);
     return w;
