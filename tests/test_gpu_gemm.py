@@ -69,11 +69,13 @@ def test_fwd_decode_swapped(fp8lib, oracle, M, splits):
     assert fp8lib.check_status() == _abi.FP8RL_OK
 
 
-@pytest.mark.parametrize("M,N,K", [(64, 1280, 3584), (256, 768, 2048), (17, 2048, 512), (300, 512, 1024)])
+@pytest.mark.parametrize("M,N,K", [(64, 1280, 3584), (256, 768, 2048), (17, 2048, 512), (300, 512, 1024),
+                                   (1, 1280, 1024), (31, 768, 512), (33, 1280, 2048), (100, 4608, 1024),
+                                   (128, 3584, 3584), (64, 37888, 3584)])
 def test_linear_fwd_quantizes_and_multiplies(fp8lib, oracle, M, N, K):
     """The fused linear: its activation codes and scales are the oracle's 1x128 quantization
     bit for bit, and its output is within the GEMM bound of the oracle's result from them
-    (the GEMM overlapping the quantizer for M <= 256)."""
+    and byte-identical to the GEMM the automatic choice runs on those codes."""
     x = synth.normal_bf16((M, K), 1.0, M + K + 5, "cuda", outlier_channels=3, outlier_scale=30.0)
     w = synth.normal_bf16((N, K), 0.02, N + 7, "cuda")
     qw, sw, _ = fp8lib.quantize_128x128(w, transpose=False)
@@ -82,8 +84,29 @@ def test_linear_fwd_quantizes_and_multiplies(fp8lib, oracle, M, N, K):
         qxr, sxr = oracle.quantize_1x128(bits16(x))
         assert_same_u8(u8(qx), qxr, "qx")
         assert_same_bits_f32(f32(sx), sxr, "sx")
-        y_ref = oracle.gemm(qxr, sxr, u8(qw), f32(sw), "fwd")
-        gemm_tolerance_check(bits16(y), y_ref, f"linear {M}x{N}x{K} rep {rep}")
+        if M * N * K <= 1 << 31:
+            y_ref = oracle.gemm(qxr, sxr, u8(qw), f32(sw), "fwd")
+            gemm_tolerance_check(bits16(y), y_ref, f"linear {M}x{N}x{K} rep {rep}")
+        # the GEMM the automatic choice runs on the same codes gives the same bytes
+        y2 = fp8lib.gemm_fwd(qx, sx, qw, sw)
+        assert torch.equal(y.view(torch.int16), y2.view(torch.int16)), f"linear {M}x{N}x{K}"
+    assert fp8lib.check_status() == _abi.FP8RL_OK
+
+
+def test_linear_fwd_strided_activation(fp8lib, oracle):
+    """The fused linear reads x with its row stride (a column slice of a wider buffer), at a
+    token count inside the 64-token padding class of the decode form."""
+    M, N, K = 40, 2048, 1536
+    big = synth.normal_bf16((M, K + 384), 1.0, 123, "cuda", outlier_channels=4, outlier_scale=30.0)
+    x = big[:, 128:128 + K]
+    w = synth.normal_bf16((N, K), 0.02, 124, "cuda")
+    qw, sw, _ = fp8lib.quantize_128x128(w, transpose=False)
+    y, qx, sx = fp8lib.linear_fwd(x, qw, sw)
+    qxr, sxr = oracle.quantize_1x128(bits16(x.contiguous()))
+    assert_same_u8(u8(qx), qxr, "qx")
+    assert_same_bits_f32(f32(sx), sxr, "sx")
+    y_ref = oracle.gemm(qxr, sxr, u8(qw), f32(sw), "fwd")
+    gemm_tolerance_check(bits16(y), y_ref, "strided linear")
     assert fp8lib.check_status() == _abi.FP8RL_OK
 
 
