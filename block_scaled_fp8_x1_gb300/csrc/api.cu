@@ -265,22 +265,22 @@ bool pair_eligible(const TiledArgs& t) {
     return t.sb_r == 1 && t.sb_kb % 4 == 0;
 }
 
-// The tiled forms: PAIR or TILED on request.  AUTO takes 256 x 256 pair tiles for the
-// block-scaled GEMMs (forward, DGrad) when their scales can travel by TMA and the tiles
-// fill every pair of SMs at least once: per SM the tensor pipe then reads 32 KB of
-// operands per K-block instead of 48 KB, and on the 32B layer's forward and DGrad shapes
-// that measured 3-10% faster than the one-SM form.  WGrad (a scale per row of both
-// operands: a multiply and an FMA per element in the epilogue) stays on the one-SM form
-// with 16 epilogue warps, which measured 3-8% faster than the pairs there.
+// The tiled forms: PAIR, MULTICAST or TILED on request.  AUTO takes 256 x 256 pair tiles
+// when every scale array can travel by TMA and the tiles fill every pair of SMs at least
+// once: per SM the tensor pipe then reads 32 KB of operands per K-block instead of 48 KB.
+// On the 32B layer's shapes that measured 3-10% faster than the one-SM form for forward
+// and DGrad (8 epilogue warps: one FMA per element) and 13% faster for WGrad (16 epilogue
+// warps: a multiply and an FMA per element, in 16-row x 32-column parts).
 fp8rl_status run_gemm(const TiledArgs& t, const fp8rl_gemm_opts* opts, int num_sms, cudaStream_t st) {
     const int variant = opts ? opts->variant : FP8RL_VARIANT_AUTO;
     if (variant == FP8RL_VARIANT_PAIR)
         return pair_eligible(t) ? run_pair(t, opts->grid, opts->epi_warps, opts->tile_n, num_sms, st) : FP8RL_ERR_SHAPE;
     if (variant == FP8RL_VARIANT_MULTICAST)
         return pair_eligible(t) ? run_mc(t, opts->grid, num_sms, st) : FP8RL_ERR_SHAPE;
-    if (variant == FP8RL_VARIANT_AUTO && t.b_mode == SCALE_BLOCK && pair_eligible(t)) {
+    if (variant == FP8RL_VARIANT_AUTO && pair_eligible(t)) {
         const int64_t pair_tiles = ((t.R1 + 255) / 256) * ((t.R2 + 255) / 256);
-        if (pair_tiles >= num_sms / 2) return run_pair(t, opts ? opts->grid : 0, 8, 256, num_sms, st);
+        if (pair_tiles >= num_sms / 2)
+            return run_pair(t, opts ? opts->grid : 0, t.b_mode == SCALE_ROW ? 16 : 8, 256, num_sms, st);
     }
     return run_tiled(t, opts ? opts->grid : 0, opts ? opts->tile_n : 0, num_sms, st);
 }

@@ -11,25 +11,28 @@
 // with A [R1, Kr] and B [R2, Kr] K-major, the same contract as the one-SM kernel in
 // gemm.cu.
 //
-// Why pairs.  The promotion needs every K-block's partial sum in its own TMEM buffer
-// until the epilogue has read it; the tensor pipe can only run as far ahead as there are
-// free buffers.  A cluster of two CTAs computes a 256 x 128 tile with M = 256 MMAs
-// (cta_group::2): each CTA holds 128 rows of A and half of B's 128 rows, and its TMEM
-// holds its own 128 x 128 FP32 partial per K-block.  So each SM keeps four partial
-// buffers in flight (instead of two of 128 x 256) for the same shared-memory traffic per
-// FLOP, and the epilogue's hand-back latency hides behind three K-blocks of MMAs.
+// Why pairs.  The tensor pipe reads the operands of every MMA from shared memory, and a
+// 128 x 256 tile on one SM moves 48 KB of A and B through it per K-block (written by TMA,
+// read by the MMAs).  A cluster of two CTAs computes a 256 x PN tile with M = 256 MMAs
+// (cta_group::2): each CTA holds 128 rows of A and half of B's PN rows, and the MMA
+// reads B's halves from both CTAs, so with PN = 256 each SM moves 32 KB per K-block for
+// the same 128 x 256 partial sum in its TMEM (two 256-column buffers).  PN = 128 keeps
+// four 128-column buffers in flight instead, at the one-SM tile's traffic per FLOP.
 //
 // Roles (per CTA; both CTAs of a pair run all roles except the MMA issuer):
-//   warp 0  lane 0: TMA copies.  Per K-block this CTA's 128x128 tile of A and 64x128 half
-//           of B into a STAGES-deep ring; both CTAs' copies complete on the leader's
-//           (rank 0) stage barrier.  Per scale group, this CTA's row scales of A and the
-//           tile's scales of B into a local scale ring.
-//   warp 1  allocates the pair's TMEM (512 columns in each CTA); in the leader, lane 0
-//           issues four M256 x N128 x K32 MMAs per K-block into one of four buffers and
-//           commits to both CTAs' barriers (stage empty, buffer full).
-//   warps 4.. epilogue: per K-block, load this CTA's 128 x 128 partial from TMEM, hand
-//           the buffer back to the leader, promote it with the block's scales into FP32
-//           registers; at the end of a tile round to BF16 and store with TMA.
+//   warp 0  TMA copies (the warp walks the loop, one elected lane issues).  Per K-block
+//           this CTA's 128x128 tile of A and PN/2 x 128 half of B into a STAGES-deep
+//           ring; both CTAs' copies complete on the leader's (rank 0) stage barrier.  Per
+//           scale group, this CTA's row scales of A and the tile's scales of B into a
+//           local scale ring.
+//   warp 1  allocates the pair's TMEM (512 columns in each CTA); in the leader, one
+//           elected lane issues four M256 x N(PN) x K32 MMAs per K-block into one of
+//           512/PN buffers and commits to both CTAs' barriers (stage empty, buffer full).
+//   warps 4.. epilogue: per K-block, load this CTA's 128 x PN partial from TMEM, hand the
+//           buffer back to the leader, promote it with the block's scales into FP32
+//           registers (WGrad: 16x256b fragments, each 16-row x 32-column part promoted
+//           while the next part's load is in flight); at the end of a tile round to BF16
+//           and store 32 x 32 boxes with TMA, double-buffered per warp.
 // Every mbarrier wait is bounded; on timeout the waiting role records
 // FP8RL_ERR_DEVICE_TIMEOUT and the CTA stops waiting, drains its MMAs and frees TMEM.
 #include "common.cuh"
@@ -325,34 +328,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
                                                     : slot[S::SLOT_A + q * 4 + (cb & 3)];
                     f2 = make_float2(fa * fb, fa * fb);
                 }
-                const float* sbv = slot + S::SLOT_A + q * kPairN + col_base;   // B row scales (WGrad)
-                #pragma unroll
-                for (int g = 0; g < NG; ++g) {
-                    uint32_t r[LPW][32];
+                if constexpr (B_MODE == SCALE_ROW) {
+                    // 16x256b fragments: rows g8 + 8h (h = 0..3) of the warp's 32 and columns
+                    // 8j + 2tq + {0,1}; parts of 16 rows x 32 columns, the next part's TMEM
+                    // load in flight while this one is promoted
+                    const int g8 = lane >> 2, tq = lane & 3;
+                    float fr[4];
+                    const uint32_t fra = smem_u32(slot) + 4u * (uint32_t)(q * 128 + quad * 32 + g8);
                     #pragma unroll
-                    for (int h = 0; h < LPW; ++h) tmem_ld_32x32b_x32(tb + (g * LPW + h) * 32, r[h]);
+                    for (int h = 0; h < 4; ++h)
+                        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(fr[h]) : "r"(fra + 32u * h));
+                    const uint32_t sba = smem_u32(slot) + 4u * (uint32_t)(S::SLOT_A + q * kPairN + col_base + 2 * tq);
+                    const uint32_t tb0 = tmem_base + ((uint32_t)(quad * 32) << 16) + ts * kPairN + col_base;
+                    const uint32_t tb1 = tb0 + (16u << 16);
+                    constexpr int NP = 2 * (COLS / 32);
+                    uint32_t ra[16], rb[16];
+                    float2 sc[4];
+                    tmem_ld_16x256b_x4(tb0, ra);
+                    tmem_ld_wait(ra);
                     #pragma unroll
-                    for (int h = 0; h < LPW; ++h) tmem_ld_wait(r[h]);
-                    if (g == NG - 1) {
-                        // the whole partial is in registers: hand the buffer back to the leader
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(tempty0 + 8 * ts);
-                    }
-                    #pragma unroll
-                    for (int h = 0; h < LPW; ++h) {
-                        const int c0 = (g * LPW + h) * 32;   // first of these 32 columns
-                        if constexpr (B_MODE == SCALE_ROW) {
-                            #pragma unroll
-                            for (int j = 0; j < 32; j += 4) {
-                                const float4 sc = *reinterpret_cast<const float4*>(sbv + c0 + j);
-                                const float2 s01 = __fmul2_rn(f2, make_float2(sc.x, sc.y));
-                                const float2 s23 = __fmul2_rn(f2, make_float2(sc.z, sc.w));
-                                const int c = (c0 + j) / 2;
-                                acc[c] = __ffma2_rn(make_float2(__uint_as_float(r[h][j]), __uint_as_float(r[h][j + 1])), s01, acc[c]);
-                                acc[c + 1] = __ffma2_rn(make_float2(__uint_as_float(r[h][j + 2]), __uint_as_float(r[h][j + 3])), s23, acc[c + 1]);
-                            }
+                    for (int pp = 0; pp < NP; ++pp) {
+                        const int jq = pp >> 1, hh = pp & 1;
+                        uint32_t (&cur)[16] = (pp & 1) ? rb : ra;
+                        uint32_t (&nxt)[16] = (pp & 1) ? ra : rb;
+                        if (pp + 1 < NP) {
+                            tmem_ld_16x256b_x4((((pp + 1) & 1) ? tb1 : tb0) + ((pp + 1) >> 1) * 32, nxt);
                         } else {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive_cluster(tempty0 + 8 * ts);
+                        }
+                        if (hh == 0) {
+                            #pragma unroll
+                            for (int jj = 0; jj < 4; ++jj)
+                                asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(sc[jj].x), "=f"(sc[jj].y) : "r"(sba + 32u * (jq * 4 + jj)));
+                        }
+                        #pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            #pragma unroll
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const int h = 2 * hh + h2;
+                                const int o = 4 * jj + 2 * h2;
+                                const float2 s2 = __fmul2_rn(make_float2(fr[h], fr[h]), sc[jj]);
+                                acc[h * (COLS / 8) + jq * 4 + jj] = __ffma2_rn(make_float2(__uint_as_float(cur[o]), __uint_as_float(cur[o + 1])),
+                                                                               s2, acc[h * (COLS / 8) + jq * 4 + jj]);
+                            }
+                        }
+                        if (pp + 1 < NP) tmem_ld_wait(nxt);
+                    }
+                } else {
+                    // 32x32b loads: one row and COLS columns per thread, LPW loads per wait
+                    #pragma unroll
+                    for (int g = 0; g < NG; ++g) {
+                        uint32_t r[LPW][32];
+                        #pragma unroll
+                        for (int h = 0; h < LPW; ++h) tmem_ld_32x32b_x32(tb + (g * LPW + h) * 32, r[h]);
+                        #pragma unroll
+                        for (int h = 0; h < LPW; ++h) tmem_ld_wait(r[h]);
+                        if (g == NG - 1) {
+                            // the whole partial is in registers: hand the buffer back to the leader
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive_cluster(tempty0 + 8 * ts);
+                        }
+                        #pragma unroll
+                        for (int h = 0; h < LPW; ++h) {
+                            const int c0 = (g * LPW + h) * 32;   // first of these 32 columns
                             #pragma unroll
                             for (int j = 0; j < 32; j += 2)
                                 acc[(c0 + j) / 2] = __ffma2_rn(make_float2(__uint_as_float(r[h][j]), __uint_as_float(r[h][j + 1])),
@@ -379,15 +420,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPI), 1
                 const uint32_t buf = smem_u32(stage_c + (ew * NBX + (int)(box_it % NBX)) * 2048);
                 if (lane == 0) bulk_wait_read<NBX - 1>();
                 __syncwarp();
-                #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int cc = b * 32 + c * 8;    // first of these 8 columns
-                    uint4 v;
-                    v.x = pack_bf16x2(acc[cc / 2 + 0].x, acc[cc / 2 + 0].y);
-                    v.y = pack_bf16x2(acc[cc / 2 + 1].x, acc[cc / 2 + 1].y);
-                    v.z = pack_bf16x2(acc[cc / 2 + 2].x, acc[cc / 2 + 2].y);
-                    v.w = pack_bf16x2(acc[cc / 2 + 3].x, acc[cc / 2 + 3].y);
-                    st_shared_v4(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), v);
+                if constexpr (B_MODE == SCALE_ROW) {
+                    // rows g + 8h, columns 8j + 2tq + {0,1}: one BF16 pair per (row, chunk)
+                    const int g8 = lane >> 2, tq = lane & 3;
+                    #pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const int rl = g8 + 8 * h;
+                        #pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const float2 v = acc[h * (COLS / 8) + b * 4 + c];
+                            st_shared_b32(buf + rl * 64 + ((c ^ ((rl >> 1) & 3)) << 4) + 4 * tq, pack_bf16x2(v.x, v.y));
+                        }
+                    }
+                } else {
+                    #pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int cc = b * 32 + c * 8;    // first of these 8 columns
+                        uint4 v;
+                        v.x = pack_bf16x2(acc[cc / 2 + 0].x, acc[cc / 2 + 0].y);
+                        v.y = pack_bf16x2(acc[cc / 2 + 1].x, acc[cc / 2 + 1].y);
+                        v.z = pack_bf16x2(acc[cc / 2 + 2].x, acc[cc / 2 + 2].y);
+                        v.w = pack_bf16x2(acc[cc / 2 + 3].x, acc[cc / 2 + 3].y);
+                        st_shared_v4(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), v);
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();

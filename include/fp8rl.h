@@ -219,7 +219,7 @@ typedef enum { FP8RL_OP_FWD = 0, FP8RL_OP_DGRAD = 1, FP8RL_OP_WGRAD = 2 } fp8rl_
  * scale array can be moved by TMA -- M % 4 == 0 and (K/128) % 4 == 0 for the forward GEMM,
  * M % 4 == 0 and (K/128) % 4 == 0 on the weight's block-scale rows for DGrad -- and its
  * tiles cover every pair of SMs at least once; otherwise the one-SM tiled form
- * (FP8RL_VARIANT_TILED).  WGrad takes the one-SM form (PAIR on request). */
+ * (FP8RL_VARIANT_TILED).  WGrad chooses the same way (its scale arrays always qualify). */
 FP8RL_API fp8rl_status fp8rl_gemm_fwd(const uint8_t* qx, const float* sx, const uint8_t* qw,
                             const float* sw, uint16_t* y, int64_t M, int64_t N, int64_t K,
                             void* ws, size_t ws_bytes, fp8rl_stream_t stream);
@@ -275,7 +275,7 @@ typedef struct {
                        clusters of two (0 = one per two SMs); ignored otherwise */
     int tile_n;     /* TILED: output tile width, 128 or 256 (0 = choose); PAIR: the pair
                        tile's width, 128 or 256 (0 = 256); ignored otherwise */
-    int epi_warps;  /* PAIR: epilogue warps per CTA, 8 or 16 (0 = choose); ignored otherwise */
+    int epi_warps;  /* PAIR: epilogue warps per CTA, 8 or 16 (0 = 8); ignored otherwise */
 } fp8rl_gemm_opts;
 
 /* Workspace bytes fp8rl_gemm_fwd_ex needs with these options (opts may be NULL = AUTO). */
