@@ -219,10 +219,10 @@ fp8rl_status run_pair(const TiledArgs& t, int clusters_req, int epi_req, int pn_
     p.nkb = (int)(t.Kr / 128);
     const int items = ((p.m_tiles + 1) / 2) * p.n_tiles;
     p.num_items = items;
-    choose_raster((p.m_tiles + 1) / 2, p.n_tiles, 256 * t.Kr, (int64_t)pn * t.Kr, &p.group, &p.raster_n);
-    p.timeout_ns = g_timeout_ns.load();
     int clusters = clusters_req > 0 ? clusters_req : num_sms / 2;
     clusters = std::max(1, std::min(clusters, items));
+    choose_raster((p.m_tiles + 1) / 2, p.n_tiles, 256 * t.Kr, (int64_t)pn * t.Kr, clusters, &p.group, &p.raster_n);
+    p.timeout_ns = g_timeout_ns.load();
     const int epi = epi_req == 8 || epi_req == 16 ? epi_req : 8;
     return cuda_status(launch_gemm_pair(ta, tb, tsa, tsb, tc, p, t.b_mode, epi, pn, clusters, st));
 }
@@ -249,10 +249,10 @@ fp8rl_status run_mc(const TiledArgs& t, int clusters_req, int num_sms, cudaStrea
     p.n_tiles = (int)((t.R2 + bn - 1) / bn);
     p.nkb = (int)(t.Kr / 128);
     p.num_items = ((p.m_tiles + 1) / 2) * p.n_tiles;
-    choose_raster((p.m_tiles + 1) / 2, p.n_tiles, 256 * t.Kr, (int64_t)bn * t.Kr, &p.group, &p.raster_n);
-    p.timeout_ns = g_timeout_ns.load();
     int clusters = clusters_req > 0 ? clusters_req : num_sms / 2;
     clusters = std::max(1, std::min(clusters, p.num_items));
+    choose_raster((p.m_tiles + 1) / 2, p.n_tiles, 256 * t.Kr, (int64_t)bn * t.Kr, clusters, &p.group, &p.raster_n);
+    p.timeout_ns = g_timeout_ns.load();
     return cuda_status(launch_gemm_mc(ta, tb, tsa, tsb, tc, p, t.b_mode, clusters, st));
 }
 
@@ -308,10 +308,10 @@ fp8rl_status run_tiled(const TiledArgs& t, int grid_req, int bn_req, int num_sms
     p.n_tiles = (int)((t.R2 + bn - 1) / bn);
     p.nkb = (int)(t.Kr / 128);
     p.num_items = p.m_tiles * p.n_tiles;
-    choose_raster(p.m_tiles, p.n_tiles, 128 * t.Kr, (int64_t)bn * t.Kr, &p.group, &p.raster_n);
-    p.timeout_ns = g_timeout_ns.load();
     int grid = grid_req > 0 ? grid_req : num_sms;
     grid = std::max(1, std::min(grid, p.num_items));
+    choose_raster(p.m_tiles, p.n_tiles, 128 * t.Kr, (int64_t)bn * t.Kr, grid, &p.group, &p.raster_n);
+    p.timeout_ns = g_timeout_ns.load();
     if (t.ldc % 8 != 0) return FP8RL_ERR_ALIGN;
     CUtensorMap tc;
     e = make_tmap_out(&tc, t.c, t.R1, t.R2, t.ldc);

@@ -70,10 +70,11 @@ __host__ __device__ inline void raster_tile(int tile, int m_units, int n_units, 
     *n = raster_n ? a : b;
 }
 
-// The group of raster_tile for an m_units x n_units grid of tiles whose row unit holds
-// a_unit_bytes of A and column tile b_unit_bytes of B (each across the whole reduction).
-void choose_raster(int64_t m_units, int64_t n_units, int64_t a_unit_bytes, int64_t b_unit_bytes, int* group,
-                   int* raster_n);
+// The tile order of raster_tile for an m_units x n_units grid of tiles whose row unit holds
+// a_unit_bytes of A and column tile b_unit_bytes of B (each across the whole reduction),
+// with `wave` tiles running at once.
+void choose_raster(int64_t m_units, int64_t n_units, int64_t a_unit_bytes, int64_t b_unit_bytes, int wave,
+                   int* group, int* raster_n);
 
 // Scale tensor maps (FP32; g = min(scale_group(), K-blocks) K-blocks per box): tsa over A's
 // row scales [K-block][R1], box 128 x g; tsb over B's scales, box BN x g for row scales

@@ -259,6 +259,7 @@ __global__ void __launch_bounds__(gemm_threads(B_MODE), 1)
             // split-K (decode) streams the weights (B) once: let them leave L2 first
             const uint64_t pol_a = l2_policy_evict_last();
             const uint64_t pol_b = SPLITK ? l2_policy_evict_first() : l2_policy_evict_last();
+            const uint64_t pol_s = pol_a;   // scales
             // K-blocks per scale box: the group size, or all of them when K is shorter
             const int sgrp = p.nkb < S::SG ? p.nkb : S::SG;
             uint32_t it = 0, s_issued = 0;
@@ -291,21 +292,21 @@ __global__ void __launch_bounds__(gemm_threads(B_MODE), 1)
                         const uint32_t a_bytes = (SD == SD_TMA) ? 128u * 4u * (uint32_t)sgrp : 0u;
                         if (B_MODE == SCALE_ROW) {
                             mbar_arrive_expect_tx(sb, a_bytes + (uint32_t)BN * 4u * (uint32_t)sgrp);
-                            tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, n0, kb0, pol_a);
+                            tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, n0, kb0, pol_s);
                         } else if (p.sb_kb == 1) {
                             // block scales stored [column block][K-block]: 4 K-blocks from a
                             // 4-aligned one (the box's x is a K-block index: x * 4 bytes must
                             // be a multiple of 16 whatever the group size) x the tile's
                             // BN/128 column blocks
                             mbar_arrive_expect_tx(sb, a_bytes + 16u * (BN / 128));
-                            tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, kb & ~3, n0 >> 7, pol_a);
+                            tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, kb & ~3, n0 >> 7, pol_s);
                         } else {
                             // block scales stored [K-block][column block]: 4 column blocks
                             // from a 4-aligned one, for each K-block of the group
                             mbar_arrive_expect_tx(sb, a_bytes + 16u * (uint32_t)sgrp);
-                            tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, (n0 >> 7) & ~3, kb0, pol_a);
+                            tma_load_2d(smem_u32(slot + S::SLOT_A), &tmSB, sb, (n0 >> 7) & ~3, kb0, pol_s);
                         }
-                        if (SD == SD_TMA) tma_load_2d(smem_u32(slot), &tmSA, sb, m0, kb0, pol_a);
+                        if (SD == SD_TMA) tma_load_2d(smem_u32(slot), &tmSA, sb, m0, kb0, pol_s);
                         ++s_issued;
                     }
                 }
