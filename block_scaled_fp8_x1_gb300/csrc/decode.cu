@@ -153,19 +153,37 @@ __global__ void __launch_bounds__(384, 1)
             const uint64_t pol_w = l2_policy_evict_first();   // each weight byte is read once
             const uint64_t pol_x = l2_policy_evict_last();    // every tile reads the activation
             constexpr uint32_t TX = C::W_BYTES + C::X_BYTES;
+            // The weights do not depend on the kernel that produces the activation: the
+            // first stages' weight tiles are requested before waiting for that kernel
+            // (a no-op when this grid was not launched as its dependent).
+            const uint32_t n_it = tile0 < tiles ? (uint32_t)((tiles - tile0 + tstep - 1) / tstep) * (uint32_t)nk : 0u;
+            const uint32_t n_pre = n_it < (uint32_t)STAGES ? n_it : (uint32_t)STAGES;
+            if (elect_one_sync()) {
+                for (uint32_t j = 0; j < n_pre; ++j) {
+                    const int tile = tile0 + (int)(j / (uint32_t)nk) * tstep;
+                    const int kb = kb0 + (int)(j % (uint32_t)nk);
+                    mbar_arrive_expect_tx(smem_u32(&full_bar[j]), TX);
+                    tma_load_2d(smem_u32(sW + j * C::W_BYTES), &tmW, smem_u32(&full_bar[j]), kb * 128, tile * 128, pol_w);
+                }
+            }
+            __syncwarp();
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             uint32_t it = 0;
             for (int tile = tile0; ok && tile < tiles; tile += tstep) {
                 const float* swt = p.sw + (int64_t)tile * p.sw_r;
                 for (int i = 0; i < nk; ++i, ++it) {
                     const int kb = kb0 + i;
                     const uint32_t s = it % STAGES;
-                    if (!mbar_wait(smem_u32(&empty_bar[s]), ((it / STAGES) & 1) ^ 1, p.timeout_ns, abort_flag)) {
+                    if (it >= n_pre &&
+                        !mbar_wait(smem_u32(&empty_bar[s]), ((it / STAGES) & 1) ^ 1, p.timeout_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
                     if (elect_one_sync()) {
-                        mbar_arrive_expect_tx(smem_u32(&full_bar[s]), TX);
-                        tma_load_2d(smem_u32(sW + s * C::W_BYTES), &tmW, smem_u32(&full_bar[s]), kb * 128, tile * 128, pol_w);
+                        if (it >= n_pre) {
+                            mbar_arrive_expect_tx(smem_u32(&full_bar[s]), TX);
+                            tma_load_2d(smem_u32(sW + s * C::W_BYTES), &tmW, smem_u32(&full_bar[s]), kb * 128, tile * 128, pol_w);
+                        }
                         tma_load_2d(smem_u32(sX + s * C::X_BYTES), &tmX, smem_u32(&full_bar[s]), kb * 128, 0, pol_x);
                     }
                     __syncwarp();
@@ -378,7 +396,7 @@ __global__ void __launch_bounds__(384, 1)
 
 template <int MP>
 static cudaError_t launch_decode_t(const CUtensorMap& tw, const CUtensorMap& tx, const DecodeParams& p,
-                                   int grid_clusters, int splits, cudaStream_t st) {
+                                   int grid_clusters, int splits, bool pdl, cudaStream_t st) {
     auto kern = k_decode<MP>;
     constexpr size_t smem = DecodeCfg<MP>::BYTES;
     static_assert(smem <= 227 * 1024, "shared memory budget");
@@ -389,13 +407,15 @@ static cudaError_t launch_decode_t(const CUtensorMap& tw, const CUtensorMap& tx,
     cfg.blockDim = dim3(384, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = (unsigned)splits;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, tw, tx, p);
 }
 
@@ -434,13 +454,13 @@ int decode_max_clusters(int M, int splits) {
 }
 
 cudaError_t launch_decode(const CUtensorMap& tw, const CUtensorMap& tx, const DecodeParams& p, int grid_clusters,
-                          int splits, cudaStream_t st) {
+                          int splits, bool pdl, cudaStream_t st) {
     if (splits > 1 && grid_clusters != p.tiles) return cudaErrorInvalidValue;   // one tile per cluster
     switch (decode_mp(p.M)) {
-        case 32: return launch_decode_t<32>(tw, tx, p, grid_clusters, splits, st);
-        case 64: return launch_decode_t<64>(tw, tx, p, grid_clusters, splits, st);
-        case 128: return launch_decode_t<128>(tw, tx, p, grid_clusters, splits, st);
-        default: return launch_decode_t<256>(tw, tx, p, grid_clusters, splits, st);
+        case 32: return launch_decode_t<32>(tw, tx, p, grid_clusters, splits, pdl, st);
+        case 64: return launch_decode_t<64>(tw, tx, p, grid_clusters, splits, pdl, st);
+        case 128: return launch_decode_t<128>(tw, tx, p, grid_clusters, splits, pdl, st);
+        default: return launch_decode_t<256>(tw, tx, p, grid_clusters, splits, pdl, st);
     }
 }
 

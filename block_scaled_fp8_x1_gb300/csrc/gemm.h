@@ -128,8 +128,10 @@ struct DecodeParams {
 };
 int decode_mp(int M);
 int decode_max_clusters(int M, int splits);
+// pdl: launch as a programmatic dependent of the stream's previous kernel (the kernel
+// requests its first weight tiles, then waits for that kernel before reading the activation).
 cudaError_t launch_decode(const CUtensorMap& tw, const CUtensorMap& tx, const DecodeParams& p, int grid_clusters,
-                          int splits, cudaStream_t st);
+                          int splits, bool pdl, cudaStream_t st);
 fp8rl_status read_and_clear_decode_status();
 
 // quantize.cu

@@ -46,6 +46,9 @@ __global__ void __launch_bounds__(256) k_quant_1x128(const uint16_t* __restrict_
                                                      int64_t K, int64_t ldx,
                                                      uint8_t* __restrict__ q,
                                                      float* __restrict__ s) {
+    // a grid launched as this one's dependent may start its own prologue now (it waits for
+    // this grid's completion before it reads q or s)
+    asm volatile("griddepcontrol.launch_dependents;");
     const int sub = threadIdx.x & 15;
     const int half = (threadIdx.x >> 4) & 1;
     const int warp = threadIdx.x >> 5;

@@ -302,7 +302,9 @@ FP8RL_API fp8rl_status fp8rl_gemm_wgrad_ex(const uint8_t* qdyT, const float* sdy
 
 /* One linear layer from the BF16 activation ("Core architecture": rollout and the
  * training forward pass run the same FP8 linear): x is quantized 1x128 into qx / sx
- * (exactly fp8rl_quantize_1x128), then Y = X W^T with the form fp8rl_gemm_fwd picks.
+ * (exactly fp8rl_quantize_1x128), then Y = X W^T with the form fp8rl_gemm_fwd picks.  In
+ * the decode form without a cluster split, the GEMM kernel starts streaming its weights
+ * while the quantizer finishes (programmatic dependent launch on the same stream).
  *   x : BF16 [M][ldx];  qw, sw, y, ws as for fp8rl_gemm_fwd;  qx : E4M3 [M][K] and
  *   sx : float [K/128][M] receive the quantized activation (caller-owned). */
 FP8RL_API fp8rl_status fp8rl_linear_fwd(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
