@@ -78,6 +78,14 @@ __device__ __forceinline__ uint32_t encode_pair_neg(float2 x, float s, float nr)
     const float2 d = __ffma2_rn(e, make_float2(nr, nr), qn);
     return e4m3x2(d.x, d.y);
 }
+// The same for a pair whose two elements belong to different groups (two columns of one
+// row under their 128x1 column scales): s = (s0, s1), nr = (nr0, nr1).
+__device__ __forceinline__ uint32_t encode_pair_neg2(float2 x, float2 s, float2 nr) {
+    const float2 qn = __fmul2_rn(x, nr);
+    const float2 e = __ffma2_rn(qn, s, x);
+    const float2 d = __ffma2_rn(e, nr, qn);
+    return e4m3x2(d.x, d.y);
+}
 // Four codes (two encode_pair_neg results packed) -> codes of x/s, zero groups cleared.
 __device__ __forceinline__ uint32_t flip_codes(uint32_t lo_pair, uint32_t hi_pair, uint32_t keep) {
     return ((lo_pair | (hi_pair << 16)) ^ 0x80808080u) & keep;

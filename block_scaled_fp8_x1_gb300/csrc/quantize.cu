@@ -274,15 +274,18 @@ __global__ void __launch_bounds__(256) k_rms_rstd(const uint16_t* __restrict__ x
 }
 
 // Input stages of the TMA ring (each a 128x128 BF16 tile; SiLU-mul stages gate and up).
-template <int PRO>
+template <int PRO, bool COLQ>
 struct PanelStages {
     static constexpr int NIN = (PRO == PRO_SILU) ? 2 : (PRO == PRO_SILU_BWD ? 3 : 1);
     // DEQUANT: a 128x128 code tile and its 128 row scales
     static constexpr int STAGE_BYTES = PRO == PRO_DEQUANT ? 128 * 128 + 128 * 4 : NIN * 128 * 128 * 2;
     // SiLU-mul stages 64 KB per tile: one stage lets two CTAs share an SM, which hides the
-    // copy latency better than three stages in one CTA (0.186 vs 0.242 ms at 8192x14336)
-    static constexpr int STAGES = (PRO == PRO_SILU || PRO == PRO_SILU_BWD) ? 1 : 3;
-    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 128;  // + alignment slack
+    // copy latency better than three stages in one CTA (0.186 vs 0.242 ms at 8192x14336).
+    // The 128x1 codes pass through two 16 KB shared-memory tiles (COLQ), which leaves room
+    // for two input stages of 32 KB at two CTAs per SM.
+    static constexpr int STAGES = (PRO == PRO_SILU || PRO == PRO_SILU_BWD) ? 1 : (COLQ && PRO != PRO_DEQUANT ? 2 : 3);
+    static constexpr int COLQ_OFF = ((STAGES * STAGE_BYTES + 127) / 128) * 128;
+    static constexpr size_t SMEM = (size_t)COLQ_OFF + (COLQ ? 2 * 128 * 128 : 0) + 128;  // + alignment slack
 };
 
 // A CTA works through a sequence of 128x128 tiles (see tile_at below).
@@ -290,11 +293,16 @@ struct PanelStages {
 // pull a tile into registers, and once everyone has it (the first barrier of the tile)
 // thread 0 refills that stage, so copies of the next tiles overlap the current one's math.
 // RMSNorm streams the CTA's tiles twice: pass 1 sums squares, pass 2 quantizes.
+// The 128x1 codes of a tile leave through shared memory (except after the three-input
+// SiLU-mul backward prologue, whose stage leaves no room): each thread writes its 8 columns
+// x 8 rows of codes there, and after a CTA barrier the tile goes out as 16-byte pieces, 8
+// lanes per 128-byte row of qT, instead of 16 scattered 8-byte pieces per warp store.
 template <int PRO, bool ROW_OUT, bool COL_OUT>
 __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ CUtensorMap tmx,
                                                      const __grid_constant__ CUtensorMap tmy,
                                                      const PanelArgs a) {
-    using PS = PanelStages<PRO>;
+    constexpr bool COLQ = COL_OUT && PRO != PRO_SILU_BWD;
+    using PS = PanelStages<PRO, COLQ>;
     constexpr int STAGES = PS::STAGES;
     extern __shared__ uint8_t q_smem_raw[];
     uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_smem_raw) + 127) & ~uintptr_t(127));
@@ -481,21 +489,75 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
                 c = __vmaxu2(c, __vmaxu2(__vmaxu2(wa(4, j), wa(5, j)), __vmaxu2(wa(6, j), wa(7, j))));
                 cm[j] = __vmaxu2(c, __shfl_xor_sync(0xffffffffu, c, 16));
             }
-            if (half == 0) *reinterpret_cast<uint4*>(&s_colmax[warp][cl * 4]) = make_uint4(cm[0], cm[1], cm[2], cm[3]);
+            // half h keeps the pair words 4cl + 2h, +1 (its own four columns) at word 32h + 2cl
+            *reinterpret_cast<uint2*>(&s_colmax[warp][32 * half + 2 * cl]) = half ? make_uint2(cm[2], cm[3]) : make_uint2(cm[0], cm[1]);
         }
-        // values are unpacked where they are encoded (once per direction): holding the 64
-        // unpacked floats would double the registers and halve the CTAs per SM
+        // values are unpacked where they are encoded: holding the 64 unpacked floats would
+        // double the registers and halve the CTAs per SM
         auto xrow = [&](int i, int j) { return make_float2(bf16_lo(w[i][j]), bf16_hi(w[i][j])); };
+        // this tile's qT staging buffer (two, alternating: the next tile's barrier orders
+        // this tile's reads before the writes of the tile after)
+        const uint32_t colq = smem_u32(stages + PS::COLQ_OFF) + (uint32_t)(item & 1) * (128u * 128u);
         __syncthreads();                                  // stage consumed, column maxima published
         if (tid == 0 && issued < total) issue(issued++);
 
+        // row scales: lane cl computes the scale of row (cl & 7) of its half; every lane
+        // takes the scales of its 8 rows from those lanes
+        FastScale fs = {};
         if (ROW_OUT) {
-            // lane cl computes the scale of row (cl & 7) of its half, then every lane takes
-            // the scales of its 8 rows from those lanes
             const int ri = cl & 7;
             const uint32_t pw = (ri >> 1) == 0 ? pm[0] : (ri >> 1) == 1 ? pm[1] : (ri >> 1) == 2 ? pm[2] : pm[3];
-            const FastScale fs = fast_scale(bf16_bits_amax_to_f32((ri & 1) ? (pw >> 16) : (pw & 0xFFFFu)));
+            fs = fast_scale(bf16_bits_amax_to_f32((ri & 1) ? (pw >> 16) : (pw & 0xFFFFu)));
             if (cl < 8 && m0 + R0 + ri < a.M) a.s[t * a.M + m0 + R0 + ri] = fs.s;
+        }
+        // column scales: this half computes those of columns C0 + 4*half + {0..3} (from the
+        // 8 warps' maxima) and swaps them with the other half for the remaining four
+        float cs[8], cr[8];
+        if (COL_OUT) {
+            uint32_t mx0 = 0, mx1 = 0;
+            #pragma unroll
+            for (int ww = 0; ww < 8; ++ww) {
+                const uint2 v = *reinterpret_cast<const uint2*>(&s_colmax[ww][32 * half + 2 * cl]);
+                mx0 = __vmaxu2(mx0, v.x);
+                mx1 = __vmaxu2(mx1, v.y);
+            }
+            const uint32_t mb[4] = {mx0 & 0xFFFFu, mx0 >> 16, mx1 & 0xFFFFu, mx1 >> 16};
+            float os[4], orr[4];
+            #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const FastScale f = fast_scale(bf16_bits_amax_to_f32(mb[e]));
+                os[e] = f.s;
+                orr[e] = f.nr;
+            }
+            if (warp == 0)
+                *reinterpret_cast<float4*>(a.sT + panel * a.K + k0 + C0 + 4 * half) = make_float4(os[0], os[1], os[2], os[3]);
+            #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float ts = __shfl_xor_sync(0xffffffffu, os[e], 16);
+                const float tr = __shfl_xor_sync(0xffffffffu, orr[e], 16);
+                cs[e] = half ? ts : os[e];
+                cr[e] = half ? tr : orr[e];
+                cs[4 + e] = half ? os[e] : ts;
+                cr[4 + e] = half ? orr[e] : tr;
+            }
+        }
+        // the 8 codes of column C0 + cc, rows R0 .. R0 + 7: into the qT staging tile, or
+        // straight to qT
+        auto col_store = [&](int cc, uint32_t lo, uint32_t hi) {
+            if (COLQ) {
+                // row c = C0 + cc of the staging tile holds its 8-byte pieces r8 = R0 / 8 at
+                // slot r8 ^ (2 (c/8 mod 8) + c/64): the 16 lanes of each half-warp store to 16
+                // different slots, so a store takes the minimum two wavefronts
+                const uint32_t slot = (uint32_t)((R0 >> 3) ^ (2 * (cl & 7) + (cl >> 3)));
+                asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(colq + (uint32_t)(C0 + cc) * 128u + slot * 8u),
+                             "r"(lo), "r"(hi)
+                             : "memory");
+            } else {
+                stg_v2(a.qT + (k0 + C0 + cc) * a.M + m0 + R0, lo, hi);
+            }
+        };
+        // 1x128 codes, one row at a time, any scale
+        auto row_codes = [&]() {
             #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int src = (lane & 16) | i;
@@ -514,37 +576,9 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
                 const int64_t m = m0 + R0 + i;
                 if (m < a.M) stg_v2(a.q + m * a.K + k0 + C0, lo, hi);
             }
-        }
-        if (COL_OUT) {
-            // this half computes the scales of columns C0 + 4*half + {0..3} (from the 8 warps'
-            // maxima) and swaps them with the other half for the remaining four
-            uint32_t mx0 = 0, mx1 = 0;
-            #pragma unroll
-            for (int ww = 0; ww < 8; ++ww) {
-                const uint2 v = *reinterpret_cast<const uint2*>(&s_colmax[ww][cl * 4 + 2 * half]);
-                mx0 = __vmaxu2(mx0, v.x);
-                mx1 = __vmaxu2(mx1, v.y);
-            }
-            const uint32_t mb[4] = {mx0 & 0xFFFFu, mx0 >> 16, mx1 & 0xFFFFu, mx1 >> 16};
-            float os[4], orr[4];
-            #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const FastScale f = fast_scale(bf16_bits_amax_to_f32(mb[e]));
-                os[e] = f.s;
-                orr[e] = f.nr;
-            }
-            if (warp == 0)
-                *reinterpret_cast<float4*>(a.sT + panel * a.K + k0 + C0 + 4 * half) = make_float4(os[0], os[1], os[2], os[3]);
-            float cs[8], cr[8];
-            #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float ts = __shfl_xor_sync(0xffffffffu, os[e], 16);
-                const float tr = __shfl_xor_sync(0xffffffffu, orr[e], 16);
-                cs[e] = half ? ts : os[e];
-                cr[e] = half ? tr : orr[e];
-                cs[4 + e] = half ? os[e] : ts;
-                cr[4 + e] = half ? orr[e] : tr;
-            }
+        };
+        // 128x1 codes, one column at a time (vertically adjacent pairs), any scale
+        auto col_codes = [&]() {
             #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
                 const int j = cc >> 1;
@@ -563,7 +597,83 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
                     lo = v.x | (v.y << 16);
                     hi = v.z | (v.w << 16);
                 }
-                stg_v2(a.qT + (k0 + C0 + cc) * a.M + m0 + R0, lo, hi);
+                col_store(cc, lo, hi);
+            }
+        };
+        if (ROW_OUT && COL_OUT) {
+            bool slow = fs.slow;
+            #pragma unroll
+            for (int cc = 0; cc < 8; ++cc) slow = slow || (cs[cc] > 0.0f && scale_is_slow(cs[cc]));
+            if (__any_sync(0xffffffffu, slow)) {
+                row_codes();
+                col_codes();
+            } else {
+                // No group of this warp needs a division: both directions from one unpack
+                // of each BF16 pair (columns 2j, 2j+1 of a row), the row code pair under the
+                // row's scale and the column code pair under the two columns' scales.  The
+                // column pairs of rows 2k and 2k+1 are packed as P[j][k] = bytes (r2k c2j,
+                // r2k c2j+1, r2k+1 c2j, r2k+1 c2j+1); byte permutes then give each column's
+                // 8 codes in row order.
+                float2 csp[4], crp[4];
+                #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    csp[j] = make_float2(cs[2 * j], cs[2 * j + 1]);
+                    crp[j] = make_float2(cr[2 * j], cr[2 * j + 1]);
+                }
+                uint32_t P[4][4], ev[4];
+                #pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int src = (lane & 16) | i;
+                    const float si = __shfl_sync(0xffffffffu, fs.s, src);
+                    const float nri = __shfl_sync(0xffffffffu, fs.nr, src);
+                    const uint32_t keep = si == 0.0f ? 0u : 0xFFFFFFFFu;
+                    uint32_t rc[4];
+                    #pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 x = xrow(i, j);
+                        rc[j] = encode_pair_neg(x, si, nri);
+                        const uint32_t c = encode_pair_neg2(x, csp[j], crp[j]);
+                        if (i & 1) P[j][i >> 1] = ev[j] | (c << 16);
+                        else ev[j] = c;
+                    }
+                    const int64_t m = m0 + R0 + i;
+                    if (m < a.M) stg_v2(a.q + m * a.K + k0 + C0, flip_codes(rc[0], rc[1], keep), flip_codes(rc[2], rc[3], keep));
+                }
+                #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    #pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int cc = 2 * j + e;
+                        const uint32_t keep = cs[cc] == 0.0f ? 0u : 0xFFFFFFFFu;
+                        const uint32_t sel = e ? 0x7531u : 0x6420u;
+                        col_store(cc, (__byte_perm(P[j][0], P[j][1], sel) ^ 0x80808080u) & keep,
+                                  (__byte_perm(P[j][2], P[j][3], sel) ^ 0x80808080u) & keep);
+                    }
+                }
+            }
+        } else if (ROW_OUT) {
+            row_codes();
+        } else if (COL_OUT) {
+            col_codes();
+        }
+        if (COLQ) {
+            __syncthreads();
+            {
+                // thread tid copies the 16-byte pieces id = tid + 256 i: row c = id / 8 of
+                // the staging tile, bytes 16k .. 16k + 15 (k = id % 8), i.e. its slots 2k and
+                // 2k + 1, which sit together at chunk k ^ (c/8 mod 8); 8 lanes write one
+                // 128-byte row of qT
+                #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int id = tid + 256 * i, c = id >> 3, k = id & 7;
+                    uint4 v;
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                                 : "r"(colq + (uint32_t)c * 128u + (uint32_t)((k ^ ((c >> 3) & 7)) * 16)));
+                    // rows c with c / 8 >= 8 hold the pair (2k, 2k+1) in swapped order
+                    if ((c >> 6) & 1) stg_v4(a.qT + (k0 + c) * a.M + m0 + 16 * k, v.z, v.w, v.x, v.y);
+                    else stg_v4(a.qT + (k0 + c) * a.M + m0 + 16 * k, v.x, v.y, v.z, v.w);
+                }
             }
         }
     }
@@ -852,7 +962,7 @@ static cudaError_t launch_panel_t(const PanelArgs& a, int64_t in_cols, int clust
         tm2 = tm;   // unused
     }
     auto kern = k_quant_panel<PRO, ROW_OUT, COL_OUT>;
-    constexpr size_t smem = PanelStages<PRO>::SMEM;
+    constexpr size_t smem = PanelStages<PRO, COL_OUT && PRO != PRO_SILU_BWD>::SMEM;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t ntiles = a.K / 128;
