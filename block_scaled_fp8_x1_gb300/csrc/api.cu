@@ -367,6 +367,16 @@ fp8rl_status run_decode(const uint8_t* qx, const float* sx, const uint8_t* qw, c
 // split-K form wins on every layer.
 bool decode_swapped_auto(int64_t M, int64_t N) { return M <= 64 || (M <= 128 && N <= 8192); }
 
+// 129-256 tokens against a wide weight: one 256-row pair tile per column tile already
+// fills every pair of SMs, reads each weight tile once and needs no reduction of slices,
+// so the paired training form beats the split-K form (Qwen2.5-7B gate_up 37888x3584 at
+// 256 tokens: 35.1 against 40.4 us per GEMM on GB300).
+bool decode_pair_auto(const TiledArgs& t, int num_sms) {
+    if (t.R1 <= 128 || !pair_eligible(t)) return false;
+    const int64_t pair_tiles = ((t.R1 + 255) / 256) * ((t.R2 + 255) / 256);
+    return pair_tiles >= num_sms / 2;
+}
+
 // Decode form with the weights on the MMA's M side (decode.cu).  Cluster size (split of
 // the reduction): the one that minimises waves x K-blocks per CTA, with one K-block of cost
 // for the cluster reduction, among the sizes whose clusters fit on the GPU at once.
@@ -640,6 +650,12 @@ size_t fp8rl_gemm_workspace_bytes_ex(int op, int64_t M, int64_t N, int64_t K,
         return 0;
     int sms = 0;
     if (current_device(&sms) != FP8RL_OK) sms = 148;
+    if (variant == FP8RL_VARIANT_AUTO && N % 128 == 0) {
+        TiledArgs t = {};   // the shape alone decides the route
+        t.sa_kb = M; t.sb_kb = 1; t.sb_r = K / 128; t.b_mode = SCALE_BLOCK;
+        t.R1 = M; t.R2 = N; t.Kr = K;
+        if (decode_pair_auto(t, sms)) return 0;
+    }
     const int64_t tiles = decode_tiles(M, N), nkb = K / 128;
     const int splits = (opts && opts->splits > 0) ? (int)std::min<int64_t>(opts->splits, nkb)
                                                   : choose_splits(tiles, nkb, sms);
@@ -658,21 +674,22 @@ fp8rl_status fp8rl_gemm_fwd_ex(const uint8_t* qx, const float* sx, const uint8_t
     if (!qx || !sx || !qw || !sw || !y) return FP8RL_ERR_INVALID_ARG;
     if (!aligned16(qx) || !aligned16(sx) || !aligned16(qw) || !aligned16(sw) || !aligned16(y))
         return FP8RL_ERR_ALIGN;
-    const bool swapped = variant == FP8RL_VARIANT_DECODE || (variant == FP8RL_VARIANT_AUTO && decode_swapped_auto(M, N));
-    const bool splitk = variant == FP8RL_VARIANT_SPLITK || (variant == FP8RL_VARIANT_AUTO && !swapped && M <= 256);
-    if ((swapped || splitk) && M > 256) return FP8RL_ERR_SHAPE;
     int sms = 0;
     fp8rl_status e = current_device(&sms);
     if (e != FP8RL_OK) return e;
-    if (swapped)
-        return run_decode_swap(qx, sx, qw, sw, y, M, N, K, opts ? opts->splits : 0, stream);
-    if (splitk)
-        return run_decode(qx, sx, qw, sw, y, M, N, K, ws, ws_bytes, opts ? opts->splits : 0, sms, stream);
     TiledArgs t;
     t.A = qx; t.sa = sx; t.sa_kb = M;
     t.B = qw; t.sb = sw; t.sb_kb = 1; t.sb_r = K / 128; t.b_mode = SCALE_BLOCK;
     t.c = y; t.ldc = N;
     t.R1 = M; t.R2 = N; t.Kr = K;
+    const bool swapped = variant == FP8RL_VARIANT_DECODE || (variant == FP8RL_VARIANT_AUTO && decode_swapped_auto(M, N));
+    const bool splitk = variant == FP8RL_VARIANT_SPLITK ||
+                        (variant == FP8RL_VARIANT_AUTO && !swapped && M <= 256 && !decode_pair_auto(t, sms));
+    if ((swapped || splitk) && M > 256) return FP8RL_ERR_SHAPE;
+    if (swapped)
+        return run_decode_swap(qx, sx, qw, sw, y, M, N, K, opts ? opts->splits : 0, stream);
+    if (splitk)
+        return run_decode(qx, sx, qw, sw, y, M, N, K, ws, ws_bytes, opts ? opts->splits : 0, sms, stream);
     return run_gemm(t, opts, sms, stream);
 }
 
@@ -767,15 +784,15 @@ fp8rl_status fp8rl_linear_fwd(const uint16_t* x, int64_t M, int64_t K, int64_t l
     if (e != FP8RL_OK) return e;
     e = cuda_status(launch_quant_1x128(x, M, K, ldx, qx, sx, sms, stream));
     if (e != FP8RL_OK) return e;
-    if (decode_swapped_auto(M, N))
-        return run_decode_swap(qx, sx, qw, sw, y, M, N, K, 0, stream, true);
-    if (M <= 256)
-        return run_decode(qx, sx, qw, sw, y, M, N, K, ws, ws_bytes, 0, sms, stream);
     TiledArgs t;
     t.A = qx; t.sa = sx; t.sa_kb = M;
     t.B = qw; t.sb = sw; t.sb_kb = 1; t.sb_r = K / 128; t.b_mode = SCALE_BLOCK;
     t.c = y; t.ldc = N;
     t.R1 = M; t.R2 = N; t.Kr = K;
+    if (decode_swapped_auto(M, N))
+        return run_decode_swap(qx, sx, qw, sw, y, M, N, K, 0, stream, true);
+    if (M <= 256 && !decode_pair_auto(t, sms))
+        return run_decode(qx, sx, qw, sw, y, M, N, K, ws, ws_bytes, 0, sms, stream);
     return run_gemm(t, nullptr, sms, stream);
 }
 

@@ -134,13 +134,13 @@ template <int PRO>
 __device__ __forceinline__ void rows_from_smem(const uint8_t* stage, const PanelArgs& a, int64_t k0,
                                                int R0, int C0, const float* s_rstd, const float (&rg)[8],
                                                uint32_t (&w)[8][4]) {
-    float gam[8];
+    float2 gam[4];   // gamma of columns (2j, 2j+1)
     if (PRO == PRO_RMSNORM || PRO == PRO_RMSNORM_G) {
         const uint4 gv = ldg_nc_v4(a.gamma + k0 + C0);
-        gam[0] = bf16_lo(gv.x); gam[1] = bf16_hi(gv.x);
-        gam[2] = bf16_lo(gv.y); gam[3] = bf16_hi(gv.y);
-        gam[4] = bf16_lo(gv.z); gam[5] = bf16_hi(gv.z);
-        gam[6] = bf16_lo(gv.w); gam[7] = bf16_hi(gv.w);
+        gam[0] = make_float2(bf16_lo(gv.x), bf16_hi(gv.x));
+        gam[1] = make_float2(bf16_lo(gv.y), bf16_hi(gv.y));
+        gam[2] = make_float2(bf16_lo(gv.z), bf16_hi(gv.z));
+        gam[3] = make_float2(bf16_lo(gv.w), bf16_hi(gv.w));
     }
     #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -173,11 +173,11 @@ __device__ __forceinline__ void rows_from_smem(const uint8_t* stage, const Panel
             for (int j = 0; j < 4; ++j) w[i][j] = xv[j];
         } else if (PRO == PRO_RMSNORM || PRO == PRO_RMSNORM_G) {
             const float r = (PRO == PRO_RMSNORM_G) ? rg[i] : s_rstd[R0 + i];
+            // (x * rstd) * gamma, each product rounded, on packed pairs
             #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float y0 = __fmul_rn(__fmul_rn(bf16_lo(xv[j]), r), gam[2 * j]);
-                const float y1 = __fmul_rn(__fmul_rn(bf16_hi(xv[j]), r), gam[2 * j + 1]);
-                w[i][j] = pack_bf16x2(y0, y1);
+                const float2 y = __fmul2_rn(__fmul2_rn(make_float2(bf16_lo(xv[j]), bf16_hi(xv[j])), make_float2(r, r)), gam[j]);
+                w[i][j] = pack_bf16x2(y.x, y.y);
             }
         } else if (PRO == PRO_SILU_BWD) {
             // stage: gate tile, up tile, tile of dh.  Columns [0, I) of the output are

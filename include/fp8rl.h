@@ -209,10 +209,11 @@ typedef enum { FP8RL_OP_FWD = 0, FP8RL_OP_DGRAD = 1, FP8RL_OP_WGRAD = 2 } fp8rl_
  * Small M takes a decode-shaped form.  Up to 64 tokens (and up to 128 when N <= 8192),
  * FP8RL_VARIANT_DECODE: each CTA streams 128 weight rows of one reduction slice, and the
  * slices of a tile are added in rank order inside a cluster (the result does not depend
- * on timing); no workspace.  Otherwise up to 256 tokens, FP8RL_VARIANT_SPLITK: tokens on
- * the tensor core's M side, the reduction split over CTAs whose FP32 partial sums a
- * second kernel adds in slice order;
- * it needs fp8rl_gemm_workspace_bytes(FP8RL_OP_FWD, M, N, K) bytes of workspace (no
+ * on timing); no workspace.  From 129 to 256 tokens against a weight wide enough that
+ * the paired-SM form's 256-row tiles alone cover every pair of SMs, that form (below).
+ * Otherwise up to 256 tokens, FP8RL_VARIANT_SPLITK: tokens on the tensor core's M side,
+ * the reduction split over CTAs whose FP32 partial sums a second kernel adds in slice
+ * order; it needs fp8rl_gemm_workspace_bytes(FP8RL_OP_FWD, M, N, K) bytes of workspace (no
  * initial contents required; calls that overlap in time need separate workspaces).  A
  * size of 0 means ws may be NULL.
  * Larger M takes the paired-SM form (FP8RL_VARIANT_PAIR, 256 x 256 tiles) when every

@@ -88,6 +88,8 @@ def test_workspace_sizes(abi):
     assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 128, 3584, 3584) == 0
     assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 128, 8320, 3584) > 0
     assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 256, 3584, 3584) > 0
+    # 256 tokens against a wide weight: the paired form, no workspace
+    assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 256, 37888, 3584) == 0
     assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_FWD, 8192, 3584, 3584) == 0
     assert L.fp8rl_gemm_workspace_bytes(abi.FP8RL_OP_WGRAD, 8192, 3584, 3584) == 0
     opts = abi.GemmOpts(abi.FP8RL_VARIANT_SPLITK, 4, 0)

@@ -215,7 +215,7 @@ def test_qwen7b_decode(fp8lib, oracle, M):
         qxr, sxr = oracle.quantize_1x128(bits16(x))
         assert_same_u8(u8(qx), qxr, f"{lin.name} X codes")
         assert_same_bits_f32(f32(sx), sxr, f"{lin.name} X scales")
-        y = fp8lib.gemm_fwd(qx, sx, qw, sw)       # automatic: the split-K decode form
+        y = fp8lib.gemm_fwd(qx, sx, qw, sw)       # automatic choice (gate_up at 256 tokens: the paired form)
         check_gemm_sampled(oracle, y, qxr, sxr, u8(qw), f32(sw), "fwd", 40 + idx,
                            f"decode {lin.name} M={M}")
 

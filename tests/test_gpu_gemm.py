@@ -71,7 +71,7 @@ def test_fwd_decode_swapped(fp8lib, oracle, M, splits):
 
 @pytest.mark.parametrize("M,N,K", [(64, 1280, 3584), (256, 768, 2048), (17, 2048, 512), (300, 512, 1024),
                                    (1, 1280, 1024), (31, 768, 512), (33, 1280, 2048), (100, 4608, 1024),
-                                   (128, 3584, 3584), (64, 37888, 3584)])
+                                   (128, 3584, 3584), (64, 37888, 3584), (256, 37888, 3584)])
 def test_linear_fwd_quantizes_and_multiplies(fp8lib, oracle, M, N, K):
     """The fused linear: its activation codes and scales are the oracle's 1x128 quantization
     bit for bit, and its output is within the GEMM bound of the oracle's result from them
