@@ -13,8 +13,10 @@ master weights stay BF16 and are re-quantized each step; DGrad and WGrad run in 
   backward         for each linear: quantize_1x128 dual(dY) -> gemm_dgrad -> gemm_wgrad
 
 value = GEMM FLOPs of the step / device time of the step (TFLOP/s), inputs resident in HBM
-and larger than L2.  e2e = the same with the step's inputs copied from pinned host memory
-and its results copied back inside the timed region.  Per-kernel CUDA-event times give the
+and larger than L2.  e2e = the same with the step's batch tensors (the three input
+activations and the four output gradients, 2.9 GB) copied from pinned host memory and its
+results (the layer output and the four weight gradients, 1.1 GB) copied back inside the
+timed region; the BF16 weights are model state on the device, re-quantized by the step.  Per-kernel CUDA-event times give the
 quantizers' GB/s and the roofline of the dominant kernel.  Two more workloads are reported
 beside it: the Llama-3.1-8B MLP training step at 8192 tokens, and the rollout decode
 linears of Qwen2.5-7B at 64, 128 and 256 tokens (CUDA-graph replays over weight copies
@@ -227,8 +229,12 @@ class Layer32Step:
         self.w = {n: synth.weight(w, lins[n], 10 + i, dev) for i, n in enumerate(LIN32)}
         self.dy = {n: synth.gradient(w, M32, LIN32[n][0], 20 + i, dev) for i, n in enumerate(LIN32)}
         self.eps = 1e-5
-        self.inputs = ["x_attn", "attn_out", "x_mlp", "gamma"] + [f"w.{n}" for n in LIN32] + \
-                      [f"dy.{n}" for n in LIN32]
+        # per-step batch tensors (the layer's input activations and the gradients of its
+        # outputs); the BF16 weights and gamma are model state that stays on the device and
+        # that the step itself re-quantizes, as the optimizer's updates would require
+        self.inputs = ["x_attn", "attn_out", "x_mlp"] + [f"dy.{n}" for n in LIN32]
+        # what a step hands back: the layer's output and the four weight gradients
+        self.results = ["y"] + [f"dw_{n}" for n in LIN32]
         self.outputs = {}
 
     def tensor(self, name):
@@ -527,7 +533,7 @@ def run_gpu(args):
     for n in step.inputs:
         host_in[n].copy_(step.tensor(n))
     outs = step.run()
-    host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in outs.items()}
+    host_out = {k: torch.empty_like(outs[k], device="cpu").pin_memory() for k in step.results}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     sets = [step, Layer32Step(dev)]               # device input sets, used alternately
@@ -552,9 +558,9 @@ def run_gpu(args):
         computed[i % 2].record(comp)
         down.wait_event(computed[i % 2])
         with torch.cuda.stream(down):
-            for k, v in o.items():
-                v.record_stream(down)
-                host_out[k].copy_(v, non_blocking=True)
+            for k in host_out:
+                o[k].record_stream(down)
+                host_out[k].copy_(o[k], non_blocking=True)
 
     def e2e_steps(n):
         upload(0)
@@ -635,7 +641,7 @@ def run_gpu(args):
         "roofline": roof,
         "e2e": {"value": round(job_rate(step_flops, world, ms_e2e) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4),
-                "copies": "every step's inputs up from pinned host memory and results down, on two copy streams overlapping the neighbouring steps' compute"},
+                "copies": "every step's batch tensors (X_attn, attention output, X_mlp, the four dY) up from pinned host memory and its results (y, the four dW) down, on two copy streams overlapping the neighbouring steps' compute; the BF16 weights stay on the device as model state and are re-quantized by the step"},
         "gpu_launches": Layer32Step.LAUNCHES_PER_STEP * args.steps,
         "clocks": clk,
         "kernels": kern,
