@@ -7,10 +7,10 @@
 //     dx_j     = r * gamma_j * dy_j - r^3 * x_j * S / K          (rounded to BF16)
 //     dgamma_k = sum_m dy_mk * x_mk * r_m                          (FP32)
 //
-// k_rms_bwd: each CTA takes a block of rows; thread t holds columns 8t + 2048 i of a row
-// (16-byte loads), the row's S is reduced over the CTA in a fixed order, dx is written as
-// BF16, and the thread's share of dgamma is accumulated over the CTA's rows with a
-// compensated (two-sum) FP32 pair.  The per-CTA partials go to a workspace that
+// k_rms_bwd: each CTA (one per SM) takes a block of rows; thread t holds columns
+// 8t + 8 NT i of a row (16-byte loads), the row's S is reduced over the CTA in a fixed
+// order, dx is written as BF16, and the thread's share of dgamma is accumulated over the
+// CTA's rows with a compensated (two-sum) FP32 pair.  The per-CTA partials go to a workspace that
 // k_rms_bwd_colsum adds in block order, so the result does not depend on timing.
 #include "common.cuh"
 #include "gemm.h"
@@ -19,8 +19,6 @@ namespace fp8rl {
 
 namespace {
 
-constexpr int kBwdThreads = 256;
-constexpr int kBwdChunk = 8 * kBwdThreads;   // columns per pass of the CTA over a row
 
 __device__ __forceinline__ uint4 ldg_v4(const uint16_t* p) {
     return __ldg(reinterpret_cast<const uint4*>(p));
@@ -39,12 +37,13 @@ __device__ __forceinline__ void two_sum_add(float& hi, float& lo, float v) {
 
 }  // namespace
 
-template <int NCH>
-__global__ void __launch_bounds__(kBwdThreads) k_rms_bwd(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma,
+template <int NCH, int NT>
+__global__ void __launch_bounds__(NT, 1) k_rms_bwd(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma,
                                                          const float* __restrict__ rstd, const uint16_t* __restrict__ dy,
                                                          int64_t M, int64_t K, uint16_t* __restrict__ dx,
                                                          float* __restrict__ ws) {
-    __shared__ float s_part[2][kBwdThreads / 32];
+    constexpr int kBwdChunk = 8 * NT;   // columns per pass of the CTA over a row
+    __shared__ float s_part[2][NT / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t rows = (M + gridDim.x - 1) / gridDim.x;
     const int64_t m_begin = (int64_t)blockIdx.x * rows;
@@ -70,15 +69,44 @@ __global__ void __launch_bounds__(kBwdThreads) k_rms_bwd(const uint16_t* __restr
         #pragma unroll
         for (int j = 0; j < 8; ++j) dg_hi[i][j] = dg_lo[i][j] = 0.0f;
 
+    // the loads of row m + PF run while row m is reduced and written: each thread keeps the
+    // raw words of the PF rows ahead in registers (one row at a time leaves the CTA waiting
+    // on memory latency at every row's barrier)
+    constexpr int PF = 2;
+    uint4 ra[PF][NCH], rb[PF][NCH];
+    auto load_row = [&](int64_t m, uint4 (&a)[NCH], uint4 (&b)[NCH]) {
+        #pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+            const int64_t c = (int64_t)i * kBwdChunk + 8 * tid;
+            const bool ok = valid[i] && m < m_end;
+            a[i] = ok ? ldg_v4(x + m * K + c) : make_uint4(0, 0, 0, 0);
+            b[i] = ok ? ldg_v4(dy + m * K + c) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    #pragma unroll
+    for (int f = 0; f < PF; ++f) load_row(m_begin + f, ra[f], rb[f]);
     int par = 0;
     for (int64_t m = m_begin; m < m_end; ++m, par ^= 1) {
+        uint4 ca[NCH], cb[NCH];
+        #pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+            ca[i] = ra[0][i];
+            cb[i] = rb[0][i];
+        }
+        #pragma unroll
+        for (int f = 0; f + 1 < PF; ++f)
+            #pragma unroll
+            for (int i = 0; i < NCH; ++i) {
+                ra[f][i] = ra[f + 1][i];
+                rb[f][i] = rb[f + 1][i];
+            }
+        load_row(m + PF, ra[PF - 1], rb[PF - 1]);
         float xv[NCH][8], dv[NCH][8];
         float part = 0.0f;
         #pragma unroll
         for (int i = 0; i < NCH; ++i) {
-            const int64_t c = (int64_t)i * kBwdChunk + 8 * tid;
-            const uint4 a = valid[i] ? ldg_v4(x + m * K + c) : make_uint4(0, 0, 0, 0);
-            const uint4 b = valid[i] ? ldg_v4(dy + m * K + c) : make_uint4(0, 0, 0, 0);
+            const uint4 a = ca[i];
+            const uint4 b = cb[i];
             const uint32_t av[4] = {a.x, a.y, a.z, a.w};
             const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
             #pragma unroll
@@ -98,7 +126,7 @@ __global__ void __launch_bounds__(kBwdThreads) k_rms_bwd(const uint16_t* __restr
         __syncthreads();
         float S = 0.0f;
         #pragma unroll
-        for (int w = 0; w < kBwdThreads / 32; ++w) S = __fadd_rn(S, s_part[par][w]);
+        for (int w = 0; w < NT / 32; ++w) S = __fadd_rn(S, s_part[par][w]);
         const float r = __ldg(rstd + m);
         const float coef = __fdiv_rn(__fmul_rn(__fmul_rn(__fmul_rn(r, r), r), S), (float)K);
         #pragma unroll
@@ -142,24 +170,30 @@ __global__ void __launch_bounds__(256) k_rms_bwd_colsum(const float* __restrict_
     dgamma[k] = __fadd_rn(hi, lo);
 }
 
-// Row blocks of the backward: two CTAs per SM, at most one per row.
+// Row blocks of the backward: one CTA per SM (its registers fill the SM), at most one per
+// row.
 int rmsnorm_bwd_blocks(int64_t M, int num_sms) {
-    const int64_t b = 2 * (int64_t)(num_sms > 0 ? num_sms : 148);
+    const int64_t b = (int64_t)(num_sms > 0 ? num_sms : 148);
     return (int)(M < b ? (M > 0 ? M : 1) : b);
 }
 
 cudaError_t launch_rmsnorm_bwd(const uint16_t* x, const uint16_t* gamma, const float* rstd, const uint16_t* dy,
                                int64_t M, int64_t K, uint16_t* dx, float* dgamma, float* ws, int nblocks,
                                cudaStream_t st) {
-    const int nch = (int)((K + kBwdChunk - 1) / kBwdChunk);
+    // up to 5120 columns one pass over the row with 8 columns per thread; wider rows take
+    // 256 threads and 3-4 passes (measured faster at 8192 columns: 0.169 against 0.182 ms
+    // at 16384 rows for 1024 threads, whose 64 registers allow one row of lead)
     float* part = dgamma ? ws : nullptr;
-    switch (nch) {
-        case 1: k_rms_bwd<1><<<nblocks, kBwdThreads, 0, st>>>(x, gamma, rstd, dy, M, K, dx, part); break;
-        case 2: k_rms_bwd<2><<<nblocks, kBwdThreads, 0, st>>>(x, gamma, rstd, dy, M, K, dx, part); break;
-        case 3: k_rms_bwd<3><<<nblocks, kBwdThreads, 0, st>>>(x, gamma, rstd, dy, M, K, dx, part); break;
-        case 4: k_rms_bwd<4><<<nblocks, kBwdThreads, 0, st>>>(x, gamma, rstd, dy, M, K, dx, part); break;
-        default: return cudaErrorInvalidValue;
-    }
+    if (K <= 8 * 512)
+        k_rms_bwd<1, 512><<<nblocks, 512, 0, st>>>(x, gamma, rstd, dy, M, K, dx, part);
+    else if (K <= 8 * 640)
+        k_rms_bwd<1, 640><<<nblocks, 640, 0, st>>>(x, gamma, rstd, dy, M, K, dx, part);
+    else if (K <= 3 * 2048)
+        k_rms_bwd<3, 256><<<nblocks, 256, 0, st>>>(x, gamma, rstd, dy, M, K, dx, part);
+    else if (K <= 4 * 2048)
+        k_rms_bwd<4, 256><<<nblocks, 256, 0, st>>>(x, gamma, rstd, dy, M, K, dx, part);
+    else
+        return cudaErrorInvalidValue;
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !dgamma) return e;
     k_rms_bwd_colsum<<<(unsigned)((K + 255) / 256), 256, 0, st>>>(ws, nblocks, K, dgamma);
