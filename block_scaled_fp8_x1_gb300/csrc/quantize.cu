@@ -145,24 +145,25 @@ __device__ __forceinline__ void rows_from_smem(const uint8_t* stage, const Panel
     #pragma unroll
     for (int i = 0; i < 8; ++i) {
         if (PRO == PRO_DEQUANT) {
-            // x^ = bf16(fl32(decode(code) * s_row)); decode from the format: sign, 4-bit
-            // exponent (bias 7), 3-bit mantissa, subnormal steps of 2^-9
+            // x^ = bf16(fl32(decode(code) * s_row)).  The hardware conversion decodes two
+            // codes into two FP16 values, exactly (every finite E4M3 value, subnormals
+            // included, is an FP16 value), and FP16 -> FP32 is exact.
             const uint2 c8 = *reinterpret_cast<const uint2*>(stage + (R0 + i) * 128 + C0);
             const float sr = *reinterpret_cast<const float*>(stage + 128 * 128 + 4 * (R0 + i));
             const uint32_t cw[2] = {c8.x, c8.y};
             #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                float o[2];
-                #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const uint32_t b = (cw[j >> 1] >> (8 * (2 * (j & 1) + e))) & 0xFFu;
-                    const uint32_t ex = (b >> 3) & 0xFu, mt = b & 7u;
-                    float mag = ex ? __uint_as_float(((ex + 120u) << 23) | (mt << 20))
-                                   : __fmul_rn((float)mt, 0.001953125f);
-                    mag = (b & 0x80u) ? -mag : mag;
-                    o[e] = __fmul_rn(mag, sr);
-                }
-                w[i][j] = pack_bf16x2(o[0], o[1]);
+                const uint16_t pair = (uint16_t)(cw[j >> 1] >> (16 * (j & 1)));   // codes 2j (low), 2j + 1
+                float d0, d1;
+                asm("{\n\t.reg .b32 h;\n\t.reg .f16 a, b;\n\t"
+                    "cvt.rn.f16x2.e4m3x2 h, %2;\n\t"
+                    "mov.b32 {a, b}, h;\n\t"
+                    "cvt.f32.f16 %0, a;\n\t"
+                    "cvt.f32.f16 %1, b;\n\t}"
+                    : "=f"(d0), "=f"(d1)
+                    : "h"(pair));
+                const float2 y = __fmul2_rn(make_float2(d0, d1), make_float2(sr, sr));
+                w[i][j] = pack_bf16x2(y.x, y.y);
             }
             continue;
         }
