@@ -847,6 +847,22 @@ def run_kernel(args):
             x = synth.normal_bf16((M, K), 0.02, 1, dev)
             fn = lambda: ops.quantize_128x128(x)
             work = M * K * (2 + 2) + 4 * M * K / 16384
+        elif k == "rmsnorm_bwd":
+            x = synth.normal_bf16((M, K), 1.0, 1, dev)
+            dy = synth.normal_bf16((M, K), 1e-3, 2, dev)
+            g = torch.ones(K, dtype=torch.bfloat16, device=dev)
+            _, _, _, _, rstd = ops.rmsnorm_quant(x, g, 1e-5, dual=False)
+            fn = lambda: ops.rmsnorm_bwd(x, g, rstd, dy)
+            work = M * K * (2 + 2 + 2) + 4 * M + 2 * K + 4 * K
+        elif k == "silu_mul_bwd_quant":      # shape M,I: gu [M,2I], dh [M,I]
+            gu = synth.normal_bf16((M, 2 * K), 2.0, 1, dev)
+            dh = synth.normal_bf16((M, K), 1e-3, 2, dev)
+            fn = lambda: ops.silu_mul_bwd_quant(gu, dh)
+            work = 2 * M * 2 * K + 2 * M * K + 2 * M * 2 * K + 8 * M * 2 * K / 128
+        elif k == "requantize_128x1":
+            q, s = ops.quantize_1x128(synth.normal_bf16((M, K), 1.0, 1, dev))
+            fn = lambda: ops.requantize_128x1(q, s)
+            work = M * K * (1 + 1) + 8 * M * K / 128
         else:
             raise SystemExit(f"unknown kernel {k}")
         unit = "GB/s"
@@ -878,7 +894,7 @@ def main():
     ap.add_argument("--kernel", default=None,
                     help="run one kernel form alone (for profiling): gemm_fwd, gemm_dgrad, "
                          "gemm_wgrad, gemm_decode, rmsnorm_quant, silu_mul_quant, quant_dual, "
-                         "quant_128x128")
+                         "quant_128x128, rmsnorm_bwd, silu_mul_bwd_quant, requantize_128x1")
     ap.add_argument("--shape", default=None, help="M,N,K (GEMMs) or M,K (quantizers)")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--tile-n", type=int, default=0, help="GEMM tile width (128/256) of the tiled or paired form")

@@ -26,6 +26,17 @@ __device__ __forceinline__ uint4 ldg_v4(const uint16_t* p) {
 __device__ __forceinline__ float lo16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// (hi, lo) += v with the exact two-sum, on packed pairs (a - b formed as fma(b, -1, a),
+// which is exact).
+__device__ __forceinline__ void two_sum_add2(float2& hi, float2& lo, float2 v) {
+    const float2 m1 = make_float2(-1.0f, -1.0f);
+    const float2 s = __fadd2_rn(hi, v);
+    const float2 bp = __ffma2_rn(hi, m1, s);
+    const float2 e = __fadd2_rn(__ffma2_rn(__ffma2_rn(bp, m1, s), m1, hi), __ffma2_rn(bp, m1, v));
+    hi = s;
+    lo = __fadd2_rn(lo, e);
+}
+
 // (hi, lo) += v with the exact two-sum.
 __device__ __forceinline__ void two_sum_add(float& hi, float& lo, float v) {
     const float s = __fadd_rn(hi, v);
@@ -49,7 +60,8 @@ __global__ void __launch_bounds__(NT, 1) k_rms_bwd(const uint16_t* __restrict__ 
     const int64_t m_begin = (int64_t)blockIdx.x * rows;
     const int64_t m_end = m_begin + rows < M ? m_begin + rows : M;
 
-    float gam[NCH][8];
+    // every per-element operation below runs on packed pairs (columns 2j, 2j + 1)
+    float2 gam[NCH][4];
     bool valid[NCH];
     #pragma unroll
     for (int i = 0; i < NCH; ++i) {
@@ -58,16 +70,13 @@ __global__ void __launch_bounds__(NT, 1) k_rms_bwd(const uint16_t* __restrict__ 
         const uint4 g = valid[i] ? ldg_v4(gamma + c) : make_uint4(0, 0, 0, 0);
         const uint32_t gv[4] = {g.x, g.y, g.z, g.w};
         #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            gam[i][2 * j] = lo16(gv[j]);
-            gam[i][2 * j + 1] = hi16(gv[j]);
-        }
+        for (int j = 0; j < 4; ++j) gam[i][j] = make_float2(lo16(gv[j]), hi16(gv[j]));
     }
-    float dg_hi[NCH][8], dg_lo[NCH][8];
+    float2 dg_hi[NCH][4], dg_lo[NCH][4];
     #pragma unroll
     for (int i = 0; i < NCH; ++i)
         #pragma unroll
-        for (int j = 0; j < 8; ++j) dg_hi[i][j] = dg_lo[i][j] = 0.0f;
+        for (int j = 0; j < 4; ++j) dg_hi[i][j] = dg_lo[i][j] = make_float2(0.0f, 0.0f);
 
     // the loads of row m + PF run while row m is reduced and written: each thread keeps the
     // raw words of the PF rows ahead in registers (one row at a time leaves the CTA waiting
@@ -101,8 +110,8 @@ __global__ void __launch_bounds__(NT, 1) k_rms_bwd(const uint16_t* __restrict__ 
                 rb[f][i] = rb[f + 1][i];
             }
         load_row(m + PF, ra[PF - 1], rb[PF - 1]);
-        float xv[NCH][8], dv[NCH][8];
-        float part = 0.0f;
+        float2 xv[NCH][4], dv[NCH][4];
+        float2 part2 = make_float2(0.0f, 0.0f);   // even and odd columns, summed in order
         #pragma unroll
         for (int i = 0; i < NCH; ++i) {
             const uint4 a = ca[i];
@@ -111,15 +120,14 @@ __global__ void __launch_bounds__(NT, 1) k_rms_bwd(const uint16_t* __restrict__ 
             const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
             #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                xv[i][2 * j] = lo16(av[j]);
-                xv[i][2 * j + 1] = hi16(av[j]);
-                dv[i][2 * j] = lo16(bv[j]);
-                dv[i][2 * j + 1] = hi16(bv[j]);
+                xv[i][j] = make_float2(lo16(av[j]), hi16(av[j]));
+                dv[i][j] = make_float2(lo16(bv[j]), hi16(bv[j]));
+                part2 = __ffma2_rn(__fmul2_rn(dv[i][j], gam[i][j]), xv[i][j], part2);
             }
-            #pragma unroll
-            for (int j = 0; j < 8; ++j) part = __fmaf_rn(__fmul_rn(dv[i][j], gam[i][j]), xv[i][j], part);
         }
-        // S over the row: a fixed shuffle tree in each warp, then the warps in order
+        // S over the row: the thread's two sums, a fixed shuffle tree in each warp, then
+        // the warps in order
+        float part = __fadd_rn(part2.x, part2.y);
         #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, off));
         if (lane == 0) s_part[par][warp] = part;
@@ -129,6 +137,7 @@ __global__ void __launch_bounds__(NT, 1) k_rms_bwd(const uint16_t* __restrict__ 
         for (int w = 0; w < NT / 32; ++w) S = __fadd_rn(S, s_part[par][w]);
         const float r = __ldg(rstd + m);
         const float coef = __fdiv_rn(__fmul_rn(__fmul_rn(__fmul_rn(r, r), r), S), (float)K);
+        const float2 r2 = make_float2(r, r), nc2 = make_float2(-coef, -coef);
         #pragma unroll
         for (int i = 0; i < NCH; ++i) {
             if (!valid[i]) continue;
@@ -136,15 +145,14 @@ __global__ void __launch_bounds__(NT, 1) k_rms_bwd(const uint16_t* __restrict__ 
             uint32_t o[4];
             #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float d0 = __fsub_rn(__fmul_rn(__fmul_rn(r, gam[i][2 * j]), dv[i][2 * j]), __fmul_rn(coef, xv[i][2 * j]));
-                const float d1 = __fsub_rn(__fmul_rn(__fmul_rn(r, gam[i][2 * j + 1]), dv[i][2 * j + 1]),
-                                           __fmul_rn(coef, xv[i][2 * j + 1]));
-                o[j] = pack_bf16x2(d0, d1);
+                // (r * gamma) * dy - coef * x, each product rounded, then the difference
+                const float2 d = __fadd2_rn(__fmul2_rn(__fmul2_rn(r2, gam[i][j]), dv[i][j]), __fmul2_rn(nc2, xv[i][j]));
+                o[j] = pack_bf16x2(d.x, d.y);
             }
             *reinterpret_cast<uint4*>(dx + m * K + c) = make_uint4(o[0], o[1], o[2], o[3]);
             if (ws) {
                 #pragma unroll
-                for (int j = 0; j < 8; ++j) two_sum_add(dg_hi[i][j], dg_lo[i][j], __fmul_rn(__fmul_rn(dv[i][j], xv[i][j]), r));
+                for (int j = 0; j < 4; ++j) two_sum_add2(dg_hi[i][j], dg_lo[i][j], __fmul2_rn(__fmul2_rn(dv[i][j], xv[i][j]), r2));
             }
         }
     }
@@ -155,7 +163,10 @@ __global__ void __launch_bounds__(NT, 1) k_rms_bwd(const uint16_t* __restrict__ 
             const int64_t c = (int64_t)i * kBwdChunk + 8 * tid;
             float* dst = ws + (int64_t)blockIdx.x * K + c;
             #pragma unroll
-            for (int j = 0; j < 8; ++j) dst[j] = __fadd_rn(dg_hi[i][j], dg_lo[i][j]);
+            for (int j = 0; j < 4; ++j) {
+                dst[2 * j] = __fadd_rn(dg_hi[i][j].x, dg_lo[i][j].x);
+                dst[2 * j + 1] = __fadd_rn(dg_hi[i][j].y, dg_lo[i][j].y);
+            }
         }
     }
 }
