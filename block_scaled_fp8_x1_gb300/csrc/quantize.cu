@@ -706,9 +706,10 @@ struct W128Args {
     uint8_t* qT;
     uint64_t timeout_ns;
 };
-constexpr int kW128Stages = 3;
+constexpr int kW128Stages = 2;
 constexpr int kW128StageBytes = 128 * 128 * 2;
-constexpr size_t kW128Smem = (size_t)kW128Stages * kW128StageBytes + 128;   // + alignment slack
+// + two 16 KB staging tiles for the W^T codes, + alignment slack
+constexpr size_t kW128Smem = (size_t)kW128Stages * kW128StageBytes + 2 * 128 * 128 + 128;
 
 __global__ void __launch_bounds__(256, 2) k_quant_128x128(const __grid_constant__ CUtensorMap tmw,
                                                           const W128Args a) {
@@ -831,18 +832,28 @@ __global__ void __launch_bounds__(256, 2) k_quant_128x128(const __grid_constant_
                     ct[4 * ch + 2][rh] = __byte_perm(t1, t3, 0x5410);
                     ct[4 * ch + 3][rh] = __byte_perm(t1, t3, 0x7632);
                 }
-            // 16-byte stores: lanes l and l^16 (rows R0 and R0 + 8 of W) hold the two halves
-            // of a 16-byte piece of each W^T row; half 0 stores the even W^T rows, half 1
-            // the odd ones.
+            // The W^T codes go out through a shared-memory tile, as in the panel
+            // quantizers: row c = C0 + j of the tile holds its 8-byte pieces r8 = R0 / 8 at
+            // slot r8 ^ (2 (c/8 mod 8) + c/64), so a warp store takes two wavefronts; after
+            // a CTA barrier the tile leaves as 16-byte pieces, 8 lanes per 128-byte W^T row.
+            const uint32_t colq = smem_u32(stages + kW128Stages * kW128StageBytes) + (uint32_t)(item & 1) * (128u * 128u);
+            const uint32_t slot = (uint32_t)((R0 >> 3) ^ (2 * (cl & 7) + (cl >> 3)));
             #pragma unroll
-            for (int pr = 0; pr < 4; ++pr) {
-                const uint32_t g0 = __shfl_xor_sync(0xffffffffu, half ? ct[2 * pr][0] : ct[2 * pr + 1][0], 16);
-                const uint32_t g1 = __shfl_xor_sync(0xffffffffu, half ? ct[2 * pr][1] : ct[2 * pr + 1][1], 16);
-                const uint32_t o0 = half ? ct[2 * pr + 1][0] : ct[2 * pr][0];
-                const uint32_t o1 = half ? ct[2 * pr + 1][1] : ct[2 * pr][1];
-                const int j = 2 * pr + half;
-                if (half) stg_v4(qT + (k0 + C0 + j) * N + n0 + R0 - 8, g0, g1, o0, o1);
-                else      stg_v4(qT + (k0 + C0 + j) * N + n0 + R0, o0, o1, g0, g1);
+            for (int j = 0; j < 8; ++j)
+                asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(colq + (uint32_t)(C0 + j) * 128u + slot * 8u),
+                             "r"(ct[j][0]), "r"(ct[j][1])
+                             : "memory");
+            __syncthreads();
+            #pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int id = tid + 256 * i, c = id >> 3, k = id & 7;
+                uint4 v;
+                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                             : "r"(colq + (uint32_t)c * 128u + (uint32_t)((k ^ ((c >> 3) & 7)) * 16)));
+                // rows c with c / 8 >= 8 hold the pair (2k, 2k+1) in swapped order
+                if ((c >> 6) & 1) stg_v4(qT + (k0 + c) * N + n0 + 16 * k, v.z, v.w, v.x, v.y);
+                else stg_v4(qT + (k0 + c) * N + n0 + 16 * k, v.x, v.y, v.z, v.w);
             }
         }
     }
