@@ -7,8 +7,9 @@
 // "Implementation": quantization, transposition and fused activation / RMSNorm kernels.
 //
 // All quantizers are HBM-bound.  The panel kernels read a 128-row x 128-column BF16
-// sub-tile once and emit both the 1x128 (row-group) codes and the transposed 128x1
-// (column-group) codes from registers.  Thread layout in a 256-thread CTA: warp w, lane l
+// sub-tile once and emit both the 1x128 (row-group) codes, straight from registers, and
+// the transposed 128x1 (column-group) codes, through a shared-memory tile that leaves in
+// 128-byte rows.  Thread layout in a 256-thread CTA: warp w, lane l
 // owns rows 16w + 8*(l/16) + [0,8) and columns 8*(l%16) + [0,8) of the sub-tile, so each
 // warp-wide load reads two full 256-byte rows, a row group is reduced over 16 lanes and a
 // column group over the two half-warps and the 8 warps.
