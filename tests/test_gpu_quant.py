@@ -72,6 +72,30 @@ def test_quantize_dual(fp8lib, oracle, M, K):
     assert_same_bits_f32(f32(sT), sTr, "sT")
 
 
+def test_quantize_dual_tiny_columns(fp8lib, oracle):
+    """128x1 groups whose scale is below 2^-68 (the exact-division fallback), one of them
+    of BF16 denormals, and an all-zero column, beside ordinary columns of the same tiles."""
+    M, K = 256, 512
+    x = synth.normal_bf16((M, K), 1.0, 5, "cuda").float()
+    x[128:256, 130] *= 2.0 ** -100
+    x[128:256, 131] = 0.0
+    x[0:128, 300:308] *= 2.0 ** -90
+    x[0:128, 511] = 0.0
+    x[17, 511] = 2.0 ** -133
+    x[90, 511] = -(2.0 ** -132)
+    x = x.to(torch.bfloat16)
+    q, s, qT, sT = fp8lib.quantize_1x128(x, dual=True)
+    xb = bits16(x)
+    qr, sr = oracle.quantize_1x128(xb)
+    qTr, sTr = oracle.quantize_128x1(xb)
+    assert_same_u8(u8(q), qr, "q")
+    assert_same_bits_f32(f32(s), sr, "s")
+    assert_same_u8(u8(qT), qTr, "qT")
+    assert_same_bits_f32(f32(sT), sTr, "sT")
+    st = f32(sT)
+    assert 0.0 < st[1, 130] < 2.0 ** -68 and st[1, 131] == 0.0 and 0.0 < st[0, 511] < 2.0 ** -68
+
+
 @pytest.mark.parametrize("M,K", [(128, 256), (512, 384)])
 def test_quantize_128x1(fp8lib, oracle, M, K):
     x = synth.normal_bf16((M, K), 1e-3, 11 + M, "cuda")
