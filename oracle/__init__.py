@@ -12,6 +12,8 @@ follows, is written beside the C code.
 Array conventions (all numpy, C-contiguous):
   * BF16 tensors travel as ``uint16`` bit patterns.
   * E4M3 codes are ``uint8``; scales are ``float32``.
+  * NVFP4 (E2M1) codes are packed two to a ``uint8``, element 2i in the low nibble; their
+    E4M3 block scales are ``uint8`` [rows, K/16], the per-row scales ``float32``.
 """
 from __future__ import annotations
 
@@ -73,6 +75,12 @@ def _load():
             "orc_gemm": (None, [P, I64, P, I64, P, I64, P, I64, I64, I64, I64, I64, I64, P]),
             "orc_gemm_sampled": (None, [P, I64, P, I64, P, I64, P, I64, I64, I64, I64, P, P,
                                         I64, P]),
+            "orc_e2m1_decode": (ctypes.c_double, [ctypes.c_uint8]),
+            "orc_e2m1_encode": (ctypes.c_uint8, [ctypes.c_float]),
+            "orc_e2m1_encode_array": (None, [P, P, I64]),
+            "orc_quantize_nvfp4": (None, [P, I64, I64, I64, P, P, P]),
+            "orc_gemm_nvfp4": (None, [P, P, P, I64, P, P, P, I64, I64, P]),
+            "orc_gemm_nvfp4_sampled": (None, [P, P, P, P, P, P, I64, P, P, I64, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -323,4 +331,60 @@ def gemm_sampled(A, sa, B, sb, mode: str, r1, r2):
     y = np.empty(i1.size, dtype=np.float64)
     _load().orc_gemm_sampled(_p(A), Kr, _p(sa), R1, _p(B), Kr, _p(sb), sb_kb, sb_r, sb_rdiv,
                              Kr, _p(i1), _p(i2), i1.size, _p(y))
+    return y
+
+
+# ------------------------------------------------------------------ NVFP4 (rollout format)
+
+def e2m1_decode(codes: np.ndarray) -> np.ndarray:
+    """E2M1 codes (low 4 bits) -> binary64 values."""
+    lib = _load()
+    table = np.array([lib.orc_e2m1_decode(c) for c in range(16)], dtype=np.float64)
+    return table[_c(codes, np.uint8) & 0xF]
+
+
+def e2m1_encode(v: np.ndarray) -> np.ndarray:
+    """Finite binary32 values -> E2M1 codes (RNE, saturating at +-6), one per byte."""
+    x = _c(v, np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().orc_e2m1_encode_array(_p(x), _p(out), x.size)
+    return out
+
+
+def quantize_nvfp4(x_bf16: np.ndarray):
+    """X[M,K] (BF16 bits) -> (q uint8 [M, K/2] packed E2M1, sf uint8 [M, K/16] E4M3 block
+    scales, g float32 [M] per-row scales)."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    assert K % 16 == 0
+    q = np.empty((M, K // 2), dtype=np.uint8)
+    sf = np.empty((M, K // 16), dtype=np.uint8)
+    g = np.empty(M, dtype=np.float32)
+    _load().orc_quantize_nvfp4(_p(x), M, K, K, _p(q), _p(sf), _p(g))
+    return q, sf, g
+
+
+def gemm_nvfp4(qx, sfx, gx, qw, sfw, gw):
+    """y[M,N] = gx[m] gw[n] sum_k e2m1(x) sbx e2m1(w) sbw in binary64 (unrounded)."""
+    qx, qw = _c(qx, np.uint8), _c(qw, np.uint8)
+    sfx, sfw = _c(sfx, np.uint8), _c(sfw, np.uint8)
+    gx, gw = _c(gx, np.float32), _c(gw, np.float32)
+    M, K2 = qx.shape
+    N, K2w = qw.shape
+    assert K2 == K2w and sfx.shape == (M, K2 // 8) and sfw.shape == (N, K2 // 8)
+    y = np.empty((M, N), dtype=np.float64)
+    _load().orc_gemm_nvfp4(_p(qx), _p(sfx), _p(gx), M, _p(qw), _p(sfw), _p(gw), N, 2 * K2, _p(y))
+    return y
+
+
+def gemm_nvfp4_sampled(qx, sfx, gx, qw, sfw, gw, m, n):
+    """The same as ``gemm_nvfp4`` at output positions (m[i], n[i]) only."""
+    qx, qw = _c(qx, np.uint8), _c(qw, np.uint8)
+    sfx, sfw = _c(sfx, np.uint8), _c(sfw, np.uint8)
+    gx, gw = _c(gx, np.float32), _c(gw, np.float32)
+    K = 2 * qx.shape[1]
+    im, inn = _c(m, np.int64), _c(n, np.int64)
+    y = np.empty(im.size, dtype=np.float64)
+    _load().orc_gemm_nvfp4_sampled(_p(qx), _p(sfx), _p(gx), _p(qw), _p(sfw), _p(gw), K, _p(im), _p(inn),
+                                   im.size, _p(y))
     return y

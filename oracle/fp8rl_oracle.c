@@ -38,6 +38,19 @@
  *       as the identity): with r the forward's rstd and S = sum_k dy_k*gamma_k*x_k,
  *       dx_j = r*gamma_j*dy_j - r^3*x_j*S/K in binary64, rounded to BF16;
  *       dgamma_k = sum_m dy_mk*x_mk*r_m in binary64.
+ *   R10 NVFP4, the format the QeRL page names for rollout (the pages fix nothing else, so
+ *       the format's public definition): elements are FP4 E2M1 (values 0, 0.5, 1, 1.5, 2,
+ *       3, 4, 6 and their negatives), 16 consecutive elements of a row share one E4M3
+ *       block scale, and an FP32 second-level scale is applied on top.  Reading: the
+ *       second-level scale is per row (per output channel of a weight, per token of an
+ *       activation).  For a row with amax a:  g = fl32(a / 2688)  (2688 = 6 * 448);  a
+ *       block with amax b gets the E4M3 code sb = E4M3(fl32(b / fl32(6 g))) (R3's
+ *       rounding, saturating at 448) and the decode scale d = fl32(decode(sb) * g); each
+ *       element gets code E2M1(fl32(x / d)), round to nearest even, saturating at +-6, the
+ *       sign kept for values that round to zero.  d = 0 (an all-zero row, or a block too
+ *       small for E4M3 against its row) gives codes 0.  x^ = e2m1 * decode(sb) * g.
+ *   R11 NVFP4 GEMM: y[m][n] = gx[m] * gw[n] * sum_k e2m1(x_mk) sbx * e2m1(w_nk) sbw in
+ *       binary64, unrounded (each product of decoded codes and block scales is exact).
  *
  * Every routine is written as the plain definition: scalar loops, no blocking or fusion.
  * Independent groups are spread over OpenMP threads only to make big inputs finish.
@@ -494,4 +507,109 @@ ORC_API void orc_gemm_sampled(const uint8_t* A, int64_t lda, const float* sa, in
     #pragma omp parallel for schedule(dynamic, 16) num_threads(g_threads)
     for (int64_t i = 0; i < n; ++i)
         y[i] = gemm_elem(A, lda, sa, sa_kb, B, ldb, sb, sb_kb, sb_r, sb_rdiv, Kr, r1[i], r2[i]);
+}
+
+/* ---------------------------------------------------------------- NVFP4 (R10, R11) */
+
+/* Decode an E2M1 code (bits 0-3): 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit.
+ * Exponent field 0 is subnormal (m * 0.5); the format has no infinity and no NaN. */
+ORC_API double orc_e2m1_decode(uint8_t c) {
+    int sign = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+/* Encode a finite binary32 value as E2M1: round to nearest, ties to even, saturating at
+ * +-6.  Below 2 the grid spacing is 0.5 (the subnormals 0, 0.5 and the binade [1, 2)),
+ * [2, 4) has spacing 1 and [4, 8) spacing 2.  As for E4M3, ties to the even count of
+ * spacings are ties to the even mantissa bit. */
+ORC_API uint8_t orc_e2m1_encode(float v) {
+    uint8_t sign = signbit(v) ? 0x8 : 0x0;
+    double a = fabs((double)v);
+    if (a >= 6.0) return sign | 0x7;
+    double ulp = a < 2.0 ? 0.5 : (a < 4.0 ? 1.0 : 2.0);
+    double n = a / ulp;
+    double lo = floor(n), hi = lo + 1.0;
+    double r;
+    if (n - lo < hi - n) r = lo;
+    else if (n - lo > hi - n) r = hi;
+    else r = (fmod(lo, 2.0) == 0.0) ? lo : hi;
+    double mag = r * ulp; /* one of 0, 0.5, 1, 1.5, 2, 3, 4, 6 */
+    if (mag < 1.0) return sign | (uint8_t)(mag * 2.0);
+    int e;
+    frexp(mag, &e);
+    e -= 1; /* mag in [2^e, 2^(e+1)) */
+    int m = (int)((mag / ldexp(1.0, e) - 1.0) * 2.0);
+    return sign | (uint8_t)(((e + 1) << 1) | m);
+}
+
+ORC_API void orc_e2m1_encode_array(const float* v, uint8_t* out, int64_t n) {
+    #pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_e2m1_encode(v[i]);
+}
+
+/* NVFP4 quantization of the rows of x[M][K] (BF16 bits, row stride ldx), R10.
+ * q[M][K/2]: element k of a row in bits 4*(k%2) .. 4*(k%2)+3 of byte k/2;
+ * sf[M][K/16]: the E4M3 block scales; g[M]: the per-row FP32 scales. */
+ORC_API void orc_quantize_nvfp4(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                                uint8_t* sf, float* g) {
+    #pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t r = 0; r < M; ++r) {
+        const uint16_t* row = x + r * ldx;
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float a = fabsf(orc_bf16_to_f32(row[k]));
+            if (a > amax) amax = a;
+        }
+        float gr = amax / 2688.0f;
+        g[r] = gr;
+        float g6 = 6.0f * gr;
+        for (int64_t b = 0; b < K / 16; ++b) {
+            float bmax = 0.0f;
+            for (int64_t k = 16 * b; k < 16 * b + 16; ++k) {
+                float a = fabsf(orc_bf16_to_f32(row[k]));
+                if (a > bmax) bmax = a;
+            }
+            uint8_t sb = gr > 0.0f ? orc_e4m3_encode(bmax / g6) : 0x00;
+            sf[r * (K / 16) + b] = sb;
+            float dsb = (float)orc_e4m3_decode(sb);
+            float d = dsb * gr;
+            for (int64_t k = 16 * b; k < 16 * b + 16; ++k) {
+                uint8_t c = d > 0.0f ? orc_e2m1_encode(orc_bf16_to_f32(row[k]) / d) : 0x0;
+                uint8_t* byte = q + r * (K / 2) + k / 2;
+                if (k % 2 == 0) *byte = c;
+                else *byte = (uint8_t)(*byte | (c << 4));
+            }
+        }
+    }
+}
+
+/* x^[m][k] of R10 without the per-row scale: e2m1(code) * decode(sb), exact. */
+static double nvfp4_elem(const uint8_t* q, const uint8_t* sf, int64_t K, int64_t r, int64_t k) {
+    uint8_t byte = q[r * (K / 2) + k / 2];
+    uint8_t c = (k % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+    return orc_e2m1_decode(c) * orc_e4m3_decode(sf[r * (K / 16) + k / 16]);
+}
+
+static double nvfp4_gemm_elem(const uint8_t* qx, const uint8_t* sfx, const float* gx, const uint8_t* qw,
+                              const uint8_t* sfw, const float* gw, int64_t K, int64_t m, int64_t n) {
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k) acc += nvfp4_elem(qx, sfx, K, m, k) * nvfp4_elem(qw, sfw, K, n, k);
+    return (double)gx[m] * (double)gw[n] * acc;
+}
+
+/* y[M][N] of R11 (binary64, unrounded). */
+ORC_API void orc_gemm_nvfp4(const uint8_t* qx, const uint8_t* sfx, const float* gx, int64_t M, const uint8_t* qw,
+                            const uint8_t* sfw, const float* gw, int64_t N, int64_t K, double* y) {
+    #pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) y[m * N + n] = nvfp4_gemm_elem(qx, sfx, gx, qw, sfw, gw, K, m, n);
+}
+
+/* Sampled outputs of R11: y[i] = y[m[i]][n[i]]. */
+ORC_API void orc_gemm_nvfp4_sampled(const uint8_t* qx, const uint8_t* sfx, const float* gx, const uint8_t* qw,
+                                    const uint8_t* sfw, const float* gw, int64_t K, const int64_t* m,
+                                    const int64_t* n, int64_t count, double* y) {
+    #pragma omp parallel for schedule(dynamic, 16) num_threads(g_threads)
+    for (int64_t i = 0; i < count; ++i) y[i] = nvfp4_gemm_elem(qx, sfx, gx, qw, sfw, gw, K, m[i], n[i]);
 }
