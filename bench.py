@@ -111,6 +111,13 @@ def decode_work(M, N, K):
     return 2.0 * M * N * K, N * K + 4 * (N // 128) * (K // 128) + 2 * M * K + 2 * M * N
 
 
+def decode_work_nvfp4(M, N, K):
+    """(FLOPs, algorithmic HBM bytes) of one NVFP4 decode linear: the packed E2M1 weights,
+    their E4M3 block scales (one per 16) and row scales, the BF16 activations in, the BF16
+    output."""
+    return 2.0 * M * N * K, N * K // 2 + N * K // 16 + 4 * N + 2 * M * K + 2 * M * N
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -404,29 +411,40 @@ def backward_ops_table(dev, hbm, reps=10):
     return rows
 
 
-def decode_table(dev, fp8_peak, hbm, reps=40):
+def decode_table(dev, fp8_peak, hbm, reps=40, fmt="fp8"):
     """Qwen2.5-7B decode linears at M in {64, 128, 256}: the fused linear (activation
     quantization, then the decode GEMM) per call, timed as CUDA-graph replays of `reps` calls that cycle through
     weight copies larger than L2 in total, so every call streams its weights from HBM.
-    Returns {"<linear>_m<M>": {...}} with the roofline fraction max(FLOP/peak, bytes/HBM)
-    / time."""
+    fmt "fp8": the FP8 linear (1x128 activations, 128x128 weight blocks); "nvfp4": the NVFP4
+    rollout linear (fp8_peak is then the FP4 peak).  Returns {"<linear>_m<M>": {...}} with
+    the roofline fraction max(FLOP/peak, bytes/HBM) / time."""
     import torch
     from block_scaled_fp8_x1_gb300 import _abi, ops, synth
     w = synth.QWEN7B_DECODE
     lins = {l.name: l for l in w.linears}
     rows = {}
     for li, (name, (N, K)) in enumerate(DEC7B.items()):
-        wq = ops.quantize_128x128(synth.weight(w, lins[name], 30 + li, dev), transpose=False)
-        ncopy = max(2, -(-(512 << 20) // (N * K)))
-        copies = [(wq[0].clone(), wq[1].clone()) for _ in range(ncopy)]
+        wb = synth.weight(w, lins[name], 30 + li, dev)
+        if fmt == "nvfp4":
+            wq = ops.quantize_nvfp4(wb)
+            wbytes = N * K // 2
+        else:
+            wq = ops.quantize_128x128(wb, transpose=False)[:2]
+            wbytes = N * K
+        del wb
+        ncopy = max(2, -(-(512 << 20) // wbytes))
+        copies = [tuple(t.clone() for t in wq) for _ in range(ncopy)]
         del wq
         for M in DEC_M:
             x = synth.activation(w, M, K, 40 + li, dev)
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
 
             def call(i):
-                # the fused linear: 1x128 quantization of x, then the decode GEMM overlapping it
-                ops.linear_fwd(x, copies[i % ncopy][0], copies[i % ncopy][1], out=y)
+                # the fused linear: quantization of x, then the decode GEMM overlapping it
+                if fmt == "nvfp4":
+                    ops.linear_nvfp4(x, *copies[i % ncopy], out=y)
+                else:
+                    ops.linear_fwd(x, copies[i % ncopy][0], copies[i % ncopy][1], out=y)
 
             for i in range(3):
                 call(i)
@@ -447,7 +465,7 @@ def decode_table(dev, fp8_peak, hbm, reps=40):
             e1.record()
             torch.cuda.synchronize()
             us = e0.elapsed_time(e1) * 1e3 / (5 * reps)
-            fl, by = decode_work(M, N, K)
+            fl, by = (decode_work_nvfp4 if fmt == "nvfp4" else decode_work)(M, N, K)
             roof_us = max(fl / (fp8_peak * 1e12), by / (hbm * 1e9)) * 1e6
             rows[f"{name}_m{M}"] = {"M": M, "N": N, "K": K, "us": round(us, 2),
                                     "GB/s": round(by / (us * 1e-6) / 1e9, 1),
@@ -626,6 +644,7 @@ def run_gpu(args):
         del s8
         torch.cuda.empty_cache()
         extra["qwen7b_decode"] = decode_table(dev, fp8_peak, hbm)
+        extra["qwen7b_decode_nvfp4"] = decode_table(dev, 3.0 * fp8_peak, hbm, fmt="nvfp4")
         extra["backward_ops_32b"] = backward_ops_table(dev, hbm)
 
     line = {
@@ -828,6 +847,20 @@ def run_kernel(args):
                     return ops.gemm_fwd(qa, sa, w_q, w_s, variant=var, tile_n=args.tile_n,
                                         epi_warps=args.epi)
         work, unit = 2.0 * M * N * K, "TFLOP/s"
+    elif k == "nvfp4_decode":                # shape M,N,K: the NVFP4 GEMM alone, GB/s of its bytes
+        M, N, K = dims
+        xq = ops.quantize_nvfp4(synth.normal_bf16((M, K), 1.0, 1, dev))
+        wq = ops.quantize_nvfp4(synth.normal_bf16((N, K), 0.02, 2, dev))
+        ncopy = max(1, -(-(256 << 20) // (N * K // 2)))
+        ws = [tuple(t.clone() for t in wq) for _ in range(ncopy)]
+        it = [0]
+
+        def fn():
+            w = ws[it[0] % len(ws)]
+            it[0] += 1
+            return ops.gemm_nvfp4(*xq, *w)
+        work = N * K // 2 + N * K // 16 + 4 * N + M * K // 2 + M * K // 16 + 2 * M * N
+        unit = "GB/s"
     else:
         M, K = dims
         if k == "rmsnorm_quant":
@@ -859,6 +892,10 @@ def run_kernel(args):
             dh = synth.normal_bf16((M, K), 1e-3, 2, dev)
             fn = lambda: ops.silu_mul_bwd_quant(gu, dh)
             work = 2 * M * 2 * K + 2 * M * K + 2 * M * 2 * K + 8 * M * 2 * K / 128
+        elif k == "quant_nvfp4":
+            x = synth.normal_bf16((M, K), 0.02, 1, dev)
+            fn = lambda: ops.quantize_nvfp4(x)
+            work = M * K * 2 + M * K // 2 + M * K // 16 + 4 * M
         elif k == "requantize_128x1":
             q, s = ops.quantize_1x128(synth.normal_bf16((M, K), 1.0, 1, dev))
             fn = lambda: ops.requantize_128x1(q, s)
@@ -894,7 +931,8 @@ def main():
     ap.add_argument("--kernel", default=None,
                     help="run one kernel form alone (for profiling): gemm_fwd, gemm_dgrad, "
                          "gemm_wgrad, gemm_decode, rmsnorm_quant, silu_mul_quant, quant_dual, "
-                         "quant_128x128, rmsnorm_bwd, silu_mul_bwd_quant, requantize_128x1")
+                         "quant_128x128, rmsnorm_bwd, silu_mul_bwd_quant, requantize_128x1, "
+                         "quant_nvfp4, nvfp4_decode")
     ap.add_argument("--shape", default=None, help="M,N,K (GEMMs) or M,K (quantizers)")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--tile-n", type=int, default=0, help="GEMM tile width (128/256) of the tiled or paired form")

@@ -87,7 +87,12 @@ SIGNATURES = {
     "fp8rl_linear_fwd": (ST, [P, I64, I64, I64, P, P, I64, P, P, P, P, ctypes.c_size_t, STREAM]),
     "fp8rl_gemm_fwd_decode_noalloc": (ST, [P, P, P, P, P, I64, I64, I64, STREAM]),
     "fp8rl_gemm_noalloc_scratch_bytes": (ctypes.c_size_t, []),
+    "fp8rl_nvfp4_scale_bytes": (ctypes.c_size_t, [I64, I64]),
+    "fp8rl_quantize_nvfp4": (ST, [P, I64, I64, I64, P, P, P, STREAM]),
+    "fp8rl_gemm_nvfp4": (ST, [P, P, P, P, P, P, P, I64, I64, I64, I64, ctypes.c_int, STREAM]),
+    "fp8rl_linear_nvfp4": (ST, [P, I64, I64, I64, P, P, P, I64, P, P, P, P, STREAM]),
     "fp8rl_debug_e4m3_encode": (ST, [P, P, I64, STREAM]),
+    "fp8rl_debug_e2m1_encode": (ST, [P, P, I64, STREAM]),
     "fp8rl_debug_encode_check": (ST, [ctypes.c_uint32, ctypes.c_uint32, P, P, STREAM]),
     "fp8rl_debug_wait_timeout": (ST, [ctypes.c_uint64, STREAM]),
 }

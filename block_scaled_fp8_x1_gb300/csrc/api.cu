@@ -451,6 +451,69 @@ fp8rl_status run_decode_swap(const uint8_t* qx, const float* sx, const uint8_t* 
     return cuda_status(launch_decode(tw, tx, p, grid, splits, pdl && splits == 1, st));
 }
 
+// NVFP4 decode GEMM (nvfp4.cu): the same split rule as the FP8 decode form, over K-blocks
+// of 256 elements and the clusters of the FP4 kernel that fit.
+DecodeChoice g_nvf4_choice[kMaxDevices][4];
+
+int nvf4_splits(int64_t M, int64_t tiles, int64_t nkb) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int mp = nvf4_token_tile((int)M);
+    const int cls = mp == 32 ? 0 : (mp == 64 ? 1 : (mp == 128 ? 2 : 3));
+    int maxc[9];
+    {
+        std::lock_guard<std::mutex> lk(g_dec_mu);
+        DecodeChoice& c = g_nvf4_choice[dev < kMaxDevices ? dev : 0][cls];
+        if (!c.cached) {
+            for (int sz = 1; sz <= 8; ++sz) c.max_clusters[sz] = nvf4_max_clusters((int)M, sz);
+            c.cached = 1;
+        }
+        for (int sz = 1; sz <= 8; ++sz) maxc[sz] = c.max_clusters[sz];
+    }
+    int best = 1;
+    double best_cost = 1e30;
+    for (int sz = 1; sz <= 8 && sz <= nkb; ++sz) {
+        if (maxc[sz] <= 0) continue;
+        const int64_t waves = (tiles + maxc[sz] - 1) / maxc[sz];
+        const double cost = sz == 1 ? (double)(waves * nkb) + 2.0
+                                    : (double)waves * ((double)((nkb + sz - 1) / sz) + 3.0);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = sz;
+        }
+    }
+    return best;
+}
+
+fp8rl_status run_gemm_nvf4(const uint8_t* qx, const uint8_t* sfx, const float* gx, const uint8_t* qw,
+                           const uint8_t* sfw, const float* gw, uint16_t* y, int64_t M, int64_t N, int64_t K,
+                           int64_t ldy, int splits_req, bool pdl, cudaStream_t st) {
+    const int64_t nkb = K / 256;
+    const int64_t tiles = N / 128;
+    const int splits = splits_req > 0 ? (int)std::min<int64_t>(std::min(splits_req, 8), nkb)
+                                      : nvf4_splits(M, tiles, nkb);
+    CUtensorMap tw, tx;
+    fp8rl_status e = make_tmap(&tw, qw, N, K / 2, K / 2, 128);
+    if (e != FP8RL_OK) return e;
+    e = make_tmap(&tx, qx, M, K / 2, K / 2, nvf4_token_tile((int)M));
+    if (e != FP8RL_OK) return e;
+    Nvf4Params p = {};
+    p.M = (int)M;
+    p.nkb = (int)nkb;
+    p.tiles = (int)tiles;
+    p.sfw = sfw;
+    p.sfx = sfx;
+    p.gw = gw;
+    p.gx = gx;
+    p.y = y;
+    p.ldy = ldy;
+    p.timeout_ns = g_timeout_ns.load();
+    int sms = 0;
+    current_device(&sms);
+    const int grid = splits > 1 ? (int)tiles : (int)std::min<int64_t>(tiles, std::max(sms, 1));
+    return cuda_status(launch_gemm_nvf4(tw, tx, p, grid, splits, pdl && splits == 1, st));
+}
+
 }  // namespace
 
 // ====================================================================================
@@ -491,9 +554,11 @@ fp8rl_status fp8rl_check_status(fp8rl_stream_t stream) {
     const fp8rl_status pr = read_and_clear_pair_status();
     const fp8rl_status dc = read_and_clear_decode_status();
     const fp8rl_status mc = read_and_clear_mc_status();
+    const fp8rl_status nv = read_and_clear_nvf4_status();
     if (g != FP8RL_OK) return g;
     if (pr != FP8RL_OK) return pr;
     if (mc != FP8RL_OK) return mc;
+    if (nv != FP8RL_OK) return nv;
     return dc != FP8RL_OK ? dc : q;
 }
 
@@ -796,6 +861,57 @@ fp8rl_status fp8rl_linear_fwd(const uint16_t* x, int64_t M, int64_t K, int64_t l
     return run_gemm(t, nullptr, sms, stream);
 }
 
+// ---------------------------------------------------------------- NVFP4 rollout path
+
+size_t fp8rl_nvfp4_scale_bytes(int64_t R, int64_t K) {
+    if (R <= 0 || K <= 0 || K % 256 != 0) return 0;
+    return (size_t)((R + 127) / 128) * (size_t)(K / 256) * 2048u;
+}
+
+fp8rl_status fp8rl_quantize_nvfp4(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q, uint8_t* sf,
+                                  float* g, fp8rl_stream_t stream) {
+    if (R < 0 || K <= 0 || ldx < K) return FP8RL_ERR_INVALID_ARG;
+    if (K % 256 != 0) return FP8RL_ERR_SHAPE;
+    if (R == 0) return FP8RL_OK;
+    if (!x || !q || !sf || !g) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(sf) || (ldx * 2) % 16 != 0) return FP8RL_ERR_ALIGN;
+    fp8rl_status e = current_device(nullptr);
+    if (e != FP8RL_OK) return e;
+    return cuda_status(launch_quant_nvfp4(x, R, K, ldx, q, sf, g, stream));
+}
+
+fp8rl_status fp8rl_gemm_nvfp4(const uint8_t* qx, const uint8_t* sfx, const float* gx, const uint8_t* qw,
+                              const uint8_t* sfw, const float* gw, uint16_t* y, int64_t M, int64_t N, int64_t K,
+                              int64_t ldy, int splits, fp8rl_stream_t stream) {
+    if (M < 0 || N < 0 || K <= 0 || ldy < N || splits < 0) return FP8RL_ERR_INVALID_ARG;
+    if (K % 256 != 0 || N % 128 != 0 || M > 256) return FP8RL_ERR_SHAPE;
+    if (M == 0 || N == 0) return FP8RL_OK;
+    if (!qx || !sfx || !gx || !qw || !sfw || !gw || !y) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(qx) || !aligned16(sfx) || !aligned16(qw) || !aligned16(sfw) || !aligned16(gw) ||
+        !aligned16(y) || ldy % 8 != 0)
+        return FP8RL_ERR_ALIGN;
+    fp8rl_status e = current_device(nullptr);
+    if (e != FP8RL_OK) return e;
+    return run_gemm_nvf4(qx, sfx, gx, qw, sfw, gw, y, M, N, K, ldy, splits, false, stream);
+}
+
+fp8rl_status fp8rl_linear_nvfp4(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const uint8_t* qw,
+                                const uint8_t* sfw, const float* gw, int64_t N, uint8_t* qx, uint8_t* sfx, float* gx,
+                                uint16_t* y, fp8rl_stream_t stream) {
+    if (M < 0 || N < 0 || K <= 0 || ldx < K) return FP8RL_ERR_INVALID_ARG;
+    if (K % 256 != 0 || N % 128 != 0 || M > 256) return FP8RL_ERR_SHAPE;
+    if (M == 0 || N == 0) return FP8RL_OK;
+    if (!x || !qw || !sfw || !gw || !qx || !sfx || !gx || !y) return FP8RL_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(qw) || !aligned16(sfw) || !aligned16(gw) || !aligned16(qx) ||
+        !aligned16(sfx) || !aligned16(y) || (ldx * 2) % 16 != 0)
+        return FP8RL_ERR_ALIGN;
+    fp8rl_status e = current_device(nullptr);
+    if (e != FP8RL_OK) return e;
+    e = cuda_status(launch_quant_nvfp4(x, M, K, ldx, qx, sfx, gx, stream));
+    if (e != FP8RL_OK) return e;
+    return run_gemm_nvf4(qx, sfx, gx, qw, sfw, gw, y, M, N, K, N, 0, true, stream);
+}
+
 // ---------------------------------------------------------------- no-allocation decode
 
 // Decode-shaped forward GEMM on the library's own fixed scratch array (see
@@ -839,6 +955,15 @@ fp8rl_status fp8rl_debug_e4m3_encode(const float* in, uint8_t* out, int64_t n,
     fp8rl_status e = current_device(nullptr);
     if (e != FP8RL_OK) return e;
     return cuda_status(launch_debug_e4m3(in, out, n, stream));
+}
+
+fp8rl_status fp8rl_debug_e2m1_encode(const float* in, uint8_t* out, int64_t n, fp8rl_stream_t stream) {
+    if (n < 0) return FP8RL_ERR_INVALID_ARG;
+    if (n == 0) return FP8RL_OK;
+    if (!in || !out) return FP8RL_ERR_INVALID_ARG;
+    fp8rl_status e = current_device(nullptr);
+    if (e != FP8RL_OK) return e;
+    return cuda_status(launch_debug_e2m1(in, out, n, stream));
 }
 
 fp8rl_status fp8rl_debug_encode_check(uint32_t amax_lo, uint32_t amax_hi,

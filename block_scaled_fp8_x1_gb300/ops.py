@@ -74,6 +74,15 @@ def debug_e4m3_encode(v: torch.Tensor) -> torch.Tensor:
     return out
 
 
+def debug_e2m1_encode(v: torch.Tensor) -> torch.Tensor:
+    _require(v, torch.float32, "v")
+    _contig(v, "v")
+    out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+    check(lib().fp8rl_debug_e2m1_encode(_ptr(v), _ptr(out), v.numel(), _stream(v.device)),
+          "fp8rl_debug_e2m1_encode")
+    return out
+
+
 def debug_encode_check(amax_lo: int = 1, amax_hi: int = 0x7F80):
     """(mismatches, first_bad) of the division-free encode vs IEEE division over every BF16
     group maximum in [amax_lo, amax_hi) and every BF16 x with |x| <= amax."""
@@ -345,3 +354,60 @@ def linear_fwd(x: torch.Tensor, qw, sw, out=None):
                                  _ptr(sx), _ptr(y), _ptr(wsb), wsb.numel() if wsb is not None else 0,
                                  _stream(dev)), "fp8rl_linear_fwd")
     return y, qx, sx
+
+
+# ------------------------------------------------------------------ NVFP4 rollout path
+
+def nvfp4_scale_bytes(R: int, K: int) -> int:
+    return int(lib().fp8rl_nvfp4_scale_bytes(R, K))
+
+
+def _nvfp4_buffers(R: int, K: int, dev):
+    q = torch.empty((R, K // 2), dtype=torch.uint8, device=dev)
+    sf = torch.empty(nvfp4_scale_bytes(R, K), dtype=torch.uint8, device=dev)
+    g = torch.empty(R, dtype=torch.float32, device=dev)
+    return q, sf, g
+
+
+def quantize_nvfp4(x: torch.Tensor):
+    """NVFP4 quantization of the rows of x bf16 [R,K] (K % 256 == 0): (q u8 [R, K/2] packed
+    E2M1, sf u8 block scales in the tensor core's atom layout, g f32 [R])."""
+    _require(x, torch.bfloat16, "x")
+    if x.stride(1) != 1:
+        raise ValueError("x: rows must be contiguous")
+    R, K = x.shape
+    q, sf, g = _nvfp4_buffers(R, K, x.device)
+    check(lib().fp8rl_quantize_nvfp4(_ptr(x), R, K, x.stride(0), _ptr(q), _ptr(sf), _ptr(g),
+                                     _stream(x.device)), "fp8rl_quantize_nvfp4")
+    return q, sf, g
+
+
+def gemm_nvfp4(qx, sfx, gx, qw, sfw, gw, splits: int = 0, out=None):
+    """y bf16 [M,N] from NVFP4 operands of X [M,K] and W [N,K] (decode shapes, M <= 256)."""
+    dev = qx.device
+    for t, n, dt in ((qx, "qx", torch.uint8), (sfx, "sfx", torch.uint8), (gx, "gx", torch.float32),
+                     (qw, "qw", torch.uint8), (sfw, "sfw", torch.uint8), (gw, "gw", torch.float32)):
+        _require(t, dt, n, dev)
+        _contig(t, n)
+    M, K2 = qx.shape
+    N = qw.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    check(lib().fp8rl_gemm_nvfp4(_ptr(qx), _ptr(sfx), _ptr(gx), _ptr(qw), _ptr(sfw), _ptr(gw), _ptr(y),
+                                 M, N, 2 * K2, y.stride(0), int(splits), _stream(dev)), "fp8rl_gemm_nvfp4")
+    return y
+
+
+def linear_nvfp4(x: torch.Tensor, qw, sfw, gw, out=None):
+    """One NVFP4 linear layer from the BF16 activation x [M,K]: the activation's NVFP4
+    operands and y = X W^T bf16 [M,N].  Returns (y, qx, sfx, gx)."""
+    _require(x, torch.bfloat16, "x")
+    if x.stride(1) != 1:
+        raise ValueError("x: rows must be contiguous")
+    M, K = x.shape
+    N = qw.shape[0]
+    dev = x.device
+    qx, sfx, gx = _nvfp4_buffers(M, K, dev)
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    check(lib().fp8rl_linear_nvfp4(_ptr(x), M, K, x.stride(0), _ptr(qw), _ptr(sfw), _ptr(gw), N, _ptr(qx),
+                                   _ptr(sfx), _ptr(gx), _ptr(y), _stream(dev)), "fp8rl_linear_nvfp4")
+    return y, qx, sfx, gx

@@ -344,6 +344,57 @@ FP8RL_API fp8rl_status fp8rl_gemm_fwd_decode_noalloc(const uint8_t* qx, const fl
 FP8RL_API size_t fp8rl_gemm_noalloc_scratch_bytes(void);
 
 /* ----------------------------------------------------------------------------------------
+ * NVFP4 rollout path.  "QeRL" (chatpaper.ai), abstract: rollout runs with NVFP4-quantized
+ * weights.  The page names the format only; the format is FP4 E2M1 elements (0, 0.5, 1,
+ * 1.5, 2, 3, 4, 6 and negatives), one E4M3 scale per 16 consecutive elements along K, and
+ * an FP32 scale on top, here one per row.  The tensor core's FP4 path multiplies FP4 by
+ * FP4, so the activation is quantized to NVFP4 as well, per call.
+ *
+ * Quantization of a row with maximum |x| = a (IEEE single precision, no FMA):
+ *   g = a / 2688;  block of 16 with maximum b: sb = E4M3_rne_satfinite(b / (6 g)) (0 when
+ *   g = 0), d = decode(sb) * g;  code = E2M1_rne_satfinite(x / d), 0 when d = 0.
+ * Layouts:
+ *   q  : [R][K/2] bytes; element k of a row in bits 4(k%2) .. 4(k%2)+3 of byte k/2.
+ *   sf : the tensor core's scale-factor layout, fp8rl_nvfp4_scale_bytes(R, K) bytes:
+ *        512-byte atoms of 128 rows x 4 scales (64 elements of K); atom (row group rg =
+ *        r/128, K-atom ka = k/64) at byte 512 (rg K/64 + ka); inside it the scale of row
+ *        r, K-elements 16j .. 16j+15 of the atom, at byte 16 (r%32) + 4 ((r%128)/32) + j.
+ *        Rows from R up to the next multiple of 128 hold zeros.
+ *   g  : float [R].
+ * -------------------------------------------------------------------------------------- */
+
+/* Bytes of the sf buffer of an R x K NVFP4 operand: ceil(R/128) * K/256 * 2048 (0 for
+ * R <= 0 or K not a positive multiple of 256). */
+FP8RL_API size_t fp8rl_nvfp4_scale_bytes(int64_t R, int64_t K);
+
+/* NVFP4 quantization of the rows of x (BF16 [R][ldx], ldx >= K, ldx % 8 == 0; K % 256 == 0)
+ * into q, sf, g (layouts above; caller-owned device memory, 16-byte aligned).  Used for
+ * weights (R = N output channels, once per weight update) and activations (R = M tokens,
+ * per call).  Errors: FP8RL_ERR_SHAPE (K % 256), FP8RL_ERR_ALIGN, FP8RL_ERR_INVALID_ARG. */
+FP8RL_API fp8rl_status fp8rl_quantize_nvfp4(const uint16_t* x, int64_t R, int64_t K, int64_t ldx,
+                                            uint8_t* q, uint8_t* sf, float* g, fp8rl_stream_t stream);
+
+/* Decode-shaped NVFP4 GEMM: y[m][n] = bf16_rne(gx[m] gw[n] sum_k x^(m,k) w^(n,k)), x^ and
+ * w^ the codes times their block scales, accumulated in FP32 by the tensor core (within
+ * the GEMM tolerance of the exact sum).  Operands from fp8rl_quantize_nvfp4: qx / sfx / gx
+ * of X [M][K], qw / sfw / gw of W [N][K].  y: BF16 [M][ldy], ldy >= N, ldy % 8 == 0.
+ * 1 <= M <= 256, N % 128 == 0, K % 256 == 0.  splits: slices of the reduction, one cluster
+ * of CTAs per 128-row weight tile (1..8; 0 = automatic).  No workspace. */
+FP8RL_API fp8rl_status fp8rl_gemm_nvfp4(const uint8_t* qx, const uint8_t* sfx, const float* gx,
+                                        const uint8_t* qw, const uint8_t* sfw, const float* gw,
+                                        uint16_t* y, int64_t M, int64_t N, int64_t K, int64_t ldy,
+                                        int splits, fp8rl_stream_t stream);
+
+/* One NVFP4 linear layer from the BF16 activation: x is quantized into qx / sfx / gx
+ * (exactly fp8rl_quantize_nvfp4; caller-owned), then y = fp8rl_gemm_nvfp4 with automatic
+ * splits.  The GEMM kernel starts streaming its weights while the quantizer finishes
+ * (programmatic dependent launch on the same stream) when the reduction is not split. */
+FP8RL_API fp8rl_status fp8rl_linear_nvfp4(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                                          const uint8_t* qw, const uint8_t* sfw, const float* gw,
+                                          int64_t N, uint8_t* qx, uint8_t* sfx, float* gx,
+                                          uint16_t* y, fp8rl_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
  * Diagnostics (used by the tests).
  * -------------------------------------------------------------------------------------- */
 
@@ -351,6 +402,11 @@ FP8RL_API size_t fp8rl_gemm_noalloc_scratch_bytes(void);
  * values: out[i] = E4M3_rne_satfinite(in[i]).  Device pointers. */
 FP8RL_API fp8rl_status fp8rl_debug_e4m3_encode(const float* in, uint8_t* out, int64_t n,
                                      fp8rl_stream_t stream);
+
+/* The device's E2M1 encoder (the routine fp8rl_quantize_nvfp4 uses) applied to n binary32
+ * values: out[i] = E2M1_rne_satfinite(in[i]) in bits 0-3.  Device pointers. */
+FP8RL_API fp8rl_status fp8rl_debug_e2m1_encode(const float* in, uint8_t* out, int64_t n,
+                                               fp8rl_stream_t stream);
 
 /* Checks the quantizers' division-free encode against IEEE division on the device: for
  * every BF16 group maximum with bits in [amax_lo, amax_hi) (positive finite: below 0x7F80)

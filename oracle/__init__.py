@@ -78,6 +78,7 @@ def _load():
             "orc_e2m1_decode": (ctypes.c_double, [ctypes.c_uint8]),
             "orc_e2m1_encode": (ctypes.c_uint8, [ctypes.c_float]),
             "orc_e2m1_encode_array": (None, [P, P, I64]),
+            "orc_e2m1_encode_bits_range": (None, [ctypes.c_uint32, I64, P]),
             "orc_quantize_nvfp4": (None, [P, I64, I64, I64, P, P, P]),
             "orc_gemm_nvfp4": (None, [P, P, P, I64, P, P, P, I64, I64, P]),
             "orc_gemm_nvfp4_sampled": (None, [P, P, P, P, P, P, I64, P, P, I64, P]),
@@ -348,6 +349,13 @@ def e2m1_encode(v: np.ndarray) -> np.ndarray:
     x = _c(v, np.float32)
     out = np.empty(x.shape, dtype=np.uint8)
     _load().orc_e2m1_encode_array(_p(x), _p(out), x.size)
+    return out
+
+
+def e2m1_encode_bits_range(first: int, count: int) -> np.ndarray:
+    """E2M1 codes for every binary32 bit pattern first, first+1, ..., first+count-1."""
+    out = np.empty(count, dtype=np.uint8)
+    _load().orc_e2m1_encode_bits_range(first, count, _p(out))
     return out
 
 

@@ -548,6 +548,17 @@ ORC_API void orc_e2m1_encode_array(const float* v, uint8_t* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_e2m1_encode(v[i]);
 }
 
+/* Encode every binary32 pattern in [first, first+count) (as raw bits). */
+ORC_API void orc_e2m1_encode_bits_range(uint32_t first, int64_t count, uint8_t* out) {
+    #pragma omp parallel for schedule(static) num_threads(g_threads)
+    for (int64_t i = 0; i < count; ++i) {
+        uint32_t u = first + (uint32_t)i;
+        float f;
+        memcpy(&f, &u, sizeof f);
+        out[i] = orc_e2m1_encode(f);
+    }
+}
+
 /* NVFP4 quantization of the rows of x[M][K] (BF16 bits, row stride ldx), R10.
  * q[M][K/2]: element k of a row in bits 4*(k%2) .. 4*(k%2)+3 of byte k/2;
  * sf[M][K/16]: the E4M3 block scales; g[M]: the per-row FP32 scales. */

@@ -97,3 +97,33 @@ def test_workspace_sizes(abi):
     assert need == 28 * 4 * 256 * 128 * 4
     one = abi.GemmOpts(abi.FP8RL_VARIANT_SPLITK, 1, 0)
     assert L.fp8rl_gemm_workspace_bytes_ex(abi.FP8RL_OP_FWD, 256, 3584, 3584, ctypes.byref(one)) == 0
+
+
+def test_nvfp4_host_rules(abi):
+    L = abi.lib()
+    fake = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10004)
+    null = None
+    # scale-factor bytes: ceil(R/128) row groups x K/256 K-blocks x 2 KB
+    assert L.fp8rl_nvfp4_scale_bytes(1, 256) == 2048
+    assert L.fp8rl_nvfp4_scale_bytes(129, 3584) == 2 * 14 * 2048
+    assert L.fp8rl_nvfp4_scale_bytes(37888, 3584) == 296 * 14 * 2048
+    assert L.fp8rl_nvfp4_scale_bytes(64, 384) == 0 and L.fp8rl_nvfp4_scale_bytes(0, 256) == 0
+    # K must be a multiple of 256, N of 128, M at most 256
+    assert L.fp8rl_quantize_nvfp4(fake, 4, 384, 384, fake, fake, fake, null) == abi.FP8RL_ERR_SHAPE
+    args = [fake] * 7
+    assert L.fp8rl_gemm_nvfp4(*args, 4, 128, 384, 128, 0, null) == abi.FP8RL_ERR_SHAPE
+    assert L.fp8rl_gemm_nvfp4(*args, 4, 200, 256, 200, 0, null) == abi.FP8RL_ERR_SHAPE
+    assert L.fp8rl_gemm_nvfp4(*args, 257, 128, 256, 128, 0, null) == abi.FP8RL_ERR_SHAPE
+    assert L.fp8rl_gemm_nvfp4(*args, 4, 128, 256, 64, 0, null) == abi.FP8RL_ERR_INVALID_ARG
+    assert L.fp8rl_gemm_nvfp4(*args, 4, 128, 256, 128, -1, null) == abi.FP8RL_ERR_INVALID_ARG
+    assert L.fp8rl_linear_nvfp4(fake, 300, 256, 256, fake, fake, fake, 128, fake, fake, fake, fake, null) == abi.FP8RL_ERR_SHAPE
+    # alignment and missing pointers
+    assert L.fp8rl_quantize_nvfp4(odd, 4, 256, 256, fake, fake, fake, null) == abi.FP8RL_ERR_ALIGN
+    assert L.fp8rl_quantize_nvfp4(fake, 4, 256, 260, fake, fake, fake, null) == abi.FP8RL_ERR_ALIGN
+    assert L.fp8rl_gemm_nvfp4(fake, fake, fake, odd, fake, fake, fake, 4, 128, 256, 128, 0, null) == abi.FP8RL_ERR_ALIGN
+    assert L.fp8rl_gemm_nvfp4(fake, fake, fake, fake, fake, fake, fake, 4, 128, 256, 132, 0, null) == abi.FP8RL_ERR_ALIGN
+    assert L.fp8rl_quantize_nvfp4(fake, 4, 256, 256, fake, null, fake, null) == abi.FP8RL_ERR_INVALID_ARG
+    # empty problems are no-ops
+    assert L.fp8rl_quantize_nvfp4(null, 0, 256, 256, null, null, null, null) == abi.FP8RL_OK
+    assert L.fp8rl_gemm_nvfp4(null, null, null, null, null, null, null, 0, 128, 256, 128, 0, null) == abi.FP8RL_OK

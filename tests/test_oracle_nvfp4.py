@@ -212,3 +212,11 @@ def test_gemm_nvfp4_is_the_dequantized_matmul(oracle):
     m = rng.integers(0, M, 50)
     n = rng.integers(0, N, 50)
     assert np.array_equal(oracle.gemm_nvfp4_sampled(qx, sx, gx, qw, sw, gw, m, n), y[m, n])
+
+
+def test_e2m1_bits_range_matches_array_encoder(oracle):
+    first = 0x3F000000
+    codes = oracle.e2m1_encode_bits_range(first, 1 << 16)
+    vals = np.arange(first, first + (1 << 16), dtype=np.uint32).view(np.float32)
+    assert np.array_equal(codes, oracle.e2m1_encode(vals))
+    assert np.array_equal(codes, brute_e2m1(vals))
