@@ -90,10 +90,13 @@ __device__ __forceinline__ uint2 encode_block(const uint4 (&v)[2], float d) {
 
 }  // namespace
 
-// One CTA of 128 threads per row (rows past R, up to the next multiple of 128, only zero
-// their scale factors).  Pass 1: the row's maximum (BF16 bit maxima, exact) -> g.  Pass 2:
-// per block of 16, its maximum, sb, d and the 16 codes; thread t takes blocks t, t+128, ...
-// (the row is read again from L1/L2).
+// CTA (r, c) of 128 threads: row r, blocks of 16 [c * kQuantChunk, (c+1) * kQuantChunk)
+// (rows past R, up to the next multiple of 128, only zero their scale factors).  Pass 1:
+// the whole row's maximum (BF16 bit maxima, exact) -> g, the same in every chunk's CTA.
+// Pass 2: per block of 16 of the chunk, its maximum, sb, d and the 16 codes, one block per
+// thread.  Chunking keeps a long row's divisions on many SMs.
+constexpr int kQuantChunk = 128;   // blocks of 16 per CTA
+
 __global__ void __launch_bounds__(128) k_quant_nvfp4(const uint16_t* __restrict__ x, int64_t R, int64_t K,
                                                      int64_t ldx, uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                                      float* __restrict__ g) {
@@ -102,8 +105,10 @@ __global__ void __launch_bounds__(128) k_quant_nvfp4(const uint16_t* __restrict_
     const int64_t r = blockIdx.x;
     const int tid = threadIdx.x;
     const int64_t nb = K / 16, nkb = K / 256;
+    const int64_t b_lo = (int64_t)blockIdx.y * kQuantChunk;
+    const int64_t b_hi = b_lo + kQuantChunk < nb ? b_lo + kQuantChunk : nb;
     if (r >= R) {
-        for (int64_t b = tid; b < nb; b += 128) sf[sf_offset(r, b, nkb)] = 0;
+        for (int64_t b = b_lo + tid; b < b_hi; b += 128) sf[sf_offset(r, b, nkb)] = 0;
         return;
     }
     const uint16_t* row = x + r * ldx;
@@ -121,9 +126,9 @@ __global__ void __launch_bounds__(128) k_quant_nvfp4(const uint16_t* __restrict_
     __syncthreads();
     m = max(max(s_max[0], s_max[1]), max(s_max[2], s_max[3]));
     const float gr = __fdiv_rn(bf16_bits_to_f32(m), 2688.0f);
-    if (tid == 0) g[r] = gr;
+    if (tid == 0 && blockIdx.y == 0) g[r] = gr;
     const float g6 = __fmul_rn(6.0f, gr);
-    for (int64_t b = tid; b < nb; b += 128) {
+    for (int64_t b = b_lo + tid; b < b_hi; b += 128) {
         uint4 v[2];
         v[0] = nv_ldg_v4(row + 16 * b);
         v[1] = nv_ldg_v4(row + 16 * b + 8);
@@ -158,8 +163,9 @@ __global__ void k_debug_e2m1(const float* __restrict__ in, uint8_t* __restrict__
 //     reduction and the epilogue reads TMEM once per tile: y = acc * gx[m] * gw[n].
 //   * Split-K over a cluster of S CTAs for narrow weights, reduced through distributed
 //     shared memory in rank order, as the FP8 decode GEMM does.
-// Roles (192 threads): warp 0 copies, warp 1 issues tcgen05 (one elected lane), warps 2-5
-// read the accumulator (warp w reads TMEM lane quarter w % 4).  Every wait is bounded.
+// Roles (320 threads): warp 0 copies, warp 1 issues tcgen05 (one elected lane), warps 2-9
+// read the accumulator (warp w reads TMEM lane quarter w % 4, half of the token columns).
+// Every wait is bounded.
 // ------------------------------------------------------------------------------------
 namespace {
 
@@ -247,7 +253,7 @@ __device__ __forceinline__ float4 nv_ld_dsmem_v4(uint32_t addr) {
 // K-blocks [r nkb / S, (r+1) nkb / S) and reduces token slice r); with S = 1, persistent
 // CTAs over tiles blockIdx.x, +gridDim.x, ..., storing from registers.
 template <int MP>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     k_gemm_nvf4(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                 const Nvf4Params p) {
     using C = Nvf4Cfg<MP>;
@@ -288,7 +294,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         for (int a = 0; a < NACC; ++a) {
             mbar_init(smem_u32(&tfull_bar[a]), 1);
-            mbar_init(smem_u32(&tempty_bar[a]), 4);
+            mbar_init(smem_u32(&tempty_bar[a]), 8);
         }
         mbar_init(smem_u32(drain_bar), 1);
         *abort_flag = 0;
@@ -411,43 +417,48 @@ __global__ void __launch_bounds__(192, 1)
         mbar_wait(smem_u32(drain_bar), 0, p.timeout_ns, &no_abort);
     } else {
         // ------------------------------------------------------------ accumulator readers
+        // two warps per TMEM lane quadrant, each MP/2 token columns: the whole share is
+        // loaded first and the accumulator handed back before any arithmetic or store
+        constexpr int CH = MP / 2, LW = CH >= 32 ? 32 : 16, NL = CH / LW;
         const int quad = warp & 3;
+        const int col0 = ((warp - 2) >> 2) * CH;
         const int row = quad * 32 + lane;               // weight row within the tile
-        const uint32_t tl = tmem_base + ((uint32_t)(quad * 32) << 16);
+        const uint32_t tl = tmem_base + ((uint32_t)(quad * 32) << 16) + col0;
         uint32_t lt = 0;
         for (int tile = tile0; ok && tile < tiles; tile += tstep, ++lt) {
             const uint32_t a = lt % NACC;
             ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull_bar[a]), (lt / NACC) & 1, p.timeout_ns, abort_flag));
             if (!ok) break;
             tc_fence_after();
+            uint32_t v[NL][LW];
+            #pragma unroll
+            for (int h = 0; h < NL; ++h) tmem_ld_cols(tl + a * MP + h * LW, v[h]);
+            #pragma unroll
+            for (int h = 0; h < NL; ++h) tmem_ld_wait(v[h]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[a]));
             const int n = tile * 128 + row;
-            const float gwn = p.gw[n];
-            #pragma unroll 1
-            for (int c0 = 0; c0 < MP; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tl + a * MP + c0, v);
-                tmem_ld_wait(v);
-                if (c0 + 32 == MP) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[a]));
-                }
-                if (S == 1) {
-                    uint16_t* yt = p.y + n;
+            if (S == 1) {
+                const float gwn = p.gw[n];
+                uint16_t* yt = p.y + n;
+                #pragma unroll
+                for (int h = 0; h < NL; ++h)
                     #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int t = c0 + j;
+                    for (int j = 0; j < LW; ++j) {
+                        const int t = col0 + h * LW + j;
                         if (t < p.M) {
-                            const float yv = __fmul_rn(__fmul_rn(__uint_as_float(v[j]), __ldg(p.gx + t)), gwn);
+                            const float yv = __fmul_rn(__fmul_rn(__uint_as_float(v[h][j]), __ldg(p.gx + t)), gwn);
                             yt[(int64_t)t * p.ldy] = (uint16_t)(pack_bf16x2(yv, 0.0f) & 0xFFFFu);
                         }
                     }
-                } else {
-                    // one tile per cluster: the last commit covered every MMA of this CTA,
-                    // and every copy was consumed by one, so the stage ring is free
+            } else {
+                // one tile per cluster: the last commit covered every MMA of this CTA, and
+                // every copy was consumed by one, so the stage ring is free
+                #pragma unroll
+                for (int h = 0; h < NL; ++h)
                     #pragma unroll
-                    for (int j = 0; j < 32; ++j) red[(c0 + j) * 128 + row] = __uint_as_float(v[j]);
-                }
+                    for (int j = 0; j < LW; ++j) red[(col0 + h * LW + j) * 128 + row] = __uint_as_float(v[h][j]);
             }
         }
     }
@@ -459,13 +470,13 @@ __global__ void __launch_bounds__(192, 1)
     if (S > 1) {
         cluster_sync_all();
         if (warp >= 2 && *abort_flag == 0 && tile0 < tiles) {
-            const int et = threadIdx.x - 64;                      // 0..127
+            const int et = threadIdx.x - 64;                      // 0..255
             const int n4 = p.M * 32;                              // float4s of valid tokens
             const int per = (n4 + S - 1) / S;
             const int e_end = min(n4, (rank + 1) * per);
             const uint32_t red_local = smem_u32(red);
             const int n0 = tile0 * 128;
-            for (int e = rank * per + et; e < e_end; e += 128) {
+            for (int e = rank * per + et; e < e_end; e += 256) {
                 const int tok = e >> 5;
                 const int r4 = (e & 31) * 4;
                 const uint32_t off = (uint32_t)(tok * 128 + r4) * 4u;
@@ -506,7 +517,7 @@ cudaError_t launch_nvf4_t(const CUtensorMap& tw, const CUtensorMap& tx, const Nv
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(grid_clusters * splits), 1, 1);
-    cfg.blockDim = dim3(192, 1, 1);
+    cfg.blockDim = dim3(320, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute at[2];
@@ -525,7 +536,7 @@ template <int MP>
 int nvf4_max_clusters_t(int splits) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)splits * 64, 1, 1);
-    cfg.blockDim = dim3(192, 1, 1);
+    cfg.blockDim = dim3(320, 1, 1);
     cfg.dynamicSmemBytes = Nvf4Cfg<MP>::BYTES;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -566,7 +577,8 @@ cudaError_t launch_gemm_nvf4(const CUtensorMap& tw, const CUtensorMap& tx, const
 cudaError_t launch_quant_nvfp4(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q, uint8_t* sf,
                                float* g, cudaStream_t st) {
     const int64_t rows = (R + 127) / 128 * 128;
-    k_quant_nvfp4<<<(unsigned)rows, 128, 0, st>>>(x, R, K, ldx, q, sf, g);
+    const int64_t chunks = (K / 16 + kQuantChunk - 1) / kQuantChunk;
+    k_quant_nvfp4<<<dim3((unsigned)rows, (unsigned)chunks), 128, 0, st>>>(x, R, K, ldx, q, sf, g);
     return cudaGetLastError();
 }
 
