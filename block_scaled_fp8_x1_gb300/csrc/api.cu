@@ -10,6 +10,7 @@
 
 #include "../../include/fp8rl.h"
 #include "gemm.h"
+#include "rollout.h"
 
 namespace fp8rl {
 fp8rl_status read_and_clear_device_status(cudaStream_t st);  // gemm.cu

@@ -134,31 +134,6 @@ cudaError_t launch_decode(const CUtensorMap& tw, const CUtensorMap& tx, const De
                           int splits, bool pdl, cudaStream_t st);
 fp8rl_status read_and_clear_decode_status();
 
-// nvfp4.cu: NVFP4 row quantizer and the decode-shaped FP4 GEMM (weights on the MMA's M
-// side, split-K inside a cluster of `splits` CTAs as for launch_decode).  tw: weight codes
-// [N][K/2] bytes with 128 x 128-byte boxes; tx: activation codes [M][K/2] with boxes of
-// nvf4_token_tile(M) rows x 128 bytes.  Scale factors in the tensor core's atom layout.
-struct Nvf4Params {
-    int M;                   // tokens, 1..256
-    int nkb;                 // K / 256
-    int tiles;               // N / 128
-    const uint8_t* sfw;      // weight block scales, 2 KB per (tile, K-block)
-    const uint8_t* sfx;      // activation block scales, 2 KB per (128-token group, K-block)
-    const float* gw;         // per-row scales of W [N] and X [M]
-    const float* gx;
-    uint16_t* y;             // y[m * ldy + n]
-    int64_t ldy;
-    uint64_t timeout_ns;
-};
-int nvf4_token_tile(int M);
-int nvf4_max_clusters(int M, int splits);
-cudaError_t launch_gemm_nvf4(const CUtensorMap& tw, const CUtensorMap& tx, const Nvf4Params& p, int grid_clusters,
-                             int splits, bool pdl, cudaStream_t st);
-cudaError_t launch_quant_nvfp4(const uint16_t* x, int64_t R, int64_t K, int64_t ldx, uint8_t* q, uint8_t* sf,
-                               float* g, cudaStream_t st);
-cudaError_t launch_debug_e2m1(const float* in, uint8_t* out, int64_t n, cudaStream_t st);
-fp8rl_status read_and_clear_nvf4_status();
-
 // quantize.cu
 cudaError_t launch_quant_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
                                float* s, int num_sms, cudaStream_t st);

@@ -26,6 +26,7 @@
 //   g[R]        the per-row FP32 scales.
 #include "common.cuh"
 #include "gemm.h"
+#include "rollout.h"
 
 namespace fp8rl {
 
