@@ -181,29 +181,6 @@ __device__ __forceinline__ void rows_from_smem(const uint8_t* stage, const Panel
                 const float2 y = __fmul2_rn(__fmul2_rn(make_float2(bf16_lo(xv[j]), bf16_hi(xv[j])), make_float2(r, r)), gam[j]);
                 w[i][j] = pack_bf16x2(y.x, y.y);
             }
-        } else if (PRO == PRO_SILU_BWD) {
-            // stage: gate tile, up tile, tile of dh.  Columns [0, I) of the output are
-            // dg = dh*u*s*(1 + g*(1 - s)), columns [I, 2I) are du = dh*g*s, s = sigmoid(g)
-            const uint4 u = *reinterpret_cast<const uint4*>(stage + 128 * 256 + (R0 + i) * 256 + C0 * 2);
-            const uint4 d = *reinterpret_cast<const uint4*>(stage + 2 * 128 * 256 + (R0 + i) * 256 + C0 * 2);
-            const uint32_t uv[4] = {u.x, u.y, u.z, u.w};
-            const uint32_t dv[4] = {d.x, d.y, d.z, d.w};
-            const bool part_u = k0 >= a.K / 2;
-            #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float o[2];
-                #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float g = e ? bf16_hi(xv[j]) : bf16_lo(xv[j]);
-                    const float uu = e ? bf16_hi(uv[j]) : bf16_lo(uv[j]);
-                    const float dd = e ? bf16_hi(dv[j]) : bf16_lo(dv[j]);
-                    const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
-                    o[e] = part_u ? __fmul_rn(dd, __fmul_rn(g, sg))
-                                  : __fmul_rn(__fmul_rn(__fmul_rn(dd, uu), sg),
-                                              __fmaf_rn(g, __fsub_rn(1.0f, sg), 1.0f));
-                }
-                w[i][j] = pack_bf16x2(o[0], o[1]);
-            }
         } else {  // SILU: h = bf16(silu(g) * u), silu(g) = g / (1 + exp(-g))
             const uint4 u = *reinterpret_cast<const uint4*>(stage + 128 * 256 + (R0 + i) * 256 + C0 * 2);
             const uint32_t uv[4] = {u.x, u.y, u.z, u.w};
@@ -217,6 +194,42 @@ __device__ __forceinline__ void rows_from_smem(const uint8_t* stage, const Panel
             }
         }
     }
+}
+
+// SiLU-mul backward from the staged gate, up and dh tiles (256-byte rows each, in that
+// order), for this thread's 8 rows x 8 columns: dg = dh*u*s*(1 + g*(1 - s)) into w and
+// du = dh*g*s as BF16 over the up tile, where this thread alone reads it again; the
+// sigmoid s = 1/(1 + exp(-g)) is evaluated once for both.
+__device__ __forceinline__ void silu_bwd_pair_from_smem(uint8_t* stage, int R0, int C0, uint32_t (&w)[8][4]) {
+    #pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint4 gv = *reinterpret_cast<const uint4*>(stage + (R0 + i) * 256 + C0 * 2);
+        uint4* up = reinterpret_cast<uint4*>(stage + 128 * 256 + (R0 + i) * 256 + C0 * 2);
+        const uint4 u = *up;
+        const uint4 d = *reinterpret_cast<const uint4*>(stage + 2 * 128 * 256 + (R0 + i) * 256 + C0 * 2);
+        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+        const uint32_t uv[4] = {u.x, u.y, u.z, u.w};
+        const uint32_t dv[4] = {d.x, d.y, d.z, d.w};
+        uint32_t du[4];
+        #pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float og[2], ou[2];
+            #pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float g = e ? bf16_hi(gw[j]) : bf16_lo(gw[j]);
+                const float uu = e ? bf16_hi(uv[j]) : bf16_lo(uv[j]);
+                const float dd = e ? bf16_hi(dv[j]) : bf16_lo(dv[j]);
+                const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
+                og[e] = __fmul_rn(__fmul_rn(__fmul_rn(dd, uu), sg), __fmaf_rn(g, __fsub_rn(1.0f, sg), 1.0f));
+                ou[e] = __fmul_rn(dd, __fmul_rn(g, sg));
+            }
+            w[i][j] = pack_bf16x2(og[0], og[1]);
+            du[j] = pack_bf16x2(ou[0], ou[1]);
+        }
+        *up = make_uint4(du[0], du[1], du[2], du[3]);
+    }
+    // the stage is refilled by TMA after these generic writes
+    fence_proxy_async_smem();
 }
 
 // BF16 unpacking that the compiler may not merge with the plain one: the column codes
@@ -325,19 +338,19 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
     constexpr bool PERSIST = PRO != PRO_RMSNORM;
     const int64_t rms_panel = blockIdx.y;
     const int64_t rms_m0 = rms_panel * 128;
-    const int64_t all_tiles = ((a.M + 127) / 128) * ntiles;
+    const int64_t all_tiles = ((a.M + 127) / 128) * (PRO == PRO_SILU_BWD ? ntiles / 2 : ntiles);   // items
     const int64_t t_begin = PERSIST ? 0 : (int64_t)blockIdx.x * a.tiles_per_cta;
     const int64_t t_end = (t_begin + a.tiles_per_cta < ntiles) ? t_begin + a.tiles_per_cta : ntiles;
     const int n = PERSIST ? (int)((all_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x) : (int)(t_end - t_begin);
     const int total = (PRO == PRO_RMSNORM) ? 2 * n : n;   // items streamed through the ring
     auto tile_at = [&](int it, int64_t& pnl, int64_t& tt) {
         if (PERSIST) {
+            // SiLU-mul backward: an item is a source column block, which gives both its dg
+            // and its du tile
+            const int64_t per = PRO == PRO_SILU_BWD ? ntiles / 2 : ntiles;
             const int64_t id = blockIdx.x + (int64_t)(it % n) * gridDim.x;
-            pnl = id / ntiles;
-            tt = id - pnl * ntiles;
-            // SiLU-mul backward: the dg and du tiles of one column block are neighbours in
-            // the order, so the second reads its gate and dh tiles from L2
-            if (PRO == PRO_SILU_BWD) tt = (tt & 1) ? ntiles / 2 + (tt >> 1) : (tt >> 1);
+            pnl = id / per;
+            tt = id - pnl * per;
         } else {
             pnl = rms_panel;
             tt = t_begin + it % n;
@@ -453,230 +466,249 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
         if (!ok) break;
         int64_t panel, t;
         tile_at(item, panel, t);
-        const int64_t k0 = t * 128, m0 = panel * 128;
-        uint32_t w[8][4];
-        float rg[8];
-        #pragma unroll
-        for (int i = 0; i < 8; ++i)   // rows past M (TMA zero fill) are never stored
-            rg[i] = (PRO == PRO_RMSNORM_G && m0 + R0 + i < a.M) ? __ldg(a.rstd_out + m0 + R0 + i) : 0.0f;
-        rows_from_smem<PRO>(stages + (item % STAGES) * PS::STAGE_BYTES, a, k0, R0, C0, s_rstd, rg, w);
-        // group maxima (exact BF16 values) on the packed words with the sign bits cleared
-        // rows over the 16 lanes of the half-warp, columns over this warp's
-        // 16 rows here and over the 8 warps through shared memory
-        auto wa = [&](int i, int j) { return w[i][j] & 0x7FFF7FFFu; };
-        uint32_t pm[4];   // rows (2k, 2k+1) of this half, as BF16 bits
-        if (ROW_OUT) {
-            #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint32_t m2[2];
+        const int64_t m0 = panel * 128;
+        uint8_t* const stage = stages + (item % STAGES) * PS::STAGE_BYTES;
+        // Quantize one output tile, column block tt, from this thread's BF16 words w (8 rows
+        // x 8 columns); the stage is refilled after the first barrier if `refill`.
+        auto quantize_tile = [&](uint32_t (&w)[8][4], const int64_t tt, const bool refill) {
+            const int64_t k0 = tt * 128;
+            const int64_t t = tt;
+            // group maxima (exact BF16 values) on the packed words with the sign bits cleared
+            // rows over the 16 lanes of the half-warp, columns over this warp's
+            // 16 rows here and over the 8 warps through shared memory
+            auto wa = [&](int i, int j) { return w[i][j] & 0x7FFF7FFFu; };
+            uint32_t pm[4];   // rows (2k, 2k+1) of this half, as BF16 bits
+            if (ROW_OUT) {
                 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    uint32_t v = __vmaxu2(wa(2 * k + e, 0), wa(2 * k + e, 1));
-                    v = __vmaxu2(v, __vmaxu2(wa(2 * k + e, 2), wa(2 * k + e, 3)));
-                    m2[e] = v;
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t m2[2];
+                    #pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        uint32_t v = __vmaxu2(wa(2 * k + e, 0), wa(2 * k + e, 1));
+                        v = __vmaxu2(v, __vmaxu2(wa(2 * k + e, 2), wa(2 * k + e, 3)));
+                        m2[e] = v;
+                    }
+                    // per row: max of its two halves; rows 2k (low) and 2k+1 (high) in one word
+                    pm[k] = __vmaxu2(__byte_perm(m2[0], m2[1], 0x5410), __byte_perm(m2[0], m2[1], 0x7632));
                 }
-                // per row: max of its two halves; rows 2k (low) and 2k+1 (high) in one word
-                pm[k] = __vmaxu2(__byte_perm(m2[0], m2[1], 0x5410), __byte_perm(m2[0], m2[1], 0x7632));
-            }
-            #pragma unroll
-            for (int off = 8; off >= 1; off >>= 1)
                 #pragma unroll
-                for (int k = 0; k < 4; ++k) pm[k] = __vmaxu2(pm[k], __shfl_xor_sync(0xffffffffu, pm[k], off));
-        }
-        if (COL_OUT) {
-            uint32_t cm[4];
-            #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t c = __vmaxu2(__vmaxu2(wa(0, j), wa(1, j)), __vmaxu2(wa(2, j), wa(3, j)));
-                c = __vmaxu2(c, __vmaxu2(__vmaxu2(wa(4, j), wa(5, j)), __vmaxu2(wa(6, j), wa(7, j))));
-                cm[j] = __vmaxu2(c, __shfl_xor_sync(0xffffffffu, c, 16));
+                for (int off = 8; off >= 1; off >>= 1)
+                    #pragma unroll
+                    for (int k = 0; k < 4; ++k) pm[k] = __vmaxu2(pm[k], __shfl_xor_sync(0xffffffffu, pm[k], off));
             }
-            // half h keeps the pair words 4cl + 2h, +1 (its own four columns) at word 32h + 2cl
-            *reinterpret_cast<uint2*>(&s_colmax[warp][32 * half + 2 * cl]) = half ? make_uint2(cm[2], cm[3]) : make_uint2(cm[0], cm[1]);
-        }
-        // values are unpacked where they are encoded: holding the 64 unpacked floats would
-        // double the registers and halve the CTAs per SM
-        auto xrow = [&](int i, int j) { return make_float2(bf16_lo(w[i][j]), bf16_hi(w[i][j])); };
-        // this tile's qT staging buffer (two, alternating: the next tile's barrier orders
-        // this tile's reads before the writes of the tile after)
-        const uint32_t colq = smem_u32(stages + PS::COLQ_OFF) + (uint32_t)(item & 1) * (128u * 128u);
-        __syncthreads();                                  // stage consumed, column maxima published
-        if (tid == 0 && issued < total) issue(issued++);
-
-        // row scales: lane cl computes the scale of row (cl & 7) of its half; every lane
-        // takes the scales of its 8 rows from those lanes
-        FastScale fs = {};
-        if (ROW_OUT) {
-            const int ri = cl & 7;
-            const uint32_t pw = (ri >> 1) == 0 ? pm[0] : (ri >> 1) == 1 ? pm[1] : (ri >> 1) == 2 ? pm[2] : pm[3];
-            fs = fast_scale(bf16_bits_amax_to_f32((ri & 1) ? (pw >> 16) : (pw & 0xFFFFu)));
-            if (cl < 8 && m0 + R0 + ri < a.M) a.s[t * a.M + m0 + R0 + ri] = fs.s;
-        }
-        // column scales: this half computes those of columns C0 + 4*half + {0..3} (from the
-        // 8 warps' maxima) and swaps them with the other half for the remaining four
-        float cs[8], cr[8];
-        if (COL_OUT) {
-            uint32_t mx0 = 0, mx1 = 0;
-            #pragma unroll
-            for (int ww = 0; ww < 8; ++ww) {
-                const uint2 v = *reinterpret_cast<const uint2*>(&s_colmax[ww][32 * half + 2 * cl]);
-                mx0 = __vmaxu2(mx0, v.x);
-                mx1 = __vmaxu2(mx1, v.y);
-            }
-            const uint32_t mb[4] = {mx0 & 0xFFFFu, mx0 >> 16, mx1 & 0xFFFFu, mx1 >> 16};
-            float os[4], orr[4];
-            #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const FastScale f = fast_scale(bf16_bits_amax_to_f32(mb[e]));
-                os[e] = f.s;
-                orr[e] = f.nr;
-            }
-            if (warp == 0)
-                *reinterpret_cast<float4*>(a.sT + panel * a.K + k0 + C0 + 4 * half) = make_float4(os[0], os[1], os[2], os[3]);
-            #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float ts = __shfl_xor_sync(0xffffffffu, os[e], 16);
-                const float tr = __shfl_xor_sync(0xffffffffu, orr[e], 16);
-                cs[e] = half ? ts : os[e];
-                cr[e] = half ? tr : orr[e];
-                cs[4 + e] = half ? os[e] : ts;
-                cr[4 + e] = half ? orr[e] : tr;
-            }
-        }
-        // the 8 codes of column C0 + cc, rows R0 .. R0 + 7: into the qT staging tile, or
-        // straight to qT
-        auto col_store = [&](int cc, uint32_t lo, uint32_t hi) {
-            if (COLQ) {
-                // row c = C0 + cc of the staging tile holds its 8-byte pieces r8 = R0 / 8 at
-                // slot r8 ^ (2 (c/8 mod 8) + c/64): the 16 lanes of each half-warp store to 16
-                // different slots, so a store takes the minimum two wavefronts
-                const uint32_t slot = (uint32_t)((R0 >> 3) ^ (2 * (cl & 7) + (cl >> 3)));
-                asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(colq + (uint32_t)(C0 + cc) * 128u + slot * 8u),
-                             "r"(lo), "r"(hi)
-                             : "memory");
-            } else {
-                stg_v2(a.qT + (k0 + C0 + cc) * a.M + m0 + R0, lo, hi);
-            }
-        };
-        // 1x128 codes, one row at a time, any scale
-        auto row_codes = [&]() {
-            #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int src = (lane & 16) | i;
-                const float si = __shfl_sync(0xffffffffu, fs.s, src);
-                const float nri = __shfl_sync(0xffffffffu, fs.nr, src);
-                const uint32_t keep = si == 0.0f ? 0u : 0xFFFFFFFFu;
-                uint32_t c[4];
-                #pragma unroll
-                for (int j = 0; j < 4; ++j) c[j] = encode_pair_neg(xrow(i, j), si, nri);
-                uint32_t lo = flip_codes(c[0], c[1], keep), hi = flip_codes(c[2], c[3], keep);
-                if (si > 0.0f && scale_is_slow(si)) {
-                    const uint4 v = encode4_slow(xrow(i, 0), xrow(i, 1), xrow(i, 2), xrow(i, 3), si);
-                    lo = v.x | (v.y << 16);
-                    hi = v.z | (v.w << 16);
-                }
-                const int64_t m = m0 + R0 + i;
-                if (m < a.M) stg_v2(a.q + m * a.K + k0 + C0, lo, hi);
-            }
-        };
-        // 128x1 codes, one column at a time (vertically adjacent pairs), any scale
-        auto col_codes = [&]() {
-            #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-                const int j = cc >> 1;
-                const uint32_t keep = cs[cc] == 0.0f ? 0u : 0xFFFFFFFFu;
-                float2 x[4];
-                #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    x[k] = (cc & 1) ? make_float2(bf16_hi_v(w[2 * k][j]), bf16_hi_v(w[2 * k + 1][j]))
-                                    : make_float2(bf16_lo_v(w[2 * k][j]), bf16_lo_v(w[2 * k + 1][j]));
-                uint32_t c[4];
-                #pragma unroll
-                for (int k = 0; k < 4; ++k) c[k] = encode_pair_neg(x[k], cs[cc], cr[cc]);
-                uint32_t lo = flip_codes(c[0], c[1], keep), hi = flip_codes(c[2], c[3], keep);
-                if (cs[cc] > 0.0f && scale_is_slow(cs[cc])) {
-                    const uint4 v = encode4_slow(x[0], x[1], x[2], x[3], cs[cc]);
-                    lo = v.x | (v.y << 16);
-                    hi = v.z | (v.w << 16);
-                }
-                col_store(cc, lo, hi);
-            }
-        };
-        if (ROW_OUT && COL_OUT) {
-            bool slow = fs.slow;
-            #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) slow = slow || (cs[cc] > 0.0f && scale_is_slow(cs[cc]));
-            if (__any_sync(0xffffffffu, slow)) {
-                row_codes();
-                col_codes();
-            } else {
-                // No group of this warp needs a division: both directions from one unpack
-                // of each BF16 pair (columns 2j, 2j+1 of a row), the row code pair under the
-                // row's scale and the column code pair under the two columns' scales.  The
-                // column pairs of rows 2k and 2k+1 are packed as P[j][k] = bytes (r2k c2j,
-                // r2k c2j+1, r2k+1 c2j, r2k+1 c2j+1); byte permutes then give each column's
-                // 8 codes in row order.
-                float2 csp[4], crp[4];
+            if (COL_OUT) {
+                uint32_t cm[4];
                 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    csp[j] = make_float2(cs[2 * j], cs[2 * j + 1]);
-                    crp[j] = make_float2(cr[2 * j], cr[2 * j + 1]);
+                    uint32_t c = __vmaxu2(__vmaxu2(wa(0, j), wa(1, j)), __vmaxu2(wa(2, j), wa(3, j)));
+                    c = __vmaxu2(c, __vmaxu2(__vmaxu2(wa(4, j), wa(5, j)), __vmaxu2(wa(6, j), wa(7, j))));
+                    cm[j] = __vmaxu2(c, __shfl_xor_sync(0xffffffffu, c, 16));
                 }
-                uint32_t P[4][4], ev[4];
+                // half h keeps the pair words 4cl + 2h, +1 (its own four columns) at word 32h + 2cl
+                *reinterpret_cast<uint2*>(&s_colmax[warp][32 * half + 2 * cl]) = half ? make_uint2(cm[2], cm[3]) : make_uint2(cm[0], cm[1]);
+            }
+            // values are unpacked where they are encoded: holding the 64 unpacked floats would
+            // double the registers and halve the CTAs per SM
+            auto xrow = [&](int i, int j) { return make_float2(bf16_lo(w[i][j]), bf16_hi(w[i][j])); };
+            // this tile's qT staging buffer (two, alternating: the next tile's barrier orders
+            // this tile's reads before the writes of the tile after)
+            const uint32_t colq = smem_u32(stages + PS::COLQ_OFF) + (uint32_t)(item & 1) * (128u * 128u);
+            __syncthreads();                                  // stage consumed, column maxima published
+            if (refill && tid == 0 && issued < total) issue(issued++);
+
+            // row scales: lane cl computes the scale of row (cl & 7) of its half; every lane
+            // takes the scales of its 8 rows from those lanes
+            FastScale fs = {};
+            if (ROW_OUT) {
+                const int ri = cl & 7;
+                const uint32_t pw = (ri >> 1) == 0 ? pm[0] : (ri >> 1) == 1 ? pm[1] : (ri >> 1) == 2 ? pm[2] : pm[3];
+                fs = fast_scale(bf16_bits_amax_to_f32((ri & 1) ? (pw >> 16) : (pw & 0xFFFFu)));
+                if (cl < 8 && m0 + R0 + ri < a.M) a.s[t * a.M + m0 + R0 + ri] = fs.s;
+            }
+            // column scales: this half computes those of columns C0 + 4*half + {0..3} (from the
+            // 8 warps' maxima) and swaps them with the other half for the remaining four
+            float cs[8], cr[8];
+            if (COL_OUT) {
+                uint32_t mx0 = 0, mx1 = 0;
+                #pragma unroll
+                for (int ww = 0; ww < 8; ++ww) {
+                    const uint2 v = *reinterpret_cast<const uint2*>(&s_colmax[ww][32 * half + 2 * cl]);
+                    mx0 = __vmaxu2(mx0, v.x);
+                    mx1 = __vmaxu2(mx1, v.y);
+                }
+                const uint32_t mb[4] = {mx0 & 0xFFFFu, mx0 >> 16, mx1 & 0xFFFFu, mx1 >> 16};
+                float os[4], orr[4];
+                #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const FastScale f = fast_scale(bf16_bits_amax_to_f32(mb[e]));
+                    os[e] = f.s;
+                    orr[e] = f.nr;
+                }
+                if (warp == 0)
+                    *reinterpret_cast<float4*>(a.sT + panel * a.K + k0 + C0 + 4 * half) = make_float4(os[0], os[1], os[2], os[3]);
+                #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float ts = __shfl_xor_sync(0xffffffffu, os[e], 16);
+                    const float tr = __shfl_xor_sync(0xffffffffu, orr[e], 16);
+                    cs[e] = half ? ts : os[e];
+                    cr[e] = half ? tr : orr[e];
+                    cs[4 + e] = half ? os[e] : ts;
+                    cr[4 + e] = half ? orr[e] : tr;
+                }
+            }
+            // the 8 codes of column C0 + cc, rows R0 .. R0 + 7: into the qT staging tile, or
+            // straight to qT
+            auto col_store = [&](int cc, uint32_t lo, uint32_t hi) {
+                if (COLQ) {
+                    // row c = C0 + cc of the staging tile holds its 8-byte pieces r8 = R0 / 8 at
+                    // slot r8 ^ (2 (c/8 mod 8) + c/64): the 16 lanes of each half-warp store to 16
+                    // different slots, so a store takes the minimum two wavefronts
+                    const uint32_t slot = (uint32_t)((R0 >> 3) ^ (2 * (cl & 7) + (cl >> 3)));
+                    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(colq + (uint32_t)(C0 + cc) * 128u + slot * 8u),
+                                 "r"(lo), "r"(hi)
+                                 : "memory");
+                } else {
+                    stg_v2(a.qT + (k0 + C0 + cc) * a.M + m0 + R0, lo, hi);
+                }
+            };
+            // 1x128 codes, one row at a time, any scale
+            auto row_codes = [&]() {
                 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int src = (lane & 16) | i;
                     const float si = __shfl_sync(0xffffffffu, fs.s, src);
                     const float nri = __shfl_sync(0xffffffffu, fs.nr, src);
                     const uint32_t keep = si == 0.0f ? 0u : 0xFFFFFFFFu;
-                    uint32_t rc[4];
+                    uint32_t c[4];
                     #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float2 x = xrow(i, j);
-                        rc[j] = encode_pair_neg(x, si, nri);
-                        const uint32_t c = encode_pair_neg2(x, csp[j], crp[j]);
-                        if (i & 1) P[j][i >> 1] = ev[j] | (c << 16);
-                        else ev[j] = c;
+                    for (int j = 0; j < 4; ++j) c[j] = encode_pair_neg(xrow(i, j), si, nri);
+                    uint32_t lo = flip_codes(c[0], c[1], keep), hi = flip_codes(c[2], c[3], keep);
+                    if (si > 0.0f && scale_is_slow(si)) {
+                        const uint4 v = encode4_slow(xrow(i, 0), xrow(i, 1), xrow(i, 2), xrow(i, 3), si);
+                        lo = v.x | (v.y << 16);
+                        hi = v.z | (v.w << 16);
                     }
                     const int64_t m = m0 + R0 + i;
-                    if (m < a.M) stg_v2(a.q + m * a.K + k0 + C0, flip_codes(rc[0], rc[1], keep), flip_codes(rc[2], rc[3], keep));
+                    if (m < a.M) stg_v2(a.q + m * a.K + k0 + C0, lo, hi);
                 }
+            };
+            // 128x1 codes, one column at a time (vertically adjacent pairs), any scale
+            auto col_codes = [&]() {
                 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int cc = 0; cc < 8; ++cc) {
+                    const int j = cc >> 1;
+                    const uint32_t keep = cs[cc] == 0.0f ? 0u : 0xFFFFFFFFu;
+                    float2 x[4];
                     #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int cc = 2 * j + e;
-                        const uint32_t keep = cs[cc] == 0.0f ? 0u : 0xFFFFFFFFu;
-                        const uint32_t sel = e ? 0x7531u : 0x6420u;
-                        col_store(cc, (__byte_perm(P[j][0], P[j][1], sel) ^ 0x80808080u) & keep,
-                                  (__byte_perm(P[j][2], P[j][3], sel) ^ 0x80808080u) & keep);
+                    for (int k = 0; k < 4; ++k)
+                        x[k] = (cc & 1) ? make_float2(bf16_hi_v(w[2 * k][j]), bf16_hi_v(w[2 * k + 1][j]))
+                                        : make_float2(bf16_lo_v(w[2 * k][j]), bf16_lo_v(w[2 * k + 1][j]));
+                    uint32_t c[4];
+                    #pragma unroll
+                    for (int k = 0; k < 4; ++k) c[k] = encode_pair_neg(x[k], cs[cc], cr[cc]);
+                    uint32_t lo = flip_codes(c[0], c[1], keep), hi = flip_codes(c[2], c[3], keep);
+                    if (cs[cc] > 0.0f && scale_is_slow(cs[cc])) {
+                        const uint4 v = encode4_slow(x[0], x[1], x[2], x[3], cs[cc]);
+                        lo = v.x | (v.y << 16);
+                        hi = v.z | (v.w << 16);
+                    }
+                    col_store(cc, lo, hi);
+                }
+            };
+            if (ROW_OUT && COL_OUT) {
+                bool slow = fs.slow;
+                #pragma unroll
+                for (int cc = 0; cc < 8; ++cc) slow = slow || (cs[cc] > 0.0f && scale_is_slow(cs[cc]));
+                if (__any_sync(0xffffffffu, slow)) {
+                    row_codes();
+                    col_codes();
+                } else {
+                    // No group of this warp needs a division: both directions from one unpack
+                    // of each BF16 pair (columns 2j, 2j+1 of a row), the row code pair under the
+                    // row's scale and the column code pair under the two columns' scales.  The
+                    // column pairs of rows 2k and 2k+1 are packed as P[j][k] = bytes (r2k c2j,
+                    // r2k c2j+1, r2k+1 c2j, r2k+1 c2j+1); byte permutes then give each column's
+                    // 8 codes in row order.
+                    float2 csp[4], crp[4];
+                    #pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        csp[j] = make_float2(cs[2 * j], cs[2 * j + 1]);
+                        crp[j] = make_float2(cr[2 * j], cr[2 * j + 1]);
+                    }
+                    uint32_t P[4][4], ev[4];
+                    #pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int src = (lane & 16) | i;
+                        const float si = __shfl_sync(0xffffffffu, fs.s, src);
+                        const float nri = __shfl_sync(0xffffffffu, fs.nr, src);
+                        const uint32_t keep = si == 0.0f ? 0u : 0xFFFFFFFFu;
+                        uint32_t rc[4];
+                        #pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float2 x = xrow(i, j);
+                            rc[j] = encode_pair_neg(x, si, nri);
+                            const uint32_t c = encode_pair_neg2(x, csp[j], crp[j]);
+                            if (i & 1) P[j][i >> 1] = ev[j] | (c << 16);
+                            else ev[j] = c;
+                        }
+                        const int64_t m = m0 + R0 + i;
+                        if (m < a.M) stg_v2(a.q + m * a.K + k0 + C0, flip_codes(rc[0], rc[1], keep), flip_codes(rc[2], rc[3], keep));
+                    }
+                    #pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        #pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int cc = 2 * j + e;
+                            const uint32_t keep = cs[cc] == 0.0f ? 0u : 0xFFFFFFFFu;
+                            const uint32_t sel = e ? 0x7531u : 0x6420u;
+                            col_store(cc, (__byte_perm(P[j][0], P[j][1], sel) ^ 0x80808080u) & keep,
+                                      (__byte_perm(P[j][2], P[j][3], sel) ^ 0x80808080u) & keep);
+                        }
+                    }
+                }
+            } else if (ROW_OUT) {
+                row_codes();
+            } else if (COL_OUT) {
+                col_codes();
+            }
+            if (COLQ) {
+                __syncthreads();
+                {
+                    // thread tid copies the 16-byte pieces id = tid + 256 i: row c = id / 8 of
+                    // the staging tile, bytes 16k .. 16k + 15 (k = id % 8), i.e. its slots 2k and
+                    // 2k + 1, which sit together at chunk k ^ (c/8 mod 8); 8 lanes write one
+                    // 128-byte row of qT
+                    #pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int id = tid + 256 * i, c = id >> 3, k = id & 7;
+                        uint4 v;
+                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                                     : "r"(colq + (uint32_t)c * 128u + (uint32_t)((k ^ ((c >> 3) & 7)) * 16)));
+                        // rows c with c / 8 >= 8 hold the pair (2k, 2k+1) in swapped order
+                        if ((c >> 6) & 1) stg_v4(a.qT + (k0 + c) * a.M + m0 + 16 * k, v.z, v.w, v.x, v.y);
+                        else stg_v4(a.qT + (k0 + c) * a.M + m0 + 16 * k, v.x, v.y, v.z, v.w);
                     }
                 }
             }
-        } else if (ROW_OUT) {
-            row_codes();
-        } else if (COL_OUT) {
-            col_codes();
-        }
-        if (COLQ) {
-            __syncthreads();
-            {
-                // thread tid copies the 16-byte pieces id = tid + 256 i: row c = id / 8 of
-                // the staging tile, bytes 16k .. 16k + 15 (k = id % 8), i.e. its slots 2k and
-                // 2k + 1, which sit together at chunk k ^ (c/8 mod 8); 8 lanes write one
-                // 128-byte row of qT
-                #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int id = tid + 256 * i, c = id >> 3, k = id & 7;
-                    uint4 v;
-                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                                 : "r"(colq + (uint32_t)c * 128u + (uint32_t)((k ^ ((c >> 3) & 7)) * 16)));
-                    // rows c with c / 8 >= 8 hold the pair (2k, 2k+1) in swapped order
-                    if ((c >> 6) & 1) stg_v4(a.qT + (k0 + c) * a.M + m0 + 16 * k, v.z, v.w, v.x, v.y);
-                    else stg_v4(a.qT + (k0 + c) * a.M + m0 + 16 * k, v.x, v.y, v.z, v.w);
-                }
-            }
+        };
+        uint32_t w[8][4];
+        if constexpr (PRO == PRO_SILU_BWD) {
+            // source column block t gives two output tiles: dg (block t) from the
+            // registers, then du (block ntiles/2 + t) from the stage's up slot, where the
+            // prologue left it; the sigmoid is evaluated once for both
+            silu_bwd_pair_from_smem(stage, R0, C0, w);
+            quantize_tile(w, t, false);
+            const float rg0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            rows_from_smem<PRO_COPY>(stage + 128 * 256, a, 0, R0, C0, nullptr, rg0, w);
+            quantize_tile(w, ntiles / 2 + t, true);
+        } else {
+            float rg[8];
+            #pragma unroll
+            for (int i = 0; i < 8; ++i)   // rows past M (TMA zero fill) are never stored
+                rg[i] = (PRO == PRO_RMSNORM_G && m0 + R0 + i < a.M) ? __ldg(a.rstd_out + m0 + R0 + i) : 0.0f;
+            rows_from_smem<PRO>(stage, a, t * 128, R0, C0, s_rstd, rg, w);
+            quantize_tile(w, t, true);
         }
     }
     if (tid == 0) {
@@ -992,7 +1024,7 @@ static cudaError_t launch_panel_t(const PanelArgs& a, int64_t in_cols, int clust
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem);
             return std::max(1, sms * std::max(1, per_sm));
         }();
-        const int64_t all_tiles = ((a.M + 127) / 128) * ntiles;
+        const int64_t all_tiles = ((a.M + 127) / 128) * (PRO == PRO_SILU_BWD ? ntiles / 2 : ntiles);   // items
         cfg.gridDim = dim3((unsigned)std::min<int64_t>(all_tiles, resident), 1, 1);
     }
     cfg.blockDim = dim3(256, 1, 1);
