@@ -300,7 +300,9 @@ struct PanelStages {
     // for two input stages of 32 KB at two CTAs per SM.
     static constexpr int STAGES = (PRO == PRO_SILU || PRO == PRO_SILU_BWD) ? 1 : (COLQ && PRO != PRO_DEQUANT ? 2 : 3);
     static constexpr int COLQ_OFF = ((STAGES * STAGE_BYTES + 127) / 128) * 128;
-    static constexpr size_t SMEM = (size_t)COLQ_OFF + (COLQ ? 2 * 128 * 128 : 0) + 128;  // + alignment slack
+    // (SiLU-mul backward stages its 128x1 codes in the stage's gate tile, dead after its
+    // prologue: no separate staging tiles)
+    static constexpr size_t SMEM = (size_t)COLQ_OFF + (COLQ && PRO != PRO_SILU_BWD ? 2 * 128 * 128 : 0) + 128;
 };
 
 // A CTA works through a sequence of 128x128 tiles (see tile_at below).
@@ -316,7 +318,7 @@ template <int PRO, bool ROW_OUT, bool COL_OUT>
 __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ CUtensorMap tmx,
                                                      const __grid_constant__ CUtensorMap tmy,
                                                      const PanelArgs a) {
-    constexpr bool COLQ = COL_OUT && PRO != PRO_SILU_BWD;
+    constexpr bool COLQ = COL_OUT;
     using PS = PanelStages<PRO, COLQ>;
     constexpr int STAGES = PS::STAGES;
     extern __shared__ uint8_t q_smem_raw[];
@@ -365,14 +367,16 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
         if (PRO == PRO_SILU_BWD) tma_prefetch_desc(&tmy);
     }
     __syncthreads();
-    auto issue = [&](int item) {
+    // part: 0 every tile of the item; SiLU-mul backward also 1 (the barrier's arrival and
+    // the up and dh tiles) and 2 (the gate tile), issued at different times
+    auto issue = [&](int item, int part = 0) {
         const int st = item % STAGES;
         int64_t pnl, tt;
         tile_at(item, pnl, tt);
         const int64_t k0 = tt * 128, m0 = pnl * 128;
         const uint32_t bar = smem_u32(&full_bar[st]);
         uint8_t* dst = stages + st * PS::STAGE_BYTES;
-        mbar_arrive_expect_tx(bar, PS::STAGE_BYTES);
+        if (part != 2) mbar_arrive_expect_tx(bar, PS::STAGE_BYTES);
         if (PRO == PRO_DEQUANT) {
             // the code tile and the 128 row scales of its column block (one bulk copy:
             // 512 bytes at a 16-byte-aligned offset, since M is a multiple of 128)
@@ -383,9 +387,11 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
             // the gate tile, the up tile and the tile of dh of that block
             const int64_t half_k = a.K / 2;
             const int64_t j0 = k0 < half_k ? k0 : k0 - half_k;
-            tma_load_2d(smem_u32(dst), &tmx, bar, (int)j0, (int)m0, 0);
-            tma_load_2d(smem_u32(dst + 128 * 128 * 2), &tmx, bar, (int)(half_k + j0), (int)m0, 0);
-            tma_load_2d(smem_u32(dst + 2 * 128 * 128 * 2), &tmy, bar, (int)j0, (int)m0, 0);
+            if (part != 1) tma_load_2d(smem_u32(dst), &tmx, bar, (int)j0, (int)m0, 0);
+            if (part != 2) {
+                tma_load_2d(smem_u32(dst + 128 * 128 * 2), &tmx, bar, (int)(half_k + j0), (int)m0, 0);
+                tma_load_2d(smem_u32(dst + 2 * 128 * 128 * 2), &tmy, bar, (int)j0, (int)m0, 0);
+            }
         } else {
             tma_load_2d(smem_u32(dst), &tmx, bar, (int)k0, (int)m0, 0);
             if (PRO == PRO_SILU) tma_load_2d(smem_u32(dst + 128 * 128 * 2), &tmx, bar, (int)(a.K + k0), (int)m0, 0);
@@ -469,8 +475,9 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
         const int64_t m0 = panel * 128;
         uint8_t* const stage = stages + (item % STAGES) * PS::STAGE_BYTES;
         // Quantize one output tile, column block tt, from this thread's BF16 words w (8 rows
-        // x 8 columns); the stage is refilled after the first barrier if `refill`.
-        auto quantize_tile = [&](uint32_t (&w)[8][4], const int64_t tt, const bool refill) {
+        // x 8 columns), its 128x1 codes staged at colq.  After the first barrier the stage
+        // is refilled (refill 1), has its up and dh tiles requested (refill 2), or neither.
+        auto quantize_tile = [&](uint32_t (&w)[8][4], const int64_t tt, const uint32_t colq, const int refill) {
             const int64_t k0 = tt * 128;
             const int64_t t = tt;
             // group maxima (exact BF16 values) on the packed words with the sign bits cleared
@@ -510,11 +517,11 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
             // values are unpacked where they are encoded: holding the 64 unpacked floats would
             // double the registers and halve the CTAs per SM
             auto xrow = [&](int i, int j) { return make_float2(bf16_lo(w[i][j]), bf16_hi(w[i][j])); };
-            // this tile's qT staging buffer (two, alternating: the next tile's barrier orders
-            // this tile's reads before the writes of the tile after)
-            const uint32_t colq = smem_u32(stages + PS::COLQ_OFF) + (uint32_t)(item & 1) * (128u * 128u);
             __syncthreads();                                  // stage consumed, column maxima published
-            if (refill && tid == 0 && issued < total) issue(issued++);
+            if (tid == 0 && issued < total) {
+                if (refill == 1) issue(issued++);
+                else if (refill == 2) issue(issued, 1);
+            }
 
             // row scales: lane cl computes the scale of row (cl & 7) of its half; every lane
             // takes the scales of its 8 rows from those lanes
@@ -697,18 +704,28 @@ __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ 
             // source column block t gives two output tiles: dg (block t) from the
             // registers, then du (block ntiles/2 + t) from the stage's up slot, where the
             // prologue left it; the sigmoid is evaluated once for both
+            // The gate tile is dead after the prologue: its two halves stage the two tiles'
+            // 128x1 codes, and the next item's gate tile is requested once they have left
+            // (its up and dh tiles after the du tile has been read back).
             silu_bwd_pair_from_smem(stage, R0, C0, w);
-            quantize_tile(w, t, false);
+            quantize_tile(w, t, smem_u32(stage), 0);
             const float rg0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             rows_from_smem<PRO_COPY>(stage + 128 * 256, a, 0, R0, C0, nullptr, rg0, w);
-            quantize_tile(w, ntiles / 2 + t, true);
+            quantize_tile(w, ntiles / 2 + t, smem_u32(stage) + 128u * 128u, COL_OUT ? 2 : 1);
+            if (COL_OUT) {
+                fence_proxy_async_smem();   // the staged codes are overwritten by TMA next
+                __syncthreads();
+                if (tid == 0 && issued < total) issue(issued++, 2);
+            }
         } else {
             float rg[8];
             #pragma unroll
             for (int i = 0; i < 8; ++i)   // rows past M (TMA zero fill) are never stored
                 rg[i] = (PRO == PRO_RMSNORM_G && m0 + R0 + i < a.M) ? __ldg(a.rstd_out + m0 + R0 + i) : 0.0f;
             rows_from_smem<PRO>(stage, a, t * 128, R0, C0, s_rstd, rg, w);
-            quantize_tile(w, t, true);
+            // this tile's qT staging buffer (two, alternating: the next tile's barrier orders
+            // this tile's reads before the writes of the tile after)
+            quantize_tile(w, t, smem_u32(stages + PS::COLQ_OFF) + (uint32_t)(item & 1) * (128u * 128u), 1);
         }
     }
     if (tid == 0) {
@@ -1007,7 +1024,7 @@ static cudaError_t launch_panel_t(const PanelArgs& a, int64_t in_cols, int clust
         tm2 = tm;   // unused
     }
     auto kern = k_quant_panel<PRO, ROW_OUT, COL_OUT>;
-    constexpr size_t smem = PanelStages<PRO, COL_OUT && PRO != PRO_SILU_BWD>::SMEM;
+    constexpr size_t smem = PanelStages<PRO, COL_OUT>::SMEM;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t ntiles = a.K / 128;
