@@ -24,6 +24,7 @@
 // multiplies each K-block's token scales by the weight block's scale once for everyone;
 // warps 4-11 promote each K-block's partial into FP32 registers (two warps per TMEM lane
 // quadrant, each half of the tokens), then store or run the cluster reduction.  Every mbarrier wait is bounded (FP8RL_ERR_DEVICE_TIMEOUT).
+#include "cluster.cuh"
 #include "common.cuh"
 #include "gemm.h"
 
@@ -47,31 +48,6 @@ struct DecodeCfg {
     static constexpr int NBARS = 2 * STAGES + 2 * NB + 3 * NSC + 1;
     static constexpr size_t BYTES = 1024 + STAGE_BYTES + (size_t)NSC * (SLOT + MP) * 4 + NBARS * 8 + 16;
 };
-
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_idx() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_count() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
 
 }  // namespace
 

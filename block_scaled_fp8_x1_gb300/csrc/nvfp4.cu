@@ -24,6 +24,7 @@
 //               of 128 hold zeros.  One K-block of 256 elements of one row group is 2 KB,
 //               contiguous, and each atom is one tcgen05.cp.32x128b copy to TMEM;
 //   g[R]        the per-row FP32 scales.
+#include "cluster.cuh"
 #include "common.cuh"
 #include "gemm.h"
 #include "rollout.h"
@@ -224,30 +225,6 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
-__device__ __forceinline__ uint32_t nv_cluster_nctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t nv_cluster_idx() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t nv_cluster_count() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ float4 nv_ld_dsmem_v4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-
 }  // namespace
 
 // Grid: with a cluster of S > 1 CTAs, one cluster per 128-row weight tile (CTA r streams
@@ -279,10 +256,10 @@ __global__ void __launch_bounds__(320, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int S = (int)nv_cluster_nctarank();
+    const int S = (int)cluster_nctarank();
     const int rank = (int)cluster_ctarank();
-    const int tile0 = (int)nv_cluster_idx();
-    const int tstep = (int)nv_cluster_count();
+    const int tile0 = (int)cluster_idx();
+    const int tstep = (int)cluster_count();
     const int tiles = p.tiles;
     const int kb0 = (int)(((int64_t)rank * p.nkb) / S);
     const int kb1 = (int)(((int64_t)(rank + 1) * p.nkb) / S);
@@ -483,7 +460,7 @@ __global__ void __launch_bounds__(320, 1)
                 const uint32_t off = (uint32_t)(tok * 128 + r4) * 4u;
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int j = 0; j < S; ++j) {
-                    const float4 w = nv_ld_dsmem_v4(mapa_shared(red_local + off, (uint32_t)j));
+                    const float4 w = ld_dsmem_v4(mapa_shared(red_local + off, (uint32_t)j));
                     v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
                 }
                 const float gxt = __ldg(p.gx + tok);
