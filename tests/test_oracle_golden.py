@@ -1,6 +1,7 @@
 """The oracle still reproduces its committed regression fixture bit for bit.
 
-The fixture (tests/golden/oracle_small.txt) was written by
+The fixtures (tests/golden/oracle_small.txt, and oracle_nvfp4_small.txt for the NVFP4
+routines) were written by
 tests/golden/make_oracle_fixtures.py, which calls only the oracle; see that script for the
 closed-form input.  The scheme's pages print no worked example to compare against.
 """
@@ -16,3 +17,11 @@ def test_oracle_reproduces_fixture(oracle):
     with open(os.path.join(HERE, "golden", "oracle_small.txt")) as f:
         stored = f.read()
     assert mk.render() == stored
+
+
+def test_oracle_reproduces_nvfp4_fixture(oracle):
+    sys.path.insert(0, os.path.join(HERE, "golden"))
+    import make_oracle_fixtures as mk
+    with open(os.path.join(HERE, "golden", "oracle_nvfp4_small.txt")) as f:
+        stored = f.read()
+    assert mk.render_nvfp4() == stored
