@@ -40,6 +40,18 @@ def _contig(t: torch.Tensor, name: str) -> None:
         raise ValueError(f"{name}: expected a contiguous tensor")
 
 
+def _out(out: Optional[torch.Tensor], shape, device) -> torch.Tensor:
+    """A caller-given output (bf16, on `device`, of `shape`, contiguous: the C calls write it
+    with row stride shape[1]) or a new one."""
+    if out is None:
+        return torch.empty(shape, dtype=torch.bfloat16, device=device)
+    _require(out, torch.bfloat16, "out", device)
+    if tuple(out.shape) != tuple(shape):
+        raise ValueError(f"out: expected shape {tuple(shape)}, got {tuple(out.shape)}")
+    _contig(out, "out")
+    return out
+
+
 def as_e4m3(q: torch.Tensor) -> torch.Tensor:
     """View uint8 codes as torch.float8_e4m3fn (no copy)."""
     return q.view(torch.float8_e4m3fn)
@@ -291,7 +303,7 @@ def gemm_fwd(qx, sx, qw, sw, out=None, variant: int = _abi.FP8RL_VARIANT_AUTO, s
     M, K = qx.shape
     N = qw.shape[0]
     dev = qx.device
-    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    y = _out(out, (M, N), dev)
     opts = GemmOpts(int(variant), int(splits), int(grid), int(tile_n), int(epi_warps))
     wsb = ws
     need = int(lib().fp8rl_gemm_workspace_bytes_ex(_abi.FP8RL_OP_FWD, M, N, K, ctypes.byref(opts)))
@@ -310,7 +322,7 @@ def gemm_dgrad(qdy, sdy, qwT, sw, out=None, variant: int = _abi.FP8RL_VARIANT_AU
     M, N = qdy.shape
     K = qwT.shape[0]
     dev = qdy.device
-    dx = out if out is not None else torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    dx = _out(out, (M, K), dev)
     opts = GemmOpts(int(variant), 0, int(grid), int(tile_n), int(epi_warps))
     check(lib().fp8rl_gemm_dgrad_ex(_ptr(qdy), _ptr(sdy), _ptr(qwT), _ptr(sw), _ptr(dx), M, N, K,
                                     None, 0, ctypes.byref(opts), _stream(dev)), "fp8rl_gemm_dgrad_ex")
@@ -324,7 +336,7 @@ def gemm_wgrad(qdyT, sdyT, qxT, sxT, out=None, variant: int = _abi.FP8RL_VARIANT
     N, M = qdyT.shape
     K = qxT.shape[0]
     dev = qdyT.device
-    dw = out if out is not None else torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    dw = _out(out, (N, K), dev)
     opts = GemmOpts(int(variant), 0, int(grid), int(tile_n), int(epi_warps))
     check(lib().fp8rl_gemm_wgrad_ex(_ptr(qdyT), _ptr(sdyT), _ptr(qxT), _ptr(sxT), _ptr(dw), M, N,
                                     K, None, 0, ctypes.byref(opts), _stream(dev)), "fp8rl_gemm_wgrad_ex")
@@ -347,7 +359,7 @@ def linear_fwd(x: torch.Tensor, qw, sw, out=None):
     dev = x.device
     qx = torch.empty((M, K), dtype=torch.uint8, device=dev)
     sx = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
-    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    y = _out(out, (M, N), dev)
     need = gemm_workspace_bytes(_abi.FP8RL_OP_FWD, M, N, K)
     wsb = workspace(need, dev) if need > 0 else None
     check(lib().fp8rl_linear_fwd(_ptr(x), M, K, x.stride(0), _ptr(qw), _ptr(sw), N, _ptr(qx),
@@ -392,6 +404,9 @@ def gemm_nvfp4(qx, sfx, gx, qw, sfw, gw, splits: int = 0, out=None):
     M, K2 = qx.shape
     N = qw.shape[0]
     y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    _require(y, torch.bfloat16, "out", dev)
+    if y.shape != (M, N) or y.stride(1) != 1:
+        raise ValueError("out: expected a [M, N] bf16 view with contiguous rows")
     check(lib().fp8rl_gemm_nvfp4(_ptr(qx), _ptr(sfx), _ptr(gx), _ptr(qw), _ptr(sfw), _ptr(gw), _ptr(y),
                                  M, N, 2 * K2, y.stride(0), int(splits), _stream(dev)), "fp8rl_gemm_nvfp4")
     return y
@@ -407,7 +422,7 @@ def linear_nvfp4(x: torch.Tensor, qw, sfw, gw, out=None):
     N = qw.shape[0]
     dev = x.device
     qx, sfx, gx = _nvfp4_buffers(M, K, dev)
-    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    y = _out(out, (M, N), dev)
     check(lib().fp8rl_linear_nvfp4(_ptr(x), M, K, x.stride(0), _ptr(qw), _ptr(sfw), _ptr(gw), N, _ptr(qx),
                                    _ptr(sfx), _ptr(gx), _ptr(y), _stream(dev)), "fp8rl_linear_nvfp4")
     return y, qx, sfx, gx

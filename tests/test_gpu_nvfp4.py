@@ -104,6 +104,19 @@ def test_gemm_nvfp4(fp8lib, oracle, M, splits):
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
 
 
+@pytest.mark.parametrize("splits", [1, 4])
+def test_gemm_nvfp4_strided_output(fp8lib, oracle, splits):
+    """y written into columns 128 .. 128 + N of a wider buffer (ldy > N); the columns
+    around it stay untouched."""
+    M, N, K = 100, 768, 1024
+    dev, ref, _ = operands(fp8lib, oracle, M, N, K, 91 + splits)
+    big = torch.full((M, N + 256), -7.0, dtype=torch.bfloat16, device="cuda")
+    view = big[:, 128:128 + N]
+    fp8lib.gemm_nvfp4(*dev, splits=splits, out=view)
+    gemm_tolerance_check(bits16(view), oracle.gemm_nvfp4(*ref), f"nvfp4 ldy splits={splits}")
+    assert torch.all(big[:, :128] == -7.0) and torch.all(big[:, 128 + N:] == -7.0)
+
+
 def test_gemm_nvfp4_exact(fp8lib, oracle):
     """Operands whose FP32 accumulation is exact: every block holds a +-6 element and has
     scale 224 or 448, the row scales are powers of two, so each product is 49 * 2^k times
