@@ -10,13 +10,15 @@ master weights stay BF16 and are re-quantized each step; DGrad and WGrad run in 
   forward          rmsnorm_quant(X_attn) -> gemm_fwd(qkv)
                    quantize_1x128 dual(attention output) -> gemm_fwd(o)
                    rmsnorm_quant(X_mlp) -> gemm_fwd(gate_up) -> silu_mul_quant -> gemm_fwd(down)
-  backward         for each linear: quantize_1x128 dual(dY) -> gemm_dgrad -> gemm_wgrad
+  backward         for each linear: dual-quantized dY -> gemm_dgrad -> gemm_wgrad, where dY
+                   is quantize_1x128 dual(dY) for qkv, o and down, and for gate_up
+                   silu_mul_bwd_quant(gate_up output, dH = the DGrad of down)
 
 value = GEMM FLOPs of the step / device time of the step (TFLOP/s), inputs resident in HBM
 and larger than L2.  e2e = the same with the step's batch tensors (the three input
-activations and the four output gradients, 2.9 GB) copied from pinned host memory and its
-results (the layer output and the four weight gradients, 1.1 GB) copied back inside the
-timed region; the BF16 weights are model state on the device, re-quantized by the step.  Per-kernel CUDA-event times give the
+activations and the output gradients of qkv, o and down, 1.1 GB) copied from pinned host
+memory and its results (the layer output and the four weight gradients, 1.1 GB) copied
+back inside the timed region; the BF16 weights are model state on the device, re-quantized by the step.  Per-kernel CUDA-event times give the
 quantizers' GB/s and the roofline of the dominant kernel.  Two more workloads are reported
 beside it: the Llama-3.1-8B MLP training step at 8192 tokens, and the rollout decode
 linears of Qwen2.5-7B at 64, 128 and 256 tokens (CUDA-graph replays over weight copies
@@ -50,7 +52,8 @@ M32, H32 = 16384, 5120
 LIN32 = {"qkv": (7168, 5120), "o": (5120, 5120), "gate_up": (55296, 5120), "down": (5120, 27648)}
 WORKLOAD = ("Qwen2.5-32B layer at 16384 tokens: qkv 7168x5120, o 5120x5120, gate_up "
             "55296x5120, down 5120x27648; fwd + DGrad + WGrad of all four with their "
-            "quantizers and the weight refresh")
+            "quantizers and the weight refresh; dY of gate_up from dH through the SiLU-mul "
+            "backward")
 # Llama-3.1-8B MLP at 8192 tokens (reported beside it)
 M_TOK, HID, INTER = 8192, 4096, 14336
 # Qwen2.5-7B decode linears (reported beside it)
@@ -72,6 +75,11 @@ def silu_bytes(M, I):
     return 2 * 2 * M * I + M * I + M * I + 2 * 4 * M * I / 128
 
 
+def silu_bwd_bytes(M, I):
+    """gate_up output and dH in, the dual codes and scales of [dg | du] out."""
+    return 2 * 2 * M * I + 2 * M * I + 2 * M * I + 2 * M * I + 2 * 4 * 2 * M * I / 128
+
+
 def rms_bytes(M, K):
     return dual_bytes(M * K) + 2 * K + 4 * M
 
@@ -84,7 +92,9 @@ def layer32_work():
         fl = 2.0 * M * N * K
         f[f"fwd_{name}"] = f[f"dgrad_{name}"] = f[f"wgrad_{name}"] = fl
         b[f"wq_{name}"] = wq_bytes(N * K)
-        b[f"dq_dy_{name}"] = dual_bytes(M * N)
+        if name != "gate_up":
+            b[f"dq_dy_{name}"] = dual_bytes(M * N)
+    b["silu_mul_bwd_quant"] = silu_bwd_bytes(M, LIN32["down"][1])
     b["rmsnorm_quant_attn"] = rms_bytes(M, H32)
     b["dq_attn_out"] = dual_bytes(M * H32)
     b["rmsnorm_quant_mlp"] = rms_bytes(M, H32)
@@ -101,7 +111,7 @@ def mlp8_work():
     b["rmsnorm_quant"] = rms_bytes(M_TOK, HID)
     b["silu_mul_quant"] = silu_bytes(M_TOK, INTER)
     b["dq_dy_down"] = dual_bytes(M_TOK * HID)
-    b["dq_dy_gate_up"] = dual_bytes(M_TOK * 2 * INTER)
+    b["silu_mul_bwd_quant"] = silu_bwd_bytes(M_TOK, INTER)
     return f, b
 
 
@@ -221,7 +231,9 @@ class Layer32Step:
     """Qwen2.5-32B-shaped layer at 16384 tokens: all buffers resident on the device and the
     launches of one step in order."""
 
-    LAUNCHES_PER_STEP = 26   # 4 weight, 2x2 RMSNorm, 1 dual, 4 fwd, 1 SiLU-mul, 4x3 backward
+    # 4 weight, 2x2 RMSNorm, 1 dual, 4 fwd, 1 SiLU-mul, 4x3 backward (gate_up's gradient
+    # quantizer being the SiLU-mul backward)
+    LAUNCHES_PER_STEP = 26
 
     def __init__(self, dev):
         import torch
@@ -234,12 +246,15 @@ class Layer32Step:
         self.x_mlp = synth.activation(w, M32, H32, 2, dev)
         self.gamma = torch.ones(H32, dtype=torch.bfloat16, device=dev)
         self.w = {n: synth.weight(w, lins[n], 10 + i, dev) for i, n in enumerate(LIN32)}
-        self.dy = {n: synth.gradient(w, M32, LIN32[n][0], 20 + i, dev) for i, n in enumerate(LIN32)}
+        # gradients of the linears' outputs; gate_up's comes from dH (the DGrad of down)
+        # through the SiLU-mul backward inside the step
+        self.dy = {n: synth.gradient(w, M32, LIN32[n][0], 20 + i, dev)
+                   for i, n in enumerate(LIN32) if n != "gate_up"}
         self.eps = 1e-5
         # per-step batch tensors (the layer's input activations and the gradients of its
         # outputs); the BF16 weights and gamma are model state that stays on the device and
         # that the step itself re-quantizes, as the optimizer's updates would require
-        self.inputs = ["x_attn", "attn_out", "x_mlp"] + [f"dy.{n}" for n in LIN32]
+        self.inputs = ["x_attn", "attn_out", "x_mlp"] + [f"dy.{n}" for n in self.dy]
         # what a step hands back: the layer's output and the four weight gradients
         self.results = ["y"] + [f"dw_{n}" for n in LIN32]
         self.outputs = {}
@@ -272,7 +287,11 @@ class Layer32Step:
         y = ops.gemm_fwd(q, s, qw["down"][0], qw["down"][1]); mark("fwd_down")
         out = {"qkv": qkv, "o": o, "y": y}
         for n in ("down", "gate_up", "o", "qkv"):
-            qd, sd, qdT, sdT = ops.quantize_1x128(self.dy[n], dual=True); mark(f"dq_dy_{n}")
+            if n == "gate_up":
+                # dY of gate_up = [dg | du] from its output and dH, quantized both ways
+                qd, sd, qdT, sdT = ops.silu_mul_bwd_quant(gu, out["dx_down"]); mark("silu_mul_bwd_quant")
+            else:
+                qd, sd, qdT, sdT = ops.quantize_1x128(self.dy[n], dual=True); mark(f"dq_dy_{n}")
             out[f"dx_{n}"] = ops.gemm_dgrad(qd, sd, qw[n][2], qw[n][1]); mark(f"dgrad_{n}")
             out[f"dw_{n}"] = ops.gemm_wgrad(qdT, sdT, acts[n][2], acts[n][3]); mark(f"wgrad_{n}")
         self.outputs = out
@@ -296,7 +315,6 @@ class Mlp8Step:
         self.w_gu = synth.weight(w, gate_up, 1, dev)
         self.w_d = synth.weight(w, down, 2, dev)
         self.dy_d = synth.gradient(wb, M_TOK, HID, 3, dev)
-        self.dy_gu = synth.gradient(wb, M_TOK, 2 * INTER, 4, dev)
         self.eps = w.extra["eps"]
 
     def run(self, marks=None):
@@ -312,7 +330,8 @@ class Mlp8Step:
         qdy, sdy, qdyT, sdyT = ops.quantize_1x128(self.dy_d, dual=True); mark("dq_dy_down")
         dh = ops.gemm_dgrad(qdy, sdy, qT_d, s_d); mark("dgrad_down")
         dw_d = ops.gemm_wgrad(qdyT, sdyT, qhT, shT); mark("wgrad_down")
-        qg, sg, qgT, sgT = ops.quantize_1x128(self.dy_gu, dual=True); mark("dq_dy_gate_up")
+        # dY of gate_up = [dg | du] from its output and dH, quantized both ways
+        qg, sg, qgT, sgT = ops.silu_mul_bwd_quant(gu, dh); mark("silu_mul_bwd_quant")
         dx = ops.gemm_dgrad(qg, sg, qT_gu, s_gu); mark("dgrad_gate_up")
         dw_gu = ops.gemm_wgrad(qgT, sgT, qxT, sxT); mark("wgrad_gate_up")
         return {"y": y, "dh": dh, "dx": dx, "dw_gu": dw_gu, "dw_d": dw_d}
@@ -638,7 +657,8 @@ def run_gpu(args):
         k8 = kernel_table(per_kernel(s8, 5, torch), f8, b8, fp8_peak, hbm)
         extra["llama8b_mlp_step"] = {
             "workload": "Llama-3.1-8B MLP training step at 8192 tokens (gate_up 28672x4096, "
-                        "down 4096x14336; fwd + DGrad + WGrad, weight refresh)",
+                        "down 4096x14336; fwd + DGrad + WGrad, weight refresh; dY of gate_up "
+                        "from dH through the SiLU-mul backward)",
             "ms_per_step": round(ms8, 4), "TFLOP/s": round(sum(f8.values()) / (ms8 * 1e-3) / 1e12, 1),
             "kernels": k8}
         del s8
@@ -655,12 +675,12 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD, "tokens": M32, "hidden": H32,
                    "linears": {k: list(v) for k, v in LIN32.items()},
                    "gemm_flops_per_step": step_flops,
-                   "l2": "inputs larger than L2 (X 168 MB each, W_gate_up 566 MB, dY_gate_up 1.8 GB per step)",
+                   "l2": "inputs larger than L2 (X 168 MB each, W_gate_up 566 MB, gate_up output 1.8 GB per step)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
         "e2e": {"value": round(job_rate(step_flops, world, ms_e2e) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4),
-                "copies": "every step's batch tensors (X_attn, attention output, X_mlp, the four dY) up from pinned host memory and its results (y, the four dW) down, on two copy streams overlapping the neighbouring steps' compute; the BF16 weights stay on the device as model state and are re-quantized by the step"},
+                "copies": "every step's batch tensors (X_attn, attention output, X_mlp, the dY of qkv, o and down) up from pinned host memory and its results (y, the four dW) down, on two copy streams overlapping the neighbouring steps' compute; the BF16 weights stay on the device as model state and are re-quantized by the step"},
         "gpu_launches": Layer32Step.LAUNCHES_PER_STEP * args.steps,
         "clocks": clk,
         "kernels": kern,
@@ -746,9 +766,13 @@ def oracle_step_estimate(rows: int, n_samp: int):
     t, h = timed(lambda: oracle.silu_mul(gu))
     t2, _ = timed(lambda: (oracle.quantize_1x128(h[0]), oracle.quantize_128x1(h[0])))
     est += (t + t2) * M32 / rows
-    # dual quantization of every dY, per element of the sampled activation rows
+    # dual quantization of the dY of qkv, o and down, per element of the sampled rows
     t, _ = timed(lambda: (oracle.quantize_1x128(x), oracle.quantize_128x1(x)))
-    est += t * M32 / rows * sum(N for N, _ in LIN32.values()) / H32
+    est += t * M32 / rows * sum(N for n, (N, _) in LIN32.items() if n != "gate_up") / H32
+    # the SiLU-mul backward of gate_up with the dual quantization of [dg | du]
+    dh = bits(synth.normal_bf16((rows, I), 1e-3, 10))
+    t, _ = timed(lambda: oracle.silu_mul_bwd_quant(gu, dh))
+    est += t * M32 / rows
     parts = [f"quantizers on {rows} token rows / 128 weight rows"]
     # GEMMs: sampled output elements, scaled by outputs / samples
     qx, sx = r[0], r[1]
