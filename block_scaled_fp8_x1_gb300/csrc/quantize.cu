@@ -310,10 +310,12 @@ struct PanelStages {
 // pull a tile into registers, and once everyone has it (the first barrier of the tile)
 // thread 0 refills that stage, so copies of the next tiles overlap the current one's math.
 // RMSNorm streams the CTA's tiles twice: pass 1 sums squares, pass 2 quantizes.
-// The 128x1 codes of a tile leave through shared memory (except after the three-input
-// SiLU-mul backward prologue, whose stage leaves no room): each thread writes its 8 columns
-// x 8 rows of codes there, and after a CTA barrier the tile goes out as 16-byte pieces, 8
-// lanes per 128-byte row of qT, instead of 16 scattered 8-byte pieces per warp store.
+// The 128x1 codes of a tile leave through shared memory (two staging tiles of their own;
+// the SiLU-mul backward uses its stage's gate tile, dead after its prologue): each thread
+// writes its 8 columns x 8 rows of codes there, and after a CTA barrier the tile goes out
+// as 16-byte pieces, 8 lanes per 128-byte row of qT, instead of 16 scattered 8-byte pieces
+// per warp store.  A SiLU-mul backward item is one source column block, which yields its
+// dg and its du tile from one evaluation of the sigmoid.
 template <int PRO, bool ROW_OUT, bool COL_OUT>
 __global__ void __launch_bounds__(256, 2) k_quant_panel(const __grid_constant__ CUtensorMap tmx,
                                                      const __grid_constant__ CUtensorMap tmy,
