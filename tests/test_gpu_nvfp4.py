@@ -181,3 +181,24 @@ def test_gemm_nvfp4_full_size_sampled(fp8lib, oracle, M, N, K):
     y_ref = oracle.gemm_nvfp4_sampled(*ref, m, n)
     rms = float(np.sqrt(np.mean(y_ref * y_ref)))
     gemm_tolerance_check(yb[m, n], y_ref, f"nvfp4 {M}x{N}x{K}", rms=rms)
+
+
+def test_nvfp4_linear_error_against_fp8(fp8lib, capsys):
+    """The rollout formats' error on the same BF16 operands (activation with outlier
+    channels, weights sigma 0.015): relative Frobenius error of the FP8 linear (1x128
+    activations, 128x128 weight blocks) and of the NVFP4 linear, both against the exact
+    product of the BF16 inputs.  NVFP4 keeps 1 mantissa bit against E4M3's 3, so its
+    error is the larger, and both stay bounded."""
+    M, N, K = 64, 2048, 3584
+    x = synth.normal_bf16((M, K), 1.0, 31, "cuda", outlier_channels=4, outlier_scale=30.0)
+    w = synth.normal_bf16((N, K), 0.015, 32, "cuda")
+    exact = x.double().cpu() @ w.double().cpu().T
+    qw8, sw8, _ = fp8lib.quantize_128x128(w)
+    y8, _, _ = fp8lib.linear_fwd(x, qw8, sw8)
+    q4, sf4, g4 = fp8lib.quantize_nvfp4(w)
+    y4, _, _, _ = fp8lib.linear_nvfp4(x, q4, sf4, g4)
+    err = lambda y: float(torch.linalg.norm(y.double().cpu() - exact) / torch.linalg.norm(exact))
+    e8, e4 = err(y8), err(y4)
+    with capsys.disabled():
+        print(f"\nrelative Frobenius error vs the BF16 product: FP8 {e8:.3e}, NVFP4 {e4:.3e}")
+    assert e8 < e4 < 0.2 and e8 < 0.05
